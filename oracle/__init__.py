@@ -1,0 +1,225 @@
+"""fp64 CPU oracle of the Kamera KV-reuse operator (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the product path (the CUDA library and its Python
+binding) never imports this package.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` use it.
+
+The arithmetic lives in ``kamera_oracle.c`` (plain loops, fp64); this module
+compiles it with the host C compiler and marshals numpy arrays through ctypes.
+Source of the method: "Kamera: Unified Position-Invariant Multimodal KV Cache
+for Training-Free Reuse" (gist.science technical summary), §2 "Methodology:
+the Kamera operator" and §3 "window operations".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kamera_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkamera_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MHA, GQA, MLA = 0, 1, 2
+ROTATE_HALF, INTERLEAVED = 0, 1
+PATCH_AFTER_ROTATION, PATCH_CANONICAL_FRAME = 0, 1
+MODE_REUSE, MODE_RELOCATE_IN_PLACE, MODE_PATCH_IN_PLACE = 0, 1, 2
+EFLAG_CHUNK_OOB, EFLAG_PAGE_OOB, EFLAG_PATCH_OOB, EFLAG_LEN = 1, 2, 4, 8
+
+
+class Model(ctypes.Structure):
+    _fields_ = [
+        ("family", ctypes.c_int32),
+        ("num_layers", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("rope_dim", ctypes.c_int32),
+        ("latent_dim", ctypes.c_int32),
+        ("pairing", ctypes.c_int32),
+        ("patch_frame", ctypes.c_int32),
+    ]
+
+
+ITEM_DTYPE = np.dtype(
+    [
+        ("chunk_id", np.int32),
+        ("patch_id", np.int32),
+        ("delta", np.int64),
+        ("seq", np.int32),
+        ("n_tokens", np.int32),
+        ("dst_pos", np.int64),
+    ],
+    align=True,
+)
+assert ITEM_DTYPE.itemsize == 32
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH, cc: str = "gcc") -> str:
+    """Compile the oracle into a shared library (plain -O2, no fast-math)."""
+    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library.  ``path`` selects
+    another build of the same source, e.g. a planted-mistake copy in a test."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+                build()
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_row_dim.argtypes = [ctypes.POINTER(Model)]
+    lib.oracle_row_dim.restype = i32
+    lib.oracle_theta.argtypes = [f64, i32, P]
+    lib.oracle_theta.restype = None
+    lib.oracle_rotate_region.argtypes = [P, i32, P, i64, i32]
+    lib.oracle_rotate_region.restype = None
+    lib.oracle_rotate_row.argtypes = [ctypes.POINTER(Model), P, i32, i64, P]
+    lib.oracle_rotate_row.restype = None
+    lib.oracle_row.argtypes = [ctypes.POINTER(Model), P, i32, i64, i32, P, P, P, i32, P]
+    lib.oracle_row.restype = None
+    lib.oracle_slot.argtypes = [P, i32, i64, i32, i32, i64]
+    lib.oracle_slot.restype = i64
+    lib.oracle_reuse.argtypes = [ctypes.POINTER(Model), P, i32] + [P, P, P, i32] + [P, P, P, i32, i32] + [
+        P, i32, P, i32, i32, i64, i32, P, P, P, P, P, P]
+    lib.oracle_reuse.restype = i32
+    lib.oracle_jacobi_svd.argtypes = [P, i32, i32, P, P, i32]
+    lib.oracle_jacobi_svd.restype = i32
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def model(family, num_layers, num_kv_heads=0, head_dim=0, rope_dim=0, latent_dim=0,
+          pairing=ROTATE_HALF, patch_frame=PATCH_AFTER_ROTATION) -> Model:
+    if family != MLA and rope_dim == 0:
+        rope_dim = head_dim
+    return Model(family, num_layers, num_kv_heads, head_dim, rope_dim, latent_dim, pairing, patch_frame)
+
+
+def row_dim(m: Model) -> int:
+    return m.latent_dim + m.rope_dim if m.family == MLA else m.num_kv_heads * m.head_dim
+
+
+def num_channels(m: Model) -> int:
+    return 1 if m.family == MLA else 2
+
+
+def theta(base: float, rope_dim: int, lib=None) -> np.ndarray:
+    lib = lib or load()
+    out = np.zeros(rope_dim // 2, np.float64)
+    lib.oracle_theta(float(base), int(rope_dim), _ptr(out))
+    return out
+
+
+def rotate_region(x, th, delta: int, pairing=ROTATE_HALF, lib=None) -> np.ndarray:
+    """R(delta) on one rotated region (returns a rotated copy, fp64)."""
+    lib = lib or load()
+    y = np.array(x, dtype=np.float64, copy=True)
+    th = _c(th, np.float64)
+    lib.oracle_rotate_region(_ptr(y), int(y.shape[0]), _ptr(th), int(delta), int(pairing))
+    return y
+
+
+def rotate_row(m: Model, th, channel: int, delta: int, row, lib=None) -> np.ndarray:
+    lib = lib or load()
+    y = np.array(row, dtype=np.float64, copy=True)
+    th = _c(th, np.float64)
+    lib.oracle_rotate_row(ctypes.byref(m), _ptr(th), int(channel), int(delta), _ptr(y))
+    return y
+
+
+def row(m: Model, th, channel: int, delta: int, src, u=None, vmat=None, rotate=True, lib=None) -> np.ndarray:
+    """One output row: R(delta) src + U V^T row (fp64).  ``u`` [rank], ``vmat`` [D][rank]."""
+    lib = lib or load()
+    D = row_dim(m)
+    src = _c(src, np.float64)
+    th = _c(th, np.float64)
+    out = np.zeros(D, np.float64)
+    rank = 0 if u is None else int(np.asarray(u).shape[0])
+    u = _c(u, np.float64)
+    vmat = _c(vmat, np.float64) if vmat is not None else np.zeros((D, max(rank, 1)), np.float64)
+    lib.oracle_row(ctypes.byref(m), _ptr(th), int(channel), int(delta), int(bool(rotate)), _ptr(src), _ptr(u),
+                   _ptr(vmat), rank, _ptr(out))
+    return out
+
+
+def slot(block_table, max_pages_per_seq, num_pages, page_size, seq, pos, lib=None) -> int:
+    lib = lib or load()
+    bt = _c(block_table, np.int32)
+    return int(lib.oracle_slot(_ptr(bt), int(max_pages_per_seq), int(num_pages), int(page_size), int(seq), int(pos)))
+
+
+def reuse(m: Model, th, mode, *, store=None, store_off=None, store_len=None, patch=None, patch_off=None,
+          patch_len=None, rank=0, items, block_table, num_pages, page_size, pool_k_in, pool_v_in=None, lib=None):
+    """The operator over a batch of items into fp64 images of the pool.
+
+    Inputs are bf16 bit patterns as uint16 arrays.  Returns
+    ``(err_bits, pool_k_out, pool_v_out, wrote_k, wrote_v)``; the pool images
+    have the input pool's shape [L][num_pages][P][D] (fp64) and the masks
+    [L][num_pages][P] (uint8)."""
+    lib = lib or load()
+    th = _c(th, np.float64)
+    items = np.ascontiguousarray(items, dtype=ITEM_DTYPE)
+    bt = _c(block_table, np.int32)
+    n_seqs, max_pages = bt.shape
+    pool_k_in = _c(pool_k_in, np.uint16)
+    pool_v_in = _c(pool_v_in, np.uint16)
+    pk = np.zeros(pool_k_in.shape, np.float64)
+    pv = np.zeros(pool_v_in.shape, np.float64) if pool_v_in is not None else None
+    rows_shape = pool_k_in.shape[:-1]
+    wk = np.zeros(rows_shape, np.uint8)
+    wv = np.zeros(rows_shape, np.uint8) if pool_v_in is not None else None
+    store = _c(store, np.uint16)
+    store_off = _c(store_off, np.int64)
+    store_len = _c(store_len, np.int32)
+    patch = _c(patch, np.uint16)
+    patch_off = _c(patch_off, np.int64)
+    patch_len = _c(patch_len, np.int32)
+    n_chunks = 0 if store_len is None else int(store_len.shape[0])
+    n_patches = 0 if patch_len is None else int(patch_len.shape[0])
+    err = lib.oracle_reuse(ctypes.byref(m), _ptr(th), int(mode), _ptr(store), _ptr(store_off), _ptr(store_len),
+                           n_chunks, _ptr(patch), _ptr(patch_off), _ptr(patch_len), n_patches, int(rank),
+                           _ptr(items), int(items.shape[0]), _ptr(bt), int(n_seqs), int(max_pages),
+                           int(num_pages), int(page_size), _ptr(pool_k_in), _ptr(pool_v_in), _ptr(pk), _ptr(pv),
+                           _ptr(wk), _ptr(wv))
+    return int(err), pk, pv, wk, wv
+
+
+def jacobi_svd(a, max_sweeps: int = 60, lib=None):
+    """One-sided Jacobi SVD; returns (U*Sigma [rows][cols], V [cols][cols], sigma)."""
+    lib = lib or load()
+    a = np.array(a, dtype=np.float64, copy=True, order="C")
+    rows, cols = a.shape
+    v = np.zeros((cols, cols), np.float64)
+    sig = np.zeros(cols, np.float64)
+    lib.oracle_jacobi_svd(_ptr(a), rows, cols, _ptr(v), _ptr(sig), int(max_sweeps))
+    return a, v, sig
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> fp64 (exact).  Plain widening, kept here so the
+    tests' reading of bf16 buffers does not depend on the CUDA path."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)

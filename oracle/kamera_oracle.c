@@ -1,0 +1,354 @@
+/*
+ * kamera_oracle.c -- plain, slow, fp64 CPU oracle of the Kamera KV-reuse operator.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and
+ * its Python binding) may link, load or call this file.  Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark use it.  It shares
+ * no code, header, table or helper with the CUDA path.
+ *
+ * What it computes (source: "Kamera: Unified Position-Invariant Multimodal KV
+ * Cache for Training-Free Reuse", gist.science technical summary, Italian and
+ * Chinese editions -- cited below as "Kamera"):
+ *
+ *   Kamera §2 (Methodology, the Kamera operator), reuse equation:
+ *       KV^(B|A) = R(delta) . KV(B|empty) + U_m V_m^T
+ *   Kamera §2, "Relocation R(delta)": keys are re-rotated by the RoPE phase
+ *       shift delta of the new position; an exact algebraic operation.
+ *   Kamera §2, "Patch application": the rank-m patch U_m V_m^T is added.
+ *   Kamera §2, "Unified architecture support": MHA/GQA relocate the full keys
+ *       and patch K and V; MLA relocates only the decoupled 64-dim k_rope,
+ *       reuses c_KV byte for byte and patches both channels.
+ *   Kamera §3, the three window operations (reorder with an orbit patch,
+ *       sliding-window survival with R(delta) only, recall with a fresh patch)
+ *       are all instances of the same operator with different inputs.
+ *   Kamera §2, patch formation: the top-m factors come from an SVD of the
+ *       deficit; oracle_jacobi_svd below is a one-sided (Hestenes) Jacobi SVD
+ *       used to build exact-rank test cases.
+ *
+ * Readings where the pages are silent (each one is listed in the design doc):
+ *   - RoPE pairs are rotate-half (i, i + d_r/2) unless interleaved (2i, 2i+1)
+ *     is requested; theta_i = base^(-2i/d_r) unless a table is given.
+ *   - delta is an integer position shift, the same for every token of a chunk.
+ *   - The patch is added after the rotation (the literal formula); the
+ *     "canonical frame" variant rotates (KV + U V^T) instead.
+ *   - Patch factors are per layer and per channel over the flattened H*d row
+ *     (MLA: one U over the 576-wide latent row, V rows split 512 + 64).
+ *   - Destination: position pos = dst_pos + t lands in page
+ *     block_table[seq][pos / P], slot pos % P, of a pool laid out
+ *     [layer][page][slot][D].
+ *
+ * Everything is evaluated in fp64 from the bf16 inputs (bf16 -> fp64 is exact).
+ * Error bits follow the library's convention: an item whose chunk, patch,
+ * length or sequence is invalid is skipped whole; a row whose page is invalid
+ * is skipped alone.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_EFLAG_CHUNK_OOB 1
+#define OR_EFLAG_PAGE_OOB 2
+#define OR_EFLAG_PATCH_OOB 4
+#define OR_EFLAG_LEN 8
+
+enum { OR_MHA = 0, OR_GQA = 1, OR_MLA = 2 };
+enum { OR_ROTATE_HALF = 0, OR_INTERLEAVED = 1 };
+enum { OR_PATCH_AFTER_ROTATION = 0, OR_PATCH_CANONICAL_FRAME = 1 };
+enum { OR_MODE_REUSE = 0, OR_MODE_RELOCATE_IN_PLACE = 1, OR_MODE_PATCH_IN_PLACE = 2 };
+
+typedef struct {
+  int32_t family;       /* OR_MHA, OR_GQA, OR_MLA */
+  int32_t num_layers;
+  int32_t num_kv_heads; /* MHA/GQA */
+  int32_t head_dim;     /* MHA/GQA */
+  int32_t rope_dim;     /* rotated dims per head (MHA/GQA, <= head_dim); MLA: k_rope width */
+  int32_t latent_dim;   /* MLA: c_KV width (columns 0 .. latent_dim-1 of the latent row) */
+  int32_t pairing;      /* OR_ROTATE_HALF or OR_INTERLEAVED */
+  int32_t patch_frame;  /* OR_PATCH_AFTER_ROTATION or OR_PATCH_CANONICAL_FRAME */
+} oracle_model;
+
+typedef struct {
+  int32_t chunk_id;
+  int32_t patch_id; /* -1: no patch */
+  int64_t delta;
+  int32_t seq;
+  int32_t n_tokens;
+  int64_t dst_pos;
+} oracle_item;
+
+/* ---- plain helpers --------------------------------------------------------- */
+
+/* bf16 is the top half of an IEEE binary32; widening to fp64 is exact. */
+static double bf16_bits_to_f64(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* Width of one K (or V) row: H*d for MHA/GQA, latent + k_rope for MLA. */
+int32_t oracle_row_dim(const oracle_model* m) {
+  if (m->family == OR_MLA) return m->latent_dim + m->rope_dim;
+  return m->num_kv_heads * m->head_dim;
+}
+
+/* K and V are separate channels for MHA/GQA; MLA has one latent channel. */
+int32_t oracle_num_channels(const oracle_model* m) { return m->family == OR_MLA ? 1 : 2; }
+
+/* theta_i = base^(-2i/d_r), i < d_r/2 (the standard RoPE frequency ladder). */
+void oracle_theta(double base, int32_t rope_dim, double* theta) {
+  for (int32_t i = 0; i < rope_dim / 2; ++i) theta[i] = pow(base, -2.0 * (double)i / (double)rope_dim);
+}
+
+/*
+ * R(delta) on one rotated region x[0 .. rope_dim-1]: every pair (a, b) turns
+ * by the angle delta*theta_i,
+ *     a' = a cos - b sin,   b' = b cos + a sin.
+ * Kamera §2, "Relocation R(delta)".
+ */
+void oracle_rotate_region(double* x, int32_t rope_dim, const double* theta, int64_t delta, int32_t pairing) {
+  int32_t half = rope_dim / 2;
+  for (int32_t i = 0; i < half; ++i) {
+    int32_t ia = (pairing == OR_INTERLEAVED) ? 2 * i : i;
+    int32_t ib = (pairing == OR_INTERLEAVED) ? 2 * i + 1 : i + half;
+    double phi = (double)delta * theta[i];
+    double c = cos(phi), s = sin(phi);
+    double a = x[ia], b = x[ib];
+    x[ia] = a * c - b * s;
+    x[ib] = b * c + a * s;
+  }
+}
+
+/* Apply R(delta) to every rotated region of a K row (channel 0).  The V row
+ * (channel 1) carries no position and is never rotated.  MLA: only the k_rope
+ * columns after the c_KV latent turn; c_KV is untouched. */
+void oracle_rotate_row(const oracle_model* m, const double* theta, int32_t channel, int64_t delta, double* row) {
+  if (channel != 0) return;
+  if (m->family == OR_MLA) {
+    oracle_rotate_region(row + m->latent_dim, m->rope_dim, theta, delta, m->pairing);
+    return;
+  }
+  for (int32_t h = 0; h < m->num_kv_heads; ++h)
+    oracle_rotate_region(row + (int64_t)h * m->head_dim, m->rope_dim, theta, delta, m->pairing);
+}
+
+/* One output row of the operator, in fp64.
+ *   src  [D]       canonical row (or pool row for the in-place modes)
+ *   u    [rank]    this token's row of U, or NULL for no patch
+ *   vmat [D][rank] V of this layer and channel
+ * With the patch after rotation (the literal equation):  out = R src + U V^T row.
+ * In the canonical frame:                                out = R (src + U V^T row). */
+void oracle_row(const oracle_model* m, const double* theta, int32_t channel, int64_t delta, int32_t rotate,
+                const double* src, const double* u, const double* vmat, int32_t rank, double* out) {
+  int32_t D = oracle_row_dim(m);
+  double* patch = (double*)calloc((size_t)D, sizeof(double));
+  if (u != NULL) {
+    for (int32_t j = 0; j < D; ++j) {
+      double acc = 0.0;
+      for (int32_t r = 0; r < rank; ++r) acc += u[r] * vmat[(int64_t)j * rank + r];
+      patch[j] = acc;
+    }
+  }
+  if (m->patch_frame == OR_PATCH_CANONICAL_FRAME) {
+    for (int32_t j = 0; j < D; ++j) out[j] = src[j] + patch[j];
+    if (rotate) oracle_rotate_row(m, theta, channel, delta, out);
+  } else {
+    for (int32_t j = 0; j < D; ++j) out[j] = src[j];
+    if (rotate) oracle_rotate_row(m, theta, channel, delta, out);
+    for (int32_t j = 0; j < D; ++j) out[j] += patch[j];
+  }
+  free(patch);
+}
+
+/* Destination row (layer-independent part) of logical position pos of
+ * sequence seq: page = block_table[seq][pos / P], slot = pos % P.
+ * Returns page*P + slot, or -1 if the block-table index or the page id is out
+ * of range. */
+int64_t oracle_slot(const int32_t* block_table, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                    int32_t seq, int64_t pos) {
+  if (pos < 0) return -1;
+  int64_t blk = pos / page_size;
+  if (blk >= max_pages_per_seq) return -1;
+  int64_t page = block_table[(int64_t)seq * max_pages_per_seq + blk];
+  if (page < 0 || page >= num_pages) return -1;
+  return page * page_size + pos % page_size;
+}
+
+/*
+ * The whole operator over a list of items, into fp64 images of the pool.
+ *
+ * mode OR_MODE_REUSE:             source rows come from the canonical chunk store
+ *                                 (layout per chunk [layer][channel][T][D]); keys
+ *                                 are rotated, the patch (if any) is added.
+ * mode OR_MODE_RELOCATE_IN_PLACE: source rows are the pool's own K rows at the
+ *                                 item's positions; only R(delta) applies, V is
+ *                                 not touched (sliding-window survival, Kamera §3).
+ * mode OR_MODE_PATCH_IN_PLACE:    source rows are the pool's rows; the patch is
+ *                                 added to K and V with no rotation.
+ *
+ * Patch store layout per patch, per layer, per channel: U [T][rank] then
+ * V [D][rank].  pool_*_in hold the pool's bf16 bits before the call; the fp64
+ * images pool_*_out and the written masks are filled here (every slot starts
+ * as its input value, unwritten).  pool_v_in / pool_v_out / wrote_v are
+ * unused (may be NULL) for MLA.  Returns the OR of the error bits.
+ */
+int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
+                     const uint16_t* store, const int64_t* store_off, const int32_t* store_len, int32_t n_chunks,
+                     const uint16_t* patch, const int64_t* patch_off, const int32_t* patch_len, int32_t n_patches,
+                     int32_t rank, const oracle_item* items, int32_t n_items, const int32_t* block_table,
+                     int32_t n_seqs, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                     const uint16_t* pool_k_in, const uint16_t* pool_v_in, double* pool_k_out, double* pool_v_out,
+                     uint8_t* wrote_k, uint8_t* wrote_v) {
+  const int32_t D = oracle_row_dim(m);
+  const int32_t L = m->num_layers;
+  const int32_t n_ch = oracle_num_channels(m);
+  const int64_t pool_rows = (int64_t)L * num_pages * page_size;
+  int32_t err = 0;
+
+  for (int64_t i = 0; i < pool_rows * D; ++i) {
+    pool_k_out[i] = bf16_bits_to_f64(pool_k_in[i]);
+    if (n_ch == 2) pool_v_out[i] = bf16_bits_to_f64(pool_v_in[i]);
+  }
+  memset(wrote_k, 0, (size_t)pool_rows);
+  if (n_ch == 2) memset(wrote_v, 0, (size_t)pool_rows);
+
+  double* src = (double*)malloc(sizeof(double) * (size_t)D);
+  double* out = (double*)malloc(sizeof(double) * (size_t)D);
+  double* u = (double*)malloc(sizeof(double) * (size_t)(rank > 0 ? rank : 1));
+  double* vmat = (double*)malloc(sizeof(double) * (size_t)D * (size_t)(rank > 0 ? rank : 1));
+
+  for (int32_t it = 0; it < n_items; ++it) {
+    const oracle_item* item = &items[it];
+    const int32_t T = item->n_tokens;
+    if (T == 0) continue;
+    if (T < 0 || item->dst_pos < 0) { err |= OR_EFLAG_LEN; continue; }
+    if (item->seq < 0 || item->seq >= n_seqs) { err |= OR_EFLAG_PAGE_OOB; continue; }
+    if (mode == OR_MODE_REUSE) {
+      if (item->chunk_id < 0 || item->chunk_id >= n_chunks) { err |= OR_EFLAG_CHUNK_OOB; continue; }
+      if (store_len[item->chunk_id] != T) { err |= OR_EFLAG_LEN; continue; }
+    }
+    int32_t use_patch = 0;
+    if (mode != OR_MODE_RELOCATE_IN_PLACE && rank > 0 && patch != NULL && item->patch_id >= 0) {
+      if (item->patch_id >= n_patches) { err |= OR_EFLAG_PATCH_OOB; continue; }
+      if (patch_len[item->patch_id] != T) { err |= OR_EFLAG_LEN; continue; }
+      use_patch = 1;
+    }
+    if (mode == OR_MODE_PATCH_IN_PLACE && !use_patch) continue; /* nothing to add */
+    const int32_t rotate = (mode != OR_MODE_PATCH_IN_PLACE);
+    const int32_t ch_count = (mode == OR_MODE_RELOCATE_IN_PLACE) ? 1 : n_ch;
+
+    for (int32_t l = 0; l < L; ++l) {
+      for (int32_t ch = 0; ch < ch_count; ++ch) {
+        const uint16_t* pin = (ch == 0) ? pool_k_in : pool_v_in;
+        double* pout = (ch == 0) ? pool_k_out : pool_v_out;
+        uint8_t* wrote = (ch == 0) ? wrote_k : wrote_v;
+        if (use_patch) {
+          const int64_t base = patch_off[item->patch_id] + ((int64_t)l * n_ch + ch) * (int64_t)(T + D) * rank;
+          for (int64_t j = 0; j < D; ++j)
+            for (int32_t r = 0; r < rank; ++r)
+              vmat[j * rank + r] = bf16_bits_to_f64(patch[base + ((int64_t)T + j) * rank + r]);
+        }
+        for (int32_t t = 0; t < T; ++t) {
+          const int64_t pos = item->dst_pos + t;
+          const int64_t dst = oracle_slot(block_table, max_pages_per_seq, num_pages, page_size, item->seq, pos);
+          if (dst < 0) { err |= OR_EFLAG_PAGE_OOB; continue; }
+          const int64_t dst_row = (int64_t)l * num_pages * page_size + dst;
+          if (mode == OR_MODE_REUSE) {
+            const int64_t sb = store_off[item->chunk_id] + (((int64_t)l * n_ch + ch) * T + t) * D;
+            for (int32_t j = 0; j < D; ++j) src[j] = bf16_bits_to_f64(store[sb + j]);
+          } else {
+            for (int32_t j = 0; j < D; ++j) src[j] = bf16_bits_to_f64(pin[dst_row * D + j]);
+          }
+          if (use_patch) {
+            const int64_t ub = patch_off[item->patch_id] + ((int64_t)l * n_ch + ch) * (int64_t)(T + D) * rank +
+                               (int64_t)t * rank;
+            for (int32_t r = 0; r < rank; ++r) u[r] = bf16_bits_to_f64(patch[ub + r]);
+          }
+          oracle_row(m, theta, ch, item->delta, rotate, src, use_patch ? u : NULL, vmat, rank, out);
+          for (int32_t j = 0; j < D; ++j) pout[dst_row * D + j] = out[j];
+          wrote[dst_row] = 1;
+        }
+      }
+    }
+  }
+  free(src);
+  free(out);
+  free(u);
+  free(vmat);
+  return err;
+}
+
+/*
+ * One-sided Jacobi SVD (Hestenes, 1958) of a rows x cols matrix a (row-major,
+ * fp64), rows >= cols.  On return a holds U*Sigma (columns sorted by
+ * decreasing norm), v [cols][cols] holds V (column j is the right singular
+ * vector of singular value sigma[j]).  Each sweep orthogonalises every column
+ * pair (p, q) by a plane rotation chosen so that the rotated pair is
+ * orthogonal; it stops when every pair is orthogonal to the relative
+ * tolerance.  Kamera §2 names the SVD as the step that extracts the top-m
+ * patch factors; taking the first m columns gives U_m (with Sigma folded in)
+ * and V_m.  Returns the number of sweeps used.
+ */
+int32_t oracle_jacobi_svd(double* a, int32_t rows, int32_t cols, double* v, double* sigma, int32_t max_sweeps) {
+  for (int32_t i = 0; i < cols; ++i)
+    for (int32_t j = 0; j < cols; ++j) v[(int64_t)i * cols + j] = (i == j) ? 1.0 : 0.0;
+  int32_t sweep = 0;
+  for (; sweep < max_sweeps; ++sweep) {
+    int32_t rotated = 0;
+    for (int32_t p = 0; p < cols - 1; ++p) {
+      for (int32_t q = p + 1; q < cols; ++q) {
+        double alpha = 0.0, beta = 0.0, gamma = 0.0;
+        for (int32_t k = 0; k < rows; ++k) {
+          double ap = a[(int64_t)k * cols + p], aq = a[(int64_t)k * cols + q];
+          alpha += ap * ap;
+          beta += aq * aq;
+          gamma += ap * aq;
+        }
+        if (gamma == 0.0 || fabs(gamma) <= 1e-15 * sqrt(alpha * beta)) continue;
+        rotated = 1;
+        double zeta = (beta - alpha) / (2.0 * gamma);
+        double t = (zeta >= 0.0 ? 1.0 : -1.0) / (fabs(zeta) + sqrt(1.0 + zeta * zeta));
+        double c = 1.0 / sqrt(1.0 + t * t);
+        double s = c * t;
+        for (int32_t k = 0; k < rows; ++k) {
+          double ap = a[(int64_t)k * cols + p], aq = a[(int64_t)k * cols + q];
+          a[(int64_t)k * cols + p] = c * ap - s * aq;
+          a[(int64_t)k * cols + q] = s * ap + c * aq;
+        }
+        for (int32_t k = 0; k < cols; ++k) {
+          double vp = v[(int64_t)k * cols + p], vq = v[(int64_t)k * cols + q];
+          v[(int64_t)k * cols + p] = c * vp - s * vq;
+          v[(int64_t)k * cols + q] = s * vp + c * vq;
+        }
+      }
+    }
+    if (!rotated) break;
+  }
+  for (int32_t j = 0; j < cols; ++j) {
+    double n2 = 0.0;
+    for (int32_t k = 0; k < rows; ++k) n2 += a[(int64_t)k * cols + j] * a[(int64_t)k * cols + j];
+    sigma[j] = sqrt(n2);
+  }
+  /* selection sort of the columns by decreasing sigma (cols is small) */
+  for (int32_t j = 0; j < cols; ++j) {
+    int32_t best = j;
+    for (int32_t k = j + 1; k < cols; ++k)
+      if (sigma[k] > sigma[best]) best = k;
+    if (best == j) continue;
+    double ts = sigma[j];
+    sigma[j] = sigma[best];
+    sigma[best] = ts;
+    for (int32_t k = 0; k < rows; ++k) {
+      double tmp = a[(int64_t)k * cols + j];
+      a[(int64_t)k * cols + j] = a[(int64_t)k * cols + best];
+      a[(int64_t)k * cols + best] = tmp;
+    }
+    for (int32_t k = 0; k < cols; ++k) {
+      double tmp = v[(int64_t)k * cols + j];
+      v[(int64_t)k * cols + j] = v[(int64_t)k * cols + best];
+      v[(int64_t)k * cols + best] = tmp;
+    }
+  }
+  return sweep;
+}

@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark of the Kamera KV-reuse hot path on GB300.
+
+One step = one kamera_reuse_batched call over the whole batch (every layer,
+K and V): gather the canonical chunks, re-rotate the keys by delta, add the
+rank-m patch, scatter into the paged pool.  Default workload: GQA shaped like
+Qwen2.5-VL-7B (28 layers, 4 KV heads x 128, base 1e6), 16 chunks x 1024
+tokens, rank-32 patch per layer per K/V, page 64, shuffled block table.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line.  ``value`` = reused tokens/s with inputs resident in
+HBM (device time, CUDA events on the launching stream, max over ranks);
+``e2e`` = the same metric with the step's inputs copied host->device from
+pinned memory and the pool read back inside the timed region.  Inputs
+(1.97 GB per step) are larger than L2, so no flush is needed between steps.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import workloads as W  # noqa: E402
+
+METRIC = "reused KV tokens/sec (rotate + rank-m patch), achieved HBM GB/s vs roofline"
+UNIT = "tokens/s"
+KERNEL_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_kernel.cuh",
+                  "position_invariant_kv_kamera_gb300/csrc/ptx.cuh",
+                  "position_invariant_kv_kamera_gb300/csrc/kamera_api.cu"]
+DESCRIPTIONS = {
+    "gqa_video": "GQA Qwen2.5-VL-7B-shaped: 28 layers, 4 KV heads x 128, base 1e6, 16 chunks x 1024 tokens, "
+                 "1% outlier channels x8, rank-32 patch per layer per K/V, delta in [-32768, 32768], "
+                 "page 64, shuffled block table",
+    "tiny_mha": "MHA 1 layer, 4 heads x 64, one 256-token chunk, rank 8, delta 1000, contiguous output",
+    "mla_lite": "MLA DeepSeek-V2-Lite-shaped: 27 layers, c_KV 512 + k_rope 64, 8 chunks x 2048, rank 16, page 64",
+    "sliding_window": "sliding-window survival, GQA 8B-shaped (32 layers, 8 KV heads x 128, base 5e5): 56 of 64 "
+                      "resident 1024-token chunks re-rotated in place by -8192, no patch, page 64",
+    "long_video": "long-video reorder + recall, GQA 8B-shaped: 128 permuted chunks x 1296 with rank-64 orbit "
+                  "patches + 32 recalled chunks with fresh rank-64 patches, page 64",
+}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profile_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"reuse_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != kernel_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.out = out
+        else:
+            self.out = ""
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value: float, torch, device) -> float:
+    """Max over ranks (timing only; the data path has no collective)."""
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, world: int, max_elapsed_s: float, steps: int) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return tokens_per_rank * world * steps / max_elapsed_s
+
+
+# ---- CPU oracle timing (cpu_baseline and the reference arm) -----------------------------------
+
+def oracle_sample_workload(name: str, n_items: int, n_tokens: int | None = None) -> W.Workload:
+    """A bounded sample of the workload with the same shapes: the first n_items
+    chunks (optionally truncated to n_tokens tokens each)."""
+    full = W.CONFIGS[name]()
+    if name == "gqa_video":
+        wl = W.gqa_video(n_chunks=n_items, T=n_tokens or 1024)
+    elif name == "mla_lite":
+        wl = W.mla_lite(n_chunks=n_items, T=n_tokens or 2048)
+    elif name == "long_video":
+        wl = W.long_video(n_reorder=n_items, n_recall=0, T=n_tokens or 1296)
+    elif name == "sliding_window":
+        wl = W.sliding_window(n_resident=n_items + 1, n_evict=1)
+    else:
+        wl = full
+    return wl
+
+
+def time_oracle(wl: W.Workload) -> tuple[float, int]:
+    """Seconds of one oracle call over wl (inputs generated outside the timing)."""
+    import oracle
+    from tests import harness as H
+
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
+                     wl.pairing, wl.patch_frame)
+    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    kw = {}
+    if wl.mode == "reuse":
+        kw.update(store=wl.host_store(), store_off=wl.store_off, store_len=np.array(wl.chunk_lens, np.int32))
+    if wl.rank and wl.mode != "relocate_in_place":
+        kw.update(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
+                  rank=wl.rank)
+    mode = {"reuse": oracle.MODE_REUSE, "relocate_in_place": oracle.MODE_RELOCATE_IN_PLACE,
+            "apply_patch": oracle.MODE_PATCH_IN_PLACE}[wl.mode]
+    pk_in = wl.host_pool(0)
+    pv_in = wl.host_pool(1) if wl.n_ch == 2 else None
+    del H
+    t0 = time.perf_counter()
+    oracle.reuse(m, th, mode, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
+                 page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, **kw)
+    return time.perf_counter() - t0, wl.tokens
+
+
+def cpu_baseline(name: str, budget_s: float = 15.0) -> dict:
+    """The oracle as it stands (single-threaded C, fp64) on a bounded sample."""
+    dt1, tok1 = time_oracle(oracle_sample_workload(name, 1))
+    n = max(1, min(len(W.CONFIGS[name]().items), int(budget_s / max(dt1, 1e-3))))
+    if n > 1:
+        dt, tok = time_oracle(oracle_sample_workload(name, n))
+    else:
+        dt, tok = dt1, tok1
+    return {"value": tok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of the workload's chunks, all layers and channels ({tok} tokens, {dt:.1f} s, "
+                      f"single-threaded fp64 C oracle)"}
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    name = args.workload
+    # one step = the oracle over a token sample of one chunk, all layers, sized so
+    # that warm-up + timed steps take about two minutes in total
+    full_T = {"gqa_video": 1024, "mla_lite": 2048, "long_video": 1296}.get(name)
+    dt_probe, tok_probe = time_oracle(oracle_sample_workload(name, 1, 64 if full_T else None))
+    per_tok = dt_probe / max(tok_probe, 1)
+    budget = 120.0 / (args.steps + args.warmup)
+    n_tok = max(1, min(full_T or tok_probe, int(budget / max(per_tok, 1e-9))))
+    sample = oracle_sample_workload(name, 1, n_tok if full_T else None)
+    for _ in range(args.warmup):
+        time_oracle(sample)
+    total, toks = 0.0, 0
+    for _ in range(args.steps):
+        dt, tok = time_oracle(sample)
+        total += dt
+        toks += tok
+    value = toks / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{name}: {DESCRIPTIONS.get(name, '')}",
+                       "sample_per_step": f"{sample.tokens} tokens of one chunk, all layers"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: {sample.tokens} tokens x {sample.num_layers} layers"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---- GPU arm ----------------------------------------------------------------------------------
+
+def run_gpu(args) -> None:
+    import torch
+
+    import position_invariant_kv_kamera_gb300 as pk
+    from tests import harness as H
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pk.load()
+
+    base = W.CONFIGS[args.workload]()
+    # weak scaling: every rank reuses its own batch of the same shape
+    wl = base.replace(seed=base.seed + 1000 * rank) if world > 1 else base
+    t = H.device_inputs(wl, torch, device)
+    stream = torch.cuda.current_stream(device)
+    torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        H.call(wl, t, stream=stream)
+    torch.cuda.synchronize(device)
+    if int(t["err"].item()) != 0:
+        raise RuntimeError(f"device error flag {int(t['err'].item())}")
+
+    # timed region: K launches, an event pair around each one
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)  # let the sampler start before the timed region
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            H.call(wl, t, stream=stream)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed = t_begin.elapsed_time(t_end) / 1e3
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    max_elapsed = reduce_max(elapsed, torch, device)
+    value = aggregate(wl.tokens, world, max_elapsed, args.steps)
+
+    # end to end: the step's inputs from pinned host memory, the pool read back
+    e2e = run_e2e(wl, t, torch, device, stream, min(args.steps, args.e2e_steps), H)
+    e2e_value = reduce_max_time_value(e2e, wl.tokens, world, torch, device)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks = measured_peaks()
+    alg_bytes = wl.algorithmic_bytes()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = alg_bytes / avg_launch_s / 1e9
+    traffic = profile_traffic(args.workload)
+    cpu = cpu_baseline(args.workload) if world == 1 or rank == 0 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
+                   "tokens_per_step": wl.tokens, "algorithmic_bytes_per_step": alg_bytes,
+                   "patch_flops_per_step": wl.patch_flops(),
+                   "l2": "inputs larger than L2 (no flush needed)" if alg_bytes > 4 * 129e6
+                   else "inputs smaller than L2 (warm-cache steps)",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"] + " (burst copy)",
+                     "kernel": "kamera::reuse_kernel", "launch_ms_mean": statistics.mean(launch_ms),
+                     "launch_ms_min": min(launch_ms)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(wl, t, torch, device, stream, steps: int, H) -> dict:
+    """Host-buffer variant: pinned host inputs -> device, call, pool -> host, per step."""
+    names = [n for n in ("store", "store_off", "store_len", "patch", "patch_off", "patch_len", "items",
+                         "block_table") if n in t]
+    host_in = {n: t[n].cpu().pin_memory() for n in names}
+    outs = [n for n in ("pool_k", "pool_v") if t.get(n) is not None]
+    host_out = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in outs}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def step():
+        for n in names:
+            t[n].copy_(host_in[n], non_blocking=True)
+        H.call(wl, t, stream=stream)
+        for n in outs:
+            host_out[n].copy_(t[n], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(device)
+    b = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    b.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(device)
+    return {"elapsed": b.elapsed_time(e) / 1e3, "steps": steps, "h2d": h2d, "d2h": d2h}
+
+
+def reduce_max_time_value(e2e: dict, tokens: int, world: int, torch, device) -> float:
+    mx = reduce_max(e2e["elapsed"], torch, device)
+    return aggregate(tokens, world, mx, e2e["steps"])
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * kamera.h -- C ABI of the GB300 (sm_103a) Kamera KV-reuse library.
+ *
+ * The operation (source: "Kamera: Unified Position-Invariant Multimodal KV
+ * Cache for Training-Free Reuse", gist.science technical summary, §2
+ * "Methodology: the Kamera operator"):
+ *
+ *     KV^(B|A) = R(delta) . KV(B|empty) + U_m V_m^T
+ *
+ * A canonical, position-free chunk K/V (KV(B|empty)) is gathered from a chunk
+ * store, its keys are re-rotated by the RoPE phase shift delta of the new
+ * position (§2 "Relocation R(delta)": an exact algebraic operation, not a
+ * forward pass), a rank-m conditioning patch U_m V_m^T is added (§2 "Patch
+ * application"), and the rows are scattered into a paged KV pool through a
+ * block table.  §2 "Unified architecture support": MHA/GQA relocate the full
+ * keys and patch K and V; MLA relocates only the decoupled 64-dim k_rope,
+ * reuses c_KV byte for byte and patches both channels.  §3 names three window
+ * operations, all served here: reorder with one shared orbit patch and recall
+ * with a fresh patch (kamera_reuse_batched), sliding-window survival with
+ * R(delta) only (kamera_relocate, in place).
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller owns every buffer.  The library keeps no state
+ *     between calls and allocates no memory, host or device.
+ *   - Pointers marked "device" must be device (or managed) memory of the
+ *     current device; "host" pointers are read during the call only.
+ *   - Asynchrony: work is enqueued on `stream`; KAMERA_OK means "validated and
+ *     launched".  A launch failure returns KAMERA_ERR_CUDA.  Data-dependent
+ *     problems (an id or page out of range) never fault: the affected item or
+ *     row is skipped and a bit is OR-ed into *err_flag (device int32, may be
+ *     NULL), readable after the caller synchronises the stream.  The caller
+ *     clears *err_flag.
+ *   - Layout: bf16 everywhere.  D is the row width: num_kv_heads*head_dim for
+ *     MHA/GQA, latent_dim + rope_dim for MLA.  Chunk store, per chunk c at
+ *     element offset offset[c]: [layer][channel][len[c]][D] (channel 0 = K,
+ *     1 = V; MLA has only channel 0, the latent row).  Patch store, per patch
+ *     p at element offset offset[p]: for each layer and channel, U [len[p]][m]
+ *     then V [D][m] (row-major, so V is V_m with its rows along D).  Pool: K
+ *     and V each [layer][num_pages][page_size][D]; MLA uses only `k`.
+ *     Position pos of sequence s lives at page block_table[s][pos/page_size],
+ *     slot pos % page_size.
+ *   - Alignment: every base pointer 16-byte aligned; D a multiple of 64;
+ *     chunk offsets multiples of D; patch offsets multiples of m.
+ *   - Aliasing: the source rows and the destination slots of one call must
+ *     not overlap, except for the in-place modes, where each slot is read and
+ *     written by the same item.  Two items writing the same slot is a caller
+ *     error (the result is one of the two).
+ */
+#ifndef KAMERA_H_
+#define KAMERA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA stream type (cudaStream_t), declared without the CUDA headers. */
+typedef struct CUstream_st* kamera_stream_t;
+
+#define KAMERA_ABI_VERSION 1
+
+typedef enum {
+  KAMERA_OK = 0,
+  KAMERA_ERR_NULL = 1,          /* a required pointer is NULL */
+  KAMERA_ERR_INVALID_ARG = 2,   /* a size, count or enum is out of range */
+  KAMERA_ERR_UNSUPPORTED = 3,   /* valid but not served (e.g. D not a multiple of 64) */
+  KAMERA_ERR_ALIGNMENT = 4,     /* a base pointer is not 16-byte aligned */
+  KAMERA_ERR_CUDA = 5           /* a CUDA call failed; see kamera_last_error() */
+} kamera_status;
+
+typedef enum { KAMERA_MHA = 0, KAMERA_GQA = 1, KAMERA_MLA = 2 } kamera_family;
+
+/* RoPE pair convention: rotate-half pairs (i, i + d_r/2); interleaved (2i, 2i+1). */
+typedef enum { KAMERA_ROTATE_HALF = 0, KAMERA_INTERLEAVED = 1 } kamera_pairing;
+
+/* Where the patch is added: after the rotation (the literal equation
+ * R(delta)KV + UV^T) or in the canonical frame, R(delta)(KV + UV^T). */
+typedef enum { KAMERA_PATCH_AFTER_ROTATION = 0, KAMERA_PATCH_CANONICAL_FRAME = 1 } kamera_patch_frame;
+
+/* Bits OR-ed into *err_flag by the kernels.  The offending item (or row, for
+ * PAGE_OOB) is skipped; nothing traps. */
+#define KAMERA_EFLAG_CHUNK_OOB 1  /* chunk id out of range, or its offset misaligned / past the store */
+#define KAMERA_EFLAG_PAGE_OOB 2   /* sequence, block-table index or page id out of range */
+#define KAMERA_EFLAG_PATCH_OOB 4  /* patch id out of range, or its offset misaligned / past the store */
+#define KAMERA_EFLAG_LEN 8        /* n_tokens < 0, dst_pos < 0, or n_tokens != the chunk's / patch's length */
+#define KAMERA_EFLAG_TIMEOUT 16   /* an internal pipeline wait gave up; the call's output is incomplete */
+
+/* Model description (host struct, read during the call). */
+typedef struct {
+  int32_t family;         /* kamera_family */
+  int32_t num_layers;     /* >= 1 */
+  int32_t num_kv_heads;   /* MHA/GQA: >= 1 */
+  int32_t head_dim;       /* MHA/GQA: 64, 128, 192 or 256 */
+  int32_t rope_dim;       /* MHA/GQA: rotated dims per head, 0 = head_dim, a multiple of 64;
+                             MLA: k_rope width (64) */
+  int32_t latent_dim;     /* MLA: c_KV width (512), a multiple of 64 */
+  int32_t pairing;        /* kamera_pairing */
+  int32_t patch_frame;    /* kamera_patch_frame */
+  double rope_base;       /* theta_i = rope_base^(-2i/rope_dim) when inv_freq is NULL */
+  const double* inv_freq; /* host, [rope_dim/2] explicit theta_i table, or NULL */
+} kamera_model_desc;
+
+/* Canonical chunk store: KV(B|empty) of every chunk (device memory). */
+typedef struct {
+  const void* data;       /* device bf16 [n_elems] */
+  int64_t n_elems;        /* elements in data */
+  const int64_t* offset;  /* device [n_chunks]: element offset of chunk c (a multiple of D) */
+  const int32_t* len;     /* device [n_chunks]: tokens of chunk c */
+  int32_t n_chunks;
+} kamera_chunk_store;
+
+/* Patch store: the rank-m conditioning patches U_m V_m^T (device memory). */
+typedef struct {
+  const void* data;       /* device bf16 [n_elems] */
+  int64_t n_elems;
+  const int64_t* offset;  /* device [n_patches]: element offset of patch p (a multiple of rank) */
+  const int32_t* len;     /* device [n_patches]: tokens T_p the patch was formed for */
+  int32_t n_patches;
+  int32_t rank;           /* m: 8, 16, 32 or 64 (0 = no patches) */
+} kamera_patch_store;
+
+/* Paged KV pool and block table (device memory, written by the calls). */
+typedef struct {
+  void* k;                       /* device bf16 [num_layers][num_pages][page_size][D] */
+  void* v;                       /* same shape; NULL for MLA */
+  int64_t num_pages;
+  int32_t page_size;             /* a power of two, >= 8 */
+  const int32_t* block_table;    /* device int32 [n_seqs][max_pages_per_seq] */
+  int32_t n_seqs;
+  int32_t max_pages_per_seq;
+} kamera_paged_pool;
+
+/* One chunk reuse (device array of these; 32 bytes, naturally aligned). */
+typedef struct {
+  int32_t chunk_id;   /* index into the chunk store (ignored by the in-place calls) */
+  int32_t patch_id;   /* index into the patch store; -1 = no patch for this item */
+  int64_t delta;      /* RoPE phase shift in positions: new position - stored position */
+  int32_t seq;        /* block-table row */
+  int32_t n_tokens;   /* tokens; must equal the chunk's (and the patch's) length */
+  int64_t dst_pos;    /* first logical position in the sequence */
+} kamera_reuse_item;
+
+/*
+ * kamera_reuse_batched -- Kamera §2 reuse equation over a ragged batch.
+ * For each item, layer, channel and token t: read the canonical row
+ * (chunk_id, layer, channel, t), rotate the key row's RoPE pairs by
+ * delta*theta_i (MLA: only the k_rope columns), add row t of U V^T of
+ * (patch_id, layer, channel) if patch_id >= 0 and `patches` is not NULL, round
+ * to bf16 (nearest even), and store it at position dst_pos + t of sequence
+ * `seq`.  Serves reorder (§3, one orbit patch per chunk) and recall (§3, a
+ * fresh patch).  `patches` NULL means no patch for any item.
+ */
+kamera_status kamera_reuse_batched(const kamera_model_desc* model, const kamera_chunk_store* store,
+                                   const kamera_patch_store* patches, const kamera_reuse_item* items,
+                                   int32_t n_items, const kamera_paged_pool* pool, int32_t* err_flag,
+                                   kamera_stream_t stream);
+
+/*
+ * kamera_relocate -- Kamera §2 R(delta) alone.  With a chunk store it is
+ * kamera_reuse_batched without patches.  With `store` NULL it works in place
+ * on the pool (§3 sliding-window survival): the key rows at positions
+ * dst_pos .. dst_pos+n_tokens-1 of each item are re-rotated by delta and
+ * written back to the same slots; values (and MLA c_KV) are not touched.
+ */
+kamera_status kamera_relocate(const kamera_model_desc* model, const kamera_chunk_store* store,
+                              const kamera_reuse_item* items, int32_t n_items, const kamera_paged_pool* pool,
+                              int32_t* err_flag, kamera_stream_t stream);
+
+/*
+ * kamera_apply_patch -- Kamera §2 patch application alone, in place: for each
+ * item with patch_id >= 0, add row t of U V^T of (patch_id, layer, channel) to
+ * the pool row at position dst_pos + t, for K and V (MLA: the latent row), no
+ * rotation.
+ */
+kamera_status kamera_apply_patch(const kamera_model_desc* model, const kamera_patch_store* patches,
+                                 const kamera_reuse_item* items, int32_t n_items, const kamera_paged_pool* pool,
+                                 int32_t* err_flag, kamera_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* kamera_status_string(kamera_status status);
+
+/* Detail of the last failed call on this thread ("" if none; thread-local storage). */
+const char* kamera_last_error(void);
+
+/* KAMERA_ABI_VERSION of the loaded library. */
+int32_t kamera_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KAMERA_H_ */

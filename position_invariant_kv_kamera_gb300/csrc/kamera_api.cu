@@ -1,0 +1,418 @@
+// kamera_api.cu -- host side of the C ABI declared in include/kamera.h:
+// argument validation, the per-call work description (column blocks, RoPE
+// pair table, theta ladder), TMA tensor maps, and the launch of the fused
+// kernel.  No memory is allocated; the only per-call state is the kernel's
+// parameter block.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kamera.h"
+#include "kamera_kernel.cuh"
+
+namespace kamera {
+namespace {
+
+thread_local std::string g_last_error;
+
+kamera_status fail(kamera_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kamera_status fail(kamera_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+// ---- driver entry point for tensor-map encoding (no link-time libcuda dependency) ----
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+kamera_status encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                     const cuuint32_t* box, CUtensorMapSwizzle swz, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(KAMERA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KAMERA_ERR_CUDA, "tensor map for %s: cuTensorMapEncodeTiled error %d", what, (int)r);
+  return KAMERA_OK;
+}
+
+// ---- per-device launch facts ---------------------------------------------------------------
+struct DeviceFacts {
+  int sms = 0;
+  int smem_optin = 0;
+  bool attr_set[2] = {false, false};
+};
+constexpr int kMaxDevices = 64;
+DeviceFacts g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+kamera_status device_facts(int* dev_out, DeviceFacts** facts) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(KAMERA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceFacts& f = g_dev[dev];
+  if (f.sms == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(KAMERA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                  minor);
+    cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&f.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  }
+  *dev_out = dev;
+  *facts = &f;
+  return KAMERA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+enum Mode { MODE_REUSE = 0, MODE_RELOCATE_IN_PLACE = 1, MODE_PATCH_IN_PLACE = 2 };
+
+// Optional tuning overrides (for sweeps): KAMERA_BN, KAMERA_STAGES.
+int env_int(const char* name) {
+  const char* s = getenv(name);
+  return s ? atoi(s) : 0;
+}
+
+kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chunk_store* store,
+                     const kamera_patch_store* patches, const kamera_reuse_item* items, int32_t n_items,
+                     const kamera_paged_pool* pool, int32_t* err_flag, kamera_stream_t stream) {
+  g_last_error.clear();
+  if (!model) return fail(KAMERA_ERR_NULL, "model is NULL");
+  if (!pool) return fail(KAMERA_ERR_NULL, "pool is NULL");
+  if (n_items < 0) return fail(KAMERA_ERR_INVALID_ARG, "n_items = %d", n_items);
+  if (n_items > 0 && !items) return fail(KAMERA_ERR_NULL, "items is NULL");
+  if (mode == MODE_REUSE && !store) return fail(KAMERA_ERR_NULL, "chunk store is NULL");
+  if (mode == MODE_PATCH_IN_PLACE && !patches) return fail(KAMERA_ERR_NULL, "patch store is NULL");
+
+  // ---- model -----------------------------------------------------------------------------
+  const int fam = model->family;
+  if (fam != KAMERA_MHA && fam != KAMERA_GQA && fam != KAMERA_MLA)
+    return fail(KAMERA_ERR_INVALID_ARG, "family = %d", fam);
+  if (model->num_layers < 1) return fail(KAMERA_ERR_INVALID_ARG, "num_layers = %d", model->num_layers);
+  if (model->pairing != KAMERA_ROTATE_HALF && model->pairing != KAMERA_INTERLEAVED)
+    return fail(KAMERA_ERR_INVALID_ARG, "pairing = %d", model->pairing);
+  if (model->patch_frame != KAMERA_PATCH_AFTER_ROTATION && model->patch_frame != KAMERA_PATCH_CANONICAL_FRAME)
+    return fail(KAMERA_ERR_INVALID_ARG, "patch_frame = %d", model->patch_frame);
+  int D = 0, rope = 0, heads = 0, head_stride = 0, rope_col0 = 0, n_ch_layout = 2;
+  if (fam == KAMERA_MLA) {
+    if (model->latent_dim < 64 || model->latent_dim % 64 != 0)
+      return fail(KAMERA_ERR_UNSUPPORTED, "MLA latent_dim = %d (a positive multiple of 64 is served)",
+                  model->latent_dim);
+    rope = model->rope_dim;
+    if (rope < 64 || rope % 64 != 0) return fail(KAMERA_ERR_UNSUPPORTED, "MLA rope_dim = %d", rope);
+    D = model->latent_dim + rope;
+    heads = 1;
+    head_stride = rope;
+    rope_col0 = model->latent_dim;
+    n_ch_layout = 1;
+    if (pool->v) return fail(KAMERA_ERR_INVALID_ARG, "MLA pools hold latent rows in `k`; `v` must be NULL");
+  } else {
+    if (model->num_kv_heads < 1) return fail(KAMERA_ERR_INVALID_ARG, "num_kv_heads = %d", model->num_kv_heads);
+    const int hd = model->head_dim;
+    if (hd < 64 || hd > 256 || hd % 64 != 0)
+      return fail(KAMERA_ERR_UNSUPPORTED, "head_dim = %d (64, 128, 192 or 256 are served)", hd);
+    rope = model->rope_dim == 0 ? hd : model->rope_dim;
+    if (rope < 64 || rope > hd || rope % 64 != 0)
+      return fail(KAMERA_ERR_UNSUPPORTED, "rope_dim = %d (a multiple of 64 up to head_dim)", rope);
+    D = model->num_kv_heads * hd;
+    heads = model->num_kv_heads;
+    head_stride = hd;
+  }
+  if (D > 32 * MAX_GROUPS) return fail(KAMERA_ERR_UNSUPPORTED, "row width D = %d exceeds %d", D, 32 * MAX_GROUPS);
+  const int n_pairs = rope / 2;
+  if (n_pairs > MAX_PAIRS) return fail(KAMERA_ERR_UNSUPPORTED, "rope_dim = %d", rope);
+
+  // ---- pool --------------------------------------------------------------------------------
+  if (!pool->k) return fail(KAMERA_ERR_NULL, "pool->k is NULL");
+  const bool need_v = fam != KAMERA_MLA && mode != MODE_RELOCATE_IN_PLACE;
+  if (need_v && !pool->v) return fail(KAMERA_ERR_NULL, "pool->v is NULL");
+  if (!aligned16(pool->k) || (pool->v && !aligned16(pool->v)))
+    return fail(KAMERA_ERR_ALIGNMENT, "pool base pointers must be 16-byte aligned");
+  if (!pool->block_table) return fail(KAMERA_ERR_NULL, "pool->block_table is NULL");
+  if (pool->num_pages < 1 || pool->n_seqs < 1 || pool->max_pages_per_seq < 1)
+    return fail(KAMERA_ERR_INVALID_ARG, "pool: num_pages=%lld n_seqs=%d max_pages_per_seq=%d",
+                (long long)pool->num_pages, pool->n_seqs, pool->max_pages_per_seq);
+  if (!pow2(pool->page_size) || pool->page_size < 8 || pool->page_size > (1 << 20))
+    return fail(KAMERA_ERR_INVALID_ARG, "page_size = %d (a power of two >= 8)", pool->page_size);
+  const int64_t pool_rows = (int64_t)model->num_layers * pool->num_pages * pool->page_size;
+  if (pool_rows >= (int64_t(1) << 31))
+    return fail(KAMERA_ERR_UNSUPPORTED, "pool has %lld rows per channel (< 2^31 served)", (long long)pool_rows);
+  if (err_flag && (reinterpret_cast<uintptr_t>(err_flag) & 3u))
+    return fail(KAMERA_ERR_ALIGNMENT, "err_flag must be 4-byte aligned");
+
+  // ---- stores --------------------------------------------------------------------------------
+  const bool use_store = mode == MODE_REUSE;
+  int64_t store_rows = 0;
+  if (use_store) {
+    if (!store->data || !store->offset || !store->len)
+      return fail(KAMERA_ERR_NULL, "chunk store data/offset/len is NULL");
+    if (!aligned16(store->data)) return fail(KAMERA_ERR_ALIGNMENT, "chunk store data must be 16-byte aligned");
+    if (store->n_chunks < 0 || store->n_elems < 0) return fail(KAMERA_ERR_INVALID_ARG, "chunk store sizes");
+    store_rows = store->n_elems / D;
+    if (store_rows >= (int64_t(1) << 31))
+      return fail(KAMERA_ERR_UNSUPPORTED, "chunk store has %lld rows (< 2^31 served)", (long long)store_rows);
+  }
+  const bool use_patch = mode != MODE_RELOCATE_IN_PLACE && patches && patches->rank > 0;
+  int rank = 0;
+  int64_t patch_rows = 0;
+  if (use_patch) {
+    rank = patches->rank;
+    if (rank != 8 && rank != 16 && rank != 32 && rank != 64)
+      return fail(KAMERA_ERR_INVALID_ARG, "rank = %d (8, 16, 32 or 64)", rank);
+    if (!patches->data || !patches->offset || !patches->len)
+      return fail(KAMERA_ERR_NULL, "patch store data/offset/len is NULL");
+    if (!aligned16(patches->data)) return fail(KAMERA_ERR_ALIGNMENT, "patch store data must be 16-byte aligned");
+    if (patches->n_patches < 0 || patches->n_elems < 0) return fail(KAMERA_ERR_INVALID_ARG, "patch store sizes");
+    patch_rows = patches->n_elems / rank;
+    if (patch_rows >= (int64_t(1) << 31))
+      return fail(KAMERA_ERR_UNSUPPORTED, "patch store has %lld rows (< 2^31 served)", (long long)patch_rows);
+  } else if (patches && patches->rank < 0) {
+    return fail(KAMERA_ERR_INVALID_ARG, "rank = %d", patches->rank);
+  }
+  if (mode == MODE_PATCH_IN_PLACE && !use_patch) return KAMERA_OK;  // rank 0: nothing to add
+  if (n_items == 0) return KAMERA_OK;
+
+  // ---- theta ladder and the key row's group table --------------------------------------------
+  Params p;
+  memset(&p, 0, sizeof p);
+  for (int i = 0; i < n_pairs; ++i) {
+    if (model->inv_freq) {
+      p.theta[i] = model->inv_freq[i];
+    } else {
+      if (!(model->rope_base > 0.0) || !std::isfinite(model->rope_base))
+        return fail(KAMERA_ERR_INVALID_ARG, "rope_base = %g", model->rope_base);
+      p.theta[i] = std::pow(model->rope_base, -2.0 * (double)i / (double)rope);
+    }
+    if (!std::isfinite(p.theta[i])) return fail(KAMERA_ERR_INVALID_ARG, "theta[%d] is not finite", i);
+  }
+  const int n_groups = D / 32;
+  for (int h = 0; h < heads; ++h) {
+    const int a = rope_col0 + h * head_stride;  // first rotated column of this region
+    for (int c = 0; c < rope; c += 32) {
+      const int g = (a + c) / 32;
+      if (model->pairing == KAMERA_INTERLEAVED) {
+        p.group_kind[g] = GK_INTERLEAVED;
+        p.pair_base[g] = (uint8_t)(c / 2);
+      } else if (c < rope / 2) {
+        p.group_kind[g] = (int8_t)(rope / 2 / 32);
+        p.pair_base[g] = (uint8_t)c;
+      } else {
+        p.group_kind[g] = GK_SECOND;
+      }
+    }
+  }
+
+  // ---- tile shape: BN columns per tile, smem stages ---------------------------------------------
+  int dev = 0;
+  DeviceFacts* facts = nullptr;
+  if (kamera_status st = device_facts(&dev, &facts)) return st;
+  const int kg_alloc = use_patch ? (rank / 8 < 2 ? 2 : rank / 8) : 0;
+  const int bn_env = env_int("KAMERA_BN"), st_env = env_int("KAMERA_STAGES");
+  int BN = 0, stages = 0;
+  uint32_t stage_bytes = 0;
+  const int cands[4] = {256, 192, 128, 64};
+  for (int ci = 0; ci < 4 && BN == 0; ++ci) {
+    const int bn = cands[ci];
+    if (bn_env && bn != bn_env) continue;
+    if (D % bn != 0) continue;
+    bool whole = true;  // every rotate-half pair inside one column block
+    for (int g = 0; g < n_groups; ++g)
+      if (p.group_kind[g] > 0 && (g * 32) / bn != ((g + p.group_kind[g]) * 32) / bn) whole = false;
+    if (!whole) continue;
+    const uint32_t sb = (uint32_t)bn * 256u + (use_patch ? (uint32_t)(BM + bn) * kg_alloc * 16u : 0u);
+    int s = st_env ? st_env : 4;
+    while (s >= 2 && (uint64_t)s * sb + smem_extra_bytes(s) > (uint64_t)facts->smem_optin) --s;
+    if (s < 2) continue;
+    BN = bn;
+    stages = s;
+    stage_bytes = sb;
+  }
+  if (BN == 0) return fail(KAMERA_ERR_UNSUPPORTED, "no tile shape fits D = %d, rank %d", D, rank);
+  const uint32_t smem = (uint32_t)stages * stage_bytes + smem_extra_bytes(stages);
+
+  // ---- parameters ------------------------------------------------------------------------------------
+  p.items = items;
+  p.n_items = n_items;
+  p.src_pool = use_store ? 0 : 1;
+  p.has_patches = use_patch ? 1 : 0;
+  p.need_patch = mode == MODE_PATCH_IN_PLACE ? 1 : 0;
+  p.rank = rank;
+  p.ksteps = (rank + 15) / 16;
+  p.kg_alloc = kg_alloc;
+  p.pool[0] = static_cast<uint16_t*>(pool->k);
+  p.pool[1] = static_cast<uint16_t*>(pool->v);
+  p.num_pages = pool->num_pages;
+  p.page_size = pool->page_size;
+  p.page_shift = __builtin_ctz((unsigned)pool->page_size);
+  p.block_table = pool->block_table;
+  p.n_seqs = pool->n_seqs;
+  p.max_pages = pool->max_pages_per_seq;
+  p.num_layers = model->num_layers;
+  p.D = D;
+  p.n_ch_layout = n_ch_layout;
+  p.n_ch_work = mode == MODE_RELOCATE_IN_PLACE ? 1 : n_ch_layout;
+  p.BN = BN;
+  p.stages = stages;
+  p.seg_rows = pool->page_size < BM ? pool->page_size : BM;
+  p.rotate = mode == MODE_PATCH_IN_PLACE ? 0 : 1;
+  p.frame = model->patch_frame;
+  p.n_pairs = n_pairs;
+  p.stage_bytes = stage_bytes;
+  p.canon_bytes = (uint32_t)BN * 256u;
+  p.u_bytes = use_patch ? (uint32_t)BM * kg_alloc * 16u : 0u;
+  p.v_bytes = use_patch ? (uint32_t)BN * kg_alloc * 16u : 0u;
+  uint32_t tc = 32;
+  while (tc < 2u * (uint32_t)BN) tc <<= 1;
+  p.tmem_cols = tc;
+  p.err_flag = err_flag;
+  if (mode == MODE_RELOCATE_IN_PLACE) {
+    // only the column blocks that hold rotated groups change
+    int lo = D / BN, hi = -1;
+    for (int g = 0; g < n_groups; ++g)
+      if (p.group_kind[g] != GK_PLAIN) {
+        lo = (g * 32) / BN < lo ? (g * 32) / BN : lo;
+        hi = (g * 32) / BN > hi ? (g * 32) / BN : hi;
+      }
+    p.cb_first = lo;
+    p.n_cb = hi - lo + 1;
+  } else {
+    p.cb_first = 0;
+    p.n_cb = D / BN;
+  }
+
+  // ---- tensor maps --------------------------------------------------------------------------------------
+  if (use_store) {
+    p.store_off = store->offset;
+    p.store_len = store->len;
+    p.store_elems = store->n_elems;
+    p.n_chunks = store->n_chunks;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)(store_rows > 0 ? store_rows : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BOX_COLS, (cuuint32_t)BM};
+    if (kamera_status st = encode(&p.src_map, store->data, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  "chunk store"))
+      return st;
+  } else {
+    for (int ch = 0; ch < p.n_ch_work; ++ch) {
+      const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)pool_rows};
+      const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+      const cuuint32_t box[2] = {(cuuint32_t)BOX_COLS, (cuuint32_t)p.seg_rows};
+      if (kamera_status st = encode(&p.pool_map[ch], ch == 0 ? pool->k : pool->v, 2, dims, strides, box,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, "pool"))
+        return st;
+    }
+  }
+  if (use_patch) {
+    p.patch_off = patches->offset;
+    p.patch_len = patches->len;
+    p.patch_elems = patches->n_elems;
+    p.n_patches = patches->n_patches;
+    const cuuint64_t dims[3] = {8, (cuuint64_t)(patch_rows > 0 ? patch_rows : 1), (cuuint64_t)(rank / 8)};
+    const cuuint64_t strides[2] = {(cuuint64_t)rank * 2, 16};
+    const cuuint32_t ubox[3] = {8, (cuuint32_t)BM, (cuuint32_t)(rank / 8)};
+    const cuuint32_t vbox[3] = {8, (cuuint32_t)BN, (cuuint32_t)(rank / 8)};
+    if (kamera_status st = encode(&p.u_map, patches->data, 3, dims, strides, ubox, CU_TENSOR_MAP_SWIZZLE_NONE, "U"))
+      return st;
+    if (kamera_status st = encode(&p.v_map, patches->data, 3, dims, strides, vbox, CU_TENSOR_MAP_SWIZZLE_NONE, "V"))
+      return st;
+  }
+
+  // ---- launch ----------------------------------------------------------------------------------------------
+  const void* fn = use_patch ? reinterpret_cast<const void*>(&reuse_kernel<true>)
+                             : reinterpret_cast<const void*>(&reuse_kernel<false>);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    bool& set = facts->attr_set[use_patch ? 1 : 0];
+    if (!set) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, facts->smem_optin);
+      if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      set = true;
+    }
+  }
+  const dim3 grid((unsigned)facts->sms), block(NUM_THREADS);
+  if (use_patch)
+    reuse_kernel<true><<<grid, block, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  else
+    reuse_kernel<false><<<grid, block, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return KAMERA_OK;
+}
+
+}  // namespace
+}  // namespace kamera
+
+extern "C" {
+
+kamera_status kamera_reuse_batched(const kamera_model_desc* model, const kamera_chunk_store* store,
+                                   const kamera_patch_store* patches, const kamera_reuse_item* items,
+                                   int32_t n_items, const kamera_paged_pool* pool, int32_t* err_flag,
+                                   kamera_stream_t stream) {
+  return kamera::launch(kamera::MODE_REUSE, model, store, patches, items, n_items, pool, err_flag, stream);
+}
+
+kamera_status kamera_relocate(const kamera_model_desc* model, const kamera_chunk_store* store,
+                              const kamera_reuse_item* items, int32_t n_items, const kamera_paged_pool* pool,
+                              int32_t* err_flag, kamera_stream_t stream) {
+  return kamera::launch(store ? kamera::MODE_REUSE : kamera::MODE_RELOCATE_IN_PLACE, model, store, nullptr, items,
+                        n_items, pool, err_flag, stream);
+}
+
+kamera_status kamera_apply_patch(const kamera_model_desc* model, const kamera_patch_store* patches,
+                                 const kamera_reuse_item* items, int32_t n_items, const kamera_paged_pool* pool,
+                                 int32_t* err_flag, kamera_stream_t stream) {
+  return kamera::launch(kamera::MODE_PATCH_IN_PLACE, model, nullptr, patches, items, n_items, pool, err_flag,
+                        stream);
+}
+
+const char* kamera_status_string(kamera_status status) {
+  switch (status) {
+    case KAMERA_OK: return "KAMERA_OK";
+    case KAMERA_ERR_NULL: return "KAMERA_ERR_NULL";
+    case KAMERA_ERR_INVALID_ARG: return "KAMERA_ERR_INVALID_ARG";
+    case KAMERA_ERR_UNSUPPORTED: return "KAMERA_ERR_UNSUPPORTED";
+    case KAMERA_ERR_ALIGNMENT: return "KAMERA_ERR_ALIGNMENT";
+    case KAMERA_ERR_CUDA: return "KAMERA_ERR_CUDA";
+  }
+  return "KAMERA_ERR_UNKNOWN";
+}
+
+const char* kamera_last_error(void) { return kamera::g_last_error.c_str(); }
+
+int32_t kamera_abi_version(void) { return KAMERA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,647 @@
+// kamera_kernel.cuh -- the fused Kamera reuse kernel for sm_103a.
+//
+// One persistent, warp-specialised kernel computes, for every reuse item,
+// layer, channel and token (Kamera: Unified Position-Invariant Multimodal KV
+// Cache for Training-Free Reuse, §2 reuse equation):
+//
+//     out = R(delta) . KV(B|empty) + U_m V_m^T        -> bf16 -> paged pool slot
+//
+// Work unit ("tile"): 128 destination positions (aligned to 128 in position
+// space) x BN columns of one (item, layer, channel).  Per CTA (192 threads):
+//   warp 0     TMA producer: canonical tile (64-column boxes, 128B swizzle),
+//              and for patched items the U tile [128 x m] and V tile [BN x m]
+//              (no-swizzle K-major core-matrix layout) into a ring of stages.
+//   warp 1     owns TMEM; one lane issues tcgen05.mma M=128, N=BN, K=16 steps:
+//              P = U . V^T into an fp32 TMEM accumulator (two buffers).
+//   warps 2-5  epilogue, one thread per tile row (= TMEM lane): tcgen05.ld the
+//              patch row, rotate the RoPE pairs of the key row by delta*theta_i
+//              (fp64 angle reduction, fp32 sincos, fp32 math), add, round to
+//              bf16 in place in shared memory; then the 128 threads copy the
+//              tile out row by row with coalesced 16-byte stores to the pool
+//              slots given by the block table.
+// Every wait on an mbarrier is bounded (about 2 s): on expiry the kernel sets
+// KAMERA_EFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kamera.h"
+#include "ptx.cuh"
+
+namespace kamera {
+
+constexpr int BM = 128;             // tile rows = TMEM lanes = M of the MMA
+constexpr int NUM_THREADS = 192;    // 6 warps
+constexpr int EPI_THREADS = 128;    // warps 2..5
+constexpr int MAX_GROUPS = 64;      // 32-column groups per row (D <= 2048)
+constexpr int MAX_PAIRS = 128;      // rope_dim / 2
+constexpr int BOX_COLS = 64;        // 64 bf16 = one 128-byte swizzle row
+constexpr uint32_t BOX_BYTES = BM * 128;  // one 64-column box of 128 rows
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+// group kinds (per 32-column group of a key row); a positive value is a
+// rotate-half first half whose partner group is that many groups to the right
+constexpr int8_t GK_PLAIN = 0;
+constexpr int8_t GK_SECOND = -1;
+constexpr int8_t GK_INTERLEAVED = -2;
+
+struct Params {
+  CUtensorMap src_map;      // chunk store as rows [rows][D]: box 64 x 128, 128B swizzle
+  CUtensorMap pool_map[2];  // pool K / V as rows [L*pages*P][D]: box 64 x S (S = min(P,128))
+  CUtensorMap u_map;        // patch store as (8, rows, m/8): box (8, 128, kg)
+  CUtensorMap v_map;        // patch store as (8, rows, m/8): box (8, BN, kg)
+  const kamera_reuse_item* items;
+  int32_t n_items;
+  int32_t src_pool;  // 0: gather from the chunk store, 1: in place from the pool
+  const int64_t* store_off;
+  const int32_t* store_len;
+  int64_t store_elems;
+  int32_t n_chunks;
+  int32_t has_patches;
+  const int64_t* patch_off;
+  const int32_t* patch_len;
+  int64_t patch_elems;
+  int32_t n_patches;
+  int32_t rank;
+  int32_t ksteps;    // ceil(rank / 16)
+  int32_t kg_alloc;  // 8-element K groups held in smem per operand row (>= 2)
+  int32_t need_patch;  // items without a patch have no work (patch-only mode)
+  uint16_t* pool[2];
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t page_shift;
+  const int32_t* block_table;
+  int32_t n_seqs;
+  int32_t max_pages;
+  int32_t num_layers;
+  int32_t D;
+  int32_t n_ch_layout;  // channels in the store / patch layout (2, MLA 1)
+  int32_t n_ch_work;    // channels processed (in-place relocate: keys only)
+  int32_t BN;
+  int32_t n_cb;      // column blocks processed per row
+  int32_t cb_first;  // first processed column block
+  int32_t stages;
+  int32_t seg_rows;  // rows per pool page segment in a tile (min(P, 128))
+  int32_t rotate;    // rotate channel 0
+  int32_t frame;     // kamera_patch_frame
+  int32_t n_pairs;
+  uint32_t stage_bytes, canon_bytes, u_bytes, v_bytes, tmem_cols;
+  int32_t* err_flag;
+  int8_t group_kind[MAX_GROUPS];
+  uint8_t pair_base[MAX_GROUPS];
+  double theta[MAX_PAIRS];
+};
+
+// ---- work decomposition ---------------------------------------------------------------
+
+struct Walker {
+  int32_t item;
+  int64_t base, count;
+  int64_t dst_pos, delta;
+  int32_t T, seq, chunk, patch, n_tb;
+};
+
+// Tiles of item i (0 if it is skipped); fills the walker's item fields.
+// Error bits are collected in *err (caller decides whether to report them).
+__device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker& w, int32_t& err) {
+  const kamera_reuse_item it = p.items[i];
+  w.T = it.n_tokens;
+  w.seq = it.seq;
+  w.chunk = it.chunk_id;
+  w.patch = -1;
+  w.dst_pos = it.dst_pos;
+  w.delta = it.delta;
+  w.n_tb = 0;
+  if (it.n_tokens == 0) return 0;
+  if (it.n_tokens < 0 || it.dst_pos < 0) { err |= KAMERA_EFLAG_LEN; return 0; }
+  if (it.seq < 0 || it.seq >= p.n_seqs) { err |= KAMERA_EFLAG_PAGE_OOB; return 0; }
+  const int64_t T = it.n_tokens;
+  if (!p.src_pool) {
+    if (it.chunk_id < 0 || it.chunk_id >= p.n_chunks) { err |= KAMERA_EFLAG_CHUNK_OOB; return 0; }
+    if (p.store_len[it.chunk_id] != it.n_tokens) { err |= KAMERA_EFLAG_LEN; return 0; }
+    const int64_t off = p.store_off[it.chunk_id];
+    if (off < 0 || off % p.D != 0 || off + (int64_t)p.num_layers * p.n_ch_layout * T * p.D > p.store_elems) {
+      err |= KAMERA_EFLAG_CHUNK_OOB;
+      return 0;
+    }
+  }
+  if (p.has_patches && it.patch_id >= 0) {
+    if (it.patch_id >= p.n_patches) { err |= KAMERA_EFLAG_PATCH_OOB; return 0; }
+    if (p.patch_len[it.patch_id] != it.n_tokens) { err |= KAMERA_EFLAG_LEN; return 0; }
+    const int64_t off = p.patch_off[it.patch_id];
+    if (off < 0 || off % p.rank != 0 ||
+        off + (int64_t)p.num_layers * p.n_ch_layout * (T + p.D) * p.rank > p.patch_elems) {
+      err |= KAMERA_EFLAG_PATCH_OOB;
+      return 0;
+    }
+    w.patch = it.patch_id;
+  }
+  if (p.need_patch && w.patch < 0) return 0;
+  w.n_tb = (int32_t)((it.dst_pos + T + BM - 1) / BM - it.dst_pos / BM);
+  return (int64_t)p.num_layers * p.n_ch_work * w.n_tb * p.n_cb;
+}
+
+__device__ __forceinline__ void walker_init(Walker& w) {
+  w.item = -1;
+  w.base = 0;
+  w.count = 0;
+}
+
+// Advance (monotonically) to the item holding global tile g.
+__device__ __forceinline__ void walk_to(const Params& p, Walker& w, int64_t g) {
+  while (g >= w.base + w.count) {
+    w.base += w.count;
+    ++w.item;
+    int32_t e = 0;
+    w.count = item_tiles(p, w.item, w, e);
+  }
+}
+
+struct Tile {
+  int32_t layer, ch, cb;
+  int64_t pos0;  // destination position of tile row 0
+};
+
+__device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t g) {
+  int64_t local = g - w.base;
+  Tile t;
+  t.cb = p.cb_first + (int32_t)(local % p.n_cb);
+  local /= p.n_cb;
+  const int32_t tb = (int32_t)(local % w.n_tb);
+  local /= w.n_tb;
+  t.ch = (int32_t)(local % p.n_ch_work);
+  t.layer = (int32_t)(local / p.n_ch_work);
+  t.pos0 = (w.dst_pos / BM) * BM + (int64_t)tb * BM;
+  return t;
+}
+
+// ---- shared memory ---------------------------------------------------------------------
+
+struct SmemMisc {
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int64_t total_tiles;
+};
+
+struct Smem {
+  uint8_t* stages;   // stage s at stages + s * stage_bytes
+  uint64_t* full;    // [stages]
+  uint64_t* empty;   // [stages]
+  uint64_t* tfull;   // [2]
+  uint64_t* tempty;  // [2]
+  uint64_t* drain;   // [1]
+  SmemMisc* misc;
+  float2* cs;        // [MAX_PAIRS] (cos, sin) of the current item
+  int64_t* row_dst;  // [2][BM] destination row in the pool, -1 = not stored
+};
+
+__device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
+  const uint32_t a = smem_addr(raw);
+  uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
+  Smem s;
+  s.stages = base;
+  uint8_t* q = base + (size_t)p.stages * p.stage_bytes;
+  s.full = reinterpret_cast<uint64_t*>(q);
+  s.empty = s.full + p.stages;
+  s.tfull = s.empty + p.stages;
+  s.tempty = s.tfull + 2;
+  s.drain = s.tempty + 2;
+  s.misc = reinterpret_cast<SmemMisc*>(s.drain + 1);
+  s.cs = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(s.misc) + 32);
+  s.row_dst = reinterpret_cast<int64_t*>(s.cs + MAX_PAIRS);
+  return s;
+}
+
+__host__ __device__ constexpr uint32_t smem_extra_bytes(int stages) {
+  return 1024 /*alignment slack*/ + 8u * (2u * stages + 5u) + 32u + 8u * MAX_PAIRS + 8u * 2u * BM;
+}
+
+// Bounded wait.  Returns false on abort (another role gave up) or on expiry
+// (then it raises the abort flag and the timeout error bit).
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, SmemMisc* misc, int32_t* err_flag,
+                                             bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *reinterpret_cast<volatile int32_t*>(&misc->abort_flag)) return false;
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+      *reinterpret_cast<volatile int32_t*>(&misc->abort_flag) = 1;
+      if (err_flag) atomicOr(err_flag, KAMERA_EFLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool aborted(SmemMisc* misc) {
+  return *reinterpret_cast<volatile int32_t*>(&misc->abort_flag) != 0;
+}
+
+// ---- epilogue helpers ----------------------------------------------------------------------
+
+// byte offset of 16-byte chunk (row r, tile column c, c % 8 == 0) in a 128B-swizzled tile
+__device__ __forceinline__ uint32_t canon_off(int r, int c) {
+  return (uint32_t)(c >> 6) * BOX_BYTES + (uint32_t)r * 128u + ((((uint32_t)c >> 3) & 7u) ^ ((uint32_t)r & 7u)) * 16u;
+}
+
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16);
+  f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16);
+  f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// cos/sin of delta*theta_i: the angle is formed and reduced modulo 2*pi in fp64
+// (two-constant Cody-Waite reduction), then sin/cos are taken in fp32.
+__device__ __forceinline__ float2 phase_cs(int64_t delta, double theta) {
+  const double kTwoPiHi = 6.283185307179586;        // fp64 nearest to 2*pi
+  const double kTwoPiLo = 2.4492935982947064e-16;   // 2*pi - kTwoPiHi
+  const double kInvTwoPi = 0.15915494309189535;     // 1 / (2*pi)
+  const double phi = (double)delta * theta;
+  const double k = rint(phi * kInvTwoPi);
+  double r = fma(-k, kTwoPiHi, phi);
+  r = fma(-k, kTwoPiLo, r);
+  float s, c;
+  sincosf((float)r, &s, &c);
+  return make_float2(c, s);
+}
+
+// One 32-column group without rotation: out = x + P (patched) -- written in place.
+__device__ __forceinline__ void epi_plain(uint32_t canon, int r, int c0, bool patched, uint32_t taddr) {
+  if (!patched) return;  // bit copy: the tile already holds the output
+  uint32_t acc[32];
+  tmem_ld32(taddr + (uint32_t)c0, acc);
+  tmem_ld_wait();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t a = canon + canon_off(r, c0 + 8 * k);
+    float x[8];
+    unpack8(lds128(a), x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] += __uint_as_float(acc[8 * k + e]);
+    sts128(a, pack8(x));
+  }
+}
+
+// Two 32-column groups forming rotate-half pairs (cA + e, cB + e), pair index pb + e.
+__device__ __forceinline__ void epi_rotate_half(uint32_t canon, int r, int cA, int cB, int pb, bool patched,
+                                                uint32_t taddr, const float2* cs, int frame) {
+  uint32_t accA[32], accB[32];
+  if (patched) {
+    tmem_ld32(taddr + (uint32_t)cA, accA);
+    tmem_ld32(taddr + (uint32_t)cB, accB);
+    tmem_ld_wait();
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t aA = canon + canon_off(r, cA + 8 * k);
+    const uint32_t aB = canon + canon_off(r, cB + 8 * k);
+    float xa[8], xb[8];
+    unpack8(lds128(aA), xa);
+    unpack8(lds128(aB), xb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 t = cs[pb + 8 * k + e];
+      float a = xa[e], b = xb[e];
+      if (patched && frame == KAMERA_PATCH_CANONICAL_FRAME) {
+        a += __uint_as_float(accA[8 * k + e]);
+        b += __uint_as_float(accB[8 * k + e]);
+      }
+      float ra = fmaf(a, t.x, -b * t.y);
+      float rb = fmaf(b, t.x, a * t.y);
+      if (patched && frame != KAMERA_PATCH_CANONICAL_FRAME) {
+        ra += __uint_as_float(accA[8 * k + e]);
+        rb += __uint_as_float(accB[8 * k + e]);
+      }
+      xa[e] = ra;
+      xb[e] = rb;
+    }
+    sts128(aA, pack8(xa));
+    sts128(aB, pack8(xb));
+  }
+}
+
+// One 32-column group of interleaved pairs (2e, 2e+1), pair index pb + e.
+__device__ __forceinline__ void epi_interleaved(uint32_t canon, int r, int c0, int pb, bool patched, uint32_t taddr,
+                                                const float2* cs, int frame) {
+  uint32_t acc[32];
+  if (patched) {
+    tmem_ld32(taddr + (uint32_t)c0, acc);
+    tmem_ld_wait();
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t a0 = canon + canon_off(r, c0 + 8 * k);
+    float x[8];
+    unpack8(lds128(a0), x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 t = cs[pb + 4 * k + e];
+      float a = x[2 * e], b = x[2 * e + 1];
+      if (patched && frame == KAMERA_PATCH_CANONICAL_FRAME) {
+        a += __uint_as_float(acc[8 * k + 2 * e]);
+        b += __uint_as_float(acc[8 * k + 2 * e + 1]);
+      }
+      float ra = fmaf(a, t.x, -b * t.y);
+      float rb = fmaf(b, t.x, a * t.y);
+      if (patched && frame != KAMERA_PATCH_CANONICAL_FRAME) {
+        ra += __uint_as_float(acc[8 * k + 2 * e]);
+        rb += __uint_as_float(acc[8 * k + 2 * e + 1]);
+      }
+      x[2 * e] = ra;
+      x[2 * e + 1] = rb;
+    }
+    sts128(a0, pack8(x));
+  }
+}
+
+// ---- the kernel ----------------------------------------------------------------------------------
+
+template <bool kPatch>
+__global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem sm = carve_smem(smem_raw, p);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- set-up -------------------------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], 4);
+    }
+    mbar_init(sm.drain, 1);
+    sm.misc->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (kPatch) {
+    // K groups the MMA reads but TMA never writes (rank 8 pads K to 16) stay zero
+    const int kg_load = p.rank / 8;
+    for (int s = 0; s < p.stages; ++s) {
+      uint8_t* st = sm.stages + (size_t)s * p.stage_bytes + p.canon_bytes;
+      const uint32_t u_pad = (uint32_t)(p.kg_alloc - kg_load) * BM * 16u;
+      const uint32_t v_pad = (uint32_t)(p.kg_alloc - kg_load) * p.BN * 16u;
+      uint8_t* upad = st + (uint32_t)kg_load * BM * 16u;
+      uint8_t* vpad = st + p.u_bytes + (uint32_t)kg_load * p.BN * 16u;
+      for (uint32_t i = threadIdx.x * 16u; i < u_pad; i += NUM_THREADS * 16u)
+        *reinterpret_cast<uint4*>(upad + i) = make_uint4(0, 0, 0, 0);
+      for (uint32_t i = threadIdx.x * 16u; i < v_pad; i += NUM_THREADS * 16u)
+        *reinterpret_cast<uint4*>(vpad + i) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    if (warp == 1) {
+      tmem_alloc(&sm.misc->tmem_base, p.tmem_cols);
+      tmem_relinquish();
+    }
+  }
+  if (warp == 0) {
+    // total tile count: lanes split the items; only CTA 0 reports item-level errors
+    int64_t n = 0;
+    int32_t err = 0;
+    Walker w;
+    for (int32_t i = lane; i < p.n_items; i += 32) n += item_tiles(p, i, w, err);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+      err |= __shfl_xor_sync(0xFFFFFFFFu, err, o);
+    }
+    if (lane == 0) {
+      sm.misc->total_tiles = n;
+      if (blockIdx.x == 0 && err && p.err_flag) atomicOr(p.err_flag, err);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const int64_t total = sm.misc->total_tiles;
+  const uint32_t tmem_base = kPatch ? sm.misc->tmem_base : 0u;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(p.src_pool ? &p.pool_map[0] : &p.src_map);
+      if (kPatch) {
+        tma_prefetch_desc(&p.u_map);
+        tma_prefetch_desc(&p.v_map);
+      }
+      Walker w;
+      walker_init(w);
+      uint32_t it = 0;
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+        walk_to(p, w, g);
+        const Tile t = decode(p, w, g);
+        const int s = (int)(it % (uint32_t)p.stages);
+        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) break;
+        uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+        const int col0 = t.cb * p.BN;
+        const int nbox = p.BN / BOX_COLS;
+        const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
+        // decide the loads first so the transaction byte count is exact
+        uint32_t bytes = 0;
+        int32_t seg_y[BM / 8];
+        int nseg = 0;
+        if (!p.src_pool) {
+          bytes += (uint32_t)nbox * BOX_BYTES;
+        } else {
+          nseg = BM / p.seg_rows;
+          for (int sg = 0; sg < nseg; ++sg) {
+            seg_y[sg] = -1;
+            const int64_t ps = t.pos0 + (int64_t)sg * p.seg_rows;
+            if (ps + p.seg_rows <= w.dst_pos || ps >= w.dst_pos + w.T) continue;
+            const int64_t blk = ps >> p.page_shift;
+            if (blk >= p.max_pages) continue;
+            const int32_t page = p.block_table[(int64_t)w.seq * p.max_pages + blk];
+            if (page < 0 || page >= p.num_pages) continue;
+            seg_y[sg] = (int32_t)(((int64_t)t.layer * p.num_pages + page) * p.page_size + (ps & (p.page_size - 1)));
+            bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
+          }
+        }
+        const bool patched = kPatch && w.patch >= 0;
+        if (patched) bytes += (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u;
+        mbar_arrive_expect_tx(&sm.full[s], bytes);
+        if (!p.src_pool) {
+          const int64_t y = w.chunk >= 0 ? p.store_off[w.chunk] / p.D : 0;
+          const int32_t row = (int32_t)(y + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
+          for (int b = 0; b < nbox; ++b) tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, row);
+        } else {
+          for (int sg = 0; sg < nseg; ++sg) {
+            if (seg_y[sg] < 0) continue;
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
+                          col0 + b * BOX_COLS, seg_y[sg]);
+          }
+        }
+        if (patched) {
+          const int64_t prow = p.patch_off[w.patch] / p.rank +
+                               ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
+          tma_load_3d(st + p.canon_bytes, &p.u_map, &sm.full[s], 0, (int32_t)(prow + t0), 0);
+          tma_load_3d(st + p.canon_bytes + p.u_bytes, &p.v_map, &sm.full[s], 0, (int32_t)(prow + w.T + col0), 0);
+        }
+      }
+      // drain: every stage's last fill must have landed before the CTA exits
+      const uint32_t S = (uint32_t)p.stages;
+      for (uint32_t s = 0; s < S && s < it; ++s) {
+        const uint32_t fills = (it - s + S - 1) / S;
+        wait_bounded(&sm.full[s], (fills - 1) & 1u, sm.misc, p.err_flag, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (kPatch && lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16_f32(BM, (uint32_t)p.BN);
+      const uint32_t lbo_u = BM * 16u, lbo_v = (uint32_t)p.BN * 16u;
+      Walker w;
+      walker_init(w);
+      uint32_t it = 0, pt = 0;
+      bool issued = false;
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+        walk_to(p, w, g);
+        if (w.patch < 0) continue;
+        const int s = (int)(it % (uint32_t)p.stages);
+        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
+        if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) break;
+        if (!wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t st = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
+        const uint32_t ua = st + p.canon_bytes, va = st + p.canon_bytes + p.u_bytes;
+        for (int k = 0; k < p.ksteps; ++k) {
+          const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
+          const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+          umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&sm.tfull[buf]);
+        issued = true;
+        ++pt;
+      }
+      if (issued) {
+        umma_commit(sm.drain);
+        wait_bounded(sm.drain, 0, sm.misc, p.err_flag, false);
+      }
+    }
+  } else {
+    // ================= epilogue (warps 2..5) =================
+    const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;         // tile row owned in the compute phase
+    const int et = threadIdx.x - 64;     // 0..127 in the copy-out phase
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    const int cpr = p.BN / 8;            // 16-byte chunks per tile row
+    const int drow = EPI_THREADS / cpr, dcol = EPI_THREADS % cpr;
+    Walker w;
+    walker_init(w);
+    int32_t table_item = -1;
+    uint32_t it = 0, pt = 0;
+    for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+      walk_to(p, w, g);
+      const Tile t = decode(p, w, g);
+      const int s = (int)(it % (uint32_t)p.stages);
+      const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+      const bool patched = kPatch && w.patch >= 0;
+      const bool rot = p.rotate && t.ch == 0;
+      int64_t* rdst = sm.row_dst + (it & 1u) * BM;
+
+      // destination of this thread's row; invalid rows are not stored
+      {
+        const int64_t pos = t.pos0 + r;
+        int64_t dst = -1;
+        if (pos >= w.dst_pos && pos < w.dst_pos + w.T) {
+          const int64_t blk = pos >> p.page_shift;
+          int32_t page = -1;
+          if (blk < p.max_pages) page = p.block_table[(int64_t)w.seq * p.max_pages + blk];
+          if (page >= 0 && page < p.num_pages)
+            dst = ((int64_t)t.layer * p.num_pages + page) * p.page_size + (pos & (p.page_size - 1));
+          else if (p.err_flag)
+            atomicOr(p.err_flag, KAMERA_EFLAG_PAGE_OOB);
+        }
+        rdst[r] = dst;
+      }
+      if (rot && w.item != table_item) {
+        for (int i = et; i < p.n_pairs; i += EPI_THREADS) sm.cs[i] = phase_cs(w.delta, p.theta[i]);
+        table_item = w.item;
+      }
+      // wait for the tile (and its patch accumulator); the decision to go on
+      // is taken jointly so no thread is left alone at a later barrier
+      const uint32_t buf = pt & 1u;
+      bool ok = wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag);
+      if (ok && patched) ok = wait_bounded(&sm.tfull[buf], (pt >> 1) & 1u, sm.misc, p.err_flag);
+      if (!named_bar_and(1, EPI_THREADS, ok)) break;
+      if (patched) tc_fence_after_sync();
+      const uint32_t canon = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
+      const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
+
+      // compute phase: this thread's row, in place
+      if (patched || rot) {
+        const int g0 = t.cb * (p.BN / 32);
+        for (int gl = 0; gl < p.BN / 32; ++gl) {
+          const int8_t kind = rot ? p.group_kind[g0 + gl] : GK_PLAIN;
+          if (kind == GK_SECOND) continue;
+          if (kind == GK_PLAIN) {
+            epi_plain(canon, r, gl * 32, patched, taddr);
+          } else if (kind == GK_INTERLEAVED) {
+            epi_interleaved(canon, r, gl * 32, p.pair_base[g0 + gl], patched, taddr, sm.cs, p.frame);
+          } else {
+            epi_rotate_half(canon, r, gl * 32, (gl + kind) * 32, p.pair_base[g0 + gl], patched, taddr, sm.cs,
+                            p.frame);
+          }
+        }
+      }
+      if (patched) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+        ++pt;
+      }
+      named_bar_sync(1, EPI_THREADS);
+
+      // copy-out phase: coalesced 16-byte stores of whole tile rows
+      {
+        uint16_t* dst_base = p.pool[t.ch] + (size_t)t.cb * p.BN;
+        int row = et / cpr, c = et % cpr;
+        while (row < BM) {
+          const int64_t d = rdst[row];
+          if (d >= 0) {
+            const uint4 v = lds128(canon + canon_off(row, c * 8));
+            stg128_cs(dst_base + d * p.D + c * 8, v);
+          }
+          row += drow;
+          c += dcol;
+          if (c >= cpr) {
+            c -= cpr;
+            ++row;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // our smem writes precede the next TMA fill of this stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+    }
+  }
+
+  // ---- tear-down ---------------------------------------------------------------------------
+  tc_fence_before_sync();
+  __syncthreads();
+  if (kPatch && warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace kamera

@@ -1,0 +1,153 @@
+"""The C ABI library loads, exports every entry point include/kamera.h
+declares, its structs match the binding's, and host-side validation rejects
+bad arguments with the documented status codes (CPU only: every call here
+returns before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import position_invariant_kv_kamera_gb300 as pk
+from position_invariant_kv_kamera_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "kamera.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pk.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(kamera_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch"):
+        assert n in names
+    assert set(names) == set(pk.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True, check=True).stdout
+    for name in declared_functions():
+        assert re.search(r"\bT " + name + r"\b", out), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert pk.abi_version() == 1
+    assert pk.status_string(pk.KAMERA_OK) == "KAMERA_OK"
+    assert pk.status_string(pk.KAMERA_ERR_CUDA) == "KAMERA_ERR_CUDA"
+    assert pk.status_string(99) == "KAMERA_ERR_UNKNOWN"
+
+
+def test_struct_layouts_match_header(tmp_path):
+    prog = tmp_path / "sizes.c"
+    prog.write_text(r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "kamera.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu\n", sizeof(kamera_model_desc), sizeof(kamera_chunk_store),
+         sizeof(kamera_patch_store), sizeof(kamera_paged_pool), sizeof(kamera_reuse_item));
+  printf("%zu %zu %zu %zu\n", offsetof(kamera_model_desc, rope_base), offsetof(kamera_reuse_item, delta),
+         offsetof(kamera_reuse_item, dst_pos), offsetof(kamera_paged_pool, block_table));
+  return 0;
+}
+''')
+    exe = tmp_path / "sizes"
+    subprocess.run(["gcc", "-I" + _build.INCLUDE, "-o", str(exe), str(prog)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    sizes = [int(x) for x in lines[0].split()]
+    assert sizes == [ctypes.sizeof(pk.kamera_model_desc), ctypes.sizeof(pk.kamera_chunk_store),
+                     ctypes.sizeof(pk.kamera_patch_store), ctypes.sizeof(pk.kamera_paged_pool),
+                     pk.REUSE_ITEM.itemsize]
+    offs = [int(x) for x in lines[1].split()]
+    assert offs == [pk.kamera_model_desc.rope_base.offset, pk.REUSE_ITEM.fields["delta"][1],
+                    pk.REUSE_ITEM.fields["dst_pos"][1], pk.kamera_paged_pool.block_table.offset]
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _gqa_model(**kw):
+    m = pk.model_desc(pk.KAMERA_GQA, 2, 4, 128, rope_base=1e6)
+    for k, v in kw.items():
+        setattr(m, k, v)
+    return m
+
+
+def _pool(**kw):
+    p = pk.kamera_paged_pool(FAKE, FAKE + 4096, 16, 64, FAKE + 8192, 1, 16)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _store():
+    return pk.kamera_chunk_store(FAKE, 1 << 20, FAKE, FAKE, 4)
+
+
+def _reuse(model, pool, store=None, patches=None, n=1):
+    st = store if store is not None else _store()
+    return pk.kamera_reuse_batched(model, st, patches, FAKE, n, pool, None, None, raise_on_error=False)
+
+
+def test_validation_null_pointers(lib):
+    assert pk.kamera_reuse_batched(None, _store(), None, FAKE, 1, _pool(), None, None, False) == pk.KAMERA_ERR_NULL
+    assert pk.kamera_reuse_batched(_gqa_model(), _store(), None, FAKE, 1, None, None, None, False) == pk.KAMERA_ERR_NULL
+    assert pk.kamera_reuse_batched(_gqa_model(), None, None, FAKE, 1, _pool(), None, None, False) == pk.KAMERA_ERR_NULL
+    assert pk.kamera_reuse_batched(_gqa_model(), _store(), None, None, 1, _pool(), None, None, False) == pk.KAMERA_ERR_NULL
+    assert _reuse(_gqa_model(), _pool(k=None)) == pk.KAMERA_ERR_NULL
+    assert _reuse(_gqa_model(), _pool(v=None)) == pk.KAMERA_ERR_NULL
+    assert _reuse(_gqa_model(), _pool(block_table=None)) == pk.KAMERA_ERR_NULL
+    assert pk.kamera_apply_patch(_gqa_model(), None, FAKE, 1, _pool(), None, None, False) == pk.KAMERA_ERR_NULL
+    assert "NULL" in pk.last_error()
+
+
+def test_validation_invalid_arguments(lib):
+    assert _reuse(_gqa_model(family=7), _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(num_layers=0), _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(pairing=3), _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(patch_frame=2), _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(num_kv_heads=0), _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(), _pool(page_size=48)) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(), _pool(page_size=4)) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(), _pool(num_pages=0)) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse(_gqa_model(), _pool(), n=-1) == pk.KAMERA_ERR_INVALID_ARG
+    patches = pk.kamera_patch_store(FAKE, 1 << 20, FAKE, FAKE, 4, 12)
+    assert _reuse(_gqa_model(), _pool(), patches=patches) == pk.KAMERA_ERR_INVALID_ARG
+    mla = pk.model_desc(pk.KAMERA_MLA, 2, rope_dim=64, latent_dim=512)
+    assert _reuse(mla, _pool()) == pk.KAMERA_ERR_INVALID_ARG  # MLA pools carry no V
+    bad_base = _gqa_model(rope_base=-1.0)
+    assert _reuse(bad_base, _pool()) == pk.KAMERA_ERR_INVALID_ARG
+
+
+def test_validation_unsupported_shapes(lib):
+    assert _reuse(_gqa_model(head_dim=80), _pool()) == pk.KAMERA_ERR_UNSUPPORTED
+    assert _reuse(_gqa_model(head_dim=512), _pool()) == pk.KAMERA_ERR_UNSUPPORTED
+    assert _reuse(_gqa_model(rope_dim=96), _pool()) == pk.KAMERA_ERR_UNSUPPORTED
+    assert _reuse(_gqa_model(num_kv_heads=32), _pool()) == pk.KAMERA_ERR_UNSUPPORTED  # D = 4096
+    mla = pk.model_desc(pk.KAMERA_MLA, 2, rope_dim=64, latent_dim=500)
+    assert _reuse(mla, _pool(v=None)) == pk.KAMERA_ERR_UNSUPPORTED
+    huge = _pool(num_pages=1 << 26)
+    assert _reuse(_gqa_model(), huge) == pk.KAMERA_ERR_UNSUPPORTED  # > 2^31 pool rows
+
+
+def test_validation_alignment(lib):
+    assert _reuse(_gqa_model(), _pool(k=FAKE + 8)) == pk.KAMERA_ERR_ALIGNMENT
+    st = pk.kamera_chunk_store(FAKE + 2, 1 << 20, FAKE, FAKE, 4)
+    assert _reuse(_gqa_model(), _pool(), store=st) == pk.KAMERA_ERR_ALIGNMENT
+    assert pk.kamera_reuse_batched(_gqa_model(), _store(), None, FAKE, 1, _pool(), FAKE + 2, None,
+                                   False) == pk.KAMERA_ERR_ALIGNMENT
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _reuse(_gqa_model(), _pool(), n=0) == pk.KAMERA_OK

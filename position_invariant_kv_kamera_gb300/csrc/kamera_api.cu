@@ -236,6 +236,15 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     }
   }
 
+  {
+    // alternate whole rotation units (and plain groups) between the two epilogue halves
+    int k = 0;
+    for (int g = 0; g < n_groups; ++g) {
+      if (p.group_kind[g] == GK_SECOND) continue;
+      p.owner0[g] = (uint8_t)(k++ & 1);
+    }
+  }
+
   // ---- tile shape: BN columns per tile, smem stages ---------------------------------------------
   int dev = 0;
   DeviceFacts* facts = nullptr;
@@ -326,7 +335,8 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     if (kamera_status st = encode(&p.src_map, store->data, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                                   "chunk store"))
       return st;
-  } else {
+  }
+  {
     for (int ch = 0; ch < p.n_ch_work; ++ch) {
       const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)pool_rows};
       const cuuint64_t strides[1] = {(cuuint64_t)D * 2};

@@ -7,18 +7,22 @@
 //     out = R(delta) . KV(B|empty) + U_m V_m^T        -> bf16 -> paged pool slot
 //
 // Work unit ("tile"): 128 destination positions (aligned to 128 in position
-// space) x BN columns of one (item, layer, channel).  Per CTA (192 threads):
-//   warp 0     TMA producer: canonical tile (64-column boxes, 128B swizzle),
-//              and for patched items the U tile [128 x m] and V tile [BN x m]
-//              (no-swizzle K-major core-matrix layout) into a ring of stages.
-//   warp 1     owns TMEM; one lane issues tcgen05.mma M=128, N=BN, K=16 steps:
-//              P = U . V^T into an fp32 TMEM accumulator (two buffers).
-//   warps 2-5  epilogue, one thread per tile row (= TMEM lane): tcgen05.ld the
-//              patch row, rotate the RoPE pairs of the key row by delta*theta_i
-//              (fp64 angle reduction, fp32 sincos, fp32 math), add, round to
-//              bf16 in place in shared memory; then the 128 threads copy the
-//              tile out row by row with coalesced 16-byte stores to the pool
-//              slots given by the block table.
+// space) x BN columns of one (item, layer, channel).  Per CTA (352 threads,
+// one CTA per SM):
+//   warp 0      TMA producer: the canonical tile (64-column boxes, 128B
+//               swizzle; from the chunk store, or page by page from the pool
+//               for the in-place modes) and, for patched items, the U tile
+//               [128 x m] and V tile [BN x m] (no-swizzle K-major core-matrix
+//               layout) into a ring of shared-memory stages.
+//   warp 1      owns TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16
+//               steps): P = U . V^T into an fp32 TMEM accumulator, two buffers.
+//   warp 2      TMA store issuer: whole page segments of the finished tile go
+//               to the pool with cp.async.bulk.tensor stores.
+//   warps 3-10  epilogue, two warps per TMEM lane quadrant, each half taking
+//               half of the tile's rotation units: tcgen05.ld the patch row,
+//               rotate the key row's RoPE pairs by delta*theta_i (fp64 angle
+//               reduction, fp32 sincos and math), add, round to bf16 in place;
+//               rows of partially covered pages are stored by these threads.
 // Every wait on an mbarrier is bounded (about 2 s): on expiry the kernel sets
 // KAMERA_EFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -31,8 +35,11 @@
 namespace kamera {
 
 constexpr int BM = 128;             // tile rows = TMEM lanes = M of the MMA
-constexpr int NUM_THREADS = 192;    // 6 warps
-constexpr int EPI_THREADS = 128;    // warps 2..5
+constexpr int NUM_WARPS = 11;
+constexpr int NUM_THREADS = 32 * NUM_WARPS;
+constexpr int EPI_WARP0 = 3;        // first epilogue warp
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int MAX_GROUPS = 64;      // 32-column groups per row (D <= 2048)
 constexpr int MAX_PAIRS = 128;      // rope_dim / 2
 constexpr int BOX_COLS = 64;        // 64 bf16 = one 128-byte swizzle row
@@ -45,11 +52,15 @@ constexpr int8_t GK_PLAIN = 0;
 constexpr int8_t GK_SECOND = -1;
 constexpr int8_t GK_INTERLEAVED = -2;
 
+// row_dst markers
+constexpr int64_t ROW_SKIP = -1;     // not stored (outside the item, or an invalid page)
+constexpr int64_t ROW_BY_TMA = -2;   // stored by the TMA store of its full page segment
+
 struct Params {
   CUtensorMap src_map;      // chunk store as rows [rows][D]: box 64 x 128, 128B swizzle
-  CUtensorMap pool_map[2];  // pool K / V as rows [L*pages*P][D]: box 64 x S (S = min(P,128))
-  CUtensorMap u_map;        // patch store as (8, rows, m/8): box (8, 128, kg)
-  CUtensorMap v_map;        // patch store as (8, rows, m/8): box (8, BN, kg)
+  CUtensorMap pool_map[2];  // pool K / V as rows [L*pages*P][D]: box 64 x S (S = min(P,128)), 128B swizzle
+  CUtensorMap u_map;        // patch store as (8, rows, m/8): box (8, 128, m/8)
+  CUtensorMap v_map;        // patch store as (8, rows, m/8): box (8, BN, m/8)
   const kamera_reuse_item* items;
   int32_t n_items;
   int32_t src_pool;  // 0: gather from the chunk store, 1: in place from the pool
@@ -63,8 +74,8 @@ struct Params {
   int64_t patch_elems;
   int32_t n_patches;
   int32_t rank;
-  int32_t ksteps;    // ceil(rank / 16)
-  int32_t kg_alloc;  // 8-element K groups held in smem per operand row (>= 2)
+  int32_t ksteps;      // ceil(rank / 16)
+  int32_t kg_alloc;    // 8-element K groups held in smem per operand row (>= 2)
   int32_t need_patch;  // items without a patch have no work (patch-only mode)
   uint16_t* pool[2];
   int64_t num_pages;
@@ -89,6 +100,7 @@ struct Params {
   int32_t* err_flag;
   int8_t group_kind[MAX_GROUPS];
   uint8_t pair_base[MAX_GROUPS];
+  uint8_t owner0[MAX_GROUPS];  // epilogue half that processes the unit starting at group g (rotated tiles)
   double theta[MAX_PAIRS];
 };
 
@@ -102,7 +114,7 @@ struct Walker {
 };
 
 // Tiles of item i (0 if it is skipped); fills the walker's item fields.
-// Error bits are collected in *err (caller decides whether to report them).
+// Error bits are collected in err (the caller decides whether to report them).
 __device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker& w, int32_t& err) {
   const kamera_reuse_item it = p.items[i];
   w.T = it.n_tokens;
@@ -175,6 +187,28 @@ __device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t
   return t;
 }
 
+// A page segment of a tile (rows [sg*S, sg*S + S)): its pool row, or -1 when
+// its page is out of range.  `full` = every row of the segment belongs to the item.
+struct Segment {
+  int32_t y;
+  bool full, any;
+};
+
+__device__ __forceinline__ Segment segment(const Params& p, const Walker& w, const Tile& t, int sg) {
+  Segment s;
+  const int64_t ps = t.pos0 + (int64_t)sg * p.seg_rows;
+  s.any = !(ps + p.seg_rows <= w.dst_pos || ps >= w.dst_pos + w.T);
+  s.full = ps >= w.dst_pos && ps + p.seg_rows <= w.dst_pos + w.T;
+  s.y = -1;
+  if (!s.any) return s;
+  const int64_t blk = ps >> p.page_shift;
+  if (blk >= p.max_pages) return s;
+  const int32_t page = p.block_table[(int64_t)w.seq * p.max_pages + blk];
+  if (page < 0 || page >= p.num_pages) return s;
+  s.y = (int32_t)(((int64_t)t.layer * p.num_pages + page) * p.page_size + (ps & (p.page_size - 1)));
+  return s;
+}
+
 // ---- shared memory ---------------------------------------------------------------------
 
 struct SmemMisc {
@@ -184,15 +218,16 @@ struct SmemMisc {
 };
 
 struct Smem {
-  uint8_t* stages;   // stage s at stages + s * stage_bytes
-  uint64_t* full;    // [stages]
-  uint64_t* empty;   // [stages]
-  uint64_t* tfull;   // [2]
-  uint64_t* tempty;  // [2]
-  uint64_t* drain;   // [1]
+  uint8_t* stages;     // stage s at stages + s * stage_bytes
+  uint64_t* full;      // [stages] TMA loads landed
+  uint64_t* empty;     // [stages] stage free (8 epilogue warps + the store warp)
+  uint64_t* computed;  // [stages] tile computed in place (8 epilogue warps)
+  uint64_t* tfull;     // [2] accumulator ready
+  uint64_t* tempty;    // [2] accumulator drained
+  uint64_t* drain;     // [1]
   SmemMisc* misc;
-  float2* cs;        // [MAX_PAIRS] (cos, sin) of the current item
-  int64_t* row_dst;  // [2][BM] destination row in the pool, -1 = not stored
+  float2* cs;        // [2][MAX_PAIRS] (cos, sin) tables, one per tile parity
+  int64_t* row_dst;  // [2][BM] destination row for the thread-store path, or ROW_SKIP / ROW_BY_TMA
 };
 
 __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
@@ -203,17 +238,19 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
   uint8_t* q = base + (size_t)p.stages * p.stage_bytes;
   s.full = reinterpret_cast<uint64_t*>(q);
   s.empty = s.full + p.stages;
-  s.tfull = s.empty + p.stages;
+  s.computed = s.empty + p.stages;
+  s.tfull = s.computed + p.stages;
   s.tempty = s.tfull + 2;
   s.drain = s.tempty + 2;
   s.misc = reinterpret_cast<SmemMisc*>(s.drain + 1);
-  s.cs = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(s.misc) + 32);
-  s.row_dst = reinterpret_cast<int64_t*>(s.cs + MAX_PAIRS);
+  const uintptr_t cs_at = (reinterpret_cast<uintptr_t>(s.misc) + 32 + 15) & ~uintptr_t(15);
+  s.cs = reinterpret_cast<float2*>(cs_at);
+  s.row_dst = reinterpret_cast<int64_t*>(s.cs + 2 * MAX_PAIRS);
   return s;
 }
 
 __host__ __device__ constexpr uint32_t smem_extra_bytes(int stages) {
-  return 1024 /*alignment slack*/ + 8u * (2u * stages + 5u) + 32u + 8u * MAX_PAIRS + 8u * 2u * BM;
+  return 1024 /*alignment slack*/ + 8u * (3u * stages + 5u) + 32u + 16u + 8u * 2u * MAX_PAIRS + 8u * 2u * BM;
 }
 
 // Bounded wait.  Returns false on abort (another role gave up) or on expiry
@@ -233,18 +270,9 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Sme
   }
 }
 
-__device__ __forceinline__ bool aborted(SmemMisc* misc) {
-  return *reinterpret_cast<volatile int32_t*>(&misc->abort_flag) != 0;
-}
-
 // ---- epilogue helpers ----------------------------------------------------------------------
 
-// byte offset of 16-byte chunk (row r, tile column c, c % 8 == 0) in a 128B-swizzled tile
-__device__ __forceinline__ uint32_t canon_off(int r, int c) {
-  return (uint32_t)(c >> 6) * BOX_BYTES + (uint32_t)r * 128u + ((((uint32_t)c >> 3) & 7u) ^ ((uint32_t)r & 7u)) * 16u;
-}
-
-__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+__device__ __forceinline__ void unpack8(uint4 v, float* f) {
   f[0] = __uint_as_float(v.x << 16);
   f[1] = __uint_as_float(v.x & 0xFFFF0000u);
   f[2] = __uint_as_float(v.y << 16);
@@ -260,16 +288,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+__device__ __forceinline__ uint4 pack8(const float* f) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
 // cos/sin of delta*theta_i: the angle is formed and reduced modulo 2*pi in fp64
 // (two-constant Cody-Waite reduction), then sin/cos are taken in fp32.
 __device__ __forceinline__ float2 phase_cs(int64_t delta, double theta) {
-  const double kTwoPiHi = 6.283185307179586;        // fp64 nearest to 2*pi
-  const double kTwoPiLo = 2.4492935982947064e-16;   // 2*pi - kTwoPiHi
-  const double kInvTwoPi = 0.15915494309189535;     // 1 / (2*pi)
+  const double kTwoPiHi = 6.283185307179586;       // fp64 nearest to 2*pi
+  const double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+  const double kInvTwoPi = 0.15915494309189535;    // 1 / (2*pi)
   const double phi = (double)delta * theta;
   const double k = rint(phi * kInvTwoPi);
   double r = fma(-k, kTwoPiHi, phi);
@@ -279,92 +307,144 @@ __device__ __forceinline__ float2 phase_cs(int64_t delta, double theta) {
   return make_float2(c, s);
 }
 
-// One 32-column group without rotation: out = x + P (patched) -- written in place.
-__device__ __forceinline__ void epi_plain(uint32_t canon, int r, int c0, bool patched, uint32_t taddr) {
-  if (!patched) return;  // bit copy: the tile already holds the output
-  uint32_t acc[32];
-  tmem_ld32(taddr + (uint32_t)c0, acc);
-  tmem_ld_wait();
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t a = canon + canon_off(r, c0 + 8 * k);
-    float x[8];
-    unpack8(lds128(a), x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] += __uint_as_float(acc[8 * k + e]);
-    sts128(a, pack8(x));
+// Row view of a 128B-swizzled tile: 16-byte chunk j (8 columns) of this row.
+struct RowView {
+  uint32_t base;  // tile base + row * 128
+  uint32_t sw;    // row & 7
+  __device__ __forceinline__ uint32_t chunk(int col) const {
+    return base + (uint32_t)(col >> 6) * BOX_BYTES + ((((uint32_t)col >> 3) & 7u) ^ sw) * 16u;
   }
+};
+
+// 16 columns without rotation: out = x + P (patched), written in place.
+__device__ __forceinline__ void epi_plain16(const RowView& rv, int c0, uint32_t taddr) {
+  uint32_t acc[16];
+  tmem_ld16(taddr + (uint32_t)c0, acc);
+  const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
+  const uint4 v0 = lds128(a0), v1 = lds128(a1);
+  tmem_ld_wait();
+  float x[16];
+  unpack8(v0, x);
+  unpack8(v1, x + 8);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(acc[e]);
+  sts128(a0, pack8(x));
+  sts128(a1, pack8(x + 8));
 }
 
-// Two 32-column groups forming rotate-half pairs (cA + e, cB + e), pair index pb + e.
-__device__ __forceinline__ void epi_rotate_half(uint32_t canon, int r, int cA, int cB, int pb, bool patched,
-                                                uint32_t taddr, const float2* cs, int frame) {
-  uint32_t accA[32], accB[32];
-  if (patched) {
-    tmem_ld32(taddr + (uint32_t)cA, accA);
-    tmem_ld32(taddr + (uint32_t)cB, accB);
-    tmem_ld_wait();
+// 16 rotate-half pairs (cA + e, cB + e), pair index pb + e.
+template <bool kPatched, bool kCanonicalFrame>
+__device__ __forceinline__ void epi_rotate16(const RowView& rv, int cA, int cB, int pb, uint32_t taddr,
+                                             const float2* cs) {
+  uint32_t accA[16], accB[16];
+  if (kPatched) {
+    tmem_ld16(taddr + (uint32_t)cA, accA);
+    tmem_ld16(taddr + (uint32_t)cB, accB);
   }
+  const uint32_t a0 = rv.chunk(cA), a1 = rv.chunk(cA + 8), b0 = rv.chunk(cB), b1 = rv.chunk(cB + 8);
+  const uint4 va0 = lds128(a0), va1 = lds128(a1), vb0 = lds128(b0), vb1 = lds128(b1);
+  if (kPatched) tmem_ld_wait();
+  float xa[16], xb[16];
+  unpack8(va0, xa);
+  unpack8(va1, xa + 8);
+  unpack8(vb0, xb);
+  unpack8(vb1, xb + 8);
+  const float4* cs4 = reinterpret_cast<const float4*>(cs + pb);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t aA = canon + canon_off(r, cA + 8 * k);
-    const uint32_t aB = canon + canon_off(r, cB + 8 * k);
-    float xa[8], xb[8];
-    unpack8(lds128(aA), xa);
-    unpack8(lds128(aB), xb);
+  for (int e2 = 0; e2 < 8; ++e2) {
+    const float4 t = cs4[e2];  // (cos, sin) of pairs pb + 2*e2 and pb + 2*e2 + 1
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 t = cs[pb + 8 * k + e];
+    for (int h = 0; h < 2; ++h) {
+      const int e = 2 * e2 + h;
+      const float c = h ? t.z : t.x, s = h ? t.w : t.y;
       float a = xa[e], b = xb[e];
-      if (patched && frame == KAMERA_PATCH_CANONICAL_FRAME) {
-        a += __uint_as_float(accA[8 * k + e]);
-        b += __uint_as_float(accB[8 * k + e]);
+      if (kPatched && kCanonicalFrame) {
+        a += __uint_as_float(accA[e]);
+        b += __uint_as_float(accB[e]);
       }
-      float ra = fmaf(a, t.x, -b * t.y);
-      float rb = fmaf(b, t.x, a * t.y);
-      if (patched && frame != KAMERA_PATCH_CANONICAL_FRAME) {
-        ra += __uint_as_float(accA[8 * k + e]);
-        rb += __uint_as_float(accB[8 * k + e]);
+      float ra = fmaf(a, c, -b * s);
+      float rb = fmaf(b, c, a * s);
+      if (kPatched && !kCanonicalFrame) {
+        ra += __uint_as_float(accA[e]);
+        rb += __uint_as_float(accB[e]);
       }
       xa[e] = ra;
       xb[e] = rb;
     }
-    sts128(aA, pack8(xa));
-    sts128(aB, pack8(xb));
   }
+  sts128(a0, pack8(xa));
+  sts128(a1, pack8(xa + 8));
+  sts128(b0, pack8(xb));
+  sts128(b1, pack8(xb + 8));
 }
 
-// One 32-column group of interleaved pairs (2e, 2e+1), pair index pb + e.
-__device__ __forceinline__ void epi_interleaved(uint32_t canon, int r, int c0, int pb, bool patched, uint32_t taddr,
-                                                const float2* cs, int frame) {
-  uint32_t acc[32];
-  if (patched) {
-    tmem_ld32(taddr + (uint32_t)c0, acc);
-    tmem_ld_wait();
-  }
+// 8 interleaved pairs (2e, 2e+1) in 16 columns, pair index pb + e.
+template <bool kPatched, bool kCanonicalFrame>
+__device__ __forceinline__ void epi_interleaved16(const RowView& rv, int c0, int pb, uint32_t taddr,
+                                                  const float2* cs) {
+  uint32_t acc[16];
+  if (kPatched) tmem_ld16(taddr + (uint32_t)c0, acc);
+  const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
+  const uint4 v0 = lds128(a0), v1 = lds128(a1);
+  if (kPatched) tmem_ld_wait();
+  float x[16];
+  unpack8(v0, x);
+  unpack8(v1, x + 8);
+  const float4* cs4 = reinterpret_cast<const float4*>(cs + pb);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t a0 = canon + canon_off(r, c0 + 8 * k);
-    float x[8];
-    unpack8(lds128(a0), x);
+  for (int e2 = 0; e2 < 4; ++e2) {
+    const float4 t = cs4[e2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 t = cs[pb + 4 * k + e];
+    for (int h = 0; h < 2; ++h) {
+      const int e = 2 * e2 + h;
+      const float c = h ? t.z : t.x, s = h ? t.w : t.y;
       float a = x[2 * e], b = x[2 * e + 1];
-      if (patched && frame == KAMERA_PATCH_CANONICAL_FRAME) {
-        a += __uint_as_float(acc[8 * k + 2 * e]);
-        b += __uint_as_float(acc[8 * k + 2 * e + 1]);
+      if (kPatched && kCanonicalFrame) {
+        a += __uint_as_float(acc[2 * e]);
+        b += __uint_as_float(acc[2 * e + 1]);
       }
-      float ra = fmaf(a, t.x, -b * t.y);
-      float rb = fmaf(b, t.x, a * t.y);
-      if (patched && frame != KAMERA_PATCH_CANONICAL_FRAME) {
-        ra += __uint_as_float(acc[8 * k + 2 * e]);
-        rb += __uint_as_float(acc[8 * k + 2 * e + 1]);
+      float ra = fmaf(a, c, -b * s);
+      float rb = fmaf(b, c, a * s);
+      if (kPatched && !kCanonicalFrame) {
+        ra += __uint_as_float(acc[2 * e]);
+        rb += __uint_as_float(acc[2 * e + 1]);
       }
       x[2 * e] = ra;
       x[2 * e + 1] = rb;
     }
-    sts128(a0, pack8(x));
+  }
+  sts128(a0, pack8(x));
+  sts128(a1, pack8(x + 8));
+}
+
+// One tile row's share of the compute phase for epilogue half h.
+template <bool kPatched, bool kCanonicalFrame>
+__device__ __forceinline__ void epi_row(const Params& p, const RowView& rv, int cb, bool rot, int h, uint32_t taddr,
+                                        const float2* cs) {
+  const int ng = p.BN / 32;
+  const int g0 = cb * ng;
+  for (int gl = 0; gl < ng; ++gl) {
+    const int g = g0 + gl;
+    const int8_t kind = rot ? p.group_kind[g] : GK_PLAIN;
+    if (kind == GK_SECOND) continue;
+    const int owner = rot ? p.owner0[g] : (gl & 1);
+    if (owner != h) continue;
+    const int c0 = gl * 32;
+    if (kind == GK_PLAIN) {
+      if (kPatched) {
+        epi_plain16(rv, c0, taddr);
+        epi_plain16(rv, c0 + 16, taddr);
+      }
+    } else if (kind == GK_INTERLEAVED) {
+      const int pb = p.pair_base[g];
+      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0, pb, taddr, cs);
+      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0 + 16, pb + 8, taddr, cs);
+    } else {
+      const int pb = p.pair_base[g];
+      const int cB = (gl + kind) * 32;
+      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0, cB, pb, taddr, cs);
+      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0 + 16, cB + 16, pb + 16, taddr, cs);
+    }
   }
 }
 
@@ -381,11 +461,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 4);
+      mbar_init(&sm.empty[s], EPI_WARPS + 1);
+      mbar_init(&sm.computed[s], EPI_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tfull[b], 1);
-      mbar_init(&sm.tempty[b], 4);
+      mbar_init(&sm.tempty[b], EPI_WARPS);
     }
     mbar_init(sm.drain, 1);
     sm.misc->abort_flag = 0;
@@ -432,6 +513,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   tc_fence_after_sync();
   const int64_t total = sm.misc->total_tiles;
   const uint32_t tmem_base = kPatch ? sm.misc->tmem_base : 0u;
+  const int nbox = p.BN / BOX_COLS;
+  const int nseg = BM / p.seg_rows;
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -452,41 +535,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) break;
         uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
         const int col0 = t.cb * p.BN;
-        const int nbox = p.BN / BOX_COLS;
         const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
-        // decide the loads first so the transaction byte count is exact
-        uint32_t bytes = 0;
-        int32_t seg_y[BM / 8];
-        int nseg = 0;
+        const bool patched = kPatch && w.patch >= 0;
+        // the transaction byte count first, then the copies
+        uint32_t bytes = patched ? (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u : 0u;
         if (!p.src_pool) {
           bytes += (uint32_t)nbox * BOX_BYTES;
         } else {
-          nseg = BM / p.seg_rows;
-          for (int sg = 0; sg < nseg; ++sg) {
-            seg_y[sg] = -1;
-            const int64_t ps = t.pos0 + (int64_t)sg * p.seg_rows;
-            if (ps + p.seg_rows <= w.dst_pos || ps >= w.dst_pos + w.T) continue;
-            const int64_t blk = ps >> p.page_shift;
-            if (blk >= p.max_pages) continue;
-            const int32_t page = p.block_table[(int64_t)w.seq * p.max_pages + blk];
-            if (page < 0 || page >= p.num_pages) continue;
-            seg_y[sg] = (int32_t)(((int64_t)t.layer * p.num_pages + page) * p.page_size + (ps & (p.page_size - 1)));
-            bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
-          }
+          for (int sg = 0; sg < nseg; ++sg)
+            if (segment(p, w, t, sg).y >= 0) bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
         }
-        const bool patched = kPatch && w.patch >= 0;
-        if (patched) bytes += (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u;
         mbar_arrive_expect_tx(&sm.full[s], bytes);
         if (!p.src_pool) {
-          const int64_t y = w.chunk >= 0 ? p.store_off[w.chunk] / p.D : 0;
+          const int64_t y = p.store_off[w.chunk] / p.D;
           const int32_t row = (int32_t)(y + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
           for (int b = 0; b < nbox; ++b) tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, row);
         } else {
           for (int sg = 0; sg < nseg; ++sg) {
-            if (seg_y[sg] < 0) continue;
+            const Segment seg = segment(p, w, t, sg);
+            if (seg.y < 0) continue;
             for (int b = 0; b < nbox; ++b)
               tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
-                          col0 + b * BOX_COLS, seg_y[sg]);
+                          col0 + b * BOX_COLS, seg.y);
           }
         }
         if (patched) {
@@ -537,17 +607,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         wait_bounded(sm.drain, 0, sm.misc, p.err_flag, false);
       }
     }
+  } else if (warp == 2) {
+    // ================= TMA store issuer =================
+    if (lane == 0) {
+      Walker w;
+      walker_init(w);
+      uint32_t it = 0;
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+        walk_to(p, w, g);
+        const Tile t = decode(p, w, g);
+        const int s = (int)(it % (uint32_t)p.stages);
+        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) break;
+        const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+        const int col0 = t.cb * p.BN;
+        for (int sg = 0; sg < nseg; ++sg) {
+          const Segment seg = segment(p, w, t, sg);
+          if (!seg.full || seg.y < 0) continue;
+          for (int b = 0; b < nbox; ++b)
+            tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
+                         col0 + b * BOX_COLS, seg.y);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
+        mbar_arrive(&sm.empty[s]);
+      }
+      bulk_wait_group0();
+    }
   } else {
-    // ================= epilogue (warps 2..5) =================
+    // ================= epilogue (warps 3..10) =================
+    const int e = warp - EPI_WARP0;      // 0..7
+    const int h = e >> 2;                // column half
     const int q = warp & 3;              // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;         // tile row owned in the compute phase
-    const int et = threadIdx.x - 64;     // 0..127 in the copy-out phase
+    const int et = threadIdx.x - EPI_WARP0 * 32;  // 0..255
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     const int cpr = p.BN / 8;            // 16-byte chunks per tile row
-    const int drow = EPI_THREADS / cpr, dcol = EPI_THREADS % cpr;
     Walker w;
     walker_init(w);
-    int32_t table_item = -1;
+    int32_t table_item[2] = {-1, -1};  // item whose phases each table holds
     uint32_t it = 0, pt = 0;
     for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
       walk_to(p, w, g);
@@ -558,78 +656,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       const bool rot = p.rotate && t.ch == 0;
       int64_t* rdst = sm.row_dst + (it & 1u) * BM;
 
-      // destination of this thread's row; invalid rows are not stored
-      {
+      if (h == 0) {
+        // destination of row r: whole page segments go out by TMA, the rest by threads
         const int64_t pos = t.pos0 + r;
-        int64_t dst = -1;
+        int64_t dst = ROW_SKIP;
         if (pos >= w.dst_pos && pos < w.dst_pos + w.T) {
-          const int64_t blk = pos >> p.page_shift;
-          int32_t page = -1;
-          if (blk < p.max_pages) page = p.block_table[(int64_t)w.seq * p.max_pages + blk];
-          if (page >= 0 && page < p.num_pages)
-            dst = ((int64_t)t.layer * p.num_pages + page) * p.page_size + (pos & (p.page_size - 1));
-          else if (p.err_flag)
-            atomicOr(p.err_flag, KAMERA_EFLAG_PAGE_OOB);
+          const Segment seg = segment(p, w, t, r / p.seg_rows);
+          if (seg.y < 0) {
+            if (p.err_flag) atomicOr(p.err_flag, KAMERA_EFLAG_PAGE_OOB);
+          } else {
+            dst = seg.full ? ROW_BY_TMA : (int64_t)seg.y + (r % p.seg_rows);
+          }
         }
         rdst[r] = dst;
+      } else if (rot && w.item != table_item[it & 1u]) {
+        // tables alternate by tile parity: the previous readers of this one
+        // finished before the last joint barrier
+        float2* cs = sm.cs + (it & 1u) * MAX_PAIRS;
+        for (int i = et - 128; i < p.n_pairs; i += 128) cs[i] = phase_cs(w.delta, p.theta[i]);
       }
-      if (rot && w.item != table_item) {
-        for (int i = et; i < p.n_pairs; i += EPI_THREADS) sm.cs[i] = phase_cs(w.delta, p.theta[i]);
-        table_item = w.item;
-      }
-      // wait for the tile (and its patch accumulator); the decision to go on
-      // is taken jointly so no thread is left alone at a later barrier
+      if (rot) table_item[it & 1u] = w.item;
+      const float2* cs = sm.cs + (it & 1u) * MAX_PAIRS;
+
+      // wait for the tile (and its accumulator); decide jointly whether to go on
       const uint32_t buf = pt & 1u;
       bool ok = wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag);
       if (ok && patched) ok = wait_bounded(&sm.tfull[buf], (pt >> 1) & 1u, sm.misc, p.err_flag);
       if (!named_bar_and(1, EPI_THREADS, ok)) break;
       if (patched) tc_fence_after_sync();
-      const uint32_t canon = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
-      const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
 
-      // compute phase: this thread's row, in place
-      if (patched || rot) {
-        const int g0 = t.cb * (p.BN / 32);
-        for (int gl = 0; gl < p.BN / 32; ++gl) {
-          const int8_t kind = rot ? p.group_kind[g0 + gl] : GK_PLAIN;
-          if (kind == GK_SECOND) continue;
-          if (kind == GK_PLAIN) {
-            epi_plain(canon, r, gl * 32, patched, taddr);
-          } else if (kind == GK_INTERLEAVED) {
-            epi_interleaved(canon, r, gl * 32, p.pair_base[g0 + gl], patched, taddr, sm.cs, p.frame);
-          } else {
-            epi_rotate_half(canon, r, gl * 32, (gl + kind) * 32, p.pair_base[g0 + gl], patched, taddr, sm.cs,
-                            p.frame);
-          }
-        }
-      }
+      // compute phase: this thread's row, its half of the units, in place
+      const RowView rv{smem_addr(sm.stages + (size_t)s * p.stage_bytes) + (uint32_t)r * 128u, (uint32_t)r & 7u};
+      const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
       if (patched) {
+        if (p.frame == KAMERA_PATCH_CANONICAL_FRAME)
+          epi_row<true, true>(p, rv, t.cb, rot, h, taddr, cs);
+        else
+          epi_row<true, false>(p, rv, t.cb, rot, h, taddr, cs);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[buf]);
         ++pt;
+      } else if (rot) {
+        epi_row<false, false>(p, rv, t.cb, rot, h, taddr, cs);
       }
-      named_bar_sync(1, EPI_THREADS);
+      fence_proxy_async_smem();  // in-place results -> visible to the TMA store
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.computed[s]);
 
-      // copy-out phase: coalesced 16-byte stores of whole tile rows
-      {
+      // rows of partially covered pages: coalesced 16-byte stores by the threads
+      bool partial = false;
+      for (int sg = 0; sg < nseg && !partial; ++sg) {
+        const Segment seg = segment(p, w, t, sg);
+        partial = seg.any && !seg.full && seg.y >= 0;
+      }
+      if (partial) {
+        named_bar_sync(1, EPI_THREADS);
+        const uint32_t tile = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
         uint16_t* dst_base = p.pool[t.ch] + (size_t)t.cb * p.BN;
-        int row = et / cpr, c = et % cpr;
-        while (row < BM) {
+        for (int q2 = et; q2 < BM * cpr; q2 += EPI_THREADS) {
+          const int row = q2 / cpr, c = q2 % cpr;
           const int64_t d = rdst[row];
-          if (d >= 0) {
-            const uint4 v = lds128(canon + canon_off(row, c * 8));
-            stg128_cs(dst_base + d * p.D + c * 8, v);
-          }
-          row += drow;
-          c += dcol;
-          if (c >= cpr) {
-            c -= cpr;
-            ++row;
-          }
+          if (d < 0) continue;
+          const RowView rr{tile + (uint32_t)row * 128u, (uint32_t)row & 7u};
+          stg128_cs(dst_base + d * p.D + c * 8, lds128(rr.chunk(c * 8)));
         }
       }
-      fence_proxy_async_smem();  // our smem writes precede the next TMA fill of this stage
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
     }

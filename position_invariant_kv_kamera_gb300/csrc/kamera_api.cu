@@ -250,9 +250,9 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   DeviceFacts* facts = nullptr;
   if (kamera_status st = device_facts(&dev, &facts)) return st;
   const int kg_alloc = use_patch ? (rank / 8 < 2 ? 2 : rank / 8) : 0;
-  const int bn_env = env_int("KAMERA_BN"), st_env = env_int("KAMERA_STAGES");
-  int BN = 0, stages = 0;
-  uint32_t stage_bytes = 0;
+  const int bn_env = env_int("KAMERA_BN"), st_env = env_int("KAMERA_STAGES"), uv_env = env_int("KAMERA_UV_SLOTS");
+  int BN = 0, stages = 0, uv_slots = 0;
+  uint32_t stage_bytes = 0, uv_slot_bytes = 0;
   const int cands[4] = {256, 192, 128, 64};
   for (int ci = 0; ci < 4 && BN == 0; ++ci) {
     const int bn = cands[ci];
@@ -262,16 +262,26 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     for (int g = 0; g < n_groups; ++g)
       if (p.group_kind[g] > 0 && (g * 32) / bn != ((g + p.group_kind[g]) * 32) / bn) whole = false;
     if (!whole) continue;
-    const uint32_t sb = (uint32_t)bn * 256u + (use_patch ? (uint32_t)(BM + bn) * kg_alloc * 16u : 0u);
-    int s = st_env ? st_env : 4;
-    while (s >= 2 && (uint64_t)s * sb + smem_extra_bytes(s) > (uint64_t)facts->smem_optin) --s;
-    if (s < 2) continue;
-    BN = bn;
-    stages = s;
-    stage_bytes = sb;
+    const uint32_t sb = (uint32_t)bn * 256u;
+    const uint32_t ub = use_patch ? (uint32_t)(BM + bn) * kg_alloc * 16u : 0u;
+    // prefer canonical stages (they carry the HBM stream), then a second patch-factor slot
+    for (int s = 4; s >= 2 && BN == 0; --s) {
+      if (st_env && s != st_env) continue;
+      for (int u = use_patch ? 2 : 1; u >= 1 && BN == 0; --u) {
+        if (uv_env && use_patch && u != uv_env) continue;
+        const uint64_t need = (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + smem_extra_bytes(s, u);
+        if (need > (uint64_t)facts->smem_optin) continue;
+        BN = bn;
+        stages = s;
+        uv_slots = use_patch ? u : 0;
+        stage_bytes = sb;
+        uv_slot_bytes = ub;
+      }
+    }
   }
   if (BN == 0) return fail(KAMERA_ERR_UNSUPPORTED, "no tile shape fits D = %d, rank %d", D, rank);
-  const uint32_t smem = (uint32_t)stages * stage_bytes + smem_extra_bytes(stages);
+  const uint32_t smem = (uint32_t)stages * stage_bytes + (uint32_t)uv_slots * uv_slot_bytes +
+                        smem_extra_bytes(stages, uv_slots);
 
   // ---- parameters ------------------------------------------------------------------------------------
   p.items = items;
@@ -296,12 +306,13 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   p.n_ch_work = mode == MODE_RELOCATE_IN_PLACE ? 1 : n_ch_layout;
   p.BN = BN;
   p.stages = stages;
+  p.uv_slots = uv_slots;
   p.seg_rows = pool->page_size < BM ? pool->page_size : BM;
+  p.seg_shift = __builtin_ctz((unsigned)p.seg_rows);
   p.rotate = mode == MODE_PATCH_IN_PLACE ? 0 : 1;
   p.frame = model->patch_frame;
   p.n_pairs = n_pairs;
   p.stage_bytes = stage_bytes;
-  p.canon_bytes = (uint32_t)BN * 256u;
   p.u_bytes = use_patch ? (uint32_t)BM * kg_alloc * 16u : 0u;
   p.v_bytes = use_patch ? (uint32_t)BN * kg_alloc * 16u : 0u;
   uint32_t tc = 32;

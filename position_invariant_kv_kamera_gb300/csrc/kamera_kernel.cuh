@@ -35,11 +35,12 @@
 namespace kamera {
 
 constexpr int BM = 128;             // tile rows = TMEM lanes = M of the MMA
-constexpr int NUM_WARPS = 11;
+constexpr int NUM_WARPS = 12;
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 constexpr int EPI_WARP0 = 3;        // first epilogue warp
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int UV_WARP = 11;         // loads the patch factors
 constexpr int MAX_GROUPS = 64;      // 32-column groups per row (D <= 2048)
 constexpr int MAX_PAIRS = 128;      // rope_dim / 2
 constexpr int BOX_COLS = 64;        // 64 bf16 = one 128-byte swizzle row
@@ -91,12 +92,14 @@ struct Params {
   int32_t BN;
   int32_t n_cb;      // column blocks processed per row
   int32_t cb_first;  // first processed column block
-  int32_t stages;
-  int32_t seg_rows;  // rows per pool page segment in a tile (min(P, 128))
+  int32_t stages;     // canonical tile stages
+  int32_t uv_slots;   // patch-factor slots (U and V tiles)
+  int32_t seg_rows;   // rows per pool page segment in a tile (min(P, 128))
+  int32_t seg_shift;  // log2(seg_rows)
   int32_t rotate;    // rotate channel 0
   int32_t frame;     // kamera_patch_frame
   int32_t n_pairs;
-  uint32_t stage_bytes, canon_bytes, u_bytes, v_bytes, tmem_cols;
+  uint32_t stage_bytes, u_bytes, v_bytes, tmem_cols;  // stage_bytes = one canonical tile
   int32_t* err_flag;
   int8_t group_kind[MAX_GROUPS];
   uint8_t pair_base[MAX_GROUPS];
@@ -110,7 +113,8 @@ struct Walker {
   int32_t item;
   int64_t base, count;
   int64_t dst_pos, delta;
-  int32_t T, seq, chunk, patch, n_tb;
+  int32_t T, seq, chunk, patch;
+  uint32_t n_tb;
 };
 
 // Tiles of item i (0 if it is skipped); fills the walker's item fields.
@@ -149,8 +153,10 @@ __device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker
     w.patch = it.patch_id;
   }
   if (p.need_patch && w.patch < 0) return 0;
-  w.n_tb = (int32_t)((it.dst_pos + T + BM - 1) / BM - it.dst_pos / BM);
-  return (int64_t)p.num_layers * p.n_ch_work * w.n_tb * p.n_cb;
+  w.n_tb = (uint32_t)((it.dst_pos + T + BM - 1) / BM - it.dst_pos / BM);
+  const int64_t count = (int64_t)p.num_layers * p.n_ch_work * w.n_tb * p.n_cb;
+  if (count > (int64_t)0xFFFFFFFF) { err |= KAMERA_EFLAG_LEN; return 0; }  // tile decode is 32-bit
+  return count;
 }
 
 __device__ __forceinline__ void walker_init(Walker& w) {
@@ -174,17 +180,30 @@ struct Tile {
   int64_t pos0;  // destination position of tile row 0
 };
 
+// An item has fewer than 2^32 tiles (checked on the host), so the decode runs in 32 bits.
 __device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t g) {
-  int64_t local = g - w.base;
+  uint32_t local = (uint32_t)(g - w.base);
   Tile t;
-  t.cb = p.cb_first + (int32_t)(local % p.n_cb);
-  local /= p.n_cb;
-  const int32_t tb = (int32_t)(local % w.n_tb);
-  local /= w.n_tb;
-  t.ch = (int32_t)(local % p.n_ch_work);
-  t.layer = (int32_t)(local / p.n_ch_work);
-  t.pos0 = (w.dst_pos / BM) * BM + (int64_t)tb * BM;
+  const uint32_t ncb = (uint32_t)p.n_cb;
+  uint32_t q = local / ncb;
+  t.cb = p.cb_first + (int32_t)(local - q * ncb);
+  const uint32_t q2 = q / w.n_tb;
+  const uint32_t tb = q - q2 * w.n_tb;
+  const uint32_t nch = (uint32_t)p.n_ch_work;
+  t.layer = (int32_t)(q2 / nch);
+  t.ch = (int32_t)(q2 - (uint32_t)t.layer * nch);
+  t.pos0 = (w.dst_pos & ~(int64_t)(BM - 1)) + (int64_t)tb * BM;
   return t;
+}
+
+// Does the tile hold rows of a page segment that the item only partly covers?
+// (Only the segments holding the item's first and last rows can be partial.)
+__device__ __forceinline__ bool has_partial_segment(const Params& p, const Walker& w, const Tile& t) {
+  const int64_t end = w.dst_pos + w.T;
+  const int64_t m = p.seg_rows - 1;
+  const bool head = (w.dst_pos & m) != 0 && w.dst_pos >= t.pos0 && w.dst_pos < t.pos0 + BM;
+  const bool tail = (end & m) != 0 && end - 1 >= t.pos0 && end - 1 < t.pos0 + BM;
+  return head || tail;
 }
 
 // A page segment of a tile (rows [sg*S, sg*S + S)): its pool row, or -1 when
@@ -219,7 +238,10 @@ struct SmemMisc {
 
 struct Smem {
   uint8_t* stages;     // stage s at stages + s * stage_bytes
+  uint8_t* uv;         // slot u at uv + u * (u_bytes + v_bytes): U tile then V tile
   uint64_t* full;      // [stages] TMA loads landed
+  uint64_t* uv_full;   // [uv_slots] patch factors landed
+  uint64_t* uv_empty;  // [uv_slots] slot free (MMA done with it)
   uint64_t* empty;     // [stages] stage free (8 epilogue warps + the store warp)
   uint64_t* computed;  // [stages] tile computed in place (8 epilogue warps)
   uint64_t* tfull;     // [2] accumulator ready
@@ -235,11 +257,14 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
   uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
   Smem s;
   s.stages = base;
-  uint8_t* q = base + (size_t)p.stages * p.stage_bytes;
+  s.uv = base + (size_t)p.stages * p.stage_bytes;
+  uint8_t* q = s.uv + (size_t)p.uv_slots * (p.u_bytes + p.v_bytes);
   s.full = reinterpret_cast<uint64_t*>(q);
   s.empty = s.full + p.stages;
   s.computed = s.empty + p.stages;
-  s.tfull = s.computed + p.stages;
+  s.uv_full = s.computed + p.stages;
+  s.uv_empty = s.uv_full + p.uv_slots;
+  s.tfull = s.uv_empty + p.uv_slots;
   s.tempty = s.tfull + 2;
   s.drain = s.tempty + 2;
   s.misc = reinterpret_cast<SmemMisc*>(s.drain + 1);
@@ -249,8 +274,9 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
   return s;
 }
 
-__host__ __device__ constexpr uint32_t smem_extra_bytes(int stages) {
-  return 1024 /*alignment slack*/ + 8u * (3u * stages + 5u) + 32u + 16u + 8u * 2u * MAX_PAIRS + 8u * 2u * BM;
+__host__ __device__ constexpr uint32_t smem_extra_bytes(int stages, int uv_slots) {
+  return 1024 /*alignment slack*/ + 8u * (3u * stages + 2u * uv_slots + 5u) + 32u + 16u + 8u * 2u * MAX_PAIRS +
+         8u * 2u * BM;
 }
 
 // Bounded wait.  Returns false on abort (another role gave up) or on expiry
@@ -464,6 +490,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       mbar_init(&sm.empty[s], EPI_WARPS + 1);
       mbar_init(&sm.computed[s], EPI_WARPS);
     }
+    for (int u = 0; u < p.uv_slots; ++u) {
+      mbar_init(&sm.uv_full[u], 1);
+      mbar_init(&sm.uv_empty[u], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tfull[b], 1);
       mbar_init(&sm.tempty[b], EPI_WARPS);
@@ -475,12 +505,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   if (kPatch) {
     // K groups the MMA reads but TMA never writes (rank 8 pads K to 16) stay zero
     const int kg_load = p.rank / 8;
-    for (int s = 0; s < p.stages; ++s) {
-      uint8_t* st = sm.stages + (size_t)s * p.stage_bytes + p.canon_bytes;
+    for (int u = 0; u < p.uv_slots; ++u) {
+      uint8_t* slot = sm.uv + (size_t)u * (p.u_bytes + p.v_bytes);
       const uint32_t u_pad = (uint32_t)(p.kg_alloc - kg_load) * BM * 16u;
       const uint32_t v_pad = (uint32_t)(p.kg_alloc - kg_load) * p.BN * 16u;
-      uint8_t* upad = st + (uint32_t)kg_load * BM * 16u;
-      uint8_t* vpad = st + p.u_bytes + (uint32_t)kg_load * p.BN * 16u;
+      uint8_t* upad = slot + (uint32_t)kg_load * BM * 16u;
+      uint8_t* vpad = slot + p.u_bytes + (uint32_t)kg_load * p.BN * 16u;
       for (uint32_t i = threadIdx.x * 16u; i < u_pad; i += NUM_THREADS * 16u)
         *reinterpret_cast<uint4*>(upad + i) = make_uint4(0, 0, 0, 0);
       for (uint32_t i = threadIdx.x * 16u; i < v_pad; i += NUM_THREADS * 16u)
@@ -515,15 +545,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   const uint32_t tmem_base = kPatch ? sm.misc->tmem_base : 0u;
   const int nbox = p.BN / BOX_COLS;
   const int nseg = BM / p.seg_rows;
+  const uint32_t uv_bytes = p.u_bytes + p.v_bytes;
 
   if (warp == 0) {
-    // ================= TMA producer =================
+    // ================= TMA producer: canonical tiles =================
     if (lane == 0) {
       tma_prefetch_desc(p.src_pool ? &p.pool_map[0] : &p.src_map);
-      if (kPatch) {
-        tma_prefetch_desc(&p.u_map);
-        tma_prefetch_desc(&p.v_map);
-      }
       Walker w;
       walker_init(w);
       uint32_t it = 0;
@@ -535,18 +562,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) break;
         uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
         const int col0 = t.cb * p.BN;
-        const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
-        const bool patched = kPatch && w.patch >= 0;
         // the transaction byte count first, then the copies
-        uint32_t bytes = patched ? (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u : 0u;
+        uint32_t bytes = 0;
         if (!p.src_pool) {
-          bytes += (uint32_t)nbox * BOX_BYTES;
+          bytes = (uint32_t)nbox * BOX_BYTES;
         } else {
           for (int sg = 0; sg < nseg; ++sg)
             if (segment(p, w, t, sg).y >= 0) bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
         }
         mbar_arrive_expect_tx(&sm.full[s], bytes);
         if (!p.src_pool) {
+          const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
           const int64_t y = p.store_off[w.chunk] / p.D;
           const int32_t row = (int32_t)(y + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
           for (int b = 0; b < nbox; ++b) tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, row);
@@ -559,18 +585,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
                           col0 + b * BOX_COLS, seg.y);
           }
         }
-        if (patched) {
-          const int64_t prow = p.patch_off[w.patch] / p.rank +
-                               ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
-          tma_load_3d(st + p.canon_bytes, &p.u_map, &sm.full[s], 0, (int32_t)(prow + t0), 0);
-          tma_load_3d(st + p.canon_bytes + p.u_bytes, &p.v_map, &sm.full[s], 0, (int32_t)(prow + w.T + col0), 0);
-        }
       }
       // drain: every stage's last fill must have landed before the CTA exits
       const uint32_t S = (uint32_t)p.stages;
       for (uint32_t s = 0; s < S && s < it; ++s) {
         const uint32_t fills = (it - s + S - 1) / S;
         wait_bounded(&sm.full[s], (fills - 1) & 1u, sm.misc, p.err_flag, false);
+      }
+    }
+  } else if (warp == UV_WARP) {
+    // ================= TMA producer: patch factors =================
+    if (kPatch && lane == 0) {
+      tma_prefetch_desc(&p.u_map);
+      tma_prefetch_desc(&p.v_map);
+      Walker w;
+      walker_init(w);
+      uint32_t pu = 0;
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {
+        walk_to(p, w, g);
+        if (w.patch < 0) continue;
+        const Tile t = decode(p, w, g);
+        const int u = (int)(pu % (uint32_t)p.uv_slots);
+        const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
+        if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) break;
+        uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
+        mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u);
+        const int64_t t0 = t.pos0 - w.dst_pos;
+        const int64_t prow = p.patch_off[w.patch] / p.rank +
+                             ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
+        tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, (int32_t)(prow + t0), 0);
+        tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0, (int32_t)(prow + w.T + t.cb * p.BN), 0);
+        ++pu;
+      }
+      const uint32_t S = (uint32_t)p.uv_slots;
+      for (uint32_t u = 0; u < S && u < pu; ++u) {
+        const uint32_t fills = (pu - u + S - 1) / S;
+        wait_bounded(&sm.uv_full[u], (fills - 1) & 1u, sm.misc, p.err_flag, false);
       }
     }
   } else if (warp == 1) {
@@ -580,25 +630,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       const uint32_t lbo_u = BM * 16u, lbo_v = (uint32_t)p.BN * 16u;
       Walker w;
       walker_init(w);
-      uint32_t it = 0, pt = 0;
+      uint32_t pt = 0;
       bool issued = false;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {
         walk_to(p, w, g);
         if (w.patch < 0) continue;
-        const int s = (int)(it % (uint32_t)p.stages);
-        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        const int u = (int)(pt % (uint32_t)p.uv_slots);
+        const uint32_t uph = (pt / (uint32_t)p.uv_slots) & 1u;
         const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
         if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) break;
-        if (!wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag)) break;
+        if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) break;
         tc_fence_after_sync();
-        const uint32_t st = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
-        const uint32_t ua = st + p.canon_bytes, va = st + p.canon_bytes + p.u_bytes;
+        const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
         for (int k = 0; k < p.ksteps; ++k) {
           const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
           const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
           umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
         umma_commit(&sm.tfull[buf]);
+        umma_commit(&sm.uv_empty[u]);
         issued = true;
         ++pt;
       }
@@ -654,6 +704,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
       const bool patched = kPatch && w.patch >= 0;
       const bool rot = p.rotate && t.ch == 0;
+      const bool partial = has_partial_segment(p, w, t);
       int64_t* rdst = sm.row_dst + (it & 1u) * BM;
 
       if (h == 0) {
@@ -661,14 +712,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         const int64_t pos = t.pos0 + r;
         int64_t dst = ROW_SKIP;
         if (pos >= w.dst_pos && pos < w.dst_pos + w.T) {
-          const Segment seg = segment(p, w, t, r / p.seg_rows);
+          const Segment seg = segment(p, w, t, r >> p.seg_shift);
           if (seg.y < 0) {
             if (p.err_flag) atomicOr(p.err_flag, KAMERA_EFLAG_PAGE_OOB);
           } else {
-            dst = seg.full ? ROW_BY_TMA : (int64_t)seg.y + (r % p.seg_rows);
+            dst = seg.full ? ROW_BY_TMA : (int64_t)seg.y + (r & (p.seg_rows - 1));
           }
         }
-        rdst[r] = dst;
+        if (partial) rdst[r] = dst;
       } else if (rot && w.item != table_item[it & 1u]) {
         // tables alternate by tile parity: the previous readers of this one
         // finished before the last joint barrier
@@ -705,17 +756,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&sm.computed[s]);
 
       // rows of partially covered pages: coalesced 16-byte stores by the threads
-      bool partial = false;
-      for (int sg = 0; sg < nseg && !partial; ++sg) {
-        const Segment seg = segment(p, w, t, sg);
-        partial = seg.any && !seg.full && seg.y >= 0;
-      }
       if (partial) {
         named_bar_sync(1, EPI_THREADS);
         const uint32_t tile = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
         uint16_t* dst_base = p.pool[t.ch] + (size_t)t.cb * p.BN;
         for (int q2 = et; q2 < BM * cpr; q2 += EPI_THREADS) {
-          const int row = q2 / cpr, c = q2 % cpr;
+          const int row = q2 / cpr, c = q2 - (q2 / cpr) * cpr;
           const int64_t d = rdst[row];
           if (d < 0) continue;
           const RowView rr{tile + (uint32_t)row * 128u, (uint32_t)row & 7u};

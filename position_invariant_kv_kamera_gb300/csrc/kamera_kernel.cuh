@@ -6,9 +6,10 @@
 //
 //     out = R(delta) . KV(B|empty) + U_m V_m^T        -> bf16 -> paged pool slot
 //
-// Work unit ("tile"): 128 destination positions (aligned to 128 in position
-// space) x BN columns of one (item, layer, channel).  Per CTA (352 threads,
-// one CTA per SM):
+// Work unit ("row block"): 128 destination positions (aligned to 128 in
+// position space) of one (item, layer, channel); it is processed as tiles of
+// BN columns.  CTAs take row blocks round-robin.  Per CTA (384 threads, one
+// CTA per SM):
 //   warp 0      TMA producer: the canonical tile (64-column boxes, 128B
 //               swizzle; from the chunk store, or page by page from the pool
 //               for the in-place modes) and, for patched items, the U tile
@@ -18,6 +19,7 @@
 //               steps): P = U . V^T into an fp32 TMEM accumulator, two buffers.
 //   warp 2      TMA store issuer: whole page segments of the finished tile go
 //               to the pool with cp.async.bulk.tensor stores.
+//   warp 11     TMA producer of the patch factors (U and V tiles).
 //   warps 3-10  epilogue, two warps per TMEM lane quadrant, each half taking
 //               half of the tile's rotation units: tcgen05.ld the patch row,
 //               rotate the key row's RoPE pairs by delta*theta_i (fp64 angle
@@ -117,7 +119,7 @@ struct Walker {
   uint32_t n_tb;
 };
 
-// Tiles of item i (0 if it is skipped); fills the walker's item fields.
+// Row blocks of item i (0 if it is skipped); fills the walker's item fields.
 // Error bits are collected in err (the caller decides whether to report them).
 __device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker& w, int32_t& err) {
   const kamera_reuse_item it = p.items[i];
@@ -154,8 +156,8 @@ __device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker
   }
   if (p.need_patch && w.patch < 0) return 0;
   w.n_tb = (uint32_t)((it.dst_pos + T + BM - 1) / BM - it.dst_pos / BM);
-  const int64_t count = (int64_t)p.num_layers * p.n_ch_work * w.n_tb * p.n_cb;
-  if (count > (int64_t)0xFFFFFFFF) { err |= KAMERA_EFLAG_LEN; return 0; }  // tile decode is 32-bit
+  const int64_t count = (int64_t)p.num_layers * p.n_ch_work * w.n_tb;
+  if (count > (int64_t)0xFFFFFFFF) { err |= KAMERA_EFLAG_LEN; return 0; }  // the decode is 32-bit
   return count;
 }
 
@@ -165,7 +167,7 @@ __device__ __forceinline__ void walker_init(Walker& w) {
   w.count = 0;
 }
 
-// Advance (monotonically) to the item holding global tile g.
+// Advance (monotonically) to the item holding global row block g.
 __device__ __forceinline__ void walk_to(const Params& p, Walker& w, int64_t g) {
   while (g >= w.base + w.count) {
     w.base += w.count;
@@ -180,18 +182,18 @@ struct Tile {
   int64_t pos0;  // destination position of tile row 0
 };
 
-// An item has fewer than 2^32 tiles (checked on the host), so the decode runs in 32 bits.
+// Row block g of the walker's item (order: layer, channel, token block); an
+// item has fewer than 2^32 row blocks, so the decode runs in 32 bits.  The
+// column block is filled in by the caller's inner loop.
 __device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t g) {
-  uint32_t local = (uint32_t)(g - w.base);
+  const uint32_t local = (uint32_t)(g - w.base);
   Tile t;
-  const uint32_t ncb = (uint32_t)p.n_cb;
-  uint32_t q = local / ncb;
-  t.cb = p.cb_first + (int32_t)(local - q * ncb);
-  const uint32_t q2 = q / w.n_tb;
-  const uint32_t tb = q - q2 * w.n_tb;
+  const uint32_t q = local / w.n_tb;
+  const uint32_t tb = local - q * w.n_tb;
   const uint32_t nch = (uint32_t)p.n_ch_work;
-  t.layer = (int32_t)(q2 / nch);
-  t.ch = (int32_t)(q2 - (uint32_t)t.layer * nch);
+  t.layer = (int32_t)(q / nch);
+  t.ch = (int32_t)(q - (uint32_t)t.layer * nch);
+  t.cb = p.cb_first;
   t.pos0 = (w.dst_pos & ~(int64_t)(BM - 1)) + (int64_t)tb * BM;
   return t;
 }
@@ -554,35 +556,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t it = 0;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+      bool go = true;
+      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
         walk_to(p, w, g);
-        const Tile t = decode(p, w, g);
-        const int s = (int)(it % (uint32_t)p.stages);
-        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
-        if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) break;
-        uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
-        const int col0 = t.cb * p.BN;
-        // the transaction byte count first, then the copies
-        uint32_t bytes = 0;
-        if (!p.src_pool) {
-          bytes = (uint32_t)nbox * BOX_BYTES;
-        } else {
-          for (int sg = 0; sg < nseg; ++sg)
-            if (segment(p, w, t, sg).y >= 0) bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
-        }
-        mbar_arrive_expect_tx(&sm.full[s], bytes);
-        if (!p.src_pool) {
-          const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
-          const int64_t y = p.store_off[w.chunk] / p.D;
-          const int32_t row = (int32_t)(y + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
-          for (int b = 0; b < nbox; ++b) tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, row);
-        } else {
+        Tile t = decode(p, w, g);
+        // pool rows of the row block's page segments (in-place source)
+        int32_t seg_y[BM / 8];
+        uint32_t bytes = (uint32_t)nbox * BOX_BYTES;
+        if (p.src_pool) {
+          bytes = 0;
           for (int sg = 0; sg < nseg; ++sg) {
-            const Segment seg = segment(p, w, t, sg);
-            if (seg.y < 0) continue;
+            seg_y[sg] = segment(p, w, t, sg).y;
+            if (seg_y[sg] >= 0) bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
+          }
+        }
+        const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
+        const int32_t src_row =
+            p.src_pool ? 0
+                       : (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
+        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
+          const int s = (int)(it % (uint32_t)p.stages);
+          const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+          if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+          uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+          const int col0 = (p.cb_first + cbi) * p.BN;
+          mbar_arrive_expect_tx(&sm.full[s], bytes);
+          if (!p.src_pool) {
             for (int b = 0; b < nbox; ++b)
-              tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
-                          col0 + b * BOX_COLS, seg.y);
+              tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, src_row);
+          } else {
+            for (int sg = 0; sg < nseg; ++sg) {
+              if (seg_y[sg] < 0) continue;
+              for (int b = 0; b < nbox; ++b)
+                tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
+                            col0 + b * BOX_COLS, seg_y[sg]);
+            }
           }
         }
       }
@@ -601,21 +609,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t pu = 0;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {
+      bool go = true;
+      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
         walk_to(p, w, g);
         if (w.patch < 0) continue;
         const Tile t = decode(p, w, g);
-        const int u = (int)(pu % (uint32_t)p.uv_slots);
-        const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
-        if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) break;
-        uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
-        mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u);
-        const int64_t t0 = t.pos0 - w.dst_pos;
         const int64_t prow = p.patch_off[w.patch] / p.rank +
                              ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
-        tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, (int32_t)(prow + t0), 0);
-        tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0, (int32_t)(prow + w.T + t.cb * p.BN), 0);
-        ++pu;
+        const int32_t u_row = (int32_t)(prow + (t.pos0 - w.dst_pos));
+        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++pu) {
+          const int u = (int)(pu % (uint32_t)p.uv_slots);
+          const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
+          if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+          uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
+          mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u);
+          tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, u_row, 0);
+          tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0,
+                      (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), 0);
+        }
       }
       const uint32_t S = (uint32_t)p.uv_slots;
       for (uint32_t u = 0; u < S && u < pu; ++u) {
@@ -631,26 +642,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t pt = 0;
-      bool issued = false;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {
+      bool issued = false, go = true;
+      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
         walk_to(p, w, g);
         if (w.patch < 0) continue;
-        const int u = (int)(pt % (uint32_t)p.uv_slots);
-        const uint32_t uph = (pt / (uint32_t)p.uv_slots) & 1u;
-        const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
-        if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) break;
-        if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) break;
-        tc_fence_after_sync();
-        const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
-        for (int k = 0; k < p.ksteps; ++k) {
-          const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
-          const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
-          umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++pt) {
+          const int u = (int)(pt % (uint32_t)p.uv_slots);
+          const uint32_t uph = (pt / (uint32_t)p.uv_slots) & 1u;
+          const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
+          if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+          if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) { go = false; break; }
+          tc_fence_after_sync();
+          const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
+          for (int k = 0; k < p.ksteps; ++k) {
+            const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
+            const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+            umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&sm.tfull[buf]);
+          umma_commit(&sm.uv_empty[u]);
+          issued = true;
         }
-        umma_commit(&sm.tfull[buf]);
-        umma_commit(&sm.uv_empty[u]);
-        issued = true;
-        ++pt;
       }
       if (issued) {
         umma_commit(sm.drain);
@@ -663,24 +675,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t it = 0;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+      bool go = true;
+      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
         walk_to(p, w, g);
         const Tile t = decode(p, w, g);
-        const int s = (int)(it % (uint32_t)p.stages);
-        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
-        if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) break;
-        const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
-        const int col0 = t.cb * p.BN;
+        int32_t seg_y[BM / 8];  // pool row of each whole, valid page segment, else -1
         for (int sg = 0; sg < nseg; ++sg) {
           const Segment seg = segment(p, w, t, sg);
-          if (!seg.full || seg.y < 0) continue;
-          for (int b = 0; b < nbox; ++b)
-            tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
-                         col0 + b * BOX_COLS, seg.y);
+          seg_y[sg] = seg.full ? seg.y : -1;
         }
-        bulk_commit_group();
-        bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
-        mbar_arrive(&sm.empty[s]);
+        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
+          const int s = (int)(it % (uint32_t)p.stages);
+          const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+          if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) { go = false; break; }
+          const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+          const int col0 = (p.cb_first + cbi) * p.BN;
+          for (int sg = 0; sg < nseg; ++sg) {
+            if (seg_y[sg] < 0) continue;
+            for (int b = 0; b < nbox; ++b)
+              tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
+                           col0 + b * BOX_COLS, seg_y[sg]);
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
+          mbar_arrive(&sm.empty[s]);
+        }
       }
       bulk_wait_group0();
     }
@@ -696,17 +715,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     Walker w;
     walker_init(w);
     int32_t table_item[2] = {-1, -1};  // item whose phases each table holds
-    uint32_t it = 0, pt = 0;
-    for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+    uint32_t it = 0, pt = 0, rbi = 0;
+    bool ok = true;  // warp-uniform: every wait of this warp so far succeeded
+    for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++rbi) {
       walk_to(p, w, g);
-      const Tile t = decode(p, w, g);
-      const int s = (int)(it % (uint32_t)p.stages);
-      const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+      Tile t = decode(p, w, g);
       const bool patched = kPatch && w.patch >= 0;
       const bool rot = p.rotate && t.ch == 0;
       const bool partial = has_partial_segment(p, w, t);
-      int64_t* rdst = sm.row_dst + (it & 1u) * BM;
-
+      // per-row-block tables alternate by parity: their previous readers
+      // finished before the last joint barrier
+      int64_t* rdst = sm.row_dst + (rbi & 1u) * BM;
+      float2* cs = sm.cs + (rbi & 1u) * MAX_PAIRS;
       if (h == 0) {
         // destination of row r: whole page segments go out by TMA, the rest by threads
         const int64_t pos = t.pos0 + r;
@@ -720,56 +740,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           }
         }
         if (partial) rdst[r] = dst;
-      } else if (rot && w.item != table_item[it & 1u]) {
-        // tables alternate by tile parity: the previous readers of this one
-        // finished before the last joint barrier
-        float2* cs = sm.cs + (it & 1u) * MAX_PAIRS;
+      } else if (rot && w.item != table_item[rbi & 1u]) {
         for (int i = et - 128; i < p.n_pairs; i += 128) cs[i] = phase_cs(w.delta, p.theta[i]);
       }
-      if (rot) table_item[it & 1u] = w.item;
-      const float2* cs = sm.cs + (it & 1u) * MAX_PAIRS;
+      if (rot) table_item[rbi & 1u] = w.item;
+      if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the tables are ready
 
-      // wait for the tile (and its accumulator); decide jointly whether to go on
-      const uint32_t buf = pt & 1u;
-      bool ok = wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag);
-      if (ok && patched) ok = wait_bounded(&sm.tfull[buf], (pt >> 1) & 1u, sm.misc, p.err_flag);
-      if (!named_bar_and(1, EPI_THREADS, ok)) break;
-      if (patched) tc_fence_after_sync();
+      const uint32_t rv_row = (uint32_t)r * 128u;
+      for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
+        t.cb = p.cb_first + cbi;
+        const int s = (int)(it % (uint32_t)p.stages);
+        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        const uint32_t buf = pt & 1u;
+        bool wok = ok && wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag);
+        if (wok && patched) wok = wait_bounded(&sm.tfull[buf], (pt >> 1) & 1u, sm.misc, p.err_flag);
+        ok = __all_sync(0xFFFFFFFFu, wok);
 
-      // compute phase: this thread's row, its half of the units, in place
-      const RowView rv{smem_addr(sm.stages + (size_t)s * p.stage_bytes) + (uint32_t)r * 128u, (uint32_t)r & 7u};
-      const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
-      if (patched) {
-        if (p.frame == KAMERA_PATCH_CANONICAL_FRAME)
-          epi_row<true, true>(p, rv, t.cb, rot, h, taddr, cs);
-        else
-          epi_row<true, false>(p, rv, t.cb, rot, h, taddr, cs);
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tempty[buf]);
-        ++pt;
-      } else if (rot) {
-        epi_row<false, false>(p, rv, t.cb, rot, h, taddr, cs);
-      }
-      fence_proxy_async_smem();  // in-place results -> visible to the TMA store
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.computed[s]);
-
-      // rows of partially covered pages: coalesced 16-byte stores by the threads
-      if (partial) {
-        named_bar_sync(1, EPI_THREADS);
+        // compute phase: this thread's row, its half of the units, in place
         const uint32_t tile = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
-        uint16_t* dst_base = p.pool[t.ch] + (size_t)t.cb * p.BN;
-        for (int q2 = et; q2 < BM * cpr; q2 += EPI_THREADS) {
-          const int row = q2 / cpr, c = q2 - (q2 / cpr) * cpr;
-          const int64_t d = rdst[row];
-          if (d < 0) continue;
-          const RowView rr{tile + (uint32_t)row * 128u, (uint32_t)row & 7u};
-          stg128_cs(dst_base + d * p.D + c * 8, lds128(rr.chunk(c * 8)));
+        if (ok) {
+          const RowView rv{tile + rv_row, (uint32_t)r & 7u};
+          const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
+          if (patched) {
+            tc_fence_after_sync();
+            if (p.frame == KAMERA_PATCH_CANONICAL_FRAME)
+              epi_row<true, true>(p, rv, t.cb, rot, h, taddr, cs);
+            else
+              epi_row<true, false>(p, rv, t.cb, rot, h, taddr, cs);
+          } else if (rot) {
+            epi_row<false, false>(p, rv, t.cb, rot, h, taddr, cs);
+          }
         }
+        if (patched) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+          ++pt;
+        }
+        fence_proxy_async_smem();  // in-place results -> visible to the TMA store
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.computed[s]);
+
+        // rows of partially covered pages: coalesced 16-byte stores by the threads
+        if (partial) {
+          named_bar_sync(1, EPI_THREADS);
+          uint16_t* dst_base = p.pool[t.ch] + (size_t)t.cb * p.BN;
+          if (ok) {
+            for (int q2 = et; q2 < BM * cpr; q2 += EPI_THREADS) {
+              const int row = q2 / cpr, c = q2 - row * cpr;
+              const int64_t d = rdst[row];
+              if (d < 0) continue;
+              const RowView rr{tile + (uint32_t)row * 128u, (uint32_t)row & 7u};
+              stg128_cs(dst_base + d * p.D + c * 8, lds128(rr.chunk(c * 8)));
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
   }
 

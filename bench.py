@@ -152,6 +152,22 @@ def reduce_max(value: float, torch, device) -> float:
     return float(t.item())
 
 
+SCALED = {  # reduced chunk counts, for profiler captures that must stay small
+    "gqa_video": lambda n: W.gqa_video(n_chunks=n),
+    "mla_lite": lambda n: W.mla_lite(n_chunks=n),
+    "sliding_window": lambda n: W.sliding_window(n_resident=n + max(1, n // 8), n_evict=max(1, n // 8)),
+    "long_video": lambda n: W.long_video(n_reorder=n - n // 4, n_recall=n // 4),
+}
+
+
+def rank_workload(name: str, rank: int, world: int, chunks: int = 0) -> W.Workload:
+    """Weak scaling: every rank reuses its own batch of the same shape (its own
+    seed); there is no data exchange between ranks.  chunks > 0 selects a
+    reduced batch of that many chunks (profiling captures only)."""
+    base = SCALED[name](chunks) if chunks and name in SCALED else W.CONFIGS[name]()
+    return base.replace(seed=base.seed + 1000 * rank) if world > 1 else base
+
+
 def aggregate(tokens_per_rank: int, world: int, max_elapsed_s: float, steps: int) -> float:
     """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
     return tokens_per_rank * world * steps / max_elapsed_s
@@ -264,9 +280,7 @@ def run_gpu(args) -> None:
     device = torch.device("cuda", local)
     pk.load()
 
-    base = W.CONFIGS[args.workload]()
-    # weak scaling: every rank reuses its own batch of the same shape
-    wl = base.replace(seed=base.seed + 1000 * rank) if world > 1 else base
+    wl = rank_workload(args.workload, rank, world, args.chunks)
     t = H.device_inputs(wl, torch, device)
     stream = torch.cuda.current_stream(device)
     torch.cuda.synchronize(device)
@@ -319,7 +333,8 @@ def run_gpu(args) -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}"
+                               + (f" [reduced to {args.chunks} chunks]" if args.chunks else ""),
                    "tokens_per_step": wl.tokens, "algorithmic_bytes_per_step": alg_bytes,
                    "patch_flops_per_step": wl.patch_flops(),
                    "l2": "inputs larger than L2 (no flush needed)" if alg_bytes > 4 * 129e6
@@ -343,32 +358,60 @@ def run_gpu(args) -> None:
 
 
 def run_e2e(wl, t, torch, device, stream, steps: int, H) -> dict:
-    """Host-buffer variant: pinned host inputs -> device, call, pool -> host, per step."""
+    """Host-buffer variant through the same public call: every step copies its
+    inputs (canonical chunks, patches, items, block table) from pinned host
+    memory to the device, runs the call, and reads the pool back to pinned
+    host memory.  Two device buffer sets and separate H2D / compute / D2H
+    streams let step i+1's upload and step i-1's download overlap step i."""
     names = [n for n in ("store", "store_off", "store_len", "patch", "patch_off", "patch_len", "items",
                          "block_table") if n in t]
-    host_in = {n: t[n].cpu().pin_memory() for n in names}
     outs = [n for n in ("pool_k", "pool_v") if t.get(n) is not None]
-    host_out = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in outs}
+    host_in = {n: t[n].cpu().pin_memory() for n in names}
+    host_out = [{n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in outs} for _ in range(2)]
+    sets = [t, {**{n: torch.empty_like(t[n]) for n in names + outs}, "err": torch.zeros_like(t["err"])}]
+    sets[1].setdefault("pool_v", None)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+    s_up, s_down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
+    for e in comp_done + down_done:
+        e.record(stream)
 
-    def step():
-        for n in names:
-            t[n].copy_(host_in[n], non_blocking=True)
-        H.call(wl, t, stream=stream)
-        for n in outs:
-            host_out[n].copy_(t[n], non_blocking=True)
+    def step(i):
+        b = i & 1
+        d = sets[b]
+        with torch.cuda.stream(s_up):
+            s_up.wait_event(comp_done[b])   # the call of step i-2 no longer reads these inputs
+            for n in names:
+                d[n].copy_(host_in[n], non_blocking=True)
+        up = torch.cuda.Event()
+        up.record(s_up)
+        stream.wait_event(up)
+        stream.wait_event(down_done[b])     # step i-2's pool has been read back
+        H.call(wl, d, stream=stream)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(comp_done[b])
+            for n in outs:
+                host_out[b][n].copy_(d[n], non_blocking=True)
+        down_done[b].record(s_down)
 
-    step()
+    step(0)
+    step(1)
     torch.cuda.synchronize(device)
-    b = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    b.record(stream)
-    for _ in range(steps):
-        step()
-    e.record(stream)
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    begin.record(s_up)
+    stream.wait_event(begin)
+    s_down.wait_event(begin)
+    for i in range(steps):
+        step(i)
+    end_c = torch.cuda.Event()
+    end_c.record(stream)
+    s_down.wait_event(end_c)
+    end.record(s_down)
     torch.cuda.synchronize(device)
-    return {"elapsed": b.elapsed_time(e) / 1e3, "steps": steps, "h2d": h2d, "d2h": d2h}
+    return {"elapsed": begin.elapsed_time(end) / 1e3, "steps": steps, "h2d": h2d, "d2h": d2h}
 
 
 def reduce_max_time_value(e2e: dict, tokens: int, world: int, torch, device) -> float:
@@ -384,6 +427,8 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="reduced batch of this many chunks (profiler captures); 0 = the full workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,0 +1,168 @@
+"""Full-size parity: the five workload shapes at their real sizes (up to the
+57 GB long-video reorder + recall), launched exactly as the benchmark
+launches them.  Sampled output rows are recomputed one by one by the fp64
+oracle from regenerated inputs; properties that hold at any size (which
+slots are written, sentinel slots untouched, bit-exact copies) are checked
+over the whole pool on the device."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import workloads as W
+from tests import harness as H
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+N_SAMPLES = 160
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def _oracle_model(wl):
+    return oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
+                        wl.pairing, wl.patch_frame)
+
+
+def _slot_rows(wl, item, t):
+    """(page, slot) of token t of an item, by brute force on the block table."""
+    pos = int(item["dst_pos"]) + t
+    return int(wl.block_table[int(item["seq"]), pos // wl.page_size]), pos % wl.page_size
+
+
+def _samples(wl, rng):
+    out = []
+    chans = 1 if wl.mode == "relocate_in_place" else wl.n_ch
+    for _ in range(N_SAMPLES):
+        i = int(rng.integers(0, len(wl.items)))
+        it = wl.items[i]
+        T = int(it["n_tokens"])
+        # bias towards chunk edges (tile and page boundaries)
+        t = int(rng.choice([0, T - 1, int(rng.integers(0, T)), min(T - 1, 127), min(T - 1, 128)]))
+        out.append((i, int(rng.integers(0, wl.num_layers)), int(rng.integers(0, chans)), t))
+    return out
+
+
+def _check_samples(wl, t, pool_init_rows=None):
+    """Oracle rows for sampled (item, layer, channel, token) against the pool."""
+    m = _oracle_model(wl)
+    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    rng = np.random.default_rng(7)
+    for (i, layer, ch, tok) in _samples(wl, rng):
+        it = wl.items[i]
+        page, slot = _slot_rows(wl, it, tok)
+        if wl.mode == "relocate_in_place":
+            src = pool_init_rows(ch, layer, page)[slot]
+        else:
+            src = wl.store_rows(int(it["chunk_id"]), layer, ch, tok, tok + 1)[0]
+        u = v = None
+        if wl.rank and int(it["patch_id"]) >= 0 and wl.mode != "relocate_in_place":
+            u = H.bits_to_f64(wl.u_rows(int(it["patch_id"]), layer, ch, tok, tok + 1)[0])
+            v = H.bits_to_f64(wl.v_rows(int(it["patch_id"]), layer, ch))
+        ref = oracle.row(m, th, ch, int(it["delta"]), H.bits_to_f64(src), u, v,
+                         rotate=wl.mode != "apply_patch")
+        pool = t["pool_k"] if ch == 0 else t["pool_v"]
+        got = H.to_bits(pool[layer, page, slot])
+        ok = H.within_tol(H.bits_to_f64(got), ref)
+        assert ok.all(), (wl.name, i, layer, ch, tok, np.abs(H.bits_to_f64(got) - ref).max())
+        if wl.family == W.MLA and u is None:
+            np.testing.assert_array_equal(got[:wl.latent_dim], src[:wl.latent_dim])
+
+
+def _written_rows_mask(wl):
+    """[num_pages * P] bool: slots that the items cover (same for every layer)."""
+    mask = np.zeros(wl.num_pages * wl.page_size, bool)
+    for it in wl.items:
+        pos = int(it["dst_pos"]) + np.arange(int(it["n_tokens"]))
+        pages = wl.block_table[int(it["seq"]), pos // wl.page_size]
+        mask[pages * wl.page_size + pos % wl.page_size] = True
+    return mask
+
+
+def _check_sentinel_coverage(wl, pool):
+    """Every covered slot fully written (no NaN sentinel left), every other
+    slot still all-sentinel."""
+    bits = pool.view(torch.int16).reshape(wl.num_layers, -1, wl.D)
+    any_sent = (bits == -1).any(dim=-1)
+    all_sent = (bits == -1).all(dim=-1)
+    mask = torch.from_numpy(_written_rows_mask(wl)).to(pool.device)
+    assert not any_sent[:, mask].any().item(), "a covered slot was not (fully) written"
+    assert all_sent[:, ~mask].all().item(), "an uncovered slot was written"
+
+
+def _gather_rows(wl, pool, item):
+    pos = int(item["dst_pos"]) + np.arange(int(item["n_tokens"]))
+    rows = wl.block_table[int(item["seq"]), pos // wl.page_size] * wl.page_size + pos % wl.page_size
+    idx = torch.from_numpy(rows.astype(np.int64)).to(pool.device)
+    return pool.reshape(wl.num_layers, -1, wl.D)[:, idx]
+
+
+def _run(wl):
+    t = H.device_inputs(wl, torch)
+    H.call(wl, t)
+    torch.cuda.synchronize()
+    assert int(t["err"].item()) == 0
+    return t
+
+
+def test_full_tiny_mha():
+    wl = W.tiny_mha()
+    t = _run(wl)
+    _check_sentinel_coverage(wl, t["pool_k"])
+    _check_sentinel_coverage(wl, t["pool_v"])
+    _check_samples(wl, t)
+
+
+def test_full_gqa_video():
+    wl = W.gqa_video()
+    t = _run(wl)
+    _check_sentinel_coverage(wl, t["pool_k"])
+    _check_sentinel_coverage(wl, t["pool_v"])
+    _check_samples(wl, t)
+
+
+@pytest.mark.parametrize("rank", [16, 0])
+def test_full_mla_lite(rank):
+    wl = W.mla_lite(rank=rank)
+    t = _run(wl)
+    _check_sentinel_coverage(wl, t["pool_k"])
+    _check_samples(wl, t)
+    if rank == 0:
+        # c_KV byte for byte, over every reused row of every layer
+        store = t["store"]
+        for it in wl.items:
+            c = int(it["chunk_id"])
+            T = int(it["n_tokens"])
+            src = store[int(wl.store_off[c]):int(wl.store_off[c]) + wl.num_layers * T * wl.D]
+            src = src.view(torch.int16).reshape(wl.num_layers, T, wl.D)[..., :wl.latent_dim]
+            got = _gather_rows(wl, t["pool_k"], it).view(torch.int16)[..., :wl.latent_dim]
+            assert torch.equal(src, got)
+
+
+def test_full_sliding_window():
+    wl = W.sliding_window()
+    t = _run(wl)
+    # V untouched, K of evicted pages untouched: compare with a fresh fill
+    assert torch.equal(t["pool_v"].view(torch.int16), wl.device_pool(torch, 1).view(torch.int16))
+    fresh_k = wl.device_pool(torch, 0)
+    surv = torch.from_numpy(np.unique(wl.block_table[0]).astype(np.int64)).cuda()
+    evicted = torch.ones(wl.num_pages, dtype=torch.bool, device="cuda")
+    evicted[surv] = False
+    assert torch.equal(t["pool_k"][:, evicted].view(torch.int16), fresh_k[:, evicted].view(torch.int16))
+    del fresh_k
+    _check_samples(wl, t, pool_init_rows=wl.pool_rows)
+
+
+def test_full_long_video():
+    wl = W.long_video()
+    t = _run(wl)
+    _check_sentinel_coverage(wl, t["pool_k"])
+    _check_sentinel_coverage(wl, t["pool_v"])
+    _check_samples(wl, t)
+    del t
+    torch.cuda.empty_cache()

@@ -249,9 +249,9 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   int dev = 0;
   DeviceFacts* facts = nullptr;
   if (kamera_status st = device_facts(&dev, &facts)) return st;
-  const int kg_alloc = use_patch ? (rank / 8 < 2 ? 2 : rank / 8) : 0;
-  const int bn_env = env_int("KAMERA_BN"), st_env = env_int("KAMERA_STAGES"), uv_env = env_int("KAMERA_UV_SLOTS");
-  int BN = 0, stages = 0, uv_slots = 0;
+  const int bn_env = env_int("KAMERA_BN"), st_env = env_int("KAMERA_STAGES"), uv_env = env_int("KAMERA_UV_SLOTS"),
+            ks_env = env_int("KAMERA_KSPLIT");
+  int BN = 0, stages = 0, uv_slots = 0, ksplit = 1, kg_alloc = 0;
   uint32_t stage_bytes = 0, uv_slot_bytes = 0;
   const int cands[4] = {256, 192, 128, 64};
   for (int ci = 0; ci < 4 && BN == 0; ++ci) {
@@ -263,25 +263,34 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
       if (p.group_kind[g] > 0 && (g * 32) / bn != ((g + p.group_kind[g]) * 32) / bn) whole = false;
     if (!whole) continue;
     const uint32_t sb = (uint32_t)bn * 256u;
-    const uint32_t ub = use_patch ? (uint32_t)(BM + bn) * kg_alloc * 16u : 0u;
-    // prefer canonical stages (they carry the HBM stream), then a second patch-factor slot
-    for (int s = 4; s >= 2 && BN == 0; --s) {
-      if (st_env && s != st_env) continue;
-      for (int u = use_patch ? 2 : 1; u >= 1 && BN == 0; --u) {
-        if (uv_env && use_patch && u != uv_env) continue;
-        const uint64_t need = (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + smem_extra_bytes(s, u);
-        if (need > (uint64_t)facts->smem_optin) continue;
-        BN = bn;
-        stages = s;
-        uv_slots = use_patch ? u : 0;
-        stage_bytes = sb;
-        uv_slot_bytes = ub;
+    // preference: two patch-factor slots (the factor loads then run ahead of
+    // the MMA), then canonical stages (they carry the HBM stream), then whole
+    // (unsplit) patch factors
+    for (int u = use_patch ? 2 : 1; u >= 1 && BN == 0; --u) {
+      if (uv_env && use_patch && u != uv_env) continue;
+      for (int s = 6; s >= 2 && BN == 0; --s) {
+        if (st_env && s != st_env) continue;
+        for (int ks = 1; ks <= (use_patch ? 4 : 1) && BN == 0; ks *= 2) {
+          if (ks_env && use_patch && ks != ks_env) continue;
+          if (use_patch && (rank / ks) % 16 != 0 && !(ks == 1 && rank == 8)) continue;  // whole K=16 steps
+          const int kg = use_patch ? (rank / 8 / ks < 2 ? 2 : rank / 8 / ks) : 0;
+          const uint32_t ub = use_patch ? (uint32_t)(BM + bn) * kg * 16u : 0u;
+          const uint64_t need = (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + smem_extra_bytes(s, u, n_pairs);
+          if (need > (uint64_t)facts->smem_optin) continue;
+          BN = bn;
+          stages = s;
+          uv_slots = use_patch ? u : 0;
+          ksplit = use_patch ? ks : 1;
+          kg_alloc = kg;
+          stage_bytes = sb;
+          uv_slot_bytes = ub;
+        }
       }
     }
   }
   if (BN == 0) return fail(KAMERA_ERR_UNSUPPORTED, "no tile shape fits D = %d, rank %d", D, rank);
   const uint32_t smem = (uint32_t)stages * stage_bytes + (uint32_t)uv_slots * uv_slot_bytes +
-                        smem_extra_bytes(stages, uv_slots);
+                        smem_extra_bytes(stages, uv_slots, n_pairs);
 
   // ---- parameters ------------------------------------------------------------------------------------
   p.items = items;
@@ -290,7 +299,8 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   p.has_patches = use_patch ? 1 : 0;
   p.need_patch = mode == MODE_PATCH_IN_PLACE ? 1 : 0;
   p.rank = rank;
-  p.ksteps = (rank + 15) / 16;
+  p.ksplit = ksplit;
+  p.ksteps = (rank / ksplit + 15) / 16;
   p.kg_alloc = kg_alloc;
   p.pool[0] = static_cast<uint16_t*>(pool->k);
   p.pool[1] = static_cast<uint16_t*>(pool->v);
@@ -355,6 +365,10 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
       if (kamera_status st = encode(&p.pool_map[ch], ch == 0 ? pool->k : pool->v, 2, dims, strides, box,
                                     CU_TENSOR_MAP_SWIZZLE_128B, "pool"))
         return st;
+      const cuuint32_t box8[2] = {(cuuint32_t)BOX_COLS, 8u};
+      if (kamera_status st = encode(&p.pool_map8[ch], ch == 0 ? pool->k : pool->v, 2, dims, strides, box8,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, "pool (8-row boxes)"))
+        return st;
     }
   }
   if (use_patch) {
@@ -364,8 +378,8 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     p.n_patches = patches->n_patches;
     const cuuint64_t dims[3] = {8, (cuuint64_t)(patch_rows > 0 ? patch_rows : 1), (cuuint64_t)(rank / 8)};
     const cuuint64_t strides[2] = {(cuuint64_t)rank * 2, 16};
-    const cuuint32_t ubox[3] = {8, (cuuint32_t)BM, (cuuint32_t)(rank / 8)};
-    const cuuint32_t vbox[3] = {8, (cuuint32_t)BN, (cuuint32_t)(rank / 8)};
+    const cuuint32_t ubox[3] = {8, (cuuint32_t)BM, (cuuint32_t)(rank / 8 / ksplit)};
+    const cuuint32_t vbox[3] = {8, (cuuint32_t)BN, (cuuint32_t)(rank / 8 / ksplit)};
     if (kamera_status st = encode(&p.u_map, patches->data, 3, dims, strides, ubox, CU_TENSOR_MAP_SWIZZLE_NONE, "U"))
       return st;
     if (kamera_status st = encode(&p.v_map, patches->data, 3, dims, strides, vbox, CU_TENSOR_MAP_SWIZZLE_NONE, "V"))

@@ -18,13 +18,15 @@
 //   warp 1      owns TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16
 //               steps): P = U . V^T into an fp32 TMEM accumulator, two buffers.
 //   warp 2      TMA store issuer: whole page segments of the finished tile go
-//               to the pool with cp.async.bulk.tensor stores.
+//               to the pool with cp.async.bulk.tensor stores (8-row boxes for
+//               the in-item part of partly covered pages).
 //   warp 11     TMA producer of the patch factors (U and V tiles).
 //   warps 3-10  epilogue, two warps per TMEM lane quadrant, each half taking
 //               half of the tile's rotation units: tcgen05.ld the patch row,
 //               rotate the key row's RoPE pairs by delta*theta_i (fp64 angle
 //               reduction, fp32 sincos and math), add, round to bf16 in place;
-//               rows of partially covered pages are stored by these threads.
+//               the few edge rows of partly covered pages that do not fill an
+//               8-row box are stored by their own threads.
 // Every wait on an mbarrier is bounded (about 2 s): on expiry the kernel sets
 // KAMERA_EFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -55,15 +57,12 @@ constexpr int8_t GK_PLAIN = 0;
 constexpr int8_t GK_SECOND = -1;
 constexpr int8_t GK_INTERLEAVED = -2;
 
-// row_dst markers
-constexpr int64_t ROW_SKIP = -1;     // not stored (outside the item, or an invalid page)
-constexpr int64_t ROW_BY_TMA = -2;   // stored by the TMA store of its full page segment
-
 struct Params {
   CUtensorMap src_map;      // chunk store as rows [rows][D]: box 64 x 128, 128B swizzle
   CUtensorMap pool_map[2];  // pool K / V as rows [L*pages*P][D]: box 64 x S (S = min(P,128)), 128B swizzle
-  CUtensorMap u_map;        // patch store as (8, rows, m/8): box (8, 128, m/8)
-  CUtensorMap v_map;        // patch store as (8, rows, m/8): box (8, BN, m/8)
+  CUtensorMap pool_map8[2]; // the same with 8-row boxes, for partly covered page segments
+  CUtensorMap u_map;        // patch store as (8, rows, m/8): box (8, 128, m/8/ksplit)
+  CUtensorMap v_map;        // patch store as (8, rows, m/8): box (8, BN, m/8/ksplit)
   const kamera_reuse_item* items;
   int32_t n_items;
   int32_t src_pool;  // 0: gather from the chunk store, 1: in place from the pool
@@ -77,8 +76,9 @@ struct Params {
   int64_t patch_elems;
   int32_t n_patches;
   int32_t rank;
-  int32_t ksteps;      // ceil(rank / 16)
-  int32_t kg_alloc;    // 8-element K groups held in smem per operand row (>= 2)
+  int32_t ksplit;      // patch factors staged in this many K chunks per tile
+  int32_t ksteps;      // K=16 MMA steps per chunk: ceil(rank / ksplit / 16)
+  int32_t kg_alloc;    // 8-element K groups held in smem per operand row and chunk (>= 2)
   int32_t need_patch;  // items without a patch have no work (patch-only mode)
   uint16_t* pool[2];
   int64_t num_pages;
@@ -198,16 +198,6 @@ __device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t
   return t;
 }
 
-// Does the tile hold rows of a page segment that the item only partly covers?
-// (Only the segments holding the item's first and last rows can be partial.)
-__device__ __forceinline__ bool has_partial_segment(const Params& p, const Walker& w, const Tile& t) {
-  const int64_t end = w.dst_pos + w.T;
-  const int64_t m = p.seg_rows - 1;
-  const bool head = (w.dst_pos & m) != 0 && w.dst_pos >= t.pos0 && w.dst_pos < t.pos0 + BM;
-  const bool tail = (end & m) != 0 && end - 1 >= t.pos0 && end - 1 < t.pos0 + BM;
-  return head || tail;
-}
-
 // A page segment of a tile (rows [sg*S, sg*S + S)): its pool row, or -1 when
 // its page is out of range.  `full` = every row of the segment belongs to the item.
 struct Segment {
@@ -250,8 +240,7 @@ struct Smem {
   uint64_t* tempty;    // [2] accumulator drained
   uint64_t* drain;     // [1]
   SmemMisc* misc;
-  float2* cs;        // [2][MAX_PAIRS] (cos, sin) tables, one per tile parity
-  int64_t* row_dst;  // [2][BM] destination row for the thread-store path, or ROW_SKIP / ROW_BY_TMA
+  float2* cs;        // [2][n_pairs_pad] (cos, sin) tables, one per row-block parity
 };
 
 __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
@@ -272,13 +261,15 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
   s.misc = reinterpret_cast<SmemMisc*>(s.drain + 1);
   const uintptr_t cs_at = (reinterpret_cast<uintptr_t>(s.misc) + 32 + 15) & ~uintptr_t(15);
   s.cs = reinterpret_cast<float2*>(cs_at);
-  s.row_dst = reinterpret_cast<int64_t*>(s.cs + 2 * MAX_PAIRS);
   return s;
 }
 
-__host__ __device__ constexpr uint32_t smem_extra_bytes(int stages, int uv_slots) {
-  return 1024 /*alignment slack*/ + 8u * (3u * stages + 2u * uv_slots + 5u) + 32u + 16u + 8u * 2u * MAX_PAIRS +
-         8u * 2u * BM;
+// rows of one phase table: the rope pairs, rounded up to a float4 multiple
+__host__ __device__ constexpr int pairs_pad(int n_pairs) { return (n_pairs + 1) & ~1; }
+
+__host__ __device__ constexpr uint32_t smem_extra_bytes(int stages, int uv_slots, int n_pairs) {
+  return 1024 /*alignment slack*/ + 8u * (3u * stages + 2u * uv_slots + 5u) + 32u + 16u +
+         8u * 2u * (uint32_t)pairs_pad(n_pairs);
 }
 
 // Bounded wait.  Returns false on abort (another role gave up) or on expiry
@@ -344,11 +335,31 @@ struct RowView {
   }
 };
 
-// 16 columns without rotation: out = x + P (patched), written in place.
-__device__ __forceinline__ void epi_plain16(const RowView& rv, int c0, uint32_t taddr) {
+// Results of 16 columns at tile column c: back into the tile (for the TMA
+// store) and, for rows of partly covered pages, straight to the pool row.
+__device__ __forceinline__ void put16(uint32_t a0, uint32_t a1, uint4 v0, uint4 v1, uint16_t* gdst, int c) {
+  sts128(a0, v0);
+  sts128(a1, v1);
+  if (gdst) {
+    stg128_cs(gdst + c, v0);
+    stg128_cs(gdst + c + 8, v1);
+  }
+}
+
+// 16 columns without rotation: out = x + P (patched); without a patch the
+// tile already holds the output and only a thread-stored row is copied out.
+template <bool kPatched>
+__device__ __forceinline__ void epi_plain16(const RowView& rv, int c0, uint32_t taddr, uint16_t* gdst) {
+  const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
+  if (!kPatched) {
+    if (gdst) {
+      stg128_cs(gdst + c0, lds128(a0));
+      stg128_cs(gdst + c0 + 8, lds128(a1));
+    }
+    return;
+  }
   uint32_t acc[16];
   tmem_ld16(taddr + (uint32_t)c0, acc);
-  const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
   const uint4 v0 = lds128(a0), v1 = lds128(a1);
   tmem_ld_wait();
   float x[16];
@@ -356,14 +367,13 @@ __device__ __forceinline__ void epi_plain16(const RowView& rv, int c0, uint32_t 
   unpack8(v1, x + 8);
 #pragma unroll
   for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(acc[e]);
-  sts128(a0, pack8(x));
-  sts128(a1, pack8(x + 8));
+  put16(a0, a1, pack8(x), pack8(x + 8), gdst, c0);
 }
 
 // 16 rotate-half pairs (cA + e, cB + e), pair index pb + e.
 template <bool kPatched, bool kCanonicalFrame>
 __device__ __forceinline__ void epi_rotate16(const RowView& rv, int cA, int cB, int pb, uint32_t taddr,
-                                             const float2* cs) {
+                                             const float2* cs, uint16_t* gdst) {
   uint32_t accA[16], accB[16];
   if (kPatched) {
     tmem_ld16(taddr + (uint32_t)cA, accA);
@@ -400,16 +410,14 @@ __device__ __forceinline__ void epi_rotate16(const RowView& rv, int cA, int cB, 
       xb[e] = rb;
     }
   }
-  sts128(a0, pack8(xa));
-  sts128(a1, pack8(xa + 8));
-  sts128(b0, pack8(xb));
-  sts128(b1, pack8(xb + 8));
+  put16(a0, a1, pack8(xa), pack8(xa + 8), gdst, cA);
+  put16(b0, b1, pack8(xb), pack8(xb + 8), gdst, cB);
 }
 
 // 8 interleaved pairs (2e, 2e+1) in 16 columns, pair index pb + e.
 template <bool kPatched, bool kCanonicalFrame>
 __device__ __forceinline__ void epi_interleaved16(const RowView& rv, int c0, int pb, uint32_t taddr,
-                                                  const float2* cs) {
+                                                  const float2* cs, uint16_t* gdst) {
   uint32_t acc[16];
   if (kPatched) tmem_ld16(taddr + (uint32_t)c0, acc);
   const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
@@ -441,14 +449,16 @@ __device__ __forceinline__ void epi_interleaved16(const RowView& rv, int c0, int
       x[2 * e + 1] = rb;
     }
   }
-  sts128(a0, pack8(x));
-  sts128(a1, pack8(x + 8));
+  put16(a0, a1, pack8(x), pack8(x + 8), gdst, c0);
 }
 
-// One tile row's share of the compute phase for epilogue half h.
+// One tile row's share of the compute phase for epilogue half h.  gdst: the
+// pool row (at the tile's first column) when this row is stored by its
+// threads, else nullptr.
 template <bool kPatched, bool kCanonicalFrame>
 __device__ __forceinline__ void epi_row(const Params& p, const RowView& rv, int cb, bool rot, int h, uint32_t taddr,
-                                        const float2* cs) {
+                                        const float2* cs, uint16_t* gdst) {
+  if (!kPatched && !rot && !gdst) return;  // bit copy of the whole tile: nothing to do
   const int ng = p.BN / 32;
   const int g0 = cb * ng;
   for (int gl = 0; gl < ng; ++gl) {
@@ -459,19 +469,17 @@ __device__ __forceinline__ void epi_row(const Params& p, const RowView& rv, int 
     if (owner != h) continue;
     const int c0 = gl * 32;
     if (kind == GK_PLAIN) {
-      if (kPatched) {
-        epi_plain16(rv, c0, taddr);
-        epi_plain16(rv, c0 + 16, taddr);
-      }
+      epi_plain16<kPatched>(rv, c0, taddr, gdst);
+      epi_plain16<kPatched>(rv, c0 + 16, taddr, gdst);
     } else if (kind == GK_INTERLEAVED) {
       const int pb = p.pair_base[g];
-      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0, pb, taddr, cs);
-      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0 + 16, pb + 8, taddr, cs);
+      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0, pb, taddr, cs, gdst);
+      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0 + 16, pb + 8, taddr, cs, gdst);
     } else {
       const int pb = p.pair_base[g];
       const int cB = (gl + kind) * 32;
-      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0, cB, pb, taddr, cs);
-      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0 + 16, cB + 16, pb + 16, taddr, cs);
+      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0, cB, pb, taddr, cs, gdst);
+      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0 + 16, cB + 16, pb + 16, taddr, cs, gdst);
     }
   }
 }
@@ -506,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   }
   if (kPatch) {
     // K groups the MMA reads but TMA never writes (rank 8 pads K to 16) stay zero
-    const int kg_load = p.rank / 8;
+    const int kg_load = p.rank / 8 / p.ksplit;  // K groups a chunk's TMA box writes
     for (int u = 0; u < p.uv_slots; ++u) {
       uint8_t* slot = sm.uv + (size_t)u * (p.u_bytes + p.v_bytes);
       const uint32_t u_pad = (uint32_t)(p.kg_alloc - kg_load) * BM * 16u;
@@ -617,15 +625,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         const int64_t prow = p.patch_off[w.patch] / p.rank +
                              ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
         const int32_t u_row = (int32_t)(prow + (t.pos0 - w.dst_pos));
-        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++pu) {
-          const int u = (int)(pu % (uint32_t)p.uv_slots);
-          const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
-          if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-          uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
-          mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)p.rank * 2u);
-          tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, u_row, 0);
-          tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0,
-                      (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), 0);
+        const int kg_chunk = p.rank / 8 / p.ksplit;  // K groups per chunk
+        for (int cbi = 0; cbi < p.n_cb && go; ++cbi) {
+          for (int kc = 0; kc < p.ksplit; ++kc, ++pu) {
+            const int u = (int)(pu % (uint32_t)p.uv_slots);
+            const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
+            if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+            uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
+            mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
+            tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, u_row, kc * kg_chunk);
+            tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0,
+                        (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), kc * kg_chunk);
+          }
         }
       }
       const uint32_t S = (uint32_t)p.uv_slots;
@@ -641,27 +652,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       const uint32_t lbo_u = BM * 16u, lbo_v = (uint32_t)p.BN * 16u;
       Walker w;
       walker_init(w);
-      uint32_t pt = 0;
+      uint32_t pt = 0, pc = 0;  // patched tiles, patch-factor chunks
       bool issued = false, go = true;
       for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
         walk_to(p, w, g);
         if (w.patch < 0) continue;
-        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++pt) {
-          const int u = (int)(pt % (uint32_t)p.uv_slots);
-          const uint32_t uph = (pt / (uint32_t)p.uv_slots) & 1u;
+        for (int cbi = 0; cbi < p.n_cb && go; ++cbi, ++pt) {
           const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
           if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-          if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) { go = false; break; }
-          tc_fence_after_sync();
-          const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
-          for (int k = 0; k < p.ksteps; ++k) {
-            const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
-            const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
-            umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+          for (int kc = 0; kc < p.ksplit; ++kc, ++pc) {
+            const int u = (int)(pc % (uint32_t)p.uv_slots);
+            const uint32_t uph = (pc / (uint32_t)p.uv_slots) & 1u;
+            if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) { go = false; break; }
+            tc_fence_after_sync();
+            const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
+            for (int k = 0; k < p.ksteps; ++k) {
+              const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
+              const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+              umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(&sm.uv_empty[u]);
+            issued = true;
           }
+          if (!go) break;
           umma_commit(&sm.tfull[buf]);
-          umma_commit(&sm.uv_empty[u]);
-          issued = true;
         }
       }
       if (issued) {
@@ -679,10 +693,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
         walk_to(p, w, g);
         const Tile t = decode(p, w, g);
-        int32_t seg_y[BM / 8];  // pool row of each whole, valid page segment, else -1
+        int32_t seg_y[BM / 8];  // pool row of each valid page segment, else -1
+        bool seg_full[BM / 8];
+        int lo8 = 0, hi8 = 0;   // 8-row sub-blocks of the row block inside the item: [lo8, hi8)
+        {
+          const int64_t a = w.dst_pos - t.pos0, b = w.dst_pos + w.T - t.pos0;
+          lo8 = a <= 0 ? 0 : (int)((a + 7) >> 3);
+          hi8 = b >= BM ? BM / 8 : (int)(b >> 3);
+        }
         for (int sg = 0; sg < nseg; ++sg) {
           const Segment seg = segment(p, w, t, sg);
-          seg_y[sg] = seg.full ? seg.y : -1;
+          seg_y[sg] = seg.y;
+          seg_full[sg] = seg.full;
         }
         for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
           const int s = (int)(it % (uint32_t)p.stages);
@@ -692,9 +714,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           const int col0 = (p.cb_first + cbi) * p.BN;
           for (int sg = 0; sg < nseg; ++sg) {
             if (seg_y[sg] < 0) continue;
-            for (int b = 0; b < nbox; ++b)
-              tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
-                           col0 + b * BOX_COLS, seg_y[sg]);
+            if (seg_full[sg]) {
+              for (int b = 0; b < nbox; ++b)
+                tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
+                             col0 + b * BOX_COLS, seg_y[sg]);
+              continue;
+            }
+            // partly covered page: its 8-row sub-blocks that lie inside the item
+            const int r0 = sg * p.seg_rows;
+            for (int k8 = r0 >> 3; k8 < ((r0 + p.seg_rows) >> 3); ++k8) {
+              if (k8 < lo8 || k8 >= hi8) continue;
+              for (int b = 0; b < nbox; ++b)
+                tma_store_2d(&p.pool_map8[t.ch], st + b * BOX_BYTES + (uint32_t)k8 * 1024u, col0 + b * BOX_COLS,
+                             seg_y[sg] + (k8 * 8 - r0));
+            }
           }
           bulk_commit_group();
           bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
@@ -708,10 +741,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     const int e = warp - EPI_WARP0;      // 0..7
     const int h = e >> 2;                // column half
     const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int r = q * 32 + lane;         // tile row owned in the compute phase
+    const int r = q * 32 + lane;         // tile row owned by this thread
     const int et = threadIdx.x - EPI_WARP0 * 32;  // 0..255
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    const int cpr = p.BN / 8;            // 16-byte chunks per tile row
     Walker w;
     walker_init(w);
     int32_t table_item[2] = {-1, -1};  // item whose phases each table holds
@@ -722,31 +754,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Tile t = decode(p, w, g);
       const bool patched = kPatch && w.patch >= 0;
       const bool rot = p.rotate && t.ch == 0;
-      const bool partial = has_partial_segment(p, w, t);
-      // per-row-block tables alternate by parity: their previous readers
-      // finished before the last joint barrier
-      int64_t* rdst = sm.row_dst + (rbi & 1u) * BM;
-      float2* cs = sm.cs + (rbi & 1u) * MAX_PAIRS;
-      if (h == 0) {
-        // destination of row r: whole page segments go out by TMA, the rest by threads
+      // destination of row r: rows of whole page segments go out with the TMA
+      // store; rows of partly covered pages are stored by their own threads
+      int64_t dst = -1;
+      {
         const int64_t pos = t.pos0 + r;
-        int64_t dst = ROW_SKIP;
         if (pos >= w.dst_pos && pos < w.dst_pos + w.T) {
           const Segment seg = segment(p, w, t, r >> p.seg_shift);
           if (seg.y < 0) {
-            if (p.err_flag) atomicOr(p.err_flag, KAMERA_EFLAG_PAGE_OOB);
-          } else {
-            dst = seg.full ? ROW_BY_TMA : (int64_t)seg.y + (r & (p.seg_rows - 1));
+            if (h == 0 && p.err_flag) atomicOr(p.err_flag, KAMERA_EFLAG_PAGE_OOB);
+          } else if (!seg.full) {
+            // an 8-row sub-block wholly inside the item goes out by TMA too
+            const int k8 = r >> 3;
+            const bool block_in = t.pos0 + k8 * 8 >= w.dst_pos && t.pos0 + k8 * 8 + 8 <= w.dst_pos + w.T;
+            if (!block_in) dst = (int64_t)seg.y + (r & (p.seg_rows - 1));
           }
         }
-        if (partial) rdst[r] = dst;
-      } else if (rot && w.item != table_item[rbi & 1u]) {
-        for (int i = et - 128; i < p.n_pairs; i += 128) cs[i] = phase_cs(w.delta, p.theta[i]);
       }
+      // phase tables alternate by row-block parity: their previous readers
+      // finished before the last joint barrier
+      float2* cs = sm.cs + (rbi & 1u) * pairs_pad(p.n_pairs);
+      if (h == 1 && rot && w.item != table_item[rbi & 1u])
+        for (int i = et - 128; i < p.n_pairs; i += 128) cs[i] = phase_cs(w.delta, p.theta[i]);
       if (rot) table_item[rbi & 1u] = w.item;
-      if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the tables are ready
+      if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the table is ready
 
-      const uint32_t rv_row = (uint32_t)r * 128u;
       for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
         t.cb = p.cb_first + cbi;
         const int s = (int)(it % (uint32_t)p.stages);
@@ -757,18 +789,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         ok = __all_sync(0xFFFFFFFFu, wok);
 
         // compute phase: this thread's row, its half of the units, in place
-        const uint32_t tile = smem_addr(sm.stages + (size_t)s * p.stage_bytes);
         if (ok) {
-          const RowView rv{tile + rv_row, (uint32_t)r & 7u};
+          const RowView rv{smem_addr(sm.stages + (size_t)s * p.stage_bytes) + (uint32_t)r * 128u, (uint32_t)r & 7u};
           const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
+          uint16_t* gdst = dst >= 0 ? p.pool[t.ch] + dst * p.D + (int64_t)t.cb * p.BN : nullptr;
           if (patched) {
             tc_fence_after_sync();
             if (p.frame == KAMERA_PATCH_CANONICAL_FRAME)
-              epi_row<true, true>(p, rv, t.cb, rot, h, taddr, cs);
+              epi_row<true, true>(p, rv, t.cb, rot, h, taddr, cs, gdst);
             else
-              epi_row<true, false>(p, rv, t.cb, rot, h, taddr, cs);
-          } else if (rot) {
-            epi_row<false, false>(p, rv, t.cb, rot, h, taddr, cs);
+              epi_row<true, false>(p, rv, t.cb, rot, h, taddr, cs, gdst);
+          } else {
+            epi_row<false, false>(p, rv, t.cb, rot, h, taddr, cs, gdst);
           }
         }
         if (patched) {
@@ -779,24 +811,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         }
         fence_proxy_async_smem();  // in-place results -> visible to the TMA store
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.computed[s]);
-
-        // rows of partially covered pages: coalesced 16-byte stores by the threads
-        if (partial) {
-          named_bar_sync(1, EPI_THREADS);
-          uint16_t* dst_base = p.pool[t.ch] + (size_t)t.cb * p.BN;
-          if (ok) {
-            for (int q2 = et; q2 < BM * cpr; q2 += EPI_THREADS) {
-              const int row = q2 / cpr, c = q2 - row * cpr;
-              const int64_t d = rdst[row];
-              if (d < 0) continue;
-              const RowView rr{tile + (uint32_t)row * 128u, (uint32_t)row & 7u};
-              stg128_cs(dst_base + d * p.D + c * 8, lds128(rr.chunk(c * 8)));
-            }
-          }
+        if (lane == 0) {
+          mbar_arrive(&sm.computed[s]);
+          mbar_arrive(&sm.empty[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
       }
     }
   }

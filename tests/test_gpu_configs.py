@@ -1,0 +1,75 @@
+"""Every launch configuration gives the same bits.  The arithmetic of each
+output element does not depend on the tile width, the number of stages or
+patch-factor slots, or on staging the patch factors in K chunks (the MMA
+accumulates the same K=16 steps in the same order), so the pools must be
+bit-identical across them -- and equal to the oracle within tolerance."""
+import os
+
+import numpy as np
+import pytest
+
+from synth import workloads as W
+from tests import harness as H
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [
+    {},
+    {"KAMERA_BN": "128"},
+    {"KAMERA_STAGES": "2"},
+    {"KAMERA_STAGES": "2", "KAMERA_UV_SLOTS": "1"},
+    {"KAMERA_KSPLIT": "2"},
+    {"KAMERA_KSPLIT": "4", "KAMERA_UV_SLOTS": "2"},
+    {"KAMERA_BN": "64", "KAMERA_STAGES": "5"},
+]
+KEYS = ("KAMERA_BN", "KAMERA_STAGES", "KAMERA_UV_SLOTS", "KAMERA_KSPLIT")
+
+WORKLOADS = {
+    "gqa_r64": lambda: W.gqa_video(num_layers=2, n_chunks=3, T=300, rank=64, page_size=16),
+    "gqa_r32_p64": lambda: W.gqa_video(num_layers=2, n_chunks=3, T=1100, rank=32, page_size=64),
+    "mla_r16": lambda: W.mla_lite(num_layers=2, n_chunks=2, T=500, rank=16),
+    "long_video_small": lambda: W.long_video(num_layers=2, n_reorder=5, n_recall=2, T=1296, rank=64),
+    "sliding": lambda: W.sliding_window(num_layers=2, n_resident=5, n_evict=1, T=256, page_size=64,
+                                        num_kv_heads=4),
+}
+
+
+@pytest.fixture(autouse=True)
+def _clean_env():
+    saved = {k: os.environ.pop(k, None) for k in KEYS}
+    yield
+    for k, v in saved.items():
+        os.environ.pop(k, None)
+        if v is not None:
+            os.environ[k] = v
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_all_launch_configurations_agree_bitwise(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    wl = WORKLOADS[name]()
+    pool = (wl.host_pool(0), wl.host_pool(1) if wl.n_ch == 2 else None)
+    results = []
+    for cfg in CONFIGS:
+        for k in KEYS:
+            os.environ.pop(k, None)
+        os.environ.update(cfg)
+        t = H.device_inputs(wl, torch, pool_host=pool)
+        st = H.call(wl, t, raise_on_error=False)
+        if st != 0:  # a forced shape that does not fit this workload
+            continue
+        torch.cuda.synchronize()
+        assert int(t["err"].item()) == 0, cfg
+        results.append((cfg, H.to_bits(t["pool_k"]), H.to_bits(t["pool_v"]) if wl.n_ch == 2 else None))
+    assert len(results) >= 3
+    base = results[0]
+    for cfg, k, v in results[1:]:
+        np.testing.assert_array_equal(k, base[1], err_msg=str(cfg))
+        if v is not None:
+            np.testing.assert_array_equal(v, base[2], err_msg=str(cfg))
+    err, ref_k, ref_v, wk, wv = H.oracle_reference(wl, pool[0], pool[1])
+    H.assert_report(H.compare_pool(base[1], pool[0], ref_k, wk))
+    if wl.n_ch == 2:
+        H.assert_report(H.compare_pool(base[2], pool[1], ref_v, wv))

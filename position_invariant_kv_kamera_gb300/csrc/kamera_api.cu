@@ -398,12 +398,21 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
       set = true;
     }
   }
-  const dim3 grid((unsigned)facts->sms), block(NUM_THREADS);
-  if (use_patch)
-    reuse_kernel<true><<<grid, block, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  else
-    reuse_kernel<false><<<grid, block, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // Programmatic dependent launch: this grid may be scheduled while the
+  // previous kernel on the stream drains; the kernel waits for it
+  // (griddepcontrol.wait) before touching global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)facts->sms);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = env_int("KAMERA_NO_PDL") ? 0 : 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = use_patch ? cudaLaunchKernelEx(&cfg, reuse_kernel<true>, p) : cudaLaunchKernelEx(&cfg, reuse_kernel<false>, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   return KAMERA_OK;
 }

@@ -494,6 +494,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
 
   // ---- set-up -------------------------------------------------------------------------------
+  // A dependent launch may start its prologue now; everything this kernel
+  // reads or writes in global memory comes after griddepcontrol.wait below.
+  grid_launch_dependents();
+  grid_dependency_wait();
+  if (warp == 0) {
+    // total row-block count: lanes split the items; only CTA 0 reports item-level errors
+    int64_t n = 0;
+    int32_t err = 0;
+    Walker w;
+    for (int32_t i = lane; i < p.n_items; i += 32) n += item_tiles(p, i, w, err);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+      err |= __shfl_xor_sync(0xFFFFFFFFu, err, o);
+    }
+    if (lane == 0) {
+      sm.misc->total_tiles = n;
+      if (blockIdx.x == 0 && err && p.err_flag) atomicOr(p.err_flag, err);
+    }
+  }
+  __syncthreads();
+  if ((int64_t)blockIdx.x >= sm.misc->total_tiles) return;  // no row block for this CTA
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -530,22 +553,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     if (warp == 1) {
       tmem_alloc(&sm.misc->tmem_base, p.tmem_cols);
       tmem_relinquish();
-    }
-  }
-  if (warp == 0) {
-    // total tile count: lanes split the items; only CTA 0 reports item-level errors
-    int64_t n = 0;
-    int32_t err = 0;
-    Walker w;
-    for (int32_t i = lane; i < p.n_items; i += 32) n += item_tiles(p, i, w, err);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
-      err |= __shfl_xor_sync(0xFFFFFFFFu, err, o);
-    }
-    if (lane == 0) {
-      sm.misc->total_tiles = n;
-      if (blockIdx.x == 0 && err && p.err_flag) atomicOr(p.err_flag, err);
     }
   }
   tc_fence_before_sync();

@@ -45,6 +45,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// ---- programmatic dependent launch -------------------------------------------------------
+// wait until the grids this launch depends on have completed and their memory is visible
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// allow a dependent launch to start (its own griddepcontrol.wait still orders its memory use)
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---- proxy fences -------------------------------------------------------------------
 // generic-proxy writes to shared memory -> visible to the async proxy (TMA, tcgen05)
 __device__ __forceinline__ void fence_proxy_async_smem() {

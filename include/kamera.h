@@ -58,7 +58,7 @@ extern "C" {
 /* The CUDA stream type (cudaStream_t), declared without the CUDA headers. */
 typedef struct CUstream_st* kamera_stream_t;
 
-#define KAMERA_ABI_VERSION 1
+#define KAMERA_ABI_VERSION 2
 
 typedef enum {
   KAMERA_OK = 0,
@@ -99,6 +99,14 @@ typedef struct {
   int32_t patch_frame;    /* kamera_patch_frame */
   double rope_base;       /* theta_i = rope_base^(-2i/rope_dim) when inv_freq is NULL */
   const double* inv_freq; /* host, [rope_dim/2] explicit theta_i table, or NULL */
+  /* Multimodal RoPE (M-RoPE): the rope pairs split into consecutive temporal /
+   * height / width sections, each turned by its own position component.
+   * rope_sections = pairs per section, summing to rope_dim/2; all 0 = one
+   * section (plain RoPE). */
+  int32_t rope_sections[3];
+  int32_t reserved0;            /* 0 */
+  const int64_t* section_delta; /* device [n_items][3], per call: each item's shift of each section;
+                                   NULL = every section takes the item's delta */
 } kamera_model_desc;
 
 /* Canonical chunk store: KV(B|empty) of every chunk (device memory). */

@@ -42,6 +42,7 @@ class Model(ctypes.Structure):
         ("latent_dim", ctypes.c_int32),
         ("pairing", ctypes.c_int32),
         ("patch_frame", ctypes.c_int32),
+        ("sections", ctypes.c_int32 * 3),
     ]
 
 
@@ -89,14 +90,16 @@ def _declare(lib):
     lib.oracle_theta.restype = None
     lib.oracle_rotate_region.argtypes = [P, i32, P, i64, i32]
     lib.oracle_rotate_region.restype = None
-    lib.oracle_rotate_row.argtypes = [ctypes.POINTER(Model), P, i32, i64, P]
+    lib.oracle_rotate_region_sections.argtypes = [P, i32, P, P, P, i32]
+    lib.oracle_rotate_region_sections.restype = None
+    lib.oracle_rotate_row.argtypes = [ctypes.POINTER(Model), P, i32, P, P]
     lib.oracle_rotate_row.restype = None
-    lib.oracle_row.argtypes = [ctypes.POINTER(Model), P, i32, i64, i32, P, P, P, i32, P]
+    lib.oracle_row.argtypes = [ctypes.POINTER(Model), P, i32, P, i32, P, P, P, i32, P]
     lib.oracle_row.restype = None
     lib.oracle_slot.argtypes = [P, i32, i64, i32, i32, i64]
     lib.oracle_slot.restype = i64
     lib.oracle_reuse.argtypes = [ctypes.POINTER(Model), P, i32] + [P, P, P, i32] + [P, P, P, i32, i32] + [
-        P, i32, P, i32, i32, i64, i32, P, P, P, P, P, P]
+        P, P, i32, P, i32, i32, i64, i32, P, P, P, P, P, P]
     lib.oracle_reuse.restype = i32
     lib.oracle_jacobi_svd.argtypes = [P, i32, i32, P, P, i32]
     lib.oracle_jacobi_svd.restype = i32
@@ -112,10 +115,17 @@ def _c(a, dtype):
 
 
 def model(family, num_layers, num_kv_heads=0, head_dim=0, rope_dim=0, latent_dim=0,
-          pairing=ROTATE_HALF, patch_frame=PATCH_AFTER_ROTATION) -> Model:
+          pairing=ROTATE_HALF, patch_frame=PATCH_AFTER_ROTATION, sections=(0, 0, 0)) -> Model:
     if family != MLA and rope_dim == 0:
         rope_dim = head_dim
-    return Model(family, num_layers, num_kv_heads, head_dim, rope_dim, latent_dim, pairing, patch_frame)
+    return Model(family, num_layers, num_kv_heads, head_dim, rope_dim, latent_dim, pairing, patch_frame,
+                 (ctypes.c_int32 * 3)(*sections))
+
+
+def _deltas(delta) -> np.ndarray:
+    """One shift, or one per M-RoPE section (t, h, w), as int64[3]."""
+    d = np.atleast_1d(np.asarray(delta, dtype=np.int64))
+    return np.ascontiguousarray(np.resize(d, 3) if d.size == 1 else d[:3])
 
 
 def row_dim(m: Model) -> int:
@@ -142,15 +152,27 @@ def rotate_region(x, th, delta: int, pairing=ROTATE_HALF, lib=None) -> np.ndarra
     return y
 
 
-def rotate_row(m: Model, th, channel: int, delta: int, row, lib=None) -> np.ndarray:
+def rotate_region_sections(x, th, deltas, sections, pairing=ROTATE_HALF, lib=None) -> np.ndarray:
+    """R with one shift per M-RoPE section on one rotated region (fp64 copy)."""
     lib = lib or load()
-    y = np.array(row, dtype=np.float64, copy=True)
+    y = np.array(x, dtype=np.float64, copy=True)
     th = _c(th, np.float64)
-    lib.oracle_rotate_row(ctypes.byref(m), _ptr(th), int(channel), int(delta), _ptr(y))
+    d = _deltas(deltas)
+    sec = np.ascontiguousarray(sections, dtype=np.int32)
+    lib.oracle_rotate_region_sections(_ptr(y), int(y.shape[0]), _ptr(th), _ptr(d), _ptr(sec), int(pairing))
     return y
 
 
-def row(m: Model, th, channel: int, delta: int, src, u=None, vmat=None, rotate=True, lib=None) -> np.ndarray:
+def rotate_row(m: Model, th, channel: int, delta, row, lib=None) -> np.ndarray:
+    lib = lib or load()
+    y = np.array(row, dtype=np.float64, copy=True)
+    th = _c(th, np.float64)
+    d = _deltas(delta)
+    lib.oracle_rotate_row(ctypes.byref(m), _ptr(th), int(channel), _ptr(d), _ptr(y))
+    return y
+
+
+def row(m: Model, th, channel: int, delta, src, u=None, vmat=None, rotate=True, lib=None) -> np.ndarray:
     """One output row: R(delta) src + U V^T row (fp64).  ``u`` [rank], ``vmat`` [D][rank]."""
     lib = lib or load()
     D = row_dim(m)
@@ -160,7 +182,8 @@ def row(m: Model, th, channel: int, delta: int, src, u=None, vmat=None, rotate=T
     rank = 0 if u is None else int(np.asarray(u).shape[0])
     u = _c(u, np.float64)
     vmat = _c(vmat, np.float64) if vmat is not None else np.zeros((D, max(rank, 1)), np.float64)
-    lib.oracle_row(ctypes.byref(m), _ptr(th), int(channel), int(delta), int(bool(rotate)), _ptr(src), _ptr(u),
+    d = _deltas(delta)
+    lib.oracle_row(ctypes.byref(m), _ptr(th), int(channel), _ptr(d), int(bool(rotate)), _ptr(src), _ptr(u),
                    _ptr(vmat), rank, _ptr(out))
     return out
 
@@ -172,7 +195,8 @@ def slot(block_table, max_pages_per_seq, num_pages, page_size, seq, pos, lib=Non
 
 
 def reuse(m: Model, th, mode, *, store=None, store_off=None, store_len=None, patch=None, patch_off=None,
-          patch_len=None, rank=0, items, block_table, num_pages, page_size, pool_k_in, pool_v_in=None, lib=None):
+          patch_len=None, rank=0, items, block_table, num_pages, page_size, pool_k_in, pool_v_in=None,
+          section_deltas=None, lib=None):
     """The operator over a batch of items into fp64 images of the pool.
 
     Inputs are bf16 bit patterns as uint16 arrays.  Returns
@@ -182,6 +206,7 @@ def reuse(m: Model, th, mode, *, store=None, store_off=None, store_len=None, pat
     lib = lib or load()
     th = _c(th, np.float64)
     items = np.ascontiguousarray(items, dtype=ITEM_DTYPE)
+    sd = None if section_deltas is None else np.ascontiguousarray(section_deltas, dtype=np.int64).reshape(-1, 3)
     bt = _c(block_table, np.int32)
     n_seqs, max_pages = bt.shape
     pool_k_in = _c(pool_k_in, np.uint16)
@@ -201,7 +226,7 @@ def reuse(m: Model, th, mode, *, store=None, store_off=None, store_len=None, pat
     n_patches = 0 if patch_len is None else int(patch_len.shape[0])
     err = lib.oracle_reuse(ctypes.byref(m), _ptr(th), int(mode), _ptr(store), _ptr(store_off), _ptr(store_len),
                            n_chunks, _ptr(patch), _ptr(patch_off), _ptr(patch_len), n_patches, int(rank),
-                           _ptr(items), int(items.shape[0]), _ptr(bt), int(n_seqs), int(max_pages),
+                           _ptr(items), _ptr(sd), int(items.shape[0]), _ptr(bt), int(n_seqs), int(max_pages),
                            int(num_pages), int(page_size), _ptr(pool_k_in), _ptr(pool_v_in), _ptr(pk), _ptr(pv),
                            _ptr(wk), _ptr(wv))
     return int(err), pk, pv, wk, wv

@@ -29,6 +29,9 @@
  *   - RoPE pairs are rotate-half (i, i + d_r/2) unless interleaved (2i, 2i+1)
  *     is requested; theta_i = base^(-2i/d_r) unless a table is given.
  *   - delta is an integer position shift, the same for every token of a chunk.
+ *     With multimodal RoPE (M-RoPE: the rope pairs split into consecutive
+ *     temporal / height / width sections, each rotated by its own position
+ *     component), each section has its own shift; one section = plain RoPE.
  *   - The patch is added after the rotation (the literal formula); the
  *     "canonical frame" variant rotates (KV + U V^T) instead.
  *   - Patch factors are per layer and per channel over the flattened H*d row
@@ -66,6 +69,7 @@ typedef struct {
   int32_t latent_dim;   /* MLA: c_KV width (columns 0 .. latent_dim-1 of the latent row) */
   int32_t pairing;      /* OR_ROTATE_HALF or OR_INTERLEAVED */
   int32_t patch_frame;  /* OR_PATCH_AFTER_ROTATION or OR_PATCH_CANONICAL_FRAME */
+  int32_t sections[3];  /* rope pairs per M-RoPE section (t, h, w); all 0 = a single section */
 } oracle_model;
 
 typedef struct {
@@ -120,17 +124,42 @@ void oracle_rotate_region(double* x, int32_t rope_dim, const double* theta, int6
   }
 }
 
+/* R(delta) with one shift per M-RoPE section: pair i belongs to section s
+ * when it lies in the s-th run of sections[s] consecutive pairs, and turns by
+ * deltas[s]*theta_i.  With no sections every pair takes deltas[0]. */
+void oracle_rotate_region_sections(double* x, int32_t rope_dim, const double* theta, const int64_t* deltas,
+                                   const int32_t* sections, int32_t pairing) {
+  int32_t half = rope_dim / 2;
+  for (int32_t i = 0; i < half; ++i) {
+    int32_t s = 0;
+    if (sections[0] + sections[1] + sections[2] > 0) {
+      if (i >= sections[0]) s = 1;
+      if (i >= sections[0] + sections[1]) s = 2;
+    }
+    int32_t ia = (pairing == OR_INTERLEAVED) ? 2 * i : i;
+    int32_t ib = (pairing == OR_INTERLEAVED) ? 2 * i + 1 : i + half;
+    double phi = (double)deltas[s] * theta[i];
+    double c = cos(phi), sn = sin(phi);
+    double a = x[ia], b = x[ib];
+    x[ia] = a * c - b * sn;
+    x[ib] = b * c + a * sn;
+  }
+}
+
 /* Apply R(delta) to every rotated region of a K row (channel 0).  The V row
  * (channel 1) carries no position and is never rotated.  MLA: only the k_rope
- * columns after the c_KV latent turn; c_KV is untouched. */
-void oracle_rotate_row(const oracle_model* m, const double* theta, int32_t channel, int64_t delta, double* row) {
+ * columns after the c_KV latent turn; c_KV is untouched.  deltas[0..2]: the
+ * shift of each M-RoPE section (only deltas[0] without sections). */
+void oracle_rotate_row(const oracle_model* m, const double* theta, int32_t channel, const int64_t* deltas,
+                       double* row) {
   if (channel != 0) return;
   if (m->family == OR_MLA) {
-    oracle_rotate_region(row + m->latent_dim, m->rope_dim, theta, delta, m->pairing);
+    oracle_rotate_region_sections(row + m->latent_dim, m->rope_dim, theta, deltas, m->sections, m->pairing);
     return;
   }
   for (int32_t h = 0; h < m->num_kv_heads; ++h)
-    oracle_rotate_region(row + (int64_t)h * m->head_dim, m->rope_dim, theta, delta, m->pairing);
+    oracle_rotate_region_sections(row + (int64_t)h * m->head_dim, m->rope_dim, theta, deltas, m->sections,
+                                  m->pairing);
 }
 
 /* One output row of the operator, in fp64.
@@ -139,7 +168,7 @@ void oracle_rotate_row(const oracle_model* m, const double* theta, int32_t chann
  *   vmat [D][rank] V of this layer and channel
  * With the patch after rotation (the literal equation):  out = R src + U V^T row.
  * In the canonical frame:                                out = R (src + U V^T row). */
-void oracle_row(const oracle_model* m, const double* theta, int32_t channel, int64_t delta, int32_t rotate,
+void oracle_row(const oracle_model* m, const double* theta, int32_t channel, const int64_t* deltas, int32_t rotate,
                 const double* src, const double* u, const double* vmat, int32_t rank, double* out) {
   int32_t D = oracle_row_dim(m);
   double* patch = (double*)calloc((size_t)D, sizeof(double));
@@ -152,10 +181,10 @@ void oracle_row(const oracle_model* m, const double* theta, int32_t channel, int
   }
   if (m->patch_frame == OR_PATCH_CANONICAL_FRAME) {
     for (int32_t j = 0; j < D; ++j) out[j] = src[j] + patch[j];
-    if (rotate) oracle_rotate_row(m, theta, channel, delta, out);
+    if (rotate) oracle_rotate_row(m, theta, channel, deltas, out);
   } else {
     for (int32_t j = 0; j < D; ++j) out[j] = src[j];
-    if (rotate) oracle_rotate_row(m, theta, channel, delta, out);
+    if (rotate) oracle_rotate_row(m, theta, channel, deltas, out);
     for (int32_t j = 0; j < D; ++j) out[j] += patch[j];
   }
   free(patch);
@@ -191,12 +220,15 @@ int64_t oracle_slot(const int32_t* block_table, int32_t max_pages_per_seq, int64
  * V [D][rank].  pool_*_in hold the pool's bf16 bits before the call; the fp64
  * images pool_*_out and the written masks are filled here (every slot starts
  * as its input value, unwritten).  pool_v_in / pool_v_out / wrote_v are
- * unused (may be NULL) for MLA.  Returns the OR of the error bits.
+ * unused (may be NULL) for MLA.  section_deltas [n_items][3] gives each
+ * item's per-section shifts when the model has M-RoPE sections (NULL: every
+ * section takes the item's delta).  Returns the OR of the error bits.
  */
 int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
                      const uint16_t* store, const int64_t* store_off, const int32_t* store_len, int32_t n_chunks,
                      const uint16_t* patch, const int64_t* patch_off, const int32_t* patch_len, int32_t n_patches,
-                     int32_t rank, const oracle_item* items, int32_t n_items, const int32_t* block_table,
+                     int32_t rank, const oracle_item* items, const int64_t* section_deltas, int32_t n_items,
+                     const int32_t* block_table,
                      int32_t n_seqs, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
                      const uint16_t* pool_k_in, const uint16_t* pool_v_in, double* pool_k_out, double* pool_v_out,
                      uint8_t* wrote_k, uint8_t* wrote_v) {
@@ -236,6 +268,9 @@ int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
     }
     if (mode == OR_MODE_PATCH_IN_PLACE && !use_patch) continue; /* nothing to add */
     const int32_t rotate = (mode != OR_MODE_PATCH_IN_PLACE);
+    int64_t deltas[3] = {item->delta, item->delta, item->delta};
+    if (section_deltas != NULL)
+      for (int32_t s = 0; s < 3; ++s) deltas[s] = section_deltas[(int64_t)it * 3 + s];
     const int32_t ch_count = (mode == OR_MODE_RELOCATE_IN_PLACE) ? 1 : n_ch;
 
     for (int32_t l = 0; l < L; ++l) {
@@ -265,7 +300,7 @@ int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
                                (int64_t)t * rank;
             for (int32_t r = 0; r < rank; ++r) u[r] = bf16_bits_to_f64(patch[ub + r]);
           }
-          oracle_row(m, theta, ch, item->delta, rotate, src, use_patch ? u : NULL, vmat, rank, out);
+          oracle_row(m, theta, ch, deltas, rotate, src, use_patch ? u : NULL, vmat, rank, out);
           for (int32_t j = 0; j < D; ++j) pout[dst_row * D + j] = out[j];
           wrote[dst_row] = 1;
         }

@@ -33,7 +33,8 @@ class kamera_model_desc(ctypes.Structure):
     _fields_ = [("family", ctypes.c_int32), ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("latent_dim", ctypes.c_int32),
                 ("pairing", ctypes.c_int32), ("patch_frame", ctypes.c_int32), ("rope_base", ctypes.c_double),
-                ("inv_freq", ctypes.c_void_p)]
+                ("inv_freq", ctypes.c_void_p), ("rope_sections", ctypes.c_int32 * 3), ("reserved0", ctypes.c_int32),
+                ("section_delta", ctypes.c_void_p)]
 
 
 class kamera_chunk_store(ctypes.Structure):
@@ -144,10 +145,13 @@ def _ptr(t) -> int | None:
 
 
 def model_desc(family, num_layers, num_kv_heads=0, head_dim=0, rope_dim=0, latent_dim=0, pairing=0, patch_frame=0,
-               rope_base=10000.0, inv_freq=None):
-    """inv_freq: optional host numpy float64 array kept alive by the returned struct."""
+               rope_base=10000.0, inv_freq=None, rope_sections=(0, 0, 0), section_delta=None):
+    """inv_freq: optional host numpy float64 array kept alive by the returned struct.
+    rope_sections: M-RoPE pairs per section; section_delta: device int64
+    tensor [n_items][3] of per-section shifts (or None)."""
     m = kamera_model_desc(family, num_layers, num_kv_heads, head_dim, rope_dim, latent_dim, pairing, patch_frame,
-                          float(rope_base), None)
+                          float(rope_base), None, (ctypes.c_int32 * 3)(*rope_sections), 0, _ptr(section_delta))
+    m._keep = section_delta
     if inv_freq is not None:
         arr = np.ascontiguousarray(inv_freq, dtype=np.float64)
         m._inv_freq = arr

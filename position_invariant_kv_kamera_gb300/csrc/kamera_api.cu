@@ -155,6 +155,14 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   if (D > 32 * MAX_GROUPS) return fail(KAMERA_ERR_UNSUPPORTED, "row width D = %d exceeds %d", D, 32 * MAX_GROUPS);
   const int n_pairs = rope / 2;
   if (n_pairs > MAX_PAIRS) return fail(KAMERA_ERR_UNSUPPORTED, "rope_dim = %d", rope);
+  const int* sec = model->rope_sections;
+  if (sec[0] < 0 || sec[1] < 0 || sec[2] < 0)
+    return fail(KAMERA_ERR_INVALID_ARG, "rope_sections = {%d, %d, %d}", sec[0], sec[1], sec[2]);
+  const int sec_sum = sec[0] + sec[1] + sec[2];
+  if (sec_sum != 0 && sec_sum != n_pairs)
+    return fail(KAMERA_ERR_INVALID_ARG, "rope_sections sum to %d, not rope_dim/2 = %d", sec_sum, n_pairs);
+  if (model->section_delta && (reinterpret_cast<uintptr_t>(model->section_delta) & 7u))
+    return fail(KAMERA_ERR_ALIGNMENT, "section_delta must be 8-byte aligned");
 
   // ---- pool --------------------------------------------------------------------------------
   if (!pool->k) return fail(KAMERA_ERR_NULL, "pool->k is NULL");
@@ -322,6 +330,9 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   p.rotate = mode == MODE_PATCH_IN_PLACE ? 0 : 1;
   p.frame = model->patch_frame;
   p.n_pairs = n_pairs;
+  p.sec_end0 = sec_sum ? sec[0] : n_pairs;
+  p.sec_end1 = sec_sum ? sec[0] + sec[1] : n_pairs;
+  p.section_delta = sec_sum ? model->section_delta : nullptr;
   p.stage_bytes = stage_bytes;
   p.u_bytes = use_patch ? (uint32_t)BM * kg_alloc * 16u : 0u;
   p.v_bytes = use_patch ? (uint32_t)BN * kg_alloc * 16u : 0u;

@@ -101,6 +101,8 @@ struct Params {
   int32_t rotate;    // rotate channel 0
   int32_t frame;     // kamera_patch_frame
   int32_t n_pairs;
+  int32_t sec_end0, sec_end1;      // M-RoPE: pairs [0, sec_end0) section 0, [sec_end0, sec_end1) section 1, rest 2
+  const int64_t* section_delta;    // [n_items][3] per-section shifts, or nullptr (every section: item delta)
   uint32_t stage_bytes, u_bytes, v_bytes, tmem_cols;  // stage_bytes = one canonical tile
   int32_t* err_flag;
   int8_t group_kind[MAX_GROUPS];
@@ -114,7 +116,8 @@ struct Params {
 struct Walker {
   int32_t item;
   int64_t base, count;
-  int64_t dst_pos, delta;
+  int64_t dst_pos;
+  int64_t d0, d1, d2;  // the item's shift of each M-RoPE section (all equal without sections)
   int32_t T, seq, chunk, patch;
   uint32_t n_tb;
 };
@@ -128,7 +131,12 @@ __device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker
   w.chunk = it.chunk_id;
   w.patch = -1;
   w.dst_pos = it.dst_pos;
-  w.delta = it.delta;
+  w.d0 = w.d1 = w.d2 = it.delta;
+  if (p.section_delta) {
+    w.d0 = p.section_delta[(int64_t)i * 3 + 0];
+    w.d1 = p.section_delta[(int64_t)i * 3 + 1];
+    w.d2 = p.section_delta[(int64_t)i * 3 + 2];
+  }
   w.n_tb = 0;
   if (it.n_tokens == 0) return 0;
   if (it.n_tokens < 0 || it.dst_pos < 0) { err |= KAMERA_EFLAG_LEN; return 0; }
@@ -782,7 +790,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       // finished before the last joint barrier
       float2* cs = sm.cs + (rbi & 1u) * pairs_pad(p.n_pairs);
       if (h == 1 && rot && w.item != table_item[rbi & 1u])
-        for (int i = et - 128; i < p.n_pairs; i += 128) cs[i] = phase_cs(w.delta, p.theta[i]);
+        for (int i = et - 128; i < p.n_pairs; i += 128)
+          cs[i] = phase_cs(i < p.sec_end0 ? w.d0 : (i < p.sec_end1 ? w.d1 : w.d2), p.theta[i]);
       if (rot) table_item[rbi & 1u] = w.item;
       if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the table is ready
 

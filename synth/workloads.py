@@ -61,6 +61,8 @@ class Workload:
     outlier_permille: int = 0
     outlier_sigma: float = 8.0
     pool_init: str = "sentinel"  # "sentinel" | "random"
+    rope_sections: tuple = (0, 0, 0)  # M-RoPE pairs per (temporal, height, width) section; zeros = plain RoPE
+    section_deltas: np.ndarray = None  # [n_items][3] per-section shifts (None: the item's delta everywhere)
 
     # ---- derived shapes ----------------------------------------------------
     def __post_init__(self):
@@ -265,6 +267,18 @@ def _random_deltas(seed: int, n: int, lo: int = -32768, hi: int = 32768) -> np.n
 
 
 # ---- the five workload shapes ----------------------------------------------------------
+
+def with_mrope(wl: Workload, sections=(16, 24, 24), seed: int | None = None) -> Workload:
+    """M-RoPE variant (the temporal / height / width split of Qwen2-VL-style
+    multimodal RoPE): a seeded temporal shift and a separate spatial shift
+    (shared by height and width) per item."""
+    seed = wl.seed if seed is None else seed
+    n = len(wl.items)
+    dt = _random_deltas(seed + 11, n)
+    ds = _random_deltas(seed + 12, n)
+    sd = np.stack([dt, ds, ds], axis=1).astype(np.int64)
+    return wl.replace(rope_sections=tuple(sections), section_deltas=sd, name=wl.name + "_mrope")
+
 
 def tiny_mha(seed: int = 0x4B414D45 + 1) -> Workload:
     """MHA, 1 layer, 4 heads x 64, one 256-token chunk, rank 8, delta 1000,

@@ -20,9 +20,10 @@ from synth import workloads as W
 ABS_TOL = 1e-3
 
 
-def model_for(wl: W.Workload):
+def model_for(wl: W.Workload, t: dict | None = None):
     return pk.model_desc(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
-                         wl.pairing, wl.patch_frame, wl.rope_base)
+                         wl.pairing, wl.patch_frame, wl.rope_base, rope_sections=wl.rope_sections,
+                         section_delta=(t or {}).get("section_delta"))
 
 
 def device_inputs(wl: W.Workload, torch, device="cuda", pool_host=None) -> dict:
@@ -47,12 +48,14 @@ def device_inputs(wl: W.Workload, torch, device="cuda", pool_host=None) -> dict:
         t["pool_k"] = wl.device_pool(torch, 0, device)
         t["pool_v"] = wl.device_pool(torch, 1, device) if wl.n_ch == 2 else None
     t["err"] = torch.zeros(1, dtype=torch.int32, device=device)
+    if wl.section_deltas is not None:
+        t["section_delta"] = torch.from_numpy(np.ascontiguousarray(wl.section_deltas, np.int64)).to(device)
     return t
 
 
 def call(wl: W.Workload, t: dict, mode: str | None = None, stream=None, raise_on_error=True) -> int:
     mode = mode or wl.mode
-    return pk.call(mode, model_for(wl), items=t["items"], pool_k=t["pool_k"], pool_v=t["pool_v"],
+    return pk.call(mode, model_for(wl, t), items=t["items"], pool_k=t["pool_k"], pool_v=t["pool_v"],
                    block_table=t["block_table"], page_size=wl.page_size, store=t.get("store"),
                    store_off=t.get("store_off"), store_len=t.get("store_len"), patch=t.get("patch"),
                    patch_off=t.get("patch_off"), patch_len=t.get("patch_len"),
@@ -84,7 +87,7 @@ def oracle_reference(wl: W.Workload, pool_k_in=None, pool_v_in=None):
     import oracle
 
     m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
-                     wl.pairing, wl.patch_frame)
+                     wl.pairing, wl.patch_frame, wl.rope_sections)
     th = oracle.theta(wl.rope_base, wl.rope_dim)
     mode = {"reuse": oracle.MODE_REUSE, "relocate": oracle.MODE_REUSE,
             "relocate_in_place": oracle.MODE_RELOCATE_IN_PLACE, "apply_patch": oracle.MODE_PATCH_IN_PLACE}[wl.mode]
@@ -97,7 +100,8 @@ def oracle_reference(wl: W.Workload, pool_k_in=None, pool_v_in=None):
         kw.update(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
                   rank=wl.rank)
     return oracle.reuse(m, th, mode, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
-                        page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, **kw)
+                        page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, section_deltas=wl.section_deltas,
+                        **kw)
 
 
 def compare_pool(gpu_bits: np.ndarray, in_bits: np.ndarray, ref: np.ndarray, wrote: np.ndarray,

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert pk.abi_version() == 1
+    assert pk.abi_version() == 2
     assert pk.status_string(pk.KAMERA_OK) == "KAMERA_OK"
     assert pk.status_string(pk.KAMERA_ERR_CUDA) == "KAMERA_ERR_CUDA"
     assert pk.status_string(99) == "KAMERA_ERR_UNKNOWN"
@@ -57,8 +57,9 @@ def test_struct_layouts_match_header(tmp_path):
 int main(void) {
   printf("%zu %zu %zu %zu %zu\n", sizeof(kamera_model_desc), sizeof(kamera_chunk_store),
          sizeof(kamera_patch_store), sizeof(kamera_paged_pool), sizeof(kamera_reuse_item));
-  printf("%zu %zu %zu %zu\n", offsetof(kamera_model_desc, rope_base), offsetof(kamera_reuse_item, delta),
-         offsetof(kamera_reuse_item, dst_pos), offsetof(kamera_paged_pool, block_table));
+  printf("%zu %zu %zu %zu %zu\n", offsetof(kamera_model_desc, rope_base), offsetof(kamera_reuse_item, delta),
+         offsetof(kamera_reuse_item, dst_pos), offsetof(kamera_paged_pool, block_table),
+         offsetof(kamera_model_desc, section_delta));
   return 0;
 }
 ''')
@@ -71,7 +72,8 @@ int main(void) {
                      pk.REUSE_ITEM.itemsize]
     offs = [int(x) for x in lines[1].split()]
     assert offs == [pk.kamera_model_desc.rope_base.offset, pk.REUSE_ITEM.fields["delta"][1],
-                    pk.REUSE_ITEM.fields["dst_pos"][1], pk.kamera_paged_pool.block_table.offset]
+                    pk.REUSE_ITEM.fields["dst_pos"][1], pk.kamera_paged_pool.block_table.offset,
+                    pk.kamera_model_desc.section_delta.offset]
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -128,6 +130,11 @@ def test_validation_invalid_arguments(lib):
     assert _reuse(mla, _pool()) == pk.KAMERA_ERR_INVALID_ARG  # MLA pools carry no V
     bad_base = _gqa_model(rope_base=-1.0)
     assert _reuse(bad_base, _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    m = _gqa_model()
+    m.rope_sections[0], m.rope_sections[1], m.rope_sections[2] = 16, 24, 23  # must sum to rope_dim/2 = 64
+    assert _reuse(m, _pool()) == pk.KAMERA_ERR_INVALID_ARG
+    m.rope_sections[2] = -1
+    assert _reuse(m, _pool()) == pk.KAMERA_ERR_INVALID_ARG
 
 
 def test_validation_unsupported_shapes(lib):

@@ -26,7 +26,7 @@ def _cuda():
 
 def _oracle_model(wl):
     return oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
-                        wl.pairing, wl.patch_frame)
+                        wl.pairing, wl.patch_frame, wl.rope_sections)
 
 
 def _slot_rows(wl, item, t):
@@ -64,8 +64,8 @@ def _check_samples(wl, t, pool_init_rows=None):
         if wl.rank and int(it["patch_id"]) >= 0 and wl.mode != "relocate_in_place":
             u = H.bits_to_f64(wl.u_rows(int(it["patch_id"]), layer, ch, tok, tok + 1)[0])
             v = H.bits_to_f64(wl.v_rows(int(it["patch_id"]), layer, ch))
-        ref = oracle.row(m, th, ch, int(it["delta"]), H.bits_to_f64(src), u, v,
-                         rotate=wl.mode != "apply_patch")
+        delta = wl.section_deltas[i] if wl.section_deltas is not None else int(it["delta"])
+        ref = oracle.row(m, th, ch, delta, H.bits_to_f64(src), u, v, rotate=wl.mode != "apply_patch")
         pool = t["pool_k"] if ch == 0 else t["pool_v"]
         got = H.to_bits(pool[layer, page, slot])
         ok = H.within_tol(H.bits_to_f64(got), ref)
@@ -123,6 +123,15 @@ def test_full_gqa_video():
     t = _run(wl)
     _check_sentinel_coverage(wl, t["pool_k"])
     _check_sentinel_coverage(wl, t["pool_v"])
+    _check_samples(wl, t)
+
+
+def test_full_gqa_video_mrope():
+    """The headline shape with multimodal RoPE sections (16/24/24 pairs) and
+    separate temporal and spatial shifts per chunk."""
+    wl = W.with_mrope(W.gqa_video())
+    t = _run(wl)
+    _check_sentinel_coverage(wl, t["pool_k"])
     _check_samples(wl, t)
 
 

@@ -53,7 +53,15 @@ def random_workload(seed: int) -> W.Workload:
     ppseq = max(1, -(-max(cursor) // P))
     num_pages = n_seqs * ppseq + int(rng.integers(0, 4))
     bt = W.shuffled_block_table(seed, n_seqs, ppseq, num_pages)
-    return W.Workload(f"fuzz{seed}", family, L, rope_base=float(rng.choice([1e4, 5e5, 1e6])),
+    mrope = {}
+    if rng.random() < 0.3:
+        npairs = (kw.get("rope_dim") or 64) // 2
+        a = int(rng.integers(0, npairs + 1))
+        b = int(rng.integers(0, npairs - a + 1))
+        sec = (a, b, npairs - a - b)
+        mrope = dict(rope_sections=sec,
+                     section_deltas=rng.integers(-70000, 70000, (len(items), 3)).astype(np.int64))
+    return W.Workload(f"fuzz{seed}", family, L, rope_base=float(rng.choice([1e4, 5e5, 1e6])), **mrope,
                       pairing=int(rng.integers(0, 2)), patch_frame=int(rng.integers(0, 2)), chunk_lens=lens,
                       rank=rank, patch_lens=lens if rank else [], items=items, page_size=P, num_pages=num_pages,
                       block_table=bt, seed=seed, sigma_uv=float(rng.choice([0.02, 0.3])), **kw)

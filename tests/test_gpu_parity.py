@@ -166,3 +166,33 @@ def test_error_flags_and_skips():
     items[1]["seq"] = 3
     items[2]["dst_pos"] = -1
     run_and_compare(wl.replace(items=items))
+
+
+@pytest.mark.parametrize("pairing", [W.ROTATE_HALF, W.INTERLEAVED])
+@pytest.mark.parametrize("rank", [0, 32])
+def test_mrope_sections(pairing, rank):
+    """M-RoPE (temporal / height / width sections of 16 / 24 / 24 pairs): each
+    section re-rotated by its own shift."""
+    wl = W.with_mrope(W.gqa_video(num_layers=2, n_chunks=3, T=200, rank=rank, page_size=16)).replace(
+        pairing=pairing)
+    if rank == 0:
+        wl = wl.replace(patch_lens=[])
+    run_and_compare(wl)
+
+
+def test_mrope_in_place_sliding_window():
+    wl = W.with_mrope(W.sliding_window(num_layers=2, n_resident=4, n_evict=1, T=128, page_size=64,
+                                       num_kv_heads=2))
+    run_and_compare(wl, pool_host=(wl.host_pool(0), wl.host_pool(1)))
+
+
+def test_mrope_equal_section_shifts_match_plain_rope_bitwise():
+    base = W.gqa_video(num_layers=1, n_chunks=2, T=150, rank=16, page_size=16)
+    sd = np.repeat(base.items["delta"][:, None], 3, axis=1)
+    wl = base.replace(rope_sections=(16, 24, 24), section_deltas=sd)
+    t0 = H.device_inputs(base, torch)
+    H.call(base, t0)
+    t1 = H.device_inputs(wl, torch)
+    H.call(wl, t1)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(H.to_bits(t0["pool_k"]), H.to_bits(t1["pool_k"]))

@@ -228,3 +228,44 @@ def test_jacobi_svd_truncation_residual_is_eckart_young(oracle_lib):
         resid = np.linalg.norm(a - us[:, :m] @ v[:, :m].T)
         np.testing.assert_allclose(resid, np.sqrt((sig[m:] ** 2).sum()), rtol=1e-10)
     np.testing.assert_allclose(v.T @ v, np.eye(20), atol=1e-12)
+
+
+def mrope_complex(x, pos3, theta, sections, pairing=oracle.ROTATE_HALF):
+    """M-RoPE written as complex multiplication: pair i of section s turns by
+    pos3[s] * theta_i (sections = consecutive runs of pairs)."""
+    h = x.shape[0] // 2
+    sec_of = np.repeat(np.arange(3), sections)
+    phase = np.asarray(pos3, np.float64)[sec_of] * theta
+    if pairing == oracle.ROTATE_HALF:
+        z = (x[:h] + 1j * x[h:]) * np.exp(1j * phase)
+        return np.concatenate([z.real, z.imag])
+    z = (x[0::2] + 1j * x[1::2]) * np.exp(1j * phase)
+    out = np.empty_like(x)
+    out[0::2], out[1::2] = z.real, z.imag
+    return out
+
+
+@pytest.mark.parametrize("pairing", [oracle.ROTATE_HALF, oracle.INTERLEAVED])
+def test_mrope_sections_shift_each_position_component(oracle_lib, pairing):
+    """Multimodal RoPE (temporal / height / width sections, e.g. 16/24/24 pairs
+    of a 128-dim head): re-rotating by (dt, dh, dw) moves each component."""
+    th = _theta_np(1e6, 128)
+    sec = (16, 24, 24)
+    for p3, d3 in [((5, 7, 9), (1000, -3, 0)), ((0, 0, 0), (32768, 17, -17)), ((100, 2, 3), (0, 0, 0))]:
+        x = rng.standard_normal(128)
+        got = oracle.rotate_region_sections(mrope_complex(x, p3, th, sec, pairing), th, d3, sec, pairing)
+        want = mrope_complex(x, np.add(p3, d3), th, sec, pairing)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-9)
+
+
+def test_mrope_equal_shifts_is_plain_rope_and_group_law(oracle_lib):
+    th = oracle.theta(1e6, 128)
+    sec = (16, 24, 24)
+    x = rng.standard_normal(128)
+    np.testing.assert_array_equal(oracle.rotate_region_sections(x, th, (77, 77, 77), sec),
+                                  oracle.rotate_region(x, th, 77))
+    a = oracle.rotate_region_sections(oracle.rotate_region_sections(x, th, (5, -9, 100), sec), th, (-2, 9, 1), sec)
+    np.testing.assert_allclose(a, oracle.rotate_region_sections(x, th, (3, 0, 101), sec), atol=1e-11)
+    # no sections: every pair takes the first shift
+    np.testing.assert_array_equal(oracle.rotate_region_sections(x, th, (5, 6, 7), (0, 0, 0)),
+                                  oracle.rotate_region(x, th, 5))

@@ -413,12 +413,91 @@ def reduce_max_time_value(e2e: dict, tokens: int, world: int, torch, device) -> 
     return aggregate(tokens, world, mx, e2e["steps"])
 
 
+# ---- patch formation (rank-m factors of a deficit) -----------------------------------------------
+
+FACTOR_SHAPE = dict(n_slabs=16 * 28 * 2, T=1024, D=512, rank=32, oversample=16, power_iters=2, true_rank=40)
+
+
+def factor_flops(T: int, D: int, k: int, m: int, q: int) -> int:
+    """Algorithmic flops of one slab: the GEMMs (Delta Omega, 2q subspace
+    products, Q^T Delta, B B^T, the two output products) and classical
+    Gram-Schmidt twice on each of the 2q+1 orthonormalised panels."""
+    gemm = 2 * T * D * k * (2 + 2 * q) + 2 * D * k * k + 2 * (T + D) * k * m
+    orth = 4 * k * k * (T + q * (T + D))
+    return gemm + orth
+
+
+def run_factor(args) -> None:
+    import torch
+
+    import position_invariant_kv_kamera_gb300 as pk
+    from synth import gen
+
+    torch.cuda.set_device(0)
+    fs = FACTOR_SHAPE
+    n, T, D, m, p, q, r = (fs[k] for k in ("n_slabs", "T", "D", "rank", "oversample", "power_iters", "true_rank"))
+    # seeded deficits of rank r (factors from the counter generator, product formed on the device)
+    st = gen.stream_id(0x4B414D45, gen.STREAM_DEFICIT)
+    A = torch.from_numpy(gen.normal_f32(st, np.arange(n * T * r, dtype=np.uint64)).reshape(n, T, r)).cuda()
+    B = torch.from_numpy(gen.normal_f32(st, np.uint64(1 << 40) + np.arange(n * D * r, dtype=np.uint64))
+                         .reshape(n, D, r)).cuda()
+    spec = torch.linspace(10, 1, r, device="cuda")
+    delta = torch.bmm(A * spec, B.transpose(1, 2)).contiguous() / float(np.sqrt(T * D))
+    del A, B
+    om = torch.from_numpy(gen.gaussian_test_matrix(0x4B414D45, D, m + p)).cuda()
+    desc = pk.factor_desc(delta, n, T, D, m, p, q, om)
+    nbytes = pk.kamera_factor_workspace_size(desc)
+    ws = torch.empty(nbytes // 4 + 64, dtype=torch.float32, device="cuda")
+    out = torch.empty(n * (T + D) * m, dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pk.kamera_factor_patches(desc, out.data_ptr(), out.data_ptr() + 2 * T * m, (T + D) * m, ws.data_ptr(),
+                                 nbytes, stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        time.sleep(0.25)
+        b.record(stream)
+        for _ in range(steps):
+            call()
+        e.record(stream)
+        torch.cuda.synchronize()
+    sec = b.elapsed_time(e) / 1e3 / steps
+    flops = n * factor_flops(T, D, m + p, m, q)
+    import json as _json
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    peak = sms * 128 * 2 * 2.07e9 / 1e12  # fp32 FMA lanes x 2 flops x max SM clock
+    # CPU: the oracle's exact Jacobi SVD of one slab
+    import oracle
+    A1 = delta[0].double().cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.jacobi_svd(A1)
+    cpu_s = time.perf_counter() - t0
+    line = {"metric": "patch formation: rank-m factors of conditioning deficits (slabs/s)", "value": n / sec,
+            "unit": "slabs/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{n} slabs of {T}x{D} (16 patches x 28 layers x K/V of the GQA video shape), "
+                                   f"rank {m}, oversample {p}, {q} subspace iterations, deficit rank {r}"},
+            "roofline": {"bound": "alu", "achieved": flops / sec / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / sec / 1e12 / peak, "traffic": None,
+                         "peak_source": f"derived: {sms} SMs x 128 fp32 FMA lanes x 2 flops x 2.07 GHz"},
+            "cpu_baseline": {"value": 1.0 / cpu_s, "unit": "slabs/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one {T}x{D} slab, exact one-sided Jacobi SVD ({cpu_s:.1f} s)"},
+            "gpu_launches": steps, "clocks": clocks.summary()}
+    print(_json.dumps(line), flush=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS))
+    ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS) + ["patch_formation"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--chunks", type=int, default=0,
@@ -428,6 +507,8 @@ def main(argv=None) -> None:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "patch_formation":
+        run_factor(args)
     else:
         run_gpu(args)
 

@@ -185,6 +185,43 @@ kamera_status kamera_apply_patch(const kamera_model_desc* model, const kamera_pa
                                  const kamera_reuse_item* items, int32_t n_items, const kamera_paged_pool* pool,
                                  int32_t* err_flag, kamera_stream_t stream);
 
+/*
+ * Patch formation -- Kamera §2 "Patch application": the patch is formed once
+ * from the deficit Delta = KV(B|A) - KV(B|empty) by an SVD that keeps the top
+ * m factors.  kamera_factor_patches computes, for every slab (one patch,
+ * layer and channel), factors U_m [T][m] and V_m [D][m] whose product is the
+ * rank-m truncation of Delta, and writes them as bf16 in the patch-store
+ * layout (U of slab s at u_out + s*out_stride elements, V at v_out +
+ * s*out_stride; for the slabs of one patch, u_out = patch base, v_out = patch
+ * base + T*m, out_stride = (T+D)*m).  U_m has orthonormal columns; V_m carries
+ * the singular values.
+ *
+ * Method: randomized range finder with q subspace iterations on a Gaussian
+ * test matrix Omega [D][k], k = m + oversample (Halko, Martinsson & Tropp
+ * 2011), fp32 throughout; exact when rank(Delta) <= k.  The caller passes
+ * Omega, and scratch memory of kamera_factor_workspace_size() bytes.
+ */
+typedef struct {
+  const float* delta;     /* device fp32: slab s at delta + s*delta_stride, [T][D] row-major */
+  int64_t delta_stride;   /* elements between slabs (>= T*D) */
+  int32_t n_slabs;
+  int32_t T, D;           /* 1 <= T <= 8192, 1 <= D <= 2048 */
+  int32_t rank;           /* m: 8, 16, 32 or 64 */
+  int32_t oversample;     /* k = rank + oversample, 1 <= k <= 96 */
+  int32_t power_iters;    /* q, 0..8 */
+  const float* omega;     /* device fp32 [D][k] row-major */
+} kamera_factor_desc;
+
+/* Scratch bytes kamera_factor_patches needs for this description on the
+ * current device (written to *bytes).  No allocation happens. */
+kamera_status kamera_factor_workspace_size(const kamera_factor_desc* desc, size_t* bytes);
+
+/* Form the factors (asynchronous on `stream`).  u_out / v_out: device bf16;
+ * workspace: device, 256-byte aligned, at least the size above; its contents
+ * are undefined afterwards. */
+kamera_status kamera_factor_patches(const kamera_factor_desc* desc, void* u_out, void* v_out, int64_t out_stride,
+                                    void* workspace, size_t workspace_bytes, kamera_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* kamera_status_string(kamera_status status);
 

@@ -25,8 +25,8 @@ KAMERA_PATCH_AFTER_ROTATION, KAMERA_PATCH_CANONICAL_FRAME = 0, 1
 KAMERA_EFLAG_CHUNK_OOB, KAMERA_EFLAG_PAGE_OOB, KAMERA_EFLAG_PATCH_OOB, KAMERA_EFLAG_LEN, KAMERA_EFLAG_TIMEOUT = (
     1, 2, 4, 8, 16)
 
-EXPORTS = ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch", "kamera_status_string",
-           "kamera_last_error", "kamera_abi_version")
+EXPORTS = ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch", "kamera_factor_workspace_size",
+           "kamera_factor_patches", "kamera_status_string", "kamera_last_error", "kamera_abi_version")
 
 
 class kamera_model_desc(ctypes.Structure):
@@ -51,6 +51,12 @@ class kamera_paged_pool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
                 ("page_size", ctypes.c_int32), ("block_table", ctypes.c_void_p), ("n_seqs", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32)]
+
+
+class kamera_factor_desc(ctypes.Structure):
+    _fields_ = [("delta", ctypes.c_void_p), ("delta_stride", ctypes.c_int64), ("n_slabs", ctypes.c_int32),
+                ("T", ctypes.c_int32), ("D", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("oversample", ctypes.c_int32), ("power_iters", ctypes.c_int32), ("omega", ctypes.c_void_p)]
 
 
 # kamera_reuse_item as a numpy record (32 bytes, naturally aligned)
@@ -88,6 +94,10 @@ def load(build_if_missing: bool = False):
         lib.kamera_apply_patch.argtypes = [P, P, P, ctypes.c_int32, P, P, P]
         for name in ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch"):
             getattr(lib, name).restype = ctypes.c_int
+        lib.kamera_factor_workspace_size.argtypes = [P, P]
+        lib.kamera_factor_workspace_size.restype = ctypes.c_int
+        lib.kamera_factor_patches.argtypes = [P, P, P, ctypes.c_int64, P, ctypes.c_size_t, P]
+        lib.kamera_factor_patches.restype = ctypes.c_int
         lib.kamera_status_string.argtypes = [ctypes.c_int]
         lib.kamera_status_string.restype = ctypes.c_char_p
         lib.kamera_last_error.argtypes = []
@@ -212,3 +222,27 @@ def call(mode: str, model, *, items, pool_k, pool_v, block_table, page_size, sto
     if mode == "apply_patch":
         return kamera_apply_patch(model, ps, _ptr(items), n_items, pool, ef, sh, raise_on_error)
     raise ValueError(f"unknown mode {mode!r}")
+
+
+# ---- patch formation ----------------------------------------------------------------------------
+
+def factor_desc(delta, n_slabs, T, D, rank, oversample, power_iters, omega, delta_stride=None):
+    """delta: device fp32 [n_slabs][T][D]; omega: device fp32 [D][rank+oversample]."""
+    d = kamera_factor_desc(_ptr(delta), int(delta_stride if delta_stride is not None else T * D), int(n_slabs),
+                           int(T), int(D), int(rank), int(oversample), int(power_iters), _ptr(omega))
+    d._keep = (delta, omega)
+    return d
+
+
+def kamera_factor_workspace_size(desc, raise_on_error=True) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().kamera_factor_workspace_size(_ref(desc), ctypes.byref(out))
+    _check(st, raise_on_error)
+    return int(out.value)
+
+
+def kamera_factor_patches(desc, u_out_ptr, v_out_ptr, out_stride, workspace_ptr, workspace_bytes, stream,
+                          raise_on_error=True) -> int:
+    st = load().kamera_factor_patches(_ref(desc), u_out_ptr, v_out_ptr, int(out_stride), workspace_ptr,
+                                      int(workspace_bytes), stream)
+    return _check(st, raise_on_error)

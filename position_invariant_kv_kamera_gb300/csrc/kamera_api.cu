@@ -16,6 +16,7 @@
 #include <string>
 
 #include "kamera.h"
+#include "kamera_factor.cuh"
 #include "kamera_kernel.cuh"
 
 namespace kamera {
@@ -428,10 +429,110 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   return KAMERA_OK;
 }
 
+// ---- patch formation -------------------------------------------------------------------------------
+
+struct FactorShape {
+  int kp, grid;
+  int64_t work_per_cta;  // floats
+};
+
+kamera_status factor_validate(const kamera_factor_desc* d) {
+  if (!d) return fail(KAMERA_ERR_NULL, "factor desc is NULL");
+  if (d->n_slabs < 0) return fail(KAMERA_ERR_INVALID_ARG, "n_slabs = %d", d->n_slabs);
+  if (d->T < 1 || d->T > 8192 || d->D < 1 || d->D > 2048)
+    return fail(KAMERA_ERR_UNSUPPORTED, "slab %d x %d (T <= 8192, D <= 2048 served)", d->T, d->D);
+  if (d->rank != 8 && d->rank != 16 && d->rank != 32 && d->rank != 64)
+    return fail(KAMERA_ERR_INVALID_ARG, "rank = %d (8, 16, 32 or 64)", d->rank);
+  const int k = d->rank + d->oversample;
+  if (d->oversample < 0 || k > factor::KMAX)
+    return fail(KAMERA_ERR_INVALID_ARG, "rank + oversample = %d (at most %d)", k, factor::KMAX);
+  if (d->power_iters < 0 || d->power_iters > 8) return fail(KAMERA_ERR_INVALID_ARG, "power_iters = %d", d->power_iters);
+  if (d->n_slabs > 1 && d->delta_stride < (int64_t)d->T * d->D)
+    return fail(KAMERA_ERR_INVALID_ARG, "delta_stride < T*D");
+  if (d->n_slabs > 0 && (!d->delta || !d->omega)) return fail(KAMERA_ERR_NULL, "delta or omega is NULL");
+  return KAMERA_OK;
+}
+
+kamera_status factor_shape(const kamera_factor_desc* d, FactorShape* fs) {
+  int dev = 0;
+  DeviceFacts* facts = nullptr;
+  if (kamera_status st = device_facts(&dev, &facts)) return st;
+  const int k = d->rank + d->oversample;
+  fs->kp = (k + 15) / 16 * 16;
+  fs->grid = d->n_slabs < facts->sms ? d->n_slabs : facts->sms;
+  fs->work_per_cta = (int64_t)fs->kp * (d->T + 2 * (int64_t)d->D);
+  return KAMERA_OK;
+}
+
+kamera_status factor_workspace_size(const kamera_factor_desc* d, size_t* bytes) {
+  g_last_error.clear();
+  if (!bytes) return fail(KAMERA_ERR_NULL, "bytes is NULL");
+  if (kamera_status st = factor_validate(d)) return st;
+  FactorShape fs;
+  if (kamera_status st = factor_shape(d, &fs)) return st;
+  *bytes = (size_t)fs.grid * (size_t)fs.work_per_cta * sizeof(float);
+  return KAMERA_OK;
+}
+
+kamera_status factor_patches(const kamera_factor_desc* d, void* u_out, void* v_out, int64_t out_stride,
+                             void* workspace, size_t workspace_bytes, kamera_stream_t stream) {
+  g_last_error.clear();
+  if (kamera_status st = factor_validate(d)) return st;
+  if (d->n_slabs == 0) return KAMERA_OK;
+  if (!u_out || !v_out || !workspace) return fail(KAMERA_ERR_NULL, "u_out, v_out or workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(d->delta) & 15u) ||
+      (reinterpret_cast<uintptr_t>(u_out) & 1u) || (reinterpret_cast<uintptr_t>(v_out) & 1u))
+    return fail(KAMERA_ERR_ALIGNMENT, "workspace must be 256-byte aligned, delta 16-byte, outputs 2-byte");
+  if (out_stride < (int64_t)d->rank * (d->T > d->D ? d->T : d->D) && d->n_slabs > 1)
+    return fail(KAMERA_ERR_INVALID_ARG, "out_stride %lld overlaps consecutive slabs", (long long)out_stride);
+  FactorShape fs;
+  if (kamera_status st = factor_shape(d, &fs)) return st;
+  if (workspace_bytes < (size_t)fs.grid * (size_t)fs.work_per_cta * sizeof(float))
+    return fail(KAMERA_ERR_INVALID_ARG, "workspace of %zu bytes is too small", workspace_bytes);
+  factor::FParams fp;
+  fp.delta = d->delta;
+  fp.delta_stride = d->delta_stride;
+  fp.n_slabs = d->n_slabs;
+  fp.T = d->T;
+  fp.D = d->D;
+  fp.m = d->rank;
+  fp.k = d->rank + d->oversample;
+  fp.kp = fs.kp;
+  fp.power_iters = d->power_iters;
+  fp.omega = d->omega;
+  fp.u_out = static_cast<uint16_t*>(u_out);
+  fp.v_out = static_cast<uint16_t*>(v_out);
+  fp.out_stride = out_stride;
+  fp.work = static_cast<float*>(workspace);
+  fp.work_per_cta = fs.work_per_cta;
+  const uint32_t smem = factor::factor_smem_bytes();
+  {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  }
+  factor::factor_kernel<<<fs.grid, factor::THREADS, smem, reinterpret_cast<cudaStream_t>(stream)>>>(fp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return KAMERA_OK;
+}
+
 }  // namespace
 }  // namespace kamera
 
 extern "C" {
+
+kamera_status kamera_factor_workspace_size(const kamera_factor_desc* desc, size_t* bytes) {
+  return kamera::factor_workspace_size(desc, bytes);
+}
+
+kamera_status kamera_factor_patches(const kamera_factor_desc* desc, void* u_out, void* v_out, int64_t out_stride,
+                                    void* workspace, size_t workspace_bytes, kamera_stream_t stream) {
+  return kamera::factor_patches(desc, u_out, v_out, out_stride, workspace, workspace_bytes, stream);
+}
 
 kamera_status kamera_reuse_batched(const kamera_model_desc* model, const kamera_chunk_store* store,
                                    const kamera_patch_store* patches, const kamera_reuse_item* items,

@@ -142,3 +142,36 @@ def uniform_int(stream: int, idx, lo: int, hi: int) -> np.ndarray:
 def permutation(stream: int, n: int) -> np.ndarray:
     """A seeded permutation of range(n): argsort of the hashes (stable)."""
     return np.argsort(hash64(stream, np.arange(n, dtype=np.uint64)), kind="stable").astype(np.int64)
+
+
+def normal_f32(stream: int, idx, sigma: float = 1.0) -> np.ndarray:
+    """fp32 N(0, sigma) variates at counter positions idx (the Irwin-Hall value
+    before any bf16 rounding)."""
+    h = hash64(stream, idx)
+    m = np.uint64(0xFFFF)
+    s = (h & m) + ((h >> np.uint64(16)) & m) + ((h >> np.uint64(32)) & m) + (h >> np.uint64(48))
+    return (s.astype(np.int64) - IH_MEAN).astype(np.float32) * scale_f32(sigma)
+
+
+STREAM_OMEGA, STREAM_DEFICIT = 8, 9
+
+
+def gaussian_test_matrix(seed: int, D: int, k: int) -> np.ndarray:
+    """Omega [D][k] fp32 N(0,1): the randomized range finder's test matrix."""
+    return normal_f32(stream_id(seed, STREAM_OMEGA), np.arange(D * k, dtype=np.uint64)).reshape(D, k)
+
+
+def low_rank_deficit(seed: int, slab: int, T: int, D: int, spectrum, noise: float = 0.0) -> np.ndarray:
+    """A synthetic deficit [T][D] fp32: A diag(spectrum) B^T / sqrt(T D) + noise
+    with A, B Gaussian -- a low-rank matrix with the given (approximate)
+    singular values plus a small full-rank floor."""
+    r = len(spectrum)
+    st = stream_id(seed, STREAM_DEFICIT)
+    base = np.uint64(slab) << np.uint64(40)
+    A = normal_f32(st, base + np.arange(T * r, dtype=np.uint64)).reshape(T, r).astype(np.float64)
+    B = normal_f32(st, base + np.uint64(1 << 36) + np.arange(D * r, dtype=np.uint64)).reshape(D, r).astype(np.float64)
+    out = (A * np.asarray(spectrum, np.float64)) @ B.T / np.sqrt(T * D)
+    if noise:
+        N = normal_f32(st, base + np.uint64(1 << 38) + np.arange(T * D, dtype=np.uint64)).reshape(T, D)
+        out = out + noise * N / np.sqrt(max(T, D))
+    return out.astype(np.float32)

@@ -55,8 +55,8 @@ def test_struct_layouts_match_header(tmp_path):
 #include <stddef.h>
 #include "kamera.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu\n", sizeof(kamera_model_desc), sizeof(kamera_chunk_store),
-         sizeof(kamera_patch_store), sizeof(kamera_paged_pool), sizeof(kamera_reuse_item));
+  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(kamera_model_desc), sizeof(kamera_chunk_store),
+         sizeof(kamera_patch_store), sizeof(kamera_paged_pool), sizeof(kamera_reuse_item), sizeof(kamera_factor_desc));
   printf("%zu %zu %zu %zu %zu\n", offsetof(kamera_model_desc, rope_base), offsetof(kamera_reuse_item, delta),
          offsetof(kamera_reuse_item, dst_pos), offsetof(kamera_paged_pool, block_table),
          offsetof(kamera_model_desc, section_delta));
@@ -69,7 +69,7 @@ int main(void) {
     sizes = [int(x) for x in lines[0].split()]
     assert sizes == [ctypes.sizeof(pk.kamera_model_desc), ctypes.sizeof(pk.kamera_chunk_store),
                      ctypes.sizeof(pk.kamera_patch_store), ctypes.sizeof(pk.kamera_paged_pool),
-                     pk.REUSE_ITEM.itemsize]
+                     pk.REUSE_ITEM.itemsize, ctypes.sizeof(pk.kamera_factor_desc)]
     offs = [int(x) for x in lines[1].split()]
     assert offs == [pk.kamera_model_desc.rope_base.offset, pk.REUSE_ITEM.fields["delta"][1],
                     pk.REUSE_ITEM.fields["dst_pos"][1], pk.kamera_paged_pool.block_table.offset,
@@ -158,3 +158,21 @@ def test_validation_alignment(lib):
 
 def test_empty_batch_is_a_no_op(lib):
     assert _reuse(_gqa_model(), _pool(), n=0) == pk.KAMERA_OK
+
+
+def test_factor_validation(lib):
+    d = pk.kamera_factor_desc(FAKE, 300 * 256, 4, 300, 256, 16, 16, 1, FAKE)
+    out = ctypes.c_size_t(0)
+    assert lib.kamera_factor_workspace_size(None, ctypes.byref(out)) == pk.KAMERA_ERR_NULL
+    bad = pk.kamera_factor_desc(FAKE, 300 * 256, 4, 300, 256, 12, 16, 1, FAKE)
+    assert lib.kamera_factor_workspace_size(ctypes.byref(bad), ctypes.byref(out)) == pk.KAMERA_ERR_INVALID_ARG
+    bad = pk.kamera_factor_desc(FAKE, 300 * 256, 4, 300, 256, 64, 40, 1, FAKE)  # k = 104 > 96
+    assert lib.kamera_factor_workspace_size(ctypes.byref(bad), ctypes.byref(out)) == pk.KAMERA_ERR_INVALID_ARG
+    bad = pk.kamera_factor_desc(FAKE, 300 * 256, 4, 300, 4096, 16, 16, 1, FAKE)
+    assert lib.kamera_factor_workspace_size(ctypes.byref(bad), ctypes.byref(out)) == pk.KAMERA_ERR_UNSUPPORTED
+    bad = pk.kamera_factor_desc(FAKE, 100, 4, 300, 256, 16, 16, 1, FAKE)  # stride < T*D
+    assert lib.kamera_factor_workspace_size(ctypes.byref(bad), ctypes.byref(out)) == pk.KAMERA_ERR_INVALID_ARG
+    assert pk.kamera_factor_patches(d, None, FAKE, 1 << 20, FAKE, 1 << 30, None, False) == pk.KAMERA_ERR_NULL
+    assert pk.kamera_factor_patches(d, FAKE, FAKE, 1 << 20, FAKE + 16, 1 << 30, None, False) == pk.KAMERA_ERR_ALIGNMENT
+    empty = pk.kamera_factor_desc(None, 0, 0, 300, 256, 16, 16, 1, None)
+    assert pk.kamera_factor_patches(empty, None, None, 0, None, 0, None, False) == pk.KAMERA_OK

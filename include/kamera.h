@@ -222,6 +222,37 @@ kamera_status kamera_factor_workspace_size(const kamera_factor_desc* desc, size_
 kamera_status kamera_factor_patches(const kamera_factor_desc* desc, void* u_out, void* v_out, int64_t out_stride,
                                     void* workspace, size_t workspace_bytes, kamera_stream_t stream);
 
+/*
+ * kamera_factor_patches_noalloc -- the same patch formation for callers that
+ * cannot allocate device memory.  No counterpart on the Kamera page: this is
+ * a deployment convenience of this library.
+ *
+ * Who needs it: code whose device memory is owned entirely by another
+ * allocator (a serving engine that carves its KV pool and buffers out of one
+ * reservation), and plugin-style hooks whose enqueue step must neither
+ * allocate nor risk the implicit device synchronisation that cudaMalloc and
+ * cudaFree can cause.  Such callers cannot provide the workspace that
+ * kamera_factor_patches asks for.
+ *
+ * The scratch instead lives in one static device array inside this library,
+ * KAMERA_FACTOR_STATIC_SCRATCH_BYTES (16 MiB) per GPU, held by every GPU that
+ * loads the library until the process exits.  The call allocates nothing and
+ * never calls cudaMalloc / cudaFree.  Fewer CTAs may run than with a workspace
+ * of full size (as many as the 16 MiB can serve), so it can be slower; the
+ * results are the same.  A description whose single slab needs more scratch
+ * than the array holds is rejected with KAMERA_ERR_UNSUPPORTED.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents; the kernel clears what it needs, so no caller action is
+ * required -- but calls that overlap on the GPU (different streams, no
+ * ordering between them) race on the array and must not be issued.
+ */
+#define KAMERA_FACTOR_STATIC_SCRATCH_BYTES (16u << 20)
+kamera_status kamera_factor_patches_noalloc(const kamera_factor_desc* desc, void* u_out, void* v_out,
+                                            int64_t out_stride, kamera_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* kamera_status_string(kamera_status status);
 

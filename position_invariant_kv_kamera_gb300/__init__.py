@@ -26,7 +26,9 @@ KAMERA_EFLAG_CHUNK_OOB, KAMERA_EFLAG_PAGE_OOB, KAMERA_EFLAG_PATCH_OOB, KAMERA_EF
     1, 2, 4, 8, 16)
 
 EXPORTS = ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch", "kamera_factor_workspace_size",
-           "kamera_factor_patches", "kamera_status_string", "kamera_last_error", "kamera_abi_version")
+           "kamera_factor_patches", "kamera_factor_patches_noalloc", "kamera_status_string", "kamera_last_error",
+           "kamera_abi_version")
+FACTOR_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class kamera_model_desc(ctypes.Structure):
@@ -98,6 +100,8 @@ def load(build_if_missing: bool = False):
         lib.kamera_factor_workspace_size.restype = ctypes.c_int
         lib.kamera_factor_patches.argtypes = [P, P, P, ctypes.c_int64, P, ctypes.c_size_t, P]
         lib.kamera_factor_patches.restype = ctypes.c_int
+        lib.kamera_factor_patches_noalloc.argtypes = [P, P, P, ctypes.c_int64, P]
+        lib.kamera_factor_patches_noalloc.restype = ctypes.c_int
         lib.kamera_status_string.argtypes = [ctypes.c_int]
         lib.kamera_status_string.restype = ctypes.c_char_p
         lib.kamera_last_error.argtypes = []
@@ -245,4 +249,12 @@ def kamera_factor_patches(desc, u_out_ptr, v_out_ptr, out_stride, workspace_ptr,
                           raise_on_error=True) -> int:
     st = load().kamera_factor_patches(_ref(desc), u_out_ptr, v_out_ptr, int(out_stride), workspace_ptr,
                                       int(workspace_bytes), stream)
+    return _check(st, raise_on_error)
+
+
+def kamera_factor_patches_noalloc(desc, u_out_ptr, v_out_ptr, out_stride, stream, raise_on_error=True) -> int:
+    """Patch formation with the library's static scratch instead of a caller
+    workspace, for callers that must not allocate device memory (see the C
+    header for the limits and the one-call-at-a-time rule)."""
+    st = load().kamera_factor_patches_noalloc(_ref(desc), u_out_ptr, v_out_ptr, int(out_stride), stream)
     return _check(st, raise_on_error)

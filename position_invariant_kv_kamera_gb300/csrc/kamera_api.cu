@@ -520,10 +520,93 @@ kamera_status factor_patches(const kamera_factor_desc* d, void* u_out, void* v_o
   return KAMERA_OK;
 }
 
+// ---- patch formation without a caller workspace --------------------------------------------------
+// Callers that cannot allocate get their scratch from this fixed array.  In
+// host code its name is only a host-side stand-in: the device address comes
+// from cudaGetSymbolAddress, looked up once per device with that device
+// current.
+constexpr size_t kStaticScratchFloats = KAMERA_FACTOR_STATIC_SCRATCH_BYTES / sizeof(float);
+static __device__ __align__(256) float g_factor_scratch[kStaticScratchFloats];
+float* g_scratch_addr[kMaxDevices] = {};
+
+kamera_status static_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(KAMERA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_factor_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(KAMERA_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_scratch_addr[dev];
+  return KAMERA_OK;
+}
+
+kamera_status factor_patches_noalloc(const kamera_factor_desc* d, void* u_out, void* v_out, int64_t out_stride,
+                                     kamera_stream_t stream) {
+  g_last_error.clear();
+  if (kamera_status st = factor_validate(d)) return st;
+  if (d->n_slabs == 0) return KAMERA_OK;
+  if (!u_out || !v_out) return fail(KAMERA_ERR_NULL, "u_out or v_out is NULL");
+  if ((reinterpret_cast<uintptr_t>(d->delta) & 15u) || (reinterpret_cast<uintptr_t>(u_out) & 1u) ||
+      (reinterpret_cast<uintptr_t>(v_out) & 1u))
+    return fail(KAMERA_ERR_ALIGNMENT, "delta must be 16-byte aligned, outputs 2-byte");
+  if (out_stride < (int64_t)d->rank * (d->T > d->D ? d->T : d->D) && d->n_slabs > 1)
+    return fail(KAMERA_ERR_INVALID_ARG, "out_stride %lld overlaps consecutive slabs", (long long)out_stride);
+  FactorShape fs;
+  if (kamera_status st = factor_shape(d, &fs)) return st;
+  if ((size_t)fs.work_per_cta > kStaticScratchFloats)
+    return fail(KAMERA_ERR_UNSUPPORTED,
+                "one %d x %d slab at k = %d needs %lld bytes of scratch; the static region holds %zu bytes",
+                d->T, d->D, fs.kp, (long long)fs.work_per_cta * 4, (size_t)KAMERA_FACTOR_STATIC_SCRATCH_BYTES);
+  const int64_t fit = (int64_t)(kStaticScratchFloats / (size_t)fs.work_per_cta);
+  const int grid = (int)(fit < fs.grid ? fit : fs.grid);
+  float* scratch = nullptr;
+  if (kamera_status st = static_scratch(&scratch)) return st;
+  factor::FParams fp;
+  fp.delta = d->delta;
+  fp.delta_stride = d->delta_stride;
+  fp.n_slabs = d->n_slabs;
+  fp.T = d->T;
+  fp.D = d->D;
+  fp.m = d->rank;
+  fp.k = d->rank + d->oversample;
+  fp.kp = fs.kp;
+  fp.power_iters = d->power_iters;
+  fp.omega = d->omega;
+  fp.u_out = static_cast<uint16_t*>(u_out);
+  fp.v_out = static_cast<uint16_t*>(v_out);
+  fp.out_stride = out_stride;
+  fp.work = scratch;
+  fp.work_per_cta = fs.work_per_cta;
+  const uint32_t smem = factor::factor_smem_bytes();
+  {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  }
+  factor::factor_kernel<<<grid, factor::THREADS, smem, reinterpret_cast<cudaStream_t>(stream)>>>(fp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return KAMERA_OK;
+}
+
 }  // namespace
 }  // namespace kamera
 
 extern "C" {
+
+kamera_status kamera_factor_patches_noalloc(const kamera_factor_desc* desc, void* u_out, void* v_out,
+                                            int64_t out_stride, kamera_stream_t stream) {
+  return kamera::factor_patches_noalloc(desc, u_out, v_out, out_stride, stream);
+}
 
 kamera_status kamera_factor_workspace_size(const kamera_factor_desc* desc, size_t* bytes) {
   return kamera::factor_workspace_size(desc, bytes);

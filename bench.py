@@ -492,12 +492,62 @@ def run_factor(args) -> None:
     print(_json.dumps(line), flush=True)
 
 
+def run_orbit(args) -> None:
+    """Orbit deficit: the mean over 4 sampled orderings of the headline batch's
+    deficits (896 slabs of 1024 x 512 fp32 per ordering).  HBM-bound."""
+    import torch
+
+    import position_invariant_kv_kamera_gb300 as pk
+
+    torch.cuda.set_device(0)
+    n_ord, per = 4, 896 * 1024 * 512
+    g = torch.Generator(device="cuda").manual_seed(0x4B414D45)
+    d = torch.randn((n_ord, per), generator=g, device="cuda", dtype=torch.float32)
+    out = torch.empty(per, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pk.kamera_orbit_mean(d.data_ptr(), n_ord, per, per, out.data_ptr(), stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 50))
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        time.sleep(0.25)
+        b.record(stream)
+        for _ in range(steps):
+            call()
+        e.record(stream)
+        torch.cuda.synchronize()
+    sec = b.elapsed_time(e) / 1e3 / steps
+    nbytes = (n_ord + 1) * per * 4
+    peaks = measured_peaks()
+    x = d[:, : 1 << 24].double().cpu().numpy()
+    import oracle
+    t0 = time.perf_counter()
+    oracle.orbit_mean(x.astype(np.float32))
+    cpu_s = time.perf_counter() - t0
+    line = {"metric": "orbit deficit: mean over sampled orderings (slabs/s)", "value": 896 / sec, "unit": "slabs/s",
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{n_ord} orderings x 896 slabs of 1024x512 fp32 deficits"},
+            "roofline": {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": nbytes / sec / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": peaks["source"] + " (burst copy)"},
+            "cpu_baseline": {"value": (1 << 24) / (1024 * 512) / cpu_s, "unit": "slabs/s", "cores": 1,
+                             "kind": "oracle", "sample": f"2^24 elements x {n_ord} orderings ({cpu_s:.2f} s)"},
+            "gpu_launches": steps, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS) + ["patch_formation"])
+    ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS) + ["patch_formation", "orbit_mean"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--chunks", type=int, default=0,
@@ -509,6 +559,8 @@ def main(argv=None) -> None:
         run_reference(args)
     elif args.workload == "patch_formation":
         run_factor(args)
+    elif args.workload == "orbit_mean":
+        run_orbit(args)
     else:
         run_gpu(args)
 

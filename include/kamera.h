@@ -223,6 +223,19 @@ kamera_status kamera_factor_patches(const kamera_factor_desc* desc, void* u_out,
                                     void* workspace, size_t workspace_bytes, kamera_stream_t stream);
 
 /*
+ * kamera_orbit_mean -- Kamera §3 "Reorder": one orbit patch, averaged over
+ * permutations, serves every ordering of a cached set.  Given the deficits of
+ * the same slabs measured under n sampled orderings (device fp32, ordering j
+ * at deltas + j*ordering_stride, n_elems values each), write their mean
+ *     out[e] = (sum_j deltas[j*ordering_stride + e]) / n
+ * (fp32, the n terms added in index order, one correctly rounded division).
+ * The mean is the deficit that kamera_factor_patches turns into the orbit
+ * patch.  out may not overlap the inputs.  Asynchronous on `stream`.
+ */
+kamera_status kamera_orbit_mean(const float* deltas, int32_t n_orderings, int64_t ordering_stride, int64_t n_elems,
+                                float* out, kamera_stream_t stream);
+
+/*
  * kamera_factor_patches_noalloc -- the same patch formation for callers that
  * cannot allocate device memory.  No counterpart on the Kamera page: this is
  * a deployment convenience of this library.

@@ -101,6 +101,8 @@ def _declare(lib):
     lib.oracle_reuse.argtypes = [ctypes.POINTER(Model), P, i32] + [P, P, P, i32] + [P, P, P, i32, i32] + [
         P, P, i32, P, i32, i32, i64, i32, P, P, P, P, P, P]
     lib.oracle_reuse.restype = i32
+    lib.oracle_orbit_mean.argtypes = [P, i32, i64, i64, P]
+    lib.oracle_orbit_mean.restype = None
     lib.oracle_jacobi_svd.argtypes = [P, i32, i32, P, P, i32]
     lib.oracle_jacobi_svd.restype = i32
     return lib
@@ -248,3 +250,14 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
     tests' reading of bf16 buffers does not depend on the CUDA path."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return b.view(np.float32).astype(np.float64)
+
+
+def orbit_mean(deltas, lib=None) -> np.ndarray:
+    """Mean over the leading axis (the sampled orderings) of fp32 deficits, in fp64."""
+    lib = lib or load()
+    d = np.ascontiguousarray(deltas, dtype=np.float32)
+    n = int(d.shape[0])
+    per = int(d.size // max(n, 1))
+    out = np.zeros(per, np.float64)
+    lib.oracle_orbit_mean(_ptr(d), n, per, per, _ptr(out))
+    return out.reshape(d.shape[1:])

@@ -387,3 +387,17 @@ int32_t oracle_jacobi_svd(double* a, int32_t rows, int32_t cols, double* v, doub
   }
   return sweep;
 }
+
+/*
+ * Orbit deficit (Kamera §3, "Reorder"): one orbit patch, averaged over
+ * permutations, serves every ordering of a cached set.  The deficit it
+ * factors is the mean of the deficits measured under n sampled orderings:
+ *     out[e] = (1/n) * sum_j deltas[j*stride + e].
+ */
+void oracle_orbit_mean(const float* deltas, int32_t n, int64_t stride, int64_t n_elems, double* out) {
+  for (int64_t e = 0; e < n_elems; ++e) {
+    double s = 0.0;
+    for (int32_t j = 0; j < n; ++j) s += (double)deltas[(int64_t)j * stride + e];
+    out[e] = s / (double)n;
+  }
+}

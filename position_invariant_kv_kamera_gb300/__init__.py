@@ -26,8 +26,8 @@ KAMERA_EFLAG_CHUNK_OOB, KAMERA_EFLAG_PAGE_OOB, KAMERA_EFLAG_PATCH_OOB, KAMERA_EF
     1, 2, 4, 8, 16)
 
 EXPORTS = ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch", "kamera_factor_workspace_size",
-           "kamera_factor_patches", "kamera_factor_patches_noalloc", "kamera_status_string", "kamera_last_error",
-           "kamera_abi_version")
+           "kamera_factor_patches", "kamera_factor_patches_noalloc", "kamera_orbit_mean", "kamera_status_string",
+           "kamera_last_error", "kamera_abi_version")
 FACTOR_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -102,6 +102,8 @@ def load(build_if_missing: bool = False):
         lib.kamera_factor_patches.restype = ctypes.c_int
         lib.kamera_factor_patches_noalloc.argtypes = [P, P, P, ctypes.c_int64, P]
         lib.kamera_factor_patches_noalloc.restype = ctypes.c_int
+        lib.kamera_orbit_mean.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, P, P]
+        lib.kamera_orbit_mean.restype = ctypes.c_int
         lib.kamera_status_string.argtypes = [ctypes.c_int]
         lib.kamera_status_string.restype = ctypes.c_char_p
         lib.kamera_last_error.argtypes = []
@@ -257,4 +259,10 @@ def kamera_factor_patches_noalloc(desc, u_out_ptr, v_out_ptr, out_stride, stream
     workspace, for callers that must not allocate device memory (see the C
     header for the limits and the one-call-at-a-time rule)."""
     st = load().kamera_factor_patches_noalloc(_ref(desc), u_out_ptr, v_out_ptr, int(out_stride), stream)
+    return _check(st, raise_on_error)
+
+
+def kamera_orbit_mean(deltas_ptr, n_orderings, ordering_stride, n_elems, out_ptr, stream, raise_on_error=True) -> int:
+    """Mean of deficits sampled under n orderings (the orbit deficit)."""
+    st = load().kamera_orbit_mean(deltas_ptr, int(n_orderings), int(ordering_stride), int(n_elems), out_ptr, stream)
     return _check(st, raise_on_error)

@@ -520,6 +520,31 @@ kamera_status factor_patches(const kamera_factor_desc* d, void* u_out, void* v_o
   return KAMERA_OK;
 }
 
+kamera_status orbit_mean(const float* deltas, int32_t n, int64_t stride, int64_t n_elems, float* out,
+                         kamera_stream_t stream) {
+  g_last_error.clear();
+  if (n < 1) return fail(KAMERA_ERR_INVALID_ARG, "n_orderings = %d", n);
+  if (n_elems < 0) return fail(KAMERA_ERR_INVALID_ARG, "n_elems = %lld", (long long)n_elems);
+  if (n > 1 && stride < n_elems) return fail(KAMERA_ERR_INVALID_ARG, "ordering_stride < n_elems");
+  if (n_elems == 0) return KAMERA_OK;
+  if (!deltas || !out) return fail(KAMERA_ERR_NULL, "deltas or out is NULL");
+  if ((reinterpret_cast<uintptr_t>(deltas) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+    return fail(KAMERA_ERR_ALIGNMENT, "deltas and out must be 4-byte aligned");
+  const char* lo_in = reinterpret_cast<const char*>(deltas);
+  const char* hi_in = lo_in + ((int64_t)(n - 1) * stride + n_elems) * 4;
+  const char* lo_out = reinterpret_cast<const char*>(out);
+  if (lo_out < hi_in && lo_in < lo_out + n_elems * 4) return fail(KAMERA_ERR_INVALID_ARG, "out overlaps the inputs");
+  int dev = 0;
+  DeviceFacts* facts = nullptr;
+  if (kamera_status st = device_facts(&dev, &facts)) return st;
+  const int64_t want = (n_elems / 4 + 255) / 256;
+  const int grid = (int)(want < 8LL * facts->sms ? (want > 0 ? want : 1) : 8LL * facts->sms);
+  factor::orbit_mean_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(deltas, n, stride, n_elems, out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return KAMERA_OK;
+}
+
 // ---- patch formation without a caller workspace --------------------------------------------------
 // Callers that cannot allocate get their scratch from this fixed array.  In
 // host code its name is only a host-side stand-in: the device address comes
@@ -606,6 +631,11 @@ extern "C" {
 kamera_status kamera_factor_patches_noalloc(const kamera_factor_desc* desc, void* u_out, void* v_out,
                                             int64_t out_stride, kamera_stream_t stream) {
   return kamera::factor_patches_noalloc(desc, u_out, v_out, out_stride, stream);
+}
+
+kamera_status kamera_orbit_mean(const float* deltas, int32_t n_orderings, int64_t ordering_stride, int64_t n_elems,
+                                float* out, kamera_stream_t stream) {
+  return kamera::orbit_mean(deltas, n_orderings, ordering_stride, n_elems, out, stream);
 }
 
 kamera_status kamera_factor_workspace_size(const kamera_factor_desc* desc, size_t* bytes) {

@@ -176,3 +176,12 @@ def test_factor_validation(lib):
     assert pk.kamera_factor_patches(d, FAKE, FAKE, 1 << 20, FAKE + 16, 1 << 30, None, False) == pk.KAMERA_ERR_ALIGNMENT
     empty = pk.kamera_factor_desc(None, 0, 0, 300, 256, 16, 16, 1, None)
     assert pk.kamera_factor_patches(empty, None, None, 0, None, 0, None, False) == pk.KAMERA_OK
+
+
+def test_orbit_mean_validation(lib):
+    assert pk.kamera_orbit_mean(FAKE, 0, 100, 100, FAKE + (1 << 20), None, False) == pk.KAMERA_ERR_INVALID_ARG
+    assert pk.kamera_orbit_mean(FAKE, 3, 50, 100, FAKE + (1 << 20), None, False) == pk.KAMERA_ERR_INVALID_ARG
+    assert pk.kamera_orbit_mean(None, 3, 100, 100, FAKE + (1 << 20), None, False) == pk.KAMERA_ERR_NULL
+    assert pk.kamera_orbit_mean(FAKE, 3, 100, 100, FAKE + 4, None, False) == pk.KAMERA_ERR_INVALID_ARG  # overlap
+    assert pk.kamera_orbit_mean(FAKE + 2, 3, 100, 100, FAKE + (1 << 20), None, False) == pk.KAMERA_ERR_ALIGNMENT
+    assert pk.kamera_orbit_mean(FAKE, 3, 100, 0, FAKE, None, False) == pk.KAMERA_OK

@@ -269,3 +269,11 @@ def test_mrope_equal_shifts_is_plain_rope_and_group_law(oracle_lib):
     # no sections: every pair takes the first shift
     np.testing.assert_array_equal(oracle.rotate_region_sections(x, th, (5, 6, 7), (0, 0, 0)),
                                   oracle.rotate_region(x, th, 5))
+
+
+def test_orbit_mean_is_the_library_mean(oracle_lib):
+    """Kamera §3 reorder: the orbit deficit is the mean over sampled orderings."""
+    d = rng.standard_normal((5, 7, 33)).astype(np.float32)
+    np.testing.assert_allclose(oracle.orbit_mean(d), d.astype(np.float64).mean(axis=0), rtol=0, atol=1e-15)
+    one = rng.standard_normal((1, 10)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.orbit_mean(one), one[0].astype(np.float64))

@@ -459,7 +459,7 @@ kamera_status factor_shape(const kamera_factor_desc* d, FactorShape* fs) {
   if (kamera_status st = device_facts(&dev, &facts)) return st;
   const int k = d->rank + d->oversample;
   fs->kp = (k + 15) / 16 * 16;
-  fs->grid = d->n_slabs < facts->sms ? d->n_slabs : facts->sms;
+  fs->grid = d->n_slabs < 2 * facts->sms ? d->n_slabs : 2 * facts->sms;  // two CTAs per SM
   fs->work_per_cta = (int64_t)fs->kp * (d->T + 2 * (int64_t)d->D);
   return KAMERA_OK;
 }
@@ -505,12 +505,13 @@ kamera_status factor_patches(const kamera_factor_desc* d, void* u_out, void* v_o
   fp.out_stride = out_stride;
   fp.work = static_cast<float*>(workspace);
   fp.work_per_cta = fs.work_per_cta;
-  const uint32_t smem = factor::factor_smem_bytes();
+  const uint32_t smem = factor::factor_smem_bytes(fs.kp, d->rank);
   {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)factor::factor_smem_bytes(factor::KMAX, 64));
     });
     if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   }
@@ -608,12 +609,13 @@ kamera_status factor_patches_noalloc(const kamera_factor_desc* d, void* u_out, v
   fp.out_stride = out_stride;
   fp.work = scratch;
   fp.work_per_cta = fs.work_per_cta;
-  const uint32_t smem = factor::factor_smem_bytes();
+  const uint32_t smem = factor::factor_smem_bytes(fs.kp, d->rank);
   {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)factor::factor_smem_bytes(factor::KMAX, 64));
     });
     if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   }

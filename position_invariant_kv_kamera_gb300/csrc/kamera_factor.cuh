@@ -16,12 +16,13 @@
 //   Q = orth(Y);  q times: Z = orth(Delta^T Q), Q = orth(Delta Z);
 //   B = Q^T Delta  [k][D];  C = B B^T = W Lambda W^T (cyclic Jacobi);
 //   U_m = Q W_m (orthonormal columns),  V_m = B^T W_m (carries Sigma).
-// orth() is classical Gram-Schmidt applied twice per column; a column whose
-// remainder falls below 1e-4 of its norm is dropped (set to zero), so deficits
-// of rank below k are handled exactly.
+// orth() is block classical Gram-Schmidt with reorthogonalisation; a column
+// whose remainder falls below 1e-4 of its norm is dropped (set to zero), so
+// deficits of rank below k are handled exactly.
 //
-// One CTA (256 threads) per slab at a time; each CTA owns a workspace region
-// (Y [k][T], Z [k][D], B [k][D], column-major panels) in global memory.
+// One CTA (256 threads, two per SM) per slab at a time; each CTA owns a
+// workspace region (Y [k][T], Z [k][D], B [k][D], column-major panels) in
+// global memory.
 #pragma once
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -47,14 +48,26 @@ struct FParams {
   int64_t work_per_cta;  // floats
 };
 
-// ---- CTA-wide fp32 GEMM: C(i,j) = sum_l A(i,l) B(l,j), arbitrary strides --------------
-// Element (i,l) of A is A[i*a_rs + l*a_cs], and so on.  Tiles of 64x64, K step
-// 16, 256 threads each owning a 4x4 block.  Out-of-range elements read as 0.
-template <typename OutT>
+// ---- CTA-wide fp32 GEMM: C(i,j) = alpha * sum_l A(i,l) B(l,j) (+ C(i,j)) ------------------
+// Element (i,l) of A is A[i*a_rs + l*a_cs], and so on.  kAK: A is contiguous
+// along K (a_cs == 1), else along M (a_rs == 1); kBK: B is contiguous along K
+// (b_rs == 1), else along N (b_cs == 1).  Each operand tile sits in shared
+// memory in its own orientation, so that global loads are coalesced and the
+// tile is written without a transposition: K-contiguous tiles as [row][20]
+// (16 used), the others as [16][64].  Every shared read is 16 bytes: four K
+// values of one row, or four rows / columns of one K index.  Tiles of 64x64,
+// K step 16, 256 threads; thread (ty, tx) owns rows 4ty..4ty+3 and columns
+// tx + 16y (K-contiguous B) or 4tx..4tx+3; the next K step is fetched into
+// registers while the current one multiplies.  Out-of-range elements read as 0.
+constexpr int KS = GK + 4;  // row stride of K-contiguous tiles (16-byte aligned rows)
+constexpr int TILE_FLOATS = GT * KS;
+
+template <typename OutT, bool kAcc, bool kAK, bool kBK>
 __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t a_cs, const float* B, int64_t b_rs,
-                     int64_t b_cs, OutT* C, int64_t c_rs, int64_t c_cs, float* sA, float* sB) {
+                     int64_t b_cs, OutT* C, int64_t c_rs, int64_t c_cs, float* sA, float* sB, float alpha = 1.f) {
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
+  constexpr int PER = GK * GT / THREADS;  // 4 elements of each operand per thread and K step
   for (int i0 = 0; i0 < M; i0 += GT) {
     for (int j0 = 0; j0 < N; j0 += GT) {
       float acc[4][4];
@@ -62,45 +75,81 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-      for (int l0 = 0; l0 < K; l0 += GK) {
-        // sA[l][i] (16 x 64), sB[l][j] (16 x 64); read along the contiguous dimension
-        for (int e = tid; e < GK * GT; e += THREADS) {
-          int i, l;
-          if (a_cs == 1) { l = e % GK; i = e / GK; } else { i = e % GT; l = e / GT; }
+      float ra[PER], rb[PER];
+      auto fetch = [&](int l0) {
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+          const int e = tid + r * THREADS;
+          const int i = kAK ? e / GK : e % GT, l = kAK ? e % GK : e / GT;
           const int gi = i0 + i, gl = l0 + l;
-          sA[l * GT + i] = (gi < M && gl < K) ? A[gi * a_rs + gl * a_cs] : 0.f;
-          int j, l2;
-          if (b_rs == 1) { l2 = e % GK; j = e / GK; } else { j = e % GT; l2 = e / GT; }
+          ra[r] = (gi < M && gl < K) ? A[gi * a_rs + gl * a_cs] : 0.f;
+          const int j = kBK ? e / GK : e % GT, l2 = kBK ? e % GK : e / GT;
           const int gj = j0 + j, gl2 = l0 + l2;
-          sB[l2 * GT + j] = (gj < N && gl2 < K) ? B[gl2 * b_rs + gj * b_cs] : 0.f;
+          rb[r] = (gj < N && gl2 < K) ? B[gl2 * b_rs + gj * b_cs] : 0.f;
         }
-        __syncthreads();
+      };
+      auto stash = [&]() {
 #pragma unroll
-        for (int l = 0; l < GK; ++l) {
-          float a[4], b[4];
+        for (int r = 0; r < PER; ++r) {
+          const int e = tid + r * THREADS;
+          if (kAK) sA[(e / GK) * KS + e % GK] = ra[r];
+          else sA[(e / GT) * GT + e % GT] = ra[r];
+          if (kBK) sB[(e / GK) * KS + e % GK] = rb[r];
+          else sB[(e / GT) * GT + e % GT] = rb[r];
+        }
+      };
+      fetch(0);
+      stash();
+      __syncthreads();
+      for (int l0 = 0; l0 < K; l0 += GK) {
+        const bool more = l0 + GK < K;
+        if (more) fetch(l0 + GK);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            a[q] = sA[l * GT + ty * 4 + q];
-            b[q] = sB[l * GT + tx * 4 + q];
+        for (int l4 = 0; l4 < GK; l4 += 4) {
+          float a[4][4], b[4][4];  // [row or column][k]
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            if (kAK) {
+              const float4 v = *reinterpret_cast<const float4*>(sA + (ty * 4 + x) * KS + l4);
+              a[x][0] = v.x; a[x][1] = v.y; a[x][2] = v.z; a[x][3] = v.w;
+            } else {
+              const float4 v = *reinterpret_cast<const float4*>(sA + (l4 + x) * GT + ty * 4);
+              a[0][x] = v.x; a[1][x] = v.y; a[2][x] = v.z; a[3][x] = v.w;
+            }
+            if (kBK) {
+              const float4 v = *reinterpret_cast<const float4*>(sB + (tx + 16 * x) * KS + l4);
+              b[x][0] = v.x; b[x][1] = v.y; b[x][2] = v.z; b[x][3] = v.w;
+            } else {
+              const float4 v = *reinterpret_cast<const float4*>(sB + (l4 + x) * GT + tx * 4);
+              b[0][x] = v.x; b[1][x] = v.y; b[2][x] = v.z; b[3][x] = v.w;
+            }
           }
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
+          for (int l = 0; l < 4; ++l)
 #pragma unroll
-            for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+              for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x][l], b[y][l], acc[x][y]);
         }
         __syncthreads();
+        if (more) {
+          stash();
+          __syncthreads();
+        }
       }
 #pragma unroll
       for (int x = 0; x < 4; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
-          const int gi = i0 + ty * 4 + x, gj = j0 + tx * 4 + y;
+          const int gi = i0 + ty * 4 + x, gj = j0 + (kBK ? tx + 16 * y : tx * 4 + y);
           if (gi < M && gj < N) {
+            float v = alpha * acc[x][y];
+            if constexpr (kAcc) v += C[gi * c_rs + gj * c_cs];
             if constexpr (sizeof(OutT) == 2) {
-              __nv_bfloat16 h = __float2bfloat16_rn(acc[x][y]);
+              __nv_bfloat16 h = __float2bfloat16_rn(v);
               C[gi * c_rs + gj * c_cs] = *reinterpret_cast<uint16_t*>(&h);
             } else {
-              C[gi * c_rs + gj * c_cs] = acc[x][y];
+              C[gi * c_rs + gj * c_cs] = v;
             }
           }
         }
@@ -120,38 +169,56 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
+constexpr int OB = 16;  // column block of the block Gram-Schmidt
+
 // Orthonormalise the k columns (length n, column j at X + j*n) in place by
-// classical Gram-Schmidt applied twice; dependent columns become zero.
-__device__ void orth_cgs2(float* X, int n, int k, float* coef, float* red) {
+// block classical Gram-Schmidt with reorthogonalisation: each block of 16
+// columns is projected off the finished columns twice (two GEMMs per pass),
+// then orthonormalised column by column inside the block (classical
+// Gram-Schmidt, twice).  A column whose remainder falls below 1e-4 of its
+// original norm is dependent and becomes zero.
+__device__ void orth_block(float* X, int n, int k, float* cblk, float* norms, float* red, float* sA, float* sB) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int j = 0; j < k; ++j) {
-    float* v = X + (int64_t)j * n;
-    float n0 = 0.f;
-    for (int t = tid; t < n; t += THREADS) n0 += v[t] * v[t];
-    n0 = sqrtf(block_sum(n0, red));
-    for (int pass = 0; pass < 2 && j > 0; ++pass) {
-      // coef[l] = <q_l, v>, one warp per column l
-      for (int l = warp; l < j; l += THREADS / 32) {
-        const float* ql = X + (int64_t)l * n;
-        float s = 0.f;
-        for (int t = lane; t < n; t += 32) s += ql[t] * v[t];
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-        if (lane == 0) coef[l] = s;
+  for (int J0 = 0; J0 < k; J0 += OB) {
+    const int b = min(OB, k - J0);
+    float* XJ = X + (int64_t)J0 * n;
+    for (int j = 0; j < b; ++j) {
+      float s = 0.f;
+      for (int t = tid; t < n; t += THREADS) s += XJ[(int64_t)j * n + t] * XJ[(int64_t)j * n + t];
+      s = block_sum(s, red);
+      if (tid == 0) norms[j] = sqrtf(s);
+    }
+    __syncthreads();
+    for (int pass = 0; pass < 2 && J0 > 0; ++pass) {
+      // cblk [J0][b] = Q_<J0^T X_J ;  X_J -= Q_<J0 cblk
+      gemm<float, false, true, true>(J0, b, n, X, n, 1, XJ, 1, n, cblk, b, 1, sA, sB);
+      gemm<float, true, false, false>(n, b, J0, X, 1, n, cblk, b, 1, XJ, 1, n, sA, sB, -1.f);
+    }
+    for (int j = 0; j < b; ++j) {
+      float* v = XJ + (int64_t)j * n;
+      for (int pass = 0; pass < 2 && j > 0; ++pass) {
+        for (int l = warp; l < j; l += THREADS / 32) {
+          const float* ql = XJ + (int64_t)l * n;
+          float s = 0.f;
+          for (int t = lane; t < n; t += 32) s += ql[t] * v[t];
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+          if (lane == 0) cblk[l] = s;
+        }
+        __syncthreads();
+        for (int t = tid; t < n; t += THREADS) {
+          float s = v[t];
+          for (int l = 0; l < j; ++l) s -= cblk[l] * XJ[(int64_t)l * n + t];
+          v[t] = s;
+        }
+        __syncthreads();
       }
-      __syncthreads();
-      for (int t = tid; t < n; t += THREADS) {
-        float s = v[t];
-        for (int l = 0; l < j; ++l) s -= coef[l] * X[(int64_t)l * n + t];
-        v[t] = s;
-      }
+      float nr = 0.f;
+      for (int t = tid; t < n; t += THREADS) nr += v[t] * v[t];
+      nr = sqrtf(block_sum(nr, red));
+      const float scale = (nr > 1e-4f * norms[j] && nr > 0.f) ? 1.f / nr : 0.f;
+      for (int t = tid; t < n; t += THREADS) v[t] *= scale;
       __syncthreads();
     }
-    float nr = 0.f;
-    for (int t = tid; t < n; t += THREADS) nr += v[t] * v[t];
-    nr = sqrtf(block_sum(nr, red));
-    const float scale = (nr > 1e-4f * n0 && nr > 0.f) ? 1.f / nr : 0.f;
-    for (int t = tid; t < n; t += THREADS) v[t] *= scale;
-    __syncthreads();
   }
 }
 
@@ -173,7 +240,7 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
     }
     off = block_sum(off, red);
     tot = block_sum(tot, red);
-    if (off <= 1e-12f * tot || tot == 0.f) break;
+    if (off <= 1e-10f * tot || tot == 0.f) break;
     for (int round = 0; round < kp - 1; ++round) {
       // pair i: players (i, kp-1-i) of the rotated ring; player 0 stays fixed
       if (tid < half) {
@@ -204,9 +271,10 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
         C[q * kp + j] = s * xp + c * xq;
       }
       __syncthreads();
-      // columns p, q of C and of W  (C <- C J, W <- W J)
+      // columns p, q of C and of W  (C <- C J, W <- W J); consecutive threads
+      // take different planes so that the column accesses spread over banks
       for (int e = tid; e < half * kp; e += THREADS) {
-        const int i = e / kp, j = e % kp;
+        const int i = e % half, j = e / half;
         const int p = (int)rot[4 * i], q = (int)rot[4 * i + 1];
         const float c = rot[4 * i + 2], s = rot[4 * i + 3];
         float xp = C[j * kp + p], xq = C[j * kp + q];
@@ -222,19 +290,25 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
   }
 }
 
-__global__ void __launch_bounds__(THREADS, 1) factor_kernel(const __grid_constant__ FParams p) {
-  extern __shared__ __align__(16) float fsm[];
-  float* sA = fsm;                       // GT*GK
-  float* sB = sA + GT * GK;              // GT*GK
-  float* C = sB + GT * GK;               // kp*kp
-  float* W = C + KMAX * KMAX;            // kp*kp
-  float* Ws = W + KMAX * KMAX;           // kp*m: sorted leading eigenvectors
-  float* coef = Ws + KMAX * 64;          // KMAX
-  float* rot = coef + KMAX;              // 4 * KMAX/2
-  float* red = rot + 2 * KMAX;           // 32
-  int* perm = reinterpret_cast<int*>(red + 32);  // KMAX
+// Shared memory of one CTA, in floats, for a given kp and m.
+__host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
+  return 2 * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + OB + 2 * kp + 32 + kp;
+}
 
+__global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
+  extern __shared__ __align__(16) float fsm[];
   const int T = p.T, D = p.D, k = p.k, kp = p.kp, m = p.m;
+  float* sA = fsm;                    // TILE_FLOATS
+  float* sB = sA + TILE_FLOATS;       // TILE_FLOATS
+  float* C = sB + TILE_FLOATS;        // kp*kp
+  float* W = C + kp * kp;             // kp*kp
+  float* Ws = W + kp * kp;            // kp*m: sorted leading eigenvectors
+  float* cblk = Ws + kp * m;          // kp*OB: block Gram-Schmidt coefficients
+  float* norms = cblk + kp * OB;      // OB
+  float* rot = norms + OB;            // 2*kp
+  float* red = rot + 2 * kp;          // 32
+  int* perm = reinterpret_cast<int*>(red + 32);  // kp
+
   float* Y = p.work + blockIdx.x * p.work_per_cta;  // [kp][T] column-major
   float* Z = Y + (int64_t)kp * T;                   // [kp][D]
   float* B = Z + (int64_t)kp * D;                   // [kp][D]: row i of B contiguous
@@ -246,18 +320,18 @@ __global__ void __launch_bounds__(THREADS, 1) factor_kernel(const __grid_constan
     // Y = Delta Omega (columns k..kp-1 stay zero)
     for (int64_t e = threadIdx.x; e < (int64_t)kp * T; e += THREADS) Y[e] = 0.f;
     __syncthreads();
-    gemm<float>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
-    orth_cgs2(Y, T, k, coef, red);
+    gemm<float, false, true, false>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
+    orth_block(Y, T, k, cblk, norms, red, sA, sB);
     for (int it = 0; it < p.power_iters; ++it) {
-      gemm<float>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);  // Z = Delta^T Q
-      orth_cgs2(Z, D, k, coef, red);
-      gemm<float>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);  // Y = Delta Z
-      orth_cgs2(Y, T, k, coef, red);
+      gemm<float, false, false, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);  // Z = Delta^T Q
+      orth_block(Z, D, k, cblk, norms, red, sA, sB);
+      gemm<float, false, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);  // Y = Delta Z
+      orth_block(Y, T, k, cblk, norms, red, sA, sB);
     }
-    gemm<float>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);    // B = Q^T Delta
+    gemm<float, false, true, false>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);    // B = Q^T Delta
     for (int e = threadIdx.x; e < kp * kp; e += THREADS) C[e] = 0.f;
     __syncthreads();
-    gemm<float>(k, k, D, B, D, 1, B, 1, D, C, kp, 1, sA, sB);   // C = B B^T
+    gemm<float, false, true, true>(k, k, D, B, D, 1, B, 1, D, C, kp, 1, sA, sB);   // C = B B^T
     jacobi_eig(C, W, kp, rot, red);
     // order the eigenpairs by decreasing eigenvalue (ties by index)
     for (int i = threadIdx.x; i < kp; i += THREADS) {
@@ -277,8 +351,8 @@ __global__ void __launch_bounds__(THREADS, 1) factor_kernel(const __grid_constan
     __syncthreads();
     uint16_t* uo = p.u_out + (int64_t)s * p.out_stride;
     uint16_t* vo = p.v_out + (int64_t)s * p.out_stride;
-    gemm<uint16_t>(T, m, kp, Y, 1, T, Ws, m, 1, uo, m, 1, sA, sB);  // U_m = Q W_m
-    gemm<uint16_t>(D, m, kp, B, 1, D, Ws, m, 1, vo, m, 1, sA, sB);  // V_m = B^T W_m
+    gemm<uint16_t, false, false, false>(T, m, kp, Y, 1, T, Ws, m, 1, uo, m, 1, sA, sB);  // U_m = Q W_m
+    gemm<uint16_t, false, false, false>(D, m, kp, B, 1, D, Ws, m, 1, vo, m, 1, sA, sB);  // V_m = B^T W_m
   }
 }
 
@@ -319,9 +393,8 @@ __global__ void orbit_mean_kernel(const float* __restrict__ d, int n, int64_t st
   }
 }
 
-__host__ __device__ constexpr uint32_t factor_smem_bytes() {
-  return (uint32_t)sizeof(float) * (2 * GT * GK + 2 * KMAX * KMAX + KMAX * 64 + KMAX + 2 * KMAX + 32) +
-         (uint32_t)sizeof(int) * KMAX;
+__host__ __device__ constexpr uint32_t factor_smem_bytes(int kp, int m) {
+  return (uint32_t)sizeof(float) * (uint32_t)factor_smem_floats(kp, m);
 }
 
 }  // namespace factor

@@ -1,0 +1,169 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each mutant plants one mistake -- a flipped sign, a swapped or shifted index,
+a dropped term, a transposed operand, an off-by-one -- into a copy of the
+oracle's C source, builds it, and runs the independent checks below (complex
+RoPE, M-RoPE, library matmul, brute-force page map, the vectorised whole-batch
+formulation, library SVD, library mean).  Every mutant must fail at least one.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.test_oracle_operator import CASES, _independent_reuse, _oracle_model
+from tests.test_oracle_pins import _theta_np, mrope_complex, rope_complex
+
+SRC = open(oracle._SRC).read()
+rng = np.random.default_rng(99)
+
+MUTANTS = [
+    ("rotation sign", "x[ia] = a * c - b * s;", "x[ia] = a * c + b * s;"),
+    ("partner update sign", "x[ib] = b * c + a * s;", "x[ib] = b * c - a * s;"),
+    ("theta exponent", "pow(base, -2.0 * (double)i / (double)rope_dim)", "pow(base, -1.0 * (double)i / (double)rope_dim)"),
+    ("delta sign", "double phi = (double)delta * theta[i];", "double phi = -(double)delta * theta[i];"),
+    ("section delta sign", "double phi = (double)deltas[s] * theta[i];", "double phi = (double)deltas[0] * theta[i];"),
+    ("section boundary", "if (i >= sections[0]) s = 1;", "if (i > sections[0]) s = 1;"),
+    ("V rotated instead of K", "if (channel != 0) return;", "if (channel != 1) return;"),
+    ("MLA rotates c_KV", "oracle_rotate_region_sections(row + m->latent_dim,", "oracle_rotate_region_sections(row + 0,"),
+    ("patch operand transposed", "acc += u[r] * vmat[(int64_t)j * rank + r];", "acc += u[r] * vmat[(int64_t)r * D + j];"),
+    ("patch dropped", "for (int32_t j = 0; j < D; ++j) out[j] += patch[j];",
+     "for (int32_t j = 0; j < D; ++j) out[j] += 0.0 * patch[j];"),
+    ("frame swapped", "if (m->patch_frame == OR_PATCH_CANONICAL_FRAME) {", "if (m->patch_frame != OR_PATCH_CANONICAL_FRAME) {"),
+    ("slot from page index", "return page * page_size + pos % page_size;", "return page * page_size + pos / page_size % page_size;"),
+    ("block index off by one", "int64_t blk = pos / page_size;", "int64_t blk = (pos + 1) / page_size;"),
+    ("store layer/channel order", "const int64_t sb = store_off[item->chunk_id] + (((int64_t)l * n_ch + ch) * T + t) * D;",
+     "const int64_t sb = store_off[item->chunk_id] + (((int64_t)ch * L + l) * T + t) * D;"),
+    ("U row shifted", "(int64_t)t * rank;", "(int64_t)(t + 1 < T ? t + 1 : t) * rank;"),
+    ("Jacobi rotation sign", "a[(int64_t)k * cols + p] = c * ap - s * aq;", "a[(int64_t)k * cols + p] = c * ap + s * aq;"),
+    ("singular values ascending", "if (sigma[k] > sigma[best]) best = k;", "if (sigma[k] < sigma[best]) best = k;"),
+    ("orbit mean divisor", "out[e] = s / (double)n;", "out[e] = s / (double)(n + 1);"),
+]
+
+
+def _build(tmp_path, name, src):
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(src)
+    oracle.build(str(c), str(so))
+    return oracle.load(str(so))
+
+
+# ---- independent checks, each raising AssertionError on a mismatch ----------------------------------------
+
+def c_theta(lib):
+    np.testing.assert_allclose(oracle.theta(1e6, 128, lib=lib), _theta_np(1e6, 128), rtol=1e-14)
+
+
+def c_rope(lib):
+    for pairing in (oracle.ROTATE_HALF, oracle.INTERLEAVED):
+        th = _theta_np(1e4, 64)
+        x = rng.standard_normal(64)
+        got = oracle.rotate_region(rope_complex(x, 5, th, pairing), th, 1234, pairing, lib=lib)
+        np.testing.assert_allclose(got, rope_complex(x, 1239, th, pairing), atol=1e-9)
+
+
+def c_row(lib):
+    m = oracle.model(oracle.GQA, 1, num_kv_heads=2, head_dim=64)
+    th = _theta_np(1e4, 64)
+    x = rng.standard_normal(128)
+    k = oracle.rotate_row(m, th, 0, 77, x, lib=lib)
+    for h in range(2):
+        np.testing.assert_allclose(k[h * 64:(h + 1) * 64], rope_complex(x[h * 64:(h + 1) * 64], 77, th), atol=1e-11)
+    np.testing.assert_array_equal(oracle.rotate_row(m, th, 1, 77, x, lib=lib), x)
+
+
+def c_mla(lib):
+    m = oracle.model(oracle.MLA, 1, rope_dim=64, latent_dim=128)
+    th = _theta_np(1e4, 64)
+    x = rng.standard_normal(192)
+    y = oracle.rotate_row(m, th, 0, 999, x, lib=lib)
+    np.testing.assert_array_equal(y[:128], x[:128])
+    np.testing.assert_allclose(y[128:], rope_complex(x[128:], 999, th), atol=1e-11)
+
+
+def c_mrope(lib):
+    th = _theta_np(1e6, 128)
+    sec = (16, 24, 24)
+    x = rng.standard_normal(128)
+    got = oracle.rotate_region_sections(mrope_complex(x, (1, 2, 3), th, sec), th, (100, -7, 40), sec, lib=lib)
+    np.testing.assert_allclose(got, mrope_complex(x, (101, -5, 43), th, sec), atol=1e-9)
+
+
+def c_patch(lib):
+    m = oracle.model(oracle.GQA, 1, num_kv_heads=2, head_dim=64)
+    th = _theta_np(1e4, 64)
+    src, u, V = rng.standard_normal(128), rng.standard_normal(8), rng.standard_normal((128, 8))
+    np.testing.assert_allclose(oracle.row(m, th, 1, 0, src, u, V, lib=lib), src + V @ u, atol=1e-12)
+    want = oracle.rotate_row(m, th, 0, 33, src, lib=lib) + V @ u
+    np.testing.assert_allclose(oracle.row(m, th, 0, 33, src, u, V, lib=lib), want, atol=1e-12)
+
+
+def c_frame(lib):
+    ma = oracle.model(oracle.GQA, 1, num_kv_heads=1, head_dim=64)
+    mc = oracle.model(oracle.GQA, 1, num_kv_heads=1, head_dim=64, patch_frame=oracle.PATCH_CANONICAL_FRAME)
+    th = _theta_np(1e4, 64)
+    src, u, V = rng.standard_normal(64), rng.standard_normal(8), rng.standard_normal((64, 8))
+    want = rope_complex(src + V @ u, 50, th)
+    np.testing.assert_allclose(oracle.row(mc, th, 0, 50, src, u, V, lib=lib), want, atol=1e-11)
+    np.testing.assert_allclose(oracle.row(ma, th, 0, 50, src, u, V, lib=lib), rope_complex(src, 50, th) + V @ u,
+                               atol=1e-11)
+
+
+def c_slot(lib):
+    P, mp, num_pages = 16, 5, 12
+    bt = rng.permutation(num_pages)[:mp].reshape(1, mp).astype(np.int32)
+    for pos in range(mp * P):
+        assert oracle.slot(bt, mp, num_pages, P, 0, pos, lib=lib) == int(bt[0, pos // P]) * P + pos % P
+
+
+def c_reuse(lib):
+    for case in ("gqa_rank16", "mla_rank8", "gqa_interleaved_canonical"):
+        wl = CASES[case]()
+        m = _oracle_model(wl)
+        th = oracle.theta(wl.rope_base, wl.rope_dim)
+        err, pk, pv, wk, wv = oracle.reuse(
+            m, th, oracle.MODE_REUSE, store=wl.host_store(), store_off=wl.store_off,
+            store_len=np.array(wl.chunk_lens, np.int32), patch=wl.host_patch(), patch_off=wl.patch_off,
+            patch_len=np.array(wl.patch_lens, np.int32), rank=wl.rank, items=wl.items, block_table=wl.block_table,
+            num_pages=wl.num_pages, page_size=wl.page_size, pool_k_in=wl.host_pool(0),
+            pool_v_in=wl.host_pool(1) if wl.n_ch == 2 else None, lib=lib)
+        ik, iv, iwk, iwv = _independent_reuse(wl)
+        np.testing.assert_array_equal(wk.astype(bool), iwk)
+        np.testing.assert_allclose(pk[iwk], ik[iwk], atol=1e-10)
+        if wl.n_ch == 2:
+            np.testing.assert_allclose(pv[iwv], iv[iwv], atol=1e-10)
+
+
+def c_svd(lib):
+    a = rng.standard_normal((30, 10))
+    us, v, sig = oracle.jacobi_svd(a, lib=lib)
+    np.testing.assert_allclose(sig, np.linalg.svd(a, compute_uv=False), rtol=1e-10)
+    np.testing.assert_allclose(us @ v.T, a, atol=1e-10)
+
+
+def c_orbit(lib):
+    d = rng.standard_normal((4, 50)).astype(np.float32)
+    np.testing.assert_allclose(oracle.orbit_mean(d, lib=lib), d.astype(np.float64).mean(axis=0), atol=1e-15)
+
+
+CHECKS = [c_theta, c_rope, c_row, c_mla, c_mrope, c_patch, c_frame, c_slot, c_reuse, c_svd, c_orbit]
+
+
+def test_unmutated_oracle_passes_every_check(tmp_path):
+    lib = _build(tmp_path, "clean", SRC)
+    for check in CHECKS:
+        check(lib)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_every_planted_mistake_is_caught(tmp_path, name, old, new):
+    assert SRC.count(old) == 1, f"mutation site not unique: {old}"
+    lib = _build(tmp_path, name.replace(" ", "_").replace("/", "_"), SRC.replace(old, new))
+    failed = []
+    for check in CHECKS:
+        try:
+            check(lib)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"no check caught the mutant '{name}'"

@@ -46,6 +46,22 @@ class Model(ctypes.Structure):
     ]
 
 
+class CStore(ctypes.Structure):
+    """A compressed canonical store (see the oracle's "compressed canonical store" section)."""
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("v_norm", ctypes.c_void_p),
+        ("row_offset", ctypes.c_void_p),
+        ("len", ctypes.c_void_p),
+        ("n_chunks", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("n_rows", ctypes.c_int64),
+        ("codebook", ctypes.c_void_p),
+    ]
+
+
 ITEM_DTYPE = np.dtype(
     [
         ("chunk_id", np.int32),
@@ -60,10 +76,16 @@ ITEM_DTYPE = np.dtype(
 assert ITEM_DTYPE.itemsize == 32
 
 
+def build_cmd(src: str = _SRC, out: str = _LIB_PATH, cc: str = "gcc") -> list[str]:
+    """The compile line: plain -O2, no fast-math, and no contraction of a*b+c
+    into a fused multiply-add (the compressed-store encoder's fp32 steps are
+    specified operation by operation)."""
+    return [cc, "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", out, src, "-lm"]
+
+
 def build(src: str = _SRC, out: str = _LIB_PATH, cc: str = "gcc") -> str:
-    """Compile the oracle into a shared library (plain -O2, no fast-math)."""
-    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-o", out, src, "-lm"]
-    subprocess.run(cmd, check=True)
+    """Compile the oracle into a shared library."""
+    subprocess.run(build_cmd(src, out, cc), check=True)
     return out
 
 
@@ -105,6 +127,23 @@ def _declare(lib):
     lib.oracle_orbit_mean.restype = None
     lib.oracle_jacobi_svd.argtypes = [P, i32, i32, P, P, i32]
     lib.oracle_jacobi_svd.restype = i32
+    lib.oracle_lloyd_max_gaussian.argtypes = [i32, i32, P]
+    lib.oracle_lloyd_max_gaussian.restype = i32
+    lib.oracle_v_codebook.argtypes = [P, P]
+    lib.oracle_v_codebook.restype = None
+    lib.oracle_quantize_k.argtypes = [P, i64, P, P]
+    lib.oracle_quantize_k.restype = None
+    lib.oracle_encode_v.argtypes = [P, i32, P, P, P]
+    lib.oracle_encode_v.restype = None
+    lib.oracle_decode_v.argtypes = [P, ctypes.c_float, i32, P, P]
+    lib.oracle_decode_v.restype = None
+    lib.oracle_decode_row.argtypes = [ctypes.POINTER(Model), ctypes.POINTER(CStore), i32, i32, i32, i32, P]
+    lib.oracle_decode_row.restype = None
+    lib.oracle_compress_store.argtypes = [ctypes.POINTER(Model), P, P, P, i32, P, P, P, P, P, P]
+    lib.oracle_compress_store.restype = None
+    lib.oracle_reuse_compressed.argtypes = [ctypes.POINTER(Model), P, ctypes.POINTER(CStore)] + [
+        P, P, P, i32, i32, P, P, i32, P, i32, i32, i64, i32, P, P, P, P, P, P]
+    lib.oracle_reuse_compressed.restype = i32
     return lib
 
 
@@ -261,3 +300,141 @@ def orbit_mean(deltas, lib=None) -> np.ndarray:
     out = np.zeros(per, np.float64)
     lib.oracle_orbit_mean(_ptr(d), n, per, per, _ptr(out))
     return out.reshape(d.shape[1:])
+
+
+# ---- compressed canonical store (PolyKV §2B) ---------------------------------------------------
+
+
+def lloyd_max_gaussian(levels: int = 8, max_rounds: int = 100000, lib=None):
+    """Lloyd-Max centroids of N(0,1) (fp64, ascending) and the rounds used."""
+    lib = lib or load()
+    c = np.zeros(levels, np.float64)
+    rounds = lib.oracle_lloyd_max_gaussian(int(levels), int(max_rounds), _ptr(c))
+    return c, int(rounds)
+
+
+def v_codebook(lib=None):
+    """The store format's fp32 codebook (8 centroids) and its 7 thresholds."""
+    lib = lib or load()
+    c = np.zeros(8, np.float32)
+    t = np.zeros(7, np.float32)
+    lib.oracle_v_codebook(_ptr(c), _ptr(t))
+    return c, t
+
+
+def quantize_k(x_bits, lib=None):
+    """One K tensor (bf16 bits, any shape) -> (int8 codes, fp32 scale)."""
+    lib = lib or load()
+    x = _c(x_bits, np.uint16)
+    q = np.zeros(x.shape, np.int8)
+    s = np.zeros(1, np.float32)
+    lib.oracle_quantize_k(_ptr(x), int(x.size), _ptr(q), _ptr(s))
+    return q, float(s[0])
+
+
+def encode_v(x_bits, lib=None):
+    """Head rows [..., n] (bf16 bits) -> (packed codes [..., 3n/8] uint8, norms [...] fp32)."""
+    lib = lib or load()
+    x = _c(x_bits, np.uint16)
+    n = int(x.shape[-1])
+    rows = x.reshape(-1, n)
+    _, t32 = v_codebook(lib)
+    packed = np.zeros((rows.shape[0], 3 * n // 8), np.uint8)
+    norm = np.zeros(rows.shape[0], np.float32)
+    for i in range(rows.shape[0]):
+        lib.oracle_encode_v(_ptr(rows[i]), n, _ptr(t32), _ptr(packed[i]), _ptr(norm[i:i + 1]))
+    return packed.reshape(x.shape[:-1] + (3 * n // 8,)), norm.reshape(x.shape[:-1])
+
+
+def decode_v(packed, norm, n: int, lib=None) -> np.ndarray:
+    """Packed head rows [..., 3n/8] and norms [...] -> decoded rows [..., n] (fp64)."""
+    lib = lib or load()
+    c32, _ = v_codebook(lib)
+    p = _c(packed, np.uint8).reshape(-1, 3 * n // 8)
+    nr = np.ascontiguousarray(norm, dtype=np.float32).reshape(-1)
+    out = np.zeros((p.shape[0], n), np.float64)
+    for i in range(p.shape[0]):
+        lib.oracle_decode_v(_ptr(p[i]), float(nr[i]), int(n), _ptr(c32), _ptr(out[i]))
+    return out.reshape(np.asarray(packed).shape[:-1] + (n,))
+
+
+class Compressed:
+    """Host arrays of a compressed store (the oracle's layout) plus its ctypes view."""
+
+    def __init__(self, k_codes, k_scale, v_codes, v_norm, row_offset, len_, codebook):
+        self.k_codes = np.ascontiguousarray(k_codes, np.int8)
+        self.k_scale = np.ascontiguousarray(k_scale, np.float32)
+        self.v_codes = np.ascontiguousarray(v_codes, np.uint8)
+        self.v_norm = np.ascontiguousarray(v_norm, np.float32)
+        self.row_offset = np.ascontiguousarray(row_offset, np.int64)
+        self.len = np.ascontiguousarray(len_, np.int32)
+        self.codebook = np.ascontiguousarray(codebook, np.float32)
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.k_codes.shape[0])
+
+    def struct(self) -> CStore:
+        return CStore(self.k_codes.ctypes.data, self.k_scale.ctypes.data, self.v_codes.ctypes.data,
+                      self.v_norm.ctypes.data, self.row_offset.ctypes.data, self.len.ctypes.data,
+                      int(self.len.shape[0]), 0, self.n_rows, self.codebook.ctypes.data)
+
+
+def compress_store(m: Model, store, store_off, store_len, row_offset=None, n_rows=None, lib=None) -> Compressed:
+    """Encode a bf16 chunk store.  Default row layout: the chunks back to back
+    (row_offset[c] = sum of L*len over the chunks before c)."""
+    lib = lib or load()
+    store = _c(store, np.uint16)
+    store_off = _c(store_off, np.int64)
+    store_len = _c(store_len, np.int32)
+    L, D, H, n = m.num_layers, row_dim(m), m.num_kv_heads, m.head_dim
+    if row_offset is None:
+        row_offset = np.concatenate([[0], np.cumsum(L * store_len.astype(np.int64))[:-1]])
+    row_offset = _c(row_offset, np.int64)
+    if n_rows is None:
+        n_rows = int((row_offset + L * store_len.astype(np.int64)).max(initial=0))
+    c32, t32 = v_codebook(lib)
+    k_codes = np.zeros((n_rows, D), np.int8)
+    k_scale = np.zeros((store_len.shape[0], L), np.float32)
+    v_codes = np.zeros((n_rows, H, 3 * n // 8), np.uint8)
+    v_norm = np.zeros((n_rows, H), np.float32)
+    lib.oracle_compress_store(ctypes.byref(m), _ptr(store), _ptr(store_off), _ptr(store_len),
+                              int(store_len.shape[0]), _ptr(row_offset), _ptr(t32), _ptr(k_codes), _ptr(k_scale),
+                              _ptr(v_codes), _ptr(v_norm))
+    return Compressed(k_codes, k_scale, v_codes, v_norm, row_offset, store_len, c32)
+
+
+def decode_row(m: Model, cs: Compressed, chunk: int, layer: int, ch: int, t: int, lib=None) -> np.ndarray:
+    lib = lib or load()
+    out = np.zeros(row_dim(m), np.float64)
+    st = cs.struct()
+    lib.oracle_decode_row(ctypes.byref(m), ctypes.byref(st), int(chunk), int(layer), int(ch), int(t), _ptr(out))
+    return out
+
+
+def reuse_compressed(m: Model, th, cs: Compressed, *, patch=None, patch_off=None, patch_len=None, rank=0, items,
+                     block_table, num_pages, page_size, pool_k_in, pool_v_in, section_deltas=None, lib=None):
+    """The reuse operator reading a compressed store; returns like ``reuse``."""
+    lib = lib or load()
+    th = _c(th, np.float64)
+    items = np.ascontiguousarray(items, dtype=ITEM_DTYPE)
+    sd = None if section_deltas is None else np.ascontiguousarray(section_deltas, dtype=np.int64).reshape(-1, 3)
+    bt = _c(block_table, np.int32)
+    n_seqs, max_pages = bt.shape
+    pool_k_in = _c(pool_k_in, np.uint16)
+    pool_v_in = _c(pool_v_in, np.uint16)
+    pk = np.zeros(pool_k_in.shape, np.float64)
+    pv = np.zeros(pool_v_in.shape, np.float64)
+    wk = np.zeros(pool_k_in.shape[:-1], np.uint8)
+    wv = np.zeros(pool_k_in.shape[:-1], np.uint8)
+    patch = _c(patch, np.uint16)
+    patch_off = _c(patch_off, np.int64)
+    patch_len = _c(patch_len, np.int32)
+    n_patches = 0 if patch_len is None else int(patch_len.shape[0])
+    st = cs.struct()
+    err = lib.oracle_reuse_compressed(ctypes.byref(m), _ptr(th), ctypes.byref(st), _ptr(patch), _ptr(patch_off),
+                                      _ptr(patch_len), n_patches, int(rank), _ptr(items), _ptr(sd),
+                                      int(items.shape[0]), _ptr(bt), int(n_seqs), int(max_pages), int(num_pages),
+                                      int(page_size), _ptr(pool_k_in), _ptr(pool_v_in), _ptr(pk), _ptr(pv),
+                                      _ptr(wk), _ptr(wv))
+    return int(err), pk, pv, wk, wv

@@ -40,6 +40,14 @@
  *     block_table[seq][pos / P], slot pos % P, of a pool laid out
  *     [layer][page][slot][D].
  *
+ * Compressed canonical store (source: "PolyKV", gist.science summary, Spanish
+ * edition, §2B "asymmetric compression scheme (TurboQuant MSE)"): K as int8
+ * with one linear scale per tensor; V as 3-bit codes of the Walsh-Hadamard
+ * rotated vector against the Lloyd-Max centroids of N(0,1), decoded by the
+ * centroid values and the inverse transform.  The section "compressed
+ * canonical store" below gives the encoder, the decoders and the reuse
+ * operator reading such a store.
+ *
  * Everything is evaluated in fp64 from the bf16 inputs (bf16 -> fp64 is exact).
  * Error bits follow the library's convention: an item whose chunk, patch,
  * length or sequence is invalid is skipped whole; a row whose page is invalid
@@ -204,6 +212,207 @@ int64_t oracle_slot(const int32_t* block_table, int32_t max_pages_per_seq, int64
   return page * page_size + pos % page_size;
 }
 
+/* ---- compressed canonical store ----------------------------------------------
+ *
+ * Source: "PolyKV" (gist.science summary, Spanish edition), §2B, the
+ * asymmetric compression scheme (TurboQuant MSE):
+ *   K: int8, linear quantisation with one scale per tensor.
+ *   V: 3 bits per coordinate.  The vector is rotated by a fast Walsh-Hadamard
+ *      transform, which spreads outliers and brings its coordinates close to
+ *      N(0,1); each coordinate is mapped to the nearest precomputed Lloyd-Max
+ *      centroid for N(0,1); decoding takes the centroid values and applies the
+ *      inverse transform.
+ *   Ratio against bf16: 16 / ((8 + 3) / 2) = 2.91.
+ *
+ * Readings (the page fixes none of these details):
+ *   - A K "tensor" is one layer's K of one chunk, [T][D].  Scale
+ *     s = max|x| / 127; code q = rint(x / s) clamped to [-127, 127] (s = 0:
+ *     every code 0); decoded value q * s.
+ *   - A V "vector" is one head's row of n = head_dim values (n a power of
+ *     two).  H is the Sylvester-ordered Hadamard matrix, H[i][j] =
+ *     (-1)^popcount(i & j), and w = H x.  The orthonormal rotation H/sqrt(n)
+ *     gives coordinates of variance ||x||^2 / n, so the N(0,1)-normalised
+ *     coordinate is z = w / ||x||.  Stored per head row: ||x|| (fp32) and
+ *     the n codes.  Decoded value: (||x|| / n) * H c[code].
+ *   - Codebook: the 8 Lloyd-Max centroids of N(0,1) rounded to fp32 (the
+ *     upper four; the lower four are their exact negatives); thresholds: the
+ *     fp32 midpoints of neighbouring centroids; code = the number of
+ *     thresholds <= z (ascending centroid order, code 0 = most negative).
+ *   - Packing: per head row 3n bits; 6-bit field i (i < n/2) holds
+ *     code[i] | code[i + n/2] << 3 and starts at bit 6i of the row's bytes
+ *     (bit b of byte k is bit 8k + b).
+ *   - Store rows: chunk c, layer l, token t is row row_offset[c] + l*T + t of
+ *     k_codes [rows][D], v_codes [rows][H][3n/8] and v_norm [rows][H];
+ *     k_scale is [chunk][layer].  MHA/GQA only (MLA has no separate V).
+ *   - The encoder's decisions are taken in fp32 with one fixed order of
+ *     operations, which is part of the format: the in-place transform with
+ *     strides 1, 2, 4, ...; the sum of squares in index order with fused
+ *     multiply-add; IEEE division and square root.  The decoders are fp64.
+ */
+
+typedef struct {
+  const int8_t* k_codes;      /* [n_rows][D] */
+  const float* k_scale;       /* [n_chunks][num_layers] */
+  const uint8_t* v_codes;     /* [n_rows][num_kv_heads][3*head_dim/8] */
+  const float* v_norm;        /* [n_rows][num_kv_heads] */
+  const int64_t* row_offset;  /* [n_chunks] */
+  const int32_t* len;         /* [n_chunks] */
+  int32_t n_chunks;
+  int32_t reserved;
+  int64_t n_rows;
+  const float* codebook;      /* [8] fp32 centroids, ascending */
+} oracle_cstore;
+
+static double normal_pdf(double x) { return exp(-0.5 * x * x) / sqrt(2.0 * acos(-1.0)); }
+static double normal_cdf(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+
+/* Lloyd-Max quantiser of N(0,1) with `levels` levels (Lloyd 1957, Max 1960):
+ * alternate the two optimality conditions,
+ *     threshold k = midpoint of centroids k-1 and k,
+ *     centroid k  = E[Z | t_k < Z < t_{k+1}] = (pdf(t_k) - pdf(t_{k+1})) / (cdf(t_{k+1}) - cdf(t_k)),
+ * (t_0 = -inf, t_levels = +inf) starting from centroids spread evenly over
+ * [-2, 2], until no centroid moves by more than 1e-15.  Returns the rounds used. */
+int32_t oracle_lloyd_max_gaussian(int32_t levels, int32_t max_rounds, double* centroids) {
+  double t[65];
+  for (int32_t k = 0; k < levels; ++k) centroids[k] = -2.0 + 4.0 * (k + 0.5) / levels;
+  int32_t round = 0;
+  for (; round < max_rounds; ++round) {
+    t[0] = -INFINITY;
+    t[levels] = INFINITY;
+    for (int32_t k = 1; k < levels; ++k) t[k] = 0.5 * (centroids[k - 1] + centroids[k]);
+    double moved = 0.0;
+    for (int32_t k = 0; k < levels; ++k) {
+      double c = (normal_pdf(t[k]) - normal_pdf(t[k + 1])) / (normal_cdf(t[k + 1]) - normal_cdf(t[k]));
+      moved = fmax(moved, fabs(c - centroids[k]));
+      centroids[k] = c;
+    }
+    if (moved <= 1e-15) break;
+  }
+  return round;
+}
+
+/* The format's codebook: c32 [8] and thresholds t32 [7] (see the readings above). */
+void oracle_v_codebook(float* c32, float* t32) {
+  double c[8];
+  oracle_lloyd_max_gaussian(8, 100000, c);
+  for (int32_t k = 4; k < 8; ++k) {
+    c32[k] = (float)c[k];
+    c32[7 - k] = -c32[k];
+  }
+  for (int32_t k = 1; k < 8; ++k) t32[k - 1] = (c32[k - 1] + c32[k]) * 0.5f;
+}
+
+static float bf16_bits_to_f32(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return f;
+}
+
+/* K of one tensor of n bf16 values: the scale and the int8 codes (fp32 decisions). */
+void oracle_quantize_k(const uint16_t* x, int64_t n, int8_t* q, float* scale) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(x[i])));
+  const float s = amax / 127.0f;
+  *scale = s;
+  for (int64_t i = 0; i < n; ++i) {
+    if (s == 0.0f) { q[i] = 0; continue; }
+    float r = nearbyintf(bf16_bits_to_f32(x[i]) / s);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    q[i] = (int8_t)r;
+  }
+}
+
+/* Code of element e of a packed head row of n codes. */
+static int32_t v_code(const uint8_t* packed, int32_t n, int32_t e) {
+  const int32_t half = n / 2;
+  const int32_t bit0 = 6 * (e % half) + (e < half ? 0 : 3);
+  int32_t code = 0;
+  for (int32_t b = 0; b < 3; ++b) code |= ((packed[(bit0 + b) / 8] >> ((bit0 + b) % 8)) & 1) << b;
+  return code;
+}
+
+/* V of one head row of n bf16 values (n <= 256): the packed codes (3n/8
+ * bytes) and ||x||.  fp32 throughout, in the format's order of operations. */
+void oracle_encode_v(const uint16_t* x_bits, int32_t n, const float* t32, uint8_t* packed, float* norm) {
+  float x[256], w[256];
+  if (n < 2 || n > 256) return;
+  for (int32_t i = 0; i < n; ++i) w[i] = x[i] = bf16_bits_to_f32(x_bits[i]);
+  for (int32_t h = 1; h < n; h *= 2)
+    for (int32_t i = 0; i < n; i += 2 * h)
+      for (int32_t j = i; j < i + h; ++j) {
+        const float a = w[j], b = w[j + h];
+        w[j] = a + b;
+        w[j + h] = a - b;
+      }
+  float acc = 0.0f;
+  for (int32_t i = 0; i < n; ++i) acc = fmaf(x[i], x[i], acc);
+  const float nr = sqrtf(acc);
+  *norm = nr;
+  memset(packed, 0, (size_t)(3 * n / 8));
+  for (int32_t e = 0; e < n; ++e) {
+    int32_t code = 0;
+    if (nr > 0.0f) {
+      const float z = w[e] / nr;
+      for (int32_t k = 0; k < 7; ++k) code += (t32[k] <= z) ? 1 : 0;
+    }
+    const int32_t bit0 = 6 * (e % (n / 2)) + (e < n / 2 ? 0 : 3);
+    for (int32_t b = 0; b < 3; ++b) packed[(bit0 + b) / 8] |= (uint8_t)(((code >> b) & 1) << ((bit0 + b) % 8));
+  }
+}
+
+/* Decoded head row: out[i] = (norm / n) * sum_j (-1)^popcount(i & j) * c32[code_j], in fp64. */
+void oracle_decode_v(const uint8_t* packed, float norm, int32_t n, const float* c32, double* out) {
+  for (int32_t i = 0; i < n; ++i) {
+    double acc = 0.0;
+    for (int32_t j = 0; j < n; ++j) {
+      const double c = (double)c32[v_code(packed, n, j)];
+      acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -c : c;
+    }
+    out[i] = (double)norm / (double)n * acc;
+  }
+}
+
+/* Canonical row (chunk c, layer l, channel ch, token t) of a compressed store, decoded in fp64. */
+void oracle_decode_row(const oracle_model* m, const oracle_cstore* cs, int32_t c, int32_t l, int32_t ch, int32_t t,
+                       double* out) {
+  const int32_t D = oracle_row_dim(m);
+  const int32_t H = m->num_kv_heads, n = m->head_dim;
+  const int64_t row = cs->row_offset[c] + (int64_t)l * cs->len[c] + t;
+  if (ch == 0) {
+    const double s = (double)cs->k_scale[(int64_t)c * m->num_layers + l];
+    for (int32_t j = 0; j < D; ++j) out[j] = (double)cs->k_codes[row * D + j] * s;
+    return;
+  }
+  for (int32_t h = 0; h < H; ++h)
+    oracle_decode_v(cs->v_codes + (row * H + h) * (3 * n / 8), cs->v_norm[row * H + h], n, cs->codebook,
+                    out + (int64_t)h * n);
+}
+
+/* Encode a bf16 chunk store (per chunk [layer][channel][T][D], MHA/GQA) into
+ * a compressed store whose row_offset / len the caller has set: one K scale
+ * per (chunk, layer), every head row of V encoded on its own. */
+void oracle_compress_store(const oracle_model* m, const uint16_t* store, const int64_t* store_off,
+                           const int32_t* len, int32_t n_chunks, const int64_t* row_offset, const float* t32,
+                           int8_t* k_codes, float* k_scale, uint8_t* v_codes, float* v_norm) {
+  const int32_t D = oracle_row_dim(m);
+  const int32_t H = m->num_kv_heads, n = m->head_dim, L = m->num_layers;
+  for (int32_t c = 0; c < n_chunks; ++c) {
+    const int64_t T = len[c];
+    for (int32_t l = 0; l < L; ++l) {
+      const uint16_t* k = store + store_off[c] + ((int64_t)l * 2 + 0) * T * D;
+      const uint16_t* v = store + store_off[c] + ((int64_t)l * 2 + 1) * T * D;
+      const int64_t row0 = row_offset[c] + (int64_t)l * T;
+      oracle_quantize_k(k, T * D, k_codes + row0 * D, &k_scale[(int64_t)c * L + l]);
+      for (int64_t t = 0; t < T; ++t)
+        for (int32_t h = 0; h < H; ++h)
+          oracle_encode_v(v + t * D + (int64_t)h * n, n, t32, v_codes + ((row0 + t) * H + h) * (3 * n / 8),
+                          &v_norm[(row0 + t) * H + h]);
+    }
+  }
+}
+
 /*
  * The whole operator over a list of items, into fp64 images of the pool.
  *
@@ -224,14 +433,15 @@ int64_t oracle_slot(const int32_t* block_table, int32_t max_pages_per_seq, int64
  * item's per-section shifts when the model has M-RoPE sections (NULL: every
  * section takes the item's delta).  Returns the OR of the error bits.
  */
-int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
-                     const uint16_t* store, const int64_t* store_off, const int32_t* store_len, int32_t n_chunks,
-                     const uint16_t* patch, const int64_t* patch_off, const int32_t* patch_len, int32_t n_patches,
-                     int32_t rank, const oracle_item* items, const int64_t* section_deltas, int32_t n_items,
-                     const int32_t* block_table,
-                     int32_t n_seqs, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
-                     const uint16_t* pool_k_in, const uint16_t* pool_v_in, double* pool_k_out, double* pool_v_out,
-                     uint8_t* wrote_k, uint8_t* wrote_v) {
+static int32_t reuse_impl(const oracle_model* m, const double* theta, int32_t mode,
+                          const uint16_t* store, const int64_t* store_off, const int32_t* store_len, int32_t n_chunks,
+                          const oracle_cstore* cs,
+                          const uint16_t* patch, const int64_t* patch_off, const int32_t* patch_len,
+                          int32_t n_patches, int32_t rank, const oracle_item* items, const int64_t* section_deltas,
+                          int32_t n_items, const int32_t* block_table,
+                          int32_t n_seqs, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                          const uint16_t* pool_k_in, const uint16_t* pool_v_in, double* pool_k_out,
+                          double* pool_v_out, uint8_t* wrote_k, uint8_t* wrote_v) {
   const int32_t D = oracle_row_dim(m);
   const int32_t L = m->num_layers;
   const int32_t n_ch = oracle_num_channels(m);
@@ -256,9 +466,15 @@ int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
     if (T == 0) continue;
     if (T < 0 || item->dst_pos < 0) { err |= OR_EFLAG_LEN; continue; }
     if (item->seq < 0 || item->seq >= n_seqs) { err |= OR_EFLAG_PAGE_OOB; continue; }
-    if (mode == OR_MODE_REUSE) {
+    if (mode == OR_MODE_REUSE && cs == NULL) {
       if (item->chunk_id < 0 || item->chunk_id >= n_chunks) { err |= OR_EFLAG_CHUNK_OOB; continue; }
       if (store_len[item->chunk_id] != T) { err |= OR_EFLAG_LEN; continue; }
+    }
+    if (mode == OR_MODE_REUSE && cs != NULL) {
+      if (item->chunk_id < 0 || item->chunk_id >= cs->n_chunks) { err |= OR_EFLAG_CHUNK_OOB; continue; }
+      if (cs->len[item->chunk_id] != T) { err |= OR_EFLAG_LEN; continue; }
+      const int64_t r0 = cs->row_offset[item->chunk_id];
+      if (r0 < 0 || r0 + (int64_t)L * T > cs->n_rows) { err |= OR_EFLAG_CHUNK_OOB; continue; }
     }
     int32_t use_patch = 0;
     if (mode != OR_MODE_RELOCATE_IN_PLACE && rank > 0 && patch != NULL && item->patch_id >= 0) {
@@ -289,7 +505,9 @@ int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
           const int64_t dst = oracle_slot(block_table, max_pages_per_seq, num_pages, page_size, item->seq, pos);
           if (dst < 0) { err |= OR_EFLAG_PAGE_OOB; continue; }
           const int64_t dst_row = (int64_t)l * num_pages * page_size + dst;
-          if (mode == OR_MODE_REUSE) {
+          if (mode == OR_MODE_REUSE && cs != NULL) {
+            oracle_decode_row(m, cs, item->chunk_id, l, ch, t, src);
+          } else if (mode == OR_MODE_REUSE) {
             const int64_t sb = store_off[item->chunk_id] + (((int64_t)l * n_ch + ch) * T + t) * D;
             for (int32_t j = 0; j < D; ++j) src[j] = bf16_bits_to_f64(store[sb + j]);
           } else {
@@ -312,6 +530,34 @@ int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
   free(u);
   free(vmat);
   return err;
+}
+
+int32_t oracle_reuse(const oracle_model* m, const double* theta, int32_t mode,
+                     const uint16_t* store, const int64_t* store_off, const int32_t* store_len, int32_t n_chunks,
+                     const uint16_t* patch, const int64_t* patch_off, const int32_t* patch_len, int32_t n_patches,
+                     int32_t rank, const oracle_item* items, const int64_t* section_deltas, int32_t n_items,
+                     const int32_t* block_table,
+                     int32_t n_seqs, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                     const uint16_t* pool_k_in, const uint16_t* pool_v_in, double* pool_k_out, double* pool_v_out,
+                     uint8_t* wrote_k, uint8_t* wrote_v) {
+  return reuse_impl(m, theta, mode, store, store_off, store_len, n_chunks, NULL, patch, patch_off, patch_len,
+                    n_patches, rank, items, section_deltas, n_items, block_table, n_seqs, max_pages_per_seq,
+                    num_pages, page_size, pool_k_in, pool_v_in, pool_k_out, pool_v_out, wrote_k, wrote_v);
+}
+
+/* The reuse operator (mode OR_MODE_REUSE) reading its canonical rows from a
+ * compressed store: every source row is first decoded (oracle_decode_row),
+ * then rotated, patched and scattered exactly as oracle_reuse does. */
+int32_t oracle_reuse_compressed(const oracle_model* m, const double* theta, const oracle_cstore* cs,
+                                const uint16_t* patch, const int64_t* patch_off, const int32_t* patch_len,
+                                int32_t n_patches, int32_t rank, const oracle_item* items,
+                                const int64_t* section_deltas, int32_t n_items, const int32_t* block_table,
+                                int32_t n_seqs, int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                                const uint16_t* pool_k_in, const uint16_t* pool_v_in, double* pool_k_out,
+                                double* pool_v_out, uint8_t* wrote_k, uint8_t* wrote_v) {
+  return reuse_impl(m, theta, OR_MODE_REUSE, NULL, NULL, NULL, 0, cs, patch, patch_off, patch_len, n_patches, rank,
+                    items, section_deltas, n_items, block_table, n_seqs, max_pages_per_seq, num_pages, page_size,
+                    pool_k_in, pool_v_in, pool_k_out, pool_v_out, wrote_k, wrote_v);
 }
 
 /*

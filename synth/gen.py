@@ -175,3 +175,20 @@ def low_rank_deficit(seed: int, slab: int, T: int, D: int, spectrum, noise: floa
         N = normal_f32(st, base + np.uint64(1 << 38) + np.arange(T * D, dtype=np.uint64)).reshape(T, D)
         out = out + noise * N / np.sqrt(max(T, D))
     return out.astype(np.float32)
+
+
+# ---- random compressed-store contents (bytes and positive scales; no encoding) ----------------
+
+STREAM_KCODE, STREAM_VCODE, STREAM_KSCALE, STREAM_VNORM = 10, 11, 12, 13
+
+
+def random_bytes(stream: int, n: int, idx0: int = 0) -> np.ndarray:
+    """n uniform bytes: the little-endian bytes of hash64 at idx0, idx0 + 1, ..."""
+    words = hash64(stream, np.uint64(idx0) + np.arange((n + 7) // 8, dtype=np.uint64))
+    return words.astype("<u8").view(np.uint8)[:n].copy()
+
+
+def uniform_f32(stream: int, idx, lo: float, hi: float) -> np.ndarray:
+    """fp32 uniform in [lo, hi) from the top 24 bits of hash64."""
+    h = hash64(stream, idx) >> np.uint64(40)
+    return (lo + (hi - lo) * (h.astype(np.float64) / float(1 << 24))).astype(np.float32)

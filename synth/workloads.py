@@ -190,6 +190,48 @@ class Workload:
                 out[layer, page] = self.pool_rows(ch, layer, page)
         return out
 
+    # ---- compressed canonical store (int8 K, 3-bit V; PolyKV §2B) ----------------------
+    @property
+    def comp_row_offset(self) -> np.ndarray:
+        """Chunks back to back: chunk c, layer l, token t is row comp_row_offset[c] + l*T_c + t."""
+        sizes = [self.num_layers * t for t in self.chunk_lens]
+        return np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64) if sizes else np.zeros(0, np.int64)
+
+    @property
+    def comp_rows(self) -> int:
+        return int(sum(self.num_layers * t for t in self.chunk_lens))
+
+    def random_compressed(self) -> dict:
+        """A compressed store filled with seeded random contents (any byte is a
+        valid code): K codes uniform in [-127, 127], V code bytes uniform,
+        per-(chunk, layer) K scales and per-head-row V norms uniform around
+        the bf16 store's scale."""
+        rows, D, H, n, L = self.comp_rows, self.D, self.num_kv_heads, self.head_dim, self.num_layers
+        kb = gen.random_bytes(self.stream(gen.STREAM_KCODE), rows * D)
+        k_codes = ((kb.astype(np.int32) % 255) - 127).astype(np.int8).reshape(rows, D)
+        v_codes = gen.random_bytes(self.stream(gen.STREAM_VCODE), rows * H * (3 * n // 8)).reshape(rows, H, -1)
+        nc = len(self.chunk_lens)
+        k_scale = gen.uniform_f32(self.stream(gen.STREAM_KSCALE), np.arange(nc * L, dtype=np.uint64),
+                                  0.5 * 4 * self.sigma_kv / 127, 1.5 * 4 * self.sigma_kv / 127).reshape(nc, L)
+        v_norm = gen.uniform_f32(self.stream(gen.STREAM_VNORM), np.arange(rows * H, dtype=np.uint64),
+                                 0.5 * self.sigma_kv * np.sqrt(n), 1.5 * self.sigma_kv * np.sqrt(n)).reshape(rows, H)
+        return dict(k_codes=k_codes, k_scale=k_scale, v_codes=v_codes, v_norm=v_norm,
+                    row_offset=self.comp_row_offset, len=np.array(self.chunk_lens, np.int32))
+
+    def compressed_bytes(self) -> int:
+        """Bytes one call must move at minimum when the canonical rows come
+        from the compressed store: K codes (1 byte/value) and V codes (3/8
+        byte/value) plus one V norm per head row read once, the bf16 output
+        rows written once, and the patch factors read once."""
+        L, D, H = self.num_layers, self.D, self.num_kv_heads
+        total = 0
+        for it in self.items:
+            T = int(it["n_tokens"])
+            total += L * T * (D + 3 * D // 8 + 4 * H) + L * 2 * T * D * 2
+            if self.rank > 0 and it["patch_id"] >= 0:
+                total += L * 2 * (T + D) * self.rank * 2
+        return total
+
     # ---- device fills (CUDA twin of the generator) ----------------------------------
     def device_store(self, torch, device="cuda"):
         from . import device as dev

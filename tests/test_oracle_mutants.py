@@ -4,13 +4,21 @@ Each mutant plants one mistake -- a flipped sign, a swapped or shifted index,
 a dropped term, a transposed operand, an off-by-one -- into a copy of the
 oracle's C source, builds it, and runs the independent checks below (complex
 RoPE, M-RoPE, library matmul, brute-force page map, the vectorised whole-batch
-formulation, library SVD, library mean).  Every mutant must fail at least one.
+formulation, library SVD, library mean, Max's quantiser table, the int8 error
+bound, scipy's Hadamard matrix, the nearest-centroid rule).  Every mutant must fail at least one.
 """
+
+import json
+import os
 
 import numpy as np
 import pytest
+from scipy import linalg
 
 import oracle
+from synth import gen
+from synth import workloads as W
+from tests.test_oracle_compressed import _independent_reuse_compressed, _pack, _unpack
 from tests.test_oracle_operator import CASES, _independent_reuse, _oracle_model
 from tests.test_oracle_pins import _theta_np, mrope_complex, rope_complex
 
@@ -38,6 +46,24 @@ MUTANTS = [
     ("Jacobi rotation sign", "a[(int64_t)k * cols + p] = c * ap - s * aq;", "a[(int64_t)k * cols + p] = c * ap + s * aq;"),
     ("singular values ascending", "if (sigma[k] > sigma[best]) best = k;", "if (sigma[k] < sigma[best]) best = k;"),
     ("orbit mean divisor", "out[e] = s / (double)n;", "out[e] = s / (double)(n + 1);"),
+    ("Lloyd centroid sign", "double c = (normal_pdf(t[k]) - normal_pdf(t[k + 1]))",
+     "double c = (normal_pdf(t[k + 1]) - normal_pdf(t[k]))"),
+    ("Lloyd threshold not a midpoint", "t[k] = 0.5 * (centroids[k - 1] + centroids[k]);",
+     "t[k] = 0.5 * (centroids[k] + centroids[k]);"),
+    ("K scale step 1/128", "const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
+    ("K code truncated", "float r = nearbyintf(bf16_bits_to_f32(x[i]) / s);", "float r = truncf(bf16_bits_to_f32(x[i]) / s);"),
+    ("Hadamard butterfly sign", "w[j + h] = a - b;", "w[j + h] = b - a;"),
+    ("V norm of the transformed row", "acc = fmaf(x[i], x[i], acc);", "acc = fmaf(w[i], w[i], acc);"),
+    ("V code of the negated coordinate", "code += (t32[k] <= z) ? 1 : 0;", "code += (t32[k] <= -z) ? 1 : 0;"),
+    ("V fields in natural order", "const int32_t bit0 = 6 * (e % half) + (e < half ? 0 : 3);",
+     "const int32_t bit0 = 3 * e;"),
+    ("Hadamard sign from i|j", "acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -c : c;",
+     "acc += (__builtin_popcount((unsigned)(i | j)) & 1) ? -c : c;"),
+    ("V decode scaled by 1/sqrt(n)", "out[i] = (double)norm / (double)n * acc;",
+     "out[i] = (double)norm / sqrt((double)n) * acc;"),
+    ("K scale index transposed", "cs->k_scale[(int64_t)c * m->num_layers + l]", "cs->k_scale[(int64_t)l * cs->n_chunks + c]"),
+    ("compressed row order token-major", "const int64_t row = cs->row_offset[c] + (int64_t)l * cs->len[c] + t;",
+     "const int64_t row = cs->row_offset[c] + (int64_t)t * m->num_layers + l;"),
 ]
 
 
@@ -147,7 +173,58 @@ def c_orbit(lib):
     np.testing.assert_allclose(oracle.orbit_mean(d, lib=lib), d.astype(np.float64).mean(axis=0), atol=1e-15)
 
 
-CHECKS = [c_theta, c_rope, c_row, c_mla, c_mrope, c_patch, c_frame, c_slot, c_reuse, c_svd, c_orbit]
+def c_codebook(lib):
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "lloyd_max_gaussian_n8.json")))
+    c32, t32 = oracle.v_codebook(lib=lib)
+    np.testing.assert_allclose(c32[4:], g["positive_outputs"], atol=g["abs_tol"])
+    np.testing.assert_allclose(t32[3:], g["positive_thresholds"][:4], atol=g["abs_tol"])
+
+
+def c_kquant(lib):
+    x = gen.f32_to_bf16_bits(rng.standard_normal(300).astype(np.float32) * 2)
+    xf = oracle.bf16_bits_to_f64(x)
+    q, s = oracle.quantize_k(x, lib=lib)
+    assert np.abs(q).max() == 127
+    assert np.all(np.abs(xf - q.astype(np.float64) * s) <= 0.5 * s * (1 + 1e-5))
+
+
+def c_vcodec(lib):
+    n = 128
+    c32, t32 = oracle.v_codebook(lib=lib)
+    Hm = linalg.hadamard(n).astype(np.float64)
+    codes = rng.integers(0, 8, n)
+    got = oracle.decode_v(_pack(codes)[None], np.array([2.0], np.float32), n, lib=lib)[0]
+    np.testing.assert_allclose(got, 2.0 / n * (Hm @ c32[codes].astype(np.float64)), atol=1e-12)
+    x = gen.f32_to_bf16_bits(rng.standard_normal((4, n)).astype(np.float32))
+    packed, norms = oracle.encode_v(x, lib=lib)
+    xf = oracle.bf16_bits_to_f64(x)
+    for r in range(4):
+        assert abs(norms[r] - np.linalg.norm(xf[r])) <= 1e-6 * np.linalg.norm(xf[r])
+        z = Hm @ xf[r] / np.linalg.norm(xf[r])
+        near = np.abs(z[:, None] - c32[None, :].astype(np.float64)).argmin(axis=1)
+        tie = np.min(np.abs(z[:, None] - t32[None, :].astype(np.float64)), axis=1) < 1e-5
+        assert np.all((_unpack(packed[r], n) == near) | tie)
+
+
+def c_reuse_comp(lib):
+    wl = W.gqa_video(num_layers=2, n_chunks=2, T=20, rank=8, page_size=16)
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim)
+    r = wl.random_compressed()
+    cs = oracle.Compressed(r["k_codes"], r["k_scale"], r["v_codes"], r["v_norm"], r["row_offset"], r["len"],
+                           oracle.v_codebook(lib=lib)[0])
+    th = oracle.theta(wl.rope_base, wl.rope_dim, lib=lib)
+    err, pk, pv, wk, wv = oracle.reuse_compressed(
+        m, th, cs, patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
+        rank=wl.rank, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages, page_size=wl.page_size,
+        pool_k_in=wl.host_pool(0), pool_v_in=wl.host_pool(1), lib=lib)
+    ik, iv, iwk, iwv = _independent_reuse_compressed(wl, cs)
+    np.testing.assert_array_equal(wk.astype(bool), iwk)
+    np.testing.assert_allclose(pk[iwk], ik[iwk], atol=1e-10)
+    np.testing.assert_allclose(pv[iwv], iv[iwv], atol=1e-10)
+
+
+CHECKS = [c_theta, c_rope, c_row, c_mla, c_mrope, c_patch, c_frame, c_slot, c_reuse, c_svd, c_orbit, c_codebook,
+          c_kquant, c_vcodec, c_reuse_comp]
 
 
 def test_unmutated_oracle_passes_every_check(tmp_path):

@@ -15,6 +15,8 @@ HBM (device time, CUDA events on the launching stream, max over ranks);
 pinned memory and the call's status read back inside the timed region.  Inputs
 (1.97 GB per step) are larger than L2, so no flush is needed between steps.
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample.
+``--workload gqa_video_compressed`` times kamera_reuse_compressed on the same
+batch read from a compressed canonical store (int8 K, 3-bit V).
 """
 from __future__ import annotations
 
@@ -52,7 +54,11 @@ DESCRIPTIONS = {
                       "resident 1024-token chunks re-rotated in place by -8192, no patch, page 64",
     "long_video": "long-video reorder + recall, GQA 8B-shaped: 128 permuted chunks x 1296 with rank-64 orbit "
                   "patches + 32 recalled chunks with fresh rank-64 patches, page 64",
+    "gqa_video_compressed": "the gqa_video batch reused from a compressed canonical store (PolyKV scheme: int8 K "
+                            "with one scale per (chunk, layer), 3-bit Walsh-Hadamard/Lloyd-Max V with one norm per "
+                            "head row), decoded on gather; store encoded on the GPU before timing",
 }
+COMPRESSED = {"gqa_video_compressed": "gqa_video"}
 
 
 def kernel_hash() -> str:
@@ -164,6 +170,7 @@ def rank_workload(name: str, rank: int, world: int, chunks: int = 0) -> W.Worklo
     """Weak scaling: every rank reuses its own batch of the same shape (its own
     seed); there is no data exchange between ranks.  chunks > 0 selects a
     reduced batch of that many chunks (profiling captures only)."""
+    name = COMPRESSED.get(name, name)
     base = SCALED[name](chunks) if chunks and name in SCALED else W.CONFIGS[name]()
     return base.replace(seed=base.seed + 1000 * rank) if world > 1 else base
 
@@ -217,8 +224,34 @@ def time_oracle(wl: W.Workload) -> tuple[float, int]:
     return time.perf_counter() - t0, wl.tokens
 
 
+def time_oracle_compressed(wl: W.Workload) -> tuple[float, int]:
+    """Seconds of one oracle reuse from a compressed store (encoded by the
+    oracle, outside the timing) over wl."""
+    import oracle
+
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim)
+    cs = oracle.compress_store(m, wl.host_store(), wl.store_off, np.array(wl.chunk_lens, np.int32))
+    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    kw = dict(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
+              rank=wl.rank) if wl.rank else {}
+    pk_in, pv_in = wl.host_pool(0), wl.host_pool(1)
+    t0 = time.perf_counter()
+    oracle.reuse_compressed(m, th, cs, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
+                            page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, **kw)
+    return time.perf_counter() - t0, wl.tokens
+
+
 def cpu_baseline(name: str, budget_s: float = 15.0) -> dict:
     """The oracle as it stands (single-threaded C, fp64) on a bounded sample."""
+    if name in COMPRESSED:
+        # the fp64 decode costs head_dim^2 operations per head row: a token sample of one chunk
+        probe = W.gqa_video(n_chunks=1, T=16)
+        dt1, tok1 = time_oracle_compressed(probe)
+        T = max(16, min(1024, int(16 * budget_s / max(dt1, 1e-3)) // 16 * 16))
+        dt, tok = time_oracle_compressed(W.gqa_video(n_chunks=1, T=T)) if T > 16 else (dt1, tok1)
+        return {"value": tok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"one chunk truncated to {T} tokens, all layers and channels ({tok} tokens, {dt:.1f} s, "
+                          f"single-threaded fp64 C oracle decoding the compressed store)"}
     dt1, tok1 = time_oracle(oracle_sample_workload(name, 1))
     n = max(1, min(len(W.CONFIGS[name]().items), int(budget_s / max(dt1, 1e-3))))
     if n > 1:
@@ -235,19 +268,22 @@ def run_reference(args) -> None:
     if rank != 0:
         return
     name = args.workload
+    comp = name in COMPRESSED
+    base = COMPRESSED.get(name, name)
+    timer = time_oracle_compressed if comp else time_oracle
     # one step = the oracle over a token sample of one chunk, all layers, sized so
     # that warm-up + timed steps take about two minutes in total
-    full_T = {"gqa_video": 1024, "mla_lite": 2048, "long_video": 1296}.get(name)
-    dt_probe, tok_probe = time_oracle(oracle_sample_workload(name, 1, 64 if full_T else None))
+    full_T = {"gqa_video": 1024, "mla_lite": 2048, "long_video": 1296}.get(base)
+    dt_probe, tok_probe = timer(oracle_sample_workload(base, 1, 16 if full_T else None))
     per_tok = dt_probe / max(tok_probe, 1)
     budget = 120.0 / (args.steps + args.warmup)
     n_tok = max(1, min(full_T or tok_probe, int(budget / max(per_tok, 1e-9))))
-    sample = oracle_sample_workload(name, 1, n_tok if full_T else None)
+    sample = oracle_sample_workload(base, 1, n_tok if full_T else None)
     for _ in range(args.warmup):
-        time_oracle(sample)
+        timer(sample)
     total, toks = 0.0, 0
     for _ in range(args.steps):
-        dt, tok = time_oracle(sample)
+        dt, tok = timer(sample)
         total += dt
         toks += tok
     value = toks / total
@@ -281,12 +317,32 @@ def run_gpu(args) -> None:
     pk.load()
 
     wl = rank_workload(args.workload, rank, world, args.chunks)
-    t = H.device_inputs(wl, torch, device)
+    comp = args.workload in COMPRESSED
     stream = torch.cuda.current_stream(device)
+    if comp:
+        # the bf16 store is encoded once on the GPU (write-once, off the timed path), then dropped
+        t = H.device_inputs(wl, torch, device)
+        cstore, ct = H.empty_compressed(wl, torch, device)
+        pk.kamera_compress_chunks(H.model_for(wl), pk.chunk_store(t["store"], t["store_off"], t["store_len"]),
+                                  cstore, t["err"].data_ptr(), stream.cuda_stream)
+        torch.cuda.synchronize(device)
+        for n in ("store", "store_off", "store_len"):
+            del t[n]
+        t.update(ct)
+
+        def one_call(d, s):
+            cs = pk.compressed_store(d["k_codes"], d["k_scale"], d["v_codes"], d["v_norm"], d["row_offset"],
+                                     d["len"])
+            return H.call_compressed(wl, d, cs, stream=s)
+    else:
+        t = H.device_inputs(wl, torch, device)
+
+        def one_call(d, s):
+            return H.call(wl, d, stream=s)
     torch.cuda.synchronize(device)
 
     for _ in range(args.warmup):
-        H.call(wl, t, stream=stream)
+        one_call(t, stream)
     torch.cuda.synchronize(device)
     if int(t["err"].item()) != 0:
         raise RuntimeError(f"device error flag {int(t['err'].item())}")
@@ -301,7 +357,7 @@ def run_gpu(args) -> None:
         t_end = torch.cuda.Event(enable_timing=True)
         t_begin.record(stream)
         for _ in range(args.steps):
-            H.call(wl, t, stream=stream)
+            one_call(t, stream)
         t_end.record(stream)
         torch.cuda.synchronize(device)
     if world > 1:
@@ -311,7 +367,7 @@ def run_gpu(args) -> None:
     value = aggregate(wl.tokens, world, max_elapsed, args.steps)
 
     # end to end: the step's inputs from pinned host memory, the pool read back
-    e2e = run_e2e(wl, t, torch, device, stream, min(args.steps, args.e2e_steps), H)
+    e2e = run_e2e(wl, t, torch, device, stream, min(args.steps, args.e2e_steps), one_call)
     e2e_value = reduce_max_time_value(e2e, wl.tokens, world, torch, device)
 
     if rank != 0:
@@ -319,7 +375,7 @@ def run_gpu(args) -> None:
             torch.distributed.destroy_process_group()
         return
     peaks = measured_peaks()
-    alg_bytes = wl.algorithmic_bytes()
+    alg_bytes = wl.compressed_bytes() if comp else wl.algorithmic_bytes()
     avg_launch_s = elapsed / args.steps  # one launch per step; consecutive launches may overlap their edges
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = profile_traffic(args.workload)
@@ -327,7 +383,8 @@ def run_gpu(args) -> None:
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8/3-bit codes in, fp32 math, bf16 out" if comp else "bf16",
+        "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}"
                                + (f" [reduced to {args.chunks} chunks]" if args.chunks else ""),
                    "tokens_per_step": wl.tokens, "algorithmic_bytes_per_step": alg_bytes,
@@ -351,7 +408,7 @@ def run_gpu(args) -> None:
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(wl, t, torch, device, stream, steps: int, H) -> dict:
+def run_e2e(wl, t, torch, device, stream, steps: int, one_call) -> dict:
     """Host-buffer variant through the same public call: every step uploads
     its inputs (canonical chunks, patches, items, block table) from pinned
     host memory, runs the call, and reads back the call's status word (the
@@ -359,8 +416,8 @@ def run_e2e(wl, t, torch, device, stream, steps: int, H) -> dict:
     it -- the analogue of a training step reading back its loss.  Two device
     buffer sets and separate upload / compute / download streams let step
     i+1's upload overlap step i."""
-    names = [n for n in ("store", "store_off", "store_len", "patch", "patch_off", "patch_len", "items",
-                         "block_table", "section_delta") if n in t]
+    names = [n for n in ("store", "store_off", "store_len", "k_codes", "k_scale", "v_codes", "v_norm", "row_offset",
+                         "len", "patch", "patch_off", "patch_len", "items", "block_table", "section_delta") if n in t]
     host_in = {n: t[n].cpu().pin_memory() for n in names}
     host_err = [torch.empty(1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
     sets = [t, {**{n: torch.empty_like(t[n]) for n in names}, "pool_k": t["pool_k"], "pool_v": t.get("pool_v"),
@@ -384,7 +441,7 @@ def run_e2e(wl, t, torch, device, stream, steps: int, H) -> dict:
         up.record(s_up)
         stream.wait_event(up)
         stream.wait_event(down_done[b])     # step i-2's status has been read back
-        H.call(wl, d, stream=stream)
+        one_call(d, stream)
         comp_done[b].record(stream)
         with torch.cuda.stream(s_down):
             s_down.wait_event(comp_done[b])
@@ -549,7 +606,8 @@ def main(argv=None) -> None:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gqa_video", choices=sorted(W.CONFIGS) + ["patch_formation", "orbit_mean"])
+    ap.add_argument("--workload", default="gqa_video",
+                    choices=sorted(W.CONFIGS) + sorted(COMPRESSED) + ["patch_formation", "orbit_mean"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--chunks", type=int, default=0,

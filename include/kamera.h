@@ -30,7 +30,8 @@
  *     row is skipped and a bit is OR-ed into *err_flag (device int32, may be
  *     NULL), readable after the caller synchronises the stream.  The caller
  *     clears *err_flag.
- *   - Layout: bf16 everywhere.  D is the row width: num_kv_heads*head_dim for
+ *   - Layout: bf16 everywhere except the compressed store (int8 / 3-bit codes,
+ *     see kamera_compressed_store).  D is the row width: num_kv_heads*head_dim for
  *     MHA/GQA, latent_dim + rope_dim for MLA.  Chunk store, per chunk c at
  *     element offset offset[c]: [layer][channel][len[c]][D] (channel 0 = K,
  *     1 = V; MLA has only channel 0, the latent row).  Patch store, per patch
@@ -58,7 +59,7 @@ extern "C" {
 /* The CUDA stream type (cudaStream_t), declared without the CUDA headers. */
 typedef struct CUstream_st* kamera_stream_t;
 
-#define KAMERA_ABI_VERSION 2
+#define KAMERA_ABI_VERSION 3
 
 typedef enum {
   KAMERA_OK = 0,
@@ -265,6 +266,80 @@ kamera_status kamera_orbit_mean(const float* deltas, int32_t n_orderings, int64_
 #define KAMERA_FACTOR_STATIC_SCRATCH_BYTES (16u << 20)
 kamera_status kamera_factor_patches_noalloc(const kamera_factor_desc* desc, void* u_out, void* v_out,
                                             int64_t out_stride, kamera_stream_t stream);
+
+/*
+ * Compressed canonical store -- the PolyKV scheme (source: "PolyKV: A Shared
+ * Asymmetrically-Compressed KV Cache Pool for Multi-Agent LLM Inference",
+ * gist.science summary, Spanish edition, §2B "asymmetric compression scheme
+ * (TurboQuant MSE)"): keys as int8 with one linear scale per tensor; values at
+ * 3 bits by rotating each vector with a fast Walsh-Hadamard transform so its
+ * coordinates approach N(0,1), then mapping each coordinate to the nearest
+ * Lloyd-Max centroid of N(0,1); decoding takes the centroid values and the
+ * inverse transform.  Against bf16 the code bytes shrink 16 / ((8+3)/2) =
+ * 2.91x (plus one fp32 norm per head row and one scale per (chunk, layer)).
+ * MHA/GQA only, head_dim 64 or 128, D a multiple of 128.
+ *
+ * Layout (device memory).  Chunk c, layer l, token t is store row
+ * row_offset[c] + l*len[c] + t.
+ *   k_codes  int8  [n_rows][D]        code q of x: rint(x / s), in [-127, 127]
+ *   k_scale  fp32  [n_chunks][layers] s = max|x| / 127 over that layer's K of
+ *                                     the chunk (the "tensor"); decoded q * s
+ *   v_codes  uint8 [n_rows][H][3*head_dim/8]: per head row of d = head_dim
+ *                  values, 6-bit field i (i < d/2) = code[i] | code[i+d/2]<<3
+ *                  at bit 6i (bit b of byte k is bit 8k+b)
+ *   v_norm   fp32  [n_rows][H]        ||x|| of the head row
+ * V codes: w = H x with H the Sylvester-ordered Hadamard matrix,
+ * H[i][j] = (-1)^popcount(i&j); z = w / ||x||; code = the number of the seven
+ * thresholds of kamera_v_codebook that are <= z (ascending centroids).
+ * Decoded head row: (||x|| / d) * H c[code].
+ */
+typedef struct {
+  void* k_codes;              /* device int8 [n_rows][D] */
+  float* k_scale;             /* device fp32 [n_chunks][num_layers] */
+  void* v_codes;              /* device uint8 [n_rows][num_kv_heads][3*head_dim/8] */
+  float* v_norm;              /* device fp32 [n_rows][num_kv_heads] */
+  const int64_t* row_offset;  /* device [n_chunks]: store row of (chunk c, layer 0, token 0) */
+  const int32_t* len;         /* device [n_chunks]: tokens of chunk c */
+  int32_t n_chunks;
+  int32_t reserved;           /* 0 */
+  int64_t n_rows;             /* rows of k_codes / v_codes / v_norm */
+} kamera_compressed_store;
+
+/*
+ * kamera_v_codebook -- the V codebook (host call, no GPU): the 8 Lloyd-Max
+ * centroids of N(0,1) rounded to fp32, ascending, exactly antisymmetric, and
+ * the 7 thresholds (fp32 midpoints of neighbouring centroids).  Either pointer
+ * may be NULL.
+ */
+kamera_status kamera_v_codebook(float centroids[8], float thresholds[7]);
+
+/*
+ * kamera_compress_chunks -- encode a bf16 chunk store (MHA/GQA layout
+ * [layer][channel][len][D] per chunk) into `dst`: its k_codes, k_scale,
+ * v_codes and v_norm are written; its row_offset, len, n_chunks and n_rows are
+ * read (n_chunks must equal src->n_chunks; each chunk's len must match).
+ * Every encoding decision is taken in fp32 in a fixed order (the transform's
+ * butterflies with strides 1, 2, 4, ...; the sum of squares in index order
+ * with fused multiply-add; IEEE division and square root), so the bytes are
+ * reproducible.  A chunk whose lengths disagree or whose rows fall outside
+ * either store is skipped with KAMERA_EFLAG_LEN / KAMERA_EFLAG_CHUNK_OOB.
+ * dst may not overlap src.  Asynchronous on `stream`.
+ */
+kamera_status kamera_compress_chunks(const kamera_model_desc* model, const kamera_chunk_store* src,
+                                     const kamera_compressed_store* dst, int32_t* err_flag, kamera_stream_t stream);
+
+/*
+ * kamera_reuse_compressed -- kamera_reuse_batched (Kamera §2 reuse equation)
+ * whose canonical rows KV(B|empty) come from a compressed store: each row is
+ * decoded (K: q * s; V: (||v|| / d) * H c[code]) in fp32 on the way from the
+ * store to the tile, then rotated, patched, rounded to bf16 once and scattered
+ * exactly as kamera_reuse_batched does.  Same items, pool, patches and error
+ * bits (a chunk whose rows run past n_rows: KAMERA_EFLAG_CHUNK_OOB).
+ */
+kamera_status kamera_reuse_compressed(const kamera_model_desc* model, const kamera_compressed_store* store,
+                                      const kamera_patch_store* patches, const kamera_reuse_item* items,
+                                      int32_t n_items, const kamera_paged_pool* pool, int32_t* err_flag,
+                                      kamera_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* kamera_status_string(kamera_status status);

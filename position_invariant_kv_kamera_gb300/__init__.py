@@ -26,8 +26,9 @@ KAMERA_EFLAG_CHUNK_OOB, KAMERA_EFLAG_PAGE_OOB, KAMERA_EFLAG_PATCH_OOB, KAMERA_EF
     1, 2, 4, 8, 16)
 
 EXPORTS = ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch", "kamera_factor_workspace_size",
-           "kamera_factor_patches", "kamera_factor_patches_noalloc", "kamera_orbit_mean", "kamera_status_string",
-           "kamera_last_error", "kamera_abi_version")
+           "kamera_factor_patches", "kamera_factor_patches_noalloc", "kamera_orbit_mean", "kamera_v_codebook",
+           "kamera_compress_chunks", "kamera_reuse_compressed", "kamera_status_string", "kamera_last_error",
+           "kamera_abi_version")
 FACTOR_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -59,6 +60,12 @@ class kamera_factor_desc(ctypes.Structure):
     _fields_ = [("delta", ctypes.c_void_p), ("delta_stride", ctypes.c_int64), ("n_slabs", ctypes.c_int32),
                 ("T", ctypes.c_int32), ("D", ctypes.c_int32), ("rank", ctypes.c_int32),
                 ("oversample", ctypes.c_int32), ("power_iters", ctypes.c_int32), ("omega", ctypes.c_void_p)]
+
+
+class kamera_compressed_store(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("v_norm", ctypes.c_void_p), ("row_offset", ctypes.c_void_p), ("len", ctypes.c_void_p),
+                ("n_chunks", ctypes.c_int32), ("reserved", ctypes.c_int32), ("n_rows", ctypes.c_int64)]
 
 
 # kamera_reuse_item as a numpy record (32 bytes, naturally aligned)
@@ -104,6 +111,12 @@ def load(build_if_missing: bool = False):
         lib.kamera_factor_patches_noalloc.restype = ctypes.c_int
         lib.kamera_orbit_mean.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, P, P]
         lib.kamera_orbit_mean.restype = ctypes.c_int
+        lib.kamera_v_codebook.argtypes = [P, P]
+        lib.kamera_v_codebook.restype = ctypes.c_int
+        lib.kamera_compress_chunks.argtypes = [P, P, P, P, P]
+        lib.kamera_compress_chunks.restype = ctypes.c_int
+        lib.kamera_reuse_compressed.argtypes = [P, P, P, P, ctypes.c_int32, P, P, P]
+        lib.kamera_reuse_compressed.restype = ctypes.c_int
         lib.kamera_status_string.argtypes = [ctypes.c_int]
         lib.kamera_status_string.restype = ctypes.c_char_p
         lib.kamera_last_error.argtypes = []
@@ -228,6 +241,47 @@ def call(mode: str, model, *, items, pool_k, pool_v, block_table, page_size, sto
     if mode == "apply_patch":
         return kamera_apply_patch(model, ps, _ptr(items), n_items, pool, ef, sh, raise_on_error)
     raise ValueError(f"unknown mode {mode!r}")
+
+
+# ---- compressed canonical store (PolyKV §2B) -----------------------------------------------------
+
+def kamera_v_codebook():
+    """(centroids fp32 [8], thresholds fp32 [7]) of the V codes (a host call)."""
+    c = np.zeros(8, np.float32)
+    t = np.zeros(7, np.float32)
+    _check(load().kamera_v_codebook(c.ctypes.data, t.ctypes.data), True)
+    return c, t
+
+
+def compressed_store(k_codes, k_scale, v_codes, v_norm, row_offset, length):
+    """Device tensors: k_codes int8 [rows][D], k_scale fp32 [n_chunks][L], v_codes
+    uint8 [rows][H][3*head_dim/8], v_norm fp32 [rows][H], row_offset int64
+    [n_chunks], length int32 [n_chunks]."""
+    s = kamera_compressed_store(_ptr(k_codes), _ptr(k_scale), _ptr(v_codes), _ptr(v_norm), _ptr(row_offset),
+                                _ptr(length), int(length.numel()), 0, int(k_codes.shape[0]))
+    s._keep = (k_codes, k_scale, v_codes, v_norm, row_offset, length)
+    return s
+
+
+def kamera_compress_chunks(model, src, dst, err_flag_ptr, stream, raise_on_error=True) -> int:
+    return _check(load().kamera_compress_chunks(_ref(model), _ref(src), _ref(dst), err_flag_ptr, stream),
+                  raise_on_error)
+
+
+def kamera_reuse_compressed(model, store, patches, items_ptr, n_items, pool, err_flag_ptr, stream,
+                            raise_on_error=True) -> int:
+    return _check(load().kamera_reuse_compressed(_ref(model), _ref(store), _ref(patches), items_ptr, n_items,
+                                                 _ref(pool), err_flag_ptr, stream), raise_on_error)
+
+
+def call_compressed(model, cstore, *, items, pool_k, pool_v, block_table, page_size, patch=None, patch_off=None,
+                    patch_len=None, rank=0, err_flag=None, stream=None, raise_on_error=True) -> int:
+    """kamera_reuse_compressed with device tensors (``cstore`` from compressed_store)."""
+    pool = paged_pool(pool_k, pool_v, block_table, page_size)
+    ps = patch_store(patch, patch_off, patch_len, rank) if (patch is not None and rank) else None
+    n_items = int(items.numel() * items.element_size() // REUSE_ITEM.itemsize)
+    return kamera_reuse_compressed(model, cstore, ps, _ptr(items), n_items, pool, _ptr(err_flag),
+                                   stream_handle(stream), raise_on_error)
 
 
 # ---- patch formation ----------------------------------------------------------------------------

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cmath>
@@ -16,6 +17,7 @@
 #include <string>
 
 #include "kamera.h"
+#include "kamera_compress.cuh"
 #include "kamera_factor.cuh"
 #include "kamera_kernel.cuh"
 
@@ -54,11 +56,12 @@ EncodeTiledFn encode_fn() {
 }
 
 kamera_status encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                     const cuuint32_t* box, CUtensorMapSwizzle swz, const char* what) {
+                     const cuuint32_t* box, CUtensorMapSwizzle swz, const char* what,
+                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(KAMERA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(KAMERA_ERR_CUDA, "tensor map for %s: cuTensorMapEncodeTiled error %d", what, (int)r);
@@ -69,7 +72,7 @@ kamera_status encode(CUtensorMap* map, const void* base, int rank, const cuuint6
 struct DeviceFacts {
   int sms = 0;
   int smem_optin = 0;
-  bool attr_set[2] = {false, false};
+  bool attr_set[4] = {false, false, false, false};
 };
 constexpr int kMaxDevices = 64;
 DeviceFacts g_dev[kMaxDevices];
@@ -100,6 +103,49 @@ kamera_status device_facts(int* dev_out, DeviceFacts** facts) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
+// ---- the V codebook: Lloyd-Max quantiser of N(0,1), 8 levels ---------------------------------
+// Symmetric form: the four positive centroids y_k with thresholds x_0 = 0,
+// x_k = (y_{k-1} + y_k) / 2, x_4 = +inf; each y_k is the mean of N(0,1) over
+// (x_k, x_{k+1}), (phi(x_k) - phi(x_{k+1})) / (Q(x_k) - Q(x_{k+1})) with Q the
+// upper tail.  Iterated (Lloyd's method) from evenly spaced values until no
+// centroid moves by more than 1e-16.
+struct Codebook {
+  float c[8];          // ascending, c[7-k] = -c[k]
+  float t[7];          // (c[k] + c[k+1]) / 2 in fp32
+  float pair_sum[64];  // c[a] + c[b] at a + 8b
+};
+
+const Codebook& codebook() {
+  static Codebook cb;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const double inv_sqrt2 = 0.70710678118654752440, inv_sqrt2pi = 0.39894228040143267794;
+    auto phi = [&](double x) { return std::isinf(x) ? 0.0 : inv_sqrt2pi * std::exp(-0.5 * x * x); };
+    auto tail = [&](double x) { return std::isinf(x) ? 0.0 : 0.5 * std::erfc(x * inv_sqrt2); };
+    double y[4] = {0.25, 0.75, 1.25, 1.75}, x[5];
+    for (int round = 0; round < 200000; ++round) {
+      x[0] = 0.0;
+      x[4] = INFINITY;
+      for (int k = 1; k < 4; ++k) x[k] = 0.5 * (y[k - 1] + y[k]);
+      double moved = 0.0;
+      for (int k = 0; k < 4; ++k) {
+        const double yk = (phi(x[k]) - phi(x[k + 1])) / (tail(x[k]) - tail(x[k + 1]));
+        moved = std::fmax(moved, std::fabs(yk - y[k]));
+        y[k] = yk;
+      }
+      if (moved <= 1e-16) break;
+    }
+    for (int k = 0; k < 4; ++k) {
+      cb.c[4 + k] = (float)y[k];
+      cb.c[3 - k] = -cb.c[4 + k];
+    }
+    for (int k = 0; k < 7; ++k) cb.t[k] = (cb.c[k] + cb.c[k + 1]) * 0.5f;
+    for (int a = 0; a < 8; ++a)
+      for (int b = 0; b < 8; ++b) cb.pair_sum[a + 8 * b] = cb.c[a] + cb.c[b];
+  });
+  return cb;
+}
+
 enum Mode { MODE_REUSE = 0, MODE_RELOCATE_IN_PLACE = 1, MODE_PATCH_IN_PLACE = 2 };
 
 // Optional tuning overrides (for sweeps): KAMERA_BN, KAMERA_STAGES.
@@ -110,13 +156,15 @@ int env_int(const char* name) {
 
 kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chunk_store* store,
                      const kamera_patch_store* patches, const kamera_reuse_item* items, int32_t n_items,
-                     const kamera_paged_pool* pool, int32_t* err_flag, kamera_stream_t stream) {
+                     const kamera_paged_pool* pool, int32_t* err_flag, kamera_stream_t stream,
+                     const kamera_compressed_store* cstore = nullptr) {
   g_last_error.clear();
+  const bool comp = cstore != nullptr;
   if (!model) return fail(KAMERA_ERR_NULL, "model is NULL");
   if (!pool) return fail(KAMERA_ERR_NULL, "pool is NULL");
   if (n_items < 0) return fail(KAMERA_ERR_INVALID_ARG, "n_items = %d", n_items);
   if (n_items > 0 && !items) return fail(KAMERA_ERR_NULL, "items is NULL");
-  if (mode == MODE_REUSE && !store) return fail(KAMERA_ERR_NULL, "chunk store is NULL");
+  if (mode == MODE_REUSE && !store && !comp) return fail(KAMERA_ERR_NULL, "chunk store is NULL");
   if (mode == MODE_PATCH_IN_PLACE && !patches) return fail(KAMERA_ERR_NULL, "patch store is NULL");
 
   // ---- model -----------------------------------------------------------------------------
@@ -154,6 +202,12 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     head_stride = hd;
   }
   if (D > 32 * MAX_GROUPS) return fail(KAMERA_ERR_UNSUPPORTED, "row width D = %d exceeds %d", D, 32 * MAX_GROUPS);
+  if (comp) {
+    if (fam == KAMERA_MLA) return fail(KAMERA_ERR_UNSUPPORTED, "the compressed store holds separate K and V (MHA/GQA)");
+    if (model->head_dim != 64 && model->head_dim != 128)
+      return fail(KAMERA_ERR_UNSUPPORTED, "compressed store: head_dim = %d (64 or 128 served)", model->head_dim);
+    if (D % 128 != 0) return fail(KAMERA_ERR_UNSUPPORTED, "compressed store: D = %d (a multiple of 128 served)", D);
+  }
   const int n_pairs = rope / 2;
   if (n_pairs > MAX_PAIRS) return fail(KAMERA_ERR_UNSUPPORTED, "rope_dim = %d", rope);
   const int* sec = model->rope_sections;
@@ -184,7 +238,21 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     return fail(KAMERA_ERR_ALIGNMENT, "err_flag must be 4-byte aligned");
 
   // ---- stores --------------------------------------------------------------------------------
-  const bool use_store = mode == MODE_REUSE;
+  if (comp) {
+    if (!cstore->k_codes || !cstore->k_scale || !cstore->v_codes || !cstore->v_norm || !cstore->row_offset ||
+        !cstore->len)
+      return fail(KAMERA_ERR_NULL, "compressed store: a pointer is NULL");
+    if (!aligned16(cstore->k_codes) || !aligned16(cstore->v_codes) ||
+        (reinterpret_cast<uintptr_t>(cstore->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(cstore->v_norm) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cstore->row_offset) & 7u) || (reinterpret_cast<uintptr_t>(cstore->len) & 3u))
+      return fail(KAMERA_ERR_ALIGNMENT, "compressed store: codes 16-byte aligned, the other arrays naturally");
+    if (cstore->n_chunks < 0 || cstore->n_rows < 0 || cstore->reserved != 0)
+      return fail(KAMERA_ERR_INVALID_ARG, "compressed store: n_chunks = %d, n_rows = %lld", cstore->n_chunks,
+                  (long long)cstore->n_rows);
+    if (cstore->n_rows >= (int64_t(1) << 31))
+      return fail(KAMERA_ERR_UNSUPPORTED, "compressed store has %lld rows (< 2^31 served)", (long long)cstore->n_rows);
+  }
+  const bool use_store = mode == MODE_REUSE && !comp;
   int64_t store_rows = 0;
   if (use_store) {
     if (!store->data || !store->offset || !store->len)
@@ -262,16 +330,20 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
             ks_env = env_int("KAMERA_KSPLIT");
   int BN = 0, stages = 0, uv_slots = 0, ksplit = 1, kg_alloc = 0;
   uint32_t stage_bytes = 0, uv_slot_bytes = 0;
+  // compressed: the stage also holds the codes (BN*128 bytes for K, more than
+  // the 3BN/8 * 128 of V), plus the replicated centroid-sum table
+  const uint32_t table_bytes = comp ? 64u * 32u * 4u : 0u;
   const int cands[4] = {256, 192, 128, 64};
   for (int ci = 0; ci < 4 && BN == 0; ++ci) {
     const int bn = cands[ci];
     if (bn_env && bn != bn_env) continue;
     if (D % bn != 0) continue;
+    if (comp && bn % 128 != 0) continue;  // 128-column K boxes; 16-byte V code boxes
     bool whole = true;  // every rotate-half pair inside one column block
     for (int g = 0; g < n_groups; ++g)
       if (p.group_kind[g] > 0 && (g * 32) / bn != ((g + p.group_kind[g]) * 32) / bn) whole = false;
     if (!whole) continue;
-    const uint32_t sb = (uint32_t)bn * 256u;
+    const uint32_t sb = (uint32_t)bn * (comp ? 384u : 256u);
     // preference: two patch-factor slots (the factor loads then run ahead of
     // the MMA), then canonical stages (they carry the HBM stream), then whole
     // (unsplit) patch factors
@@ -284,7 +356,8 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
           if (use_patch && (rank / ks) % 16 != 0 && !(ks == 1 && rank == 8)) continue;  // whole K=16 steps
           const int kg = use_patch ? (rank / 8 / ks < 2 ? 2 : rank / 8 / ks) : 0;
           const uint32_t ub = use_patch ? (uint32_t)(BM + bn) * kg * 16u : 0u;
-          const uint64_t need = (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + smem_extra_bytes(s, u, n_pairs);
+          const uint64_t need =
+              (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + table_bytes + smem_extra_bytes(s, u, n_pairs);
           if (need > (uint64_t)facts->smem_optin) continue;
           BN = bn;
           stages = s;
@@ -298,13 +371,13 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     }
   }
   if (BN == 0) return fail(KAMERA_ERR_UNSUPPORTED, "no tile shape fits D = %d, rank %d", D, rank);
-  const uint32_t smem = (uint32_t)stages * stage_bytes + (uint32_t)uv_slots * uv_slot_bytes +
+  const uint32_t smem = (uint32_t)stages * stage_bytes + (uint32_t)uv_slots * uv_slot_bytes + table_bytes +
                         smem_extra_bytes(stages, uv_slots, n_pairs);
 
   // ---- parameters ------------------------------------------------------------------------------------
   p.items = items;
   p.n_items = n_items;
-  p.src_pool = use_store ? 0 : 1;
+  p.src_pool = (use_store || comp) ? 0 : 1;
   p.has_patches = use_patch ? 1 : 0;
   p.need_patch = mode == MODE_PATCH_IN_PLACE ? 1 : 0;
   p.rank = rank;
@@ -383,6 +456,32 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
         return st;
     }
   }
+  if (comp) {
+    const Codebook& cb = codebook();
+    p.comp_row_offset = cstore->row_offset;
+    p.comp_len = cstore->len;
+    p.k_scale = cstore->k_scale;
+    p.v_norm = cstore->v_norm;
+    p.comp_rows = cstore->n_rows;
+    p.n_chunks = cstore->n_chunks;
+    p.head_dim = model->head_dim;
+    p.out_bytes = (uint32_t)BN * 256u;
+    p.table_bytes = table_bytes;
+    for (int i = 0; i < 64; ++i) p.pair_sum[i] = cb.pair_sum[i];
+    const cuuint64_t rows = (cuuint64_t)(cstore->n_rows > 0 ? cstore->n_rows : 1);
+    const cuuint64_t kdims[2] = {(cuuint64_t)D, rows};
+    const cuuint64_t kstrides[1] = {(cuuint64_t)D};
+    const cuuint32_t kbox[2] = {128u, (cuuint32_t)BM};
+    if (kamera_status st = encode(&p.kc_map, cstore->k_codes, 2, kdims, kstrides, kbox, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  "K codes", CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return st;
+    const cuuint64_t vdims[2] = {(cuuint64_t)(3 * D / 8), rows};
+    const cuuint64_t vstrides[1] = {(cuuint64_t)(3 * D / 8)};
+    const cuuint32_t vbox[2] = {(cuuint32_t)(3 * BN / 8), (cuuint32_t)BM};
+    if (kamera_status st = encode(&p.vc_map, cstore->v_codes, 2, vdims, vstrides, vbox, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                  "V codes", CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return st;
+  }
   if (use_patch) {
     p.patch_off = patches->offset;
     p.patch_len = patches->len;
@@ -399,11 +498,15 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   }
 
   // ---- launch ----------------------------------------------------------------------------------------------
-  const void* fn = use_patch ? reinterpret_cast<const void*>(&reuse_kernel<true>)
-                             : reinterpret_cast<const void*>(&reuse_kernel<false>);
+  const void* fns[4] = {reinterpret_cast<const void*>(&reuse_kernel<false, false>),
+                        reinterpret_cast<const void*>(&reuse_kernel<true, false>),
+                        reinterpret_cast<const void*>(&reuse_kernel<false, true>),
+                        reinterpret_cast<const void*>(&reuse_kernel<true, true>)};
+  const int variant = (use_patch ? 1 : 0) + (comp ? 2 : 0);
+  const void* fn = fns[variant];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    bool& set = facts->attr_set[use_patch ? 1 : 0];
+    bool& set = facts->attr_set[variant];
     if (!set) {
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, facts->smem_optin);
       if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -423,8 +526,84 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   attr[0].val.programmaticStreamSerializationAllowed = env_int("KAMERA_NO_PDL") ? 0 : 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = use_patch ? cudaLaunchKernelEx(&cfg, reuse_kernel<true>, p) : cudaLaunchKernelEx(&cfg, reuse_kernel<false>, p);
+  cudaError_t e;
+  switch (variant) {
+    case 0: e = cudaLaunchKernelEx(&cfg, reuse_kernel<false, false>, p); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, reuse_kernel<true, false>, p); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, reuse_kernel<false, true>, p); break;
+    default: e = cudaLaunchKernelEx(&cfg, reuse_kernel<true, true>, p); break;
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return KAMERA_OK;
+}
+
+// ---- compressed store encoder ---------------------------------------------------------------------
+
+kamera_status compress_chunks(const kamera_model_desc* model, const kamera_chunk_store* src,
+                              const kamera_compressed_store* dst, int32_t* err_flag, kamera_stream_t stream) {
+  g_last_error.clear();
+  if (!model || !src || !dst) return fail(KAMERA_ERR_NULL, "model, src or dst is NULL");
+  if (model->family != KAMERA_MHA && model->family != KAMERA_GQA)
+    return fail(model->family == KAMERA_MLA ? KAMERA_ERR_UNSUPPORTED : KAMERA_ERR_INVALID_ARG,
+                "compressed store: family = %d (MHA/GQA served)", model->family);
+  if (model->num_layers < 1 || model->num_kv_heads < 1)
+    return fail(KAMERA_ERR_INVALID_ARG, "num_layers = %d, num_kv_heads = %d", model->num_layers,
+                model->num_kv_heads);
+  const int hd = model->head_dim;
+  if (hd != 64 && hd != 128) return fail(KAMERA_ERR_UNSUPPORTED, "compressed store: head_dim = %d (64 or 128)", hd);
+  const int D = model->num_kv_heads * hd;
+  if (D % 128 != 0 || D > 32 * MAX_GROUPS)
+    return fail(KAMERA_ERR_UNSUPPORTED, "compressed store: D = %d (a multiple of 128 up to %d)", D, 32 * MAX_GROUPS);
+  if (src->n_chunks < 0 || dst->n_chunks != src->n_chunks)
+    return fail(KAMERA_ERR_INVALID_ARG, "n_chunks: src %d, dst %d", src->n_chunks, dst->n_chunks);
+  if (dst->n_rows < 0 || src->n_elems < 0 || dst->reserved != 0)
+    return fail(KAMERA_ERR_INVALID_ARG, "sizes: src n_elems %lld, dst n_rows %lld", (long long)src->n_elems,
+                (long long)dst->n_rows);
+  if (src->n_chunks == 0) return KAMERA_OK;
+  if (!src->data || !src->offset || !src->len || !dst->k_codes || !dst->k_scale || !dst->v_codes || !dst->v_norm ||
+      !dst->row_offset || !dst->len)
+    return fail(KAMERA_ERR_NULL, "a store pointer is NULL");
+  if (!aligned16(src->data) || !aligned16(dst->k_codes) || !aligned16(dst->v_codes) ||
+      (reinterpret_cast<uintptr_t>(dst->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(dst->v_norm) & 3u))
+    return fail(KAMERA_ERR_ALIGNMENT, "store data and codes must be 16-byte aligned");
+  if (err_flag && (reinterpret_cast<uintptr_t>(err_flag) & 3u))
+    return fail(KAMERA_ERR_ALIGNMENT, "err_flag must be 4-byte aligned");
+  if (src->n_chunks > 65535) return fail(KAMERA_ERR_UNSUPPORTED, "n_chunks = %d (<= 65535)", src->n_chunks);
+  int dev = 0;
+  DeviceFacts* facts = nullptr;
+  if (kamera_status st = device_facts(&dev, &facts)) return st;
+  const Codebook& cb = codebook();
+  compress::Args a;
+  a.store = static_cast<const uint16_t*>(src->data);
+  a.store_off = src->offset;
+  a.store_len = src->len;
+  a.store_elems = src->n_elems;
+  a.k_codes = static_cast<int8_t*>(dst->k_codes);
+  a.k_scale = dst->k_scale;
+  a.v_codes = static_cast<uint8_t*>(dst->v_codes);
+  a.v_norm = dst->v_norm;
+  a.row_offset = dst->row_offset;
+  a.len = dst->len;
+  a.rows = dst->n_rows;
+  a.n_chunks = src->n_chunks;
+  a.L = model->num_layers;
+  a.D = D;
+  a.H = model->num_kv_heads;
+  a.hd = hd;
+  for (int k = 0; k < 7; ++k) a.thresholds[k] = cb.t[k];
+  a.err_flag = err_flag;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  compress::k_scale_kernel<<<dim3((unsigned)a.L, (unsigned)a.n_chunks), 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  // about four waves of 128-thread blocks, split across the chunks
+  const int gx = (int)std::max<int64_t>(1, (int64_t)facts->sms * 16 / src->n_chunks);
+  if (hd == 128)
+    compress::encode_kernel<128><<<dim3((unsigned)gx, (unsigned)a.n_chunks), compress::THREADS, 0, s>>>(a);
+  else
+    compress::encode_kernel<64><<<dim3((unsigned)gx, (unsigned)a.n_chunks), compress::THREADS, 0, s>>>(a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   return KAMERA_OK;
 }
@@ -668,6 +847,29 @@ kamera_status kamera_apply_patch(const kamera_model_desc* model, const kamera_pa
                                  int32_t* err_flag, kamera_stream_t stream) {
   return kamera::launch(kamera::MODE_PATCH_IN_PLACE, model, nullptr, patches, items, n_items, pool, err_flag,
                         stream);
+}
+
+kamera_status kamera_v_codebook(float centroids[8], float thresholds[7]) {
+  const kamera::Codebook& cb = kamera::codebook();
+  if (centroids) memcpy(centroids, cb.c, sizeof cb.c);
+  if (thresholds) memcpy(thresholds, cb.t, sizeof cb.t);
+  return KAMERA_OK;
+}
+
+kamera_status kamera_compress_chunks(const kamera_model_desc* model, const kamera_chunk_store* src,
+                                     const kamera_compressed_store* dst, int32_t* err_flag, kamera_stream_t stream) {
+  return kamera::compress_chunks(model, src, dst, err_flag, stream);
+}
+
+kamera_status kamera_reuse_compressed(const kamera_model_desc* model, const kamera_compressed_store* store,
+                                      const kamera_patch_store* patches, const kamera_reuse_item* items,
+                                      int32_t n_items, const kamera_paged_pool* pool, int32_t* err_flag,
+                                      kamera_stream_t stream) {
+  if (!store) {
+    kamera::g_last_error = "compressed store is NULL";
+    return KAMERA_ERR_NULL;
+  }
+  return kamera::launch(kamera::MODE_REUSE, model, nullptr, patches, items, n_items, pool, err_flag, stream, store);
 }
 
 const char* kamera_status_string(kamera_status status) {

@@ -27,6 +27,15 @@
 //               reduction, fp32 sincos and math), add, round to bf16 in place;
 //               the few edge rows of partly covered pages that do not fill an
 //               8-row box are stored by their own threads.
+// Compressed canonical store (kComp; PolyKV, gist.science summary, §2B): the
+// producer stages int8 K codes (128-column boxes, 128B swizzle) or packed 3-bit
+// V codes behind the stage's bf16 output tile, and the epilogue decodes them
+// on the fly -- K: code * per-(chunk, layer) scale; V: each 6-bit field
+// (codes i and i + d/2) becomes x_i +- x_{i+d/2} by one lookup in a
+// lane-replicated table of centroid sums, then a Walsh-Hadamard transform of
+// length d/2 in registers and the scale ||v|| / d.  Each epilogue half decodes
+// its half of every head.  The decoded row then takes the same rotation,
+// patch and store as a bf16 canonical row.
 // Every wait on an mbarrier is bounded (about 2 s): on expiry the kernel sets
 // KAMERA_EFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -105,6 +114,18 @@ struct Params {
   const int64_t* section_delta;    // [n_items][3] per-section shifts, or nullptr (every section: item delta)
   uint32_t stage_bytes, u_bytes, v_bytes, tmem_cols;  // stage_bytes = one canonical tile
   int32_t* err_flag;
+  // compressed canonical store (kComp)
+  CUtensorMap kc_map;  // K codes as rows [rows][D] uint8: box 128 x 128, 128B swizzle
+  CUtensorMap vc_map;  // V codes as rows [rows][3D/8] uint8: box 3BN/8 x 128, no swizzle
+  const int64_t* comp_row_offset;  // [n_chunks]: chunk c, layer l, token t at row offset[c] + l*T + t
+  const int32_t* comp_len;         // [n_chunks]
+  const float* k_scale;            // [n_chunks][num_layers]
+  const float* v_norm;             // [rows][D / head_dim]
+  int64_t comp_rows;
+  int32_t head_dim;
+  uint32_t out_bytes;    // bf16 output tile at the start of each stage; the codes follow it
+  uint32_t table_bytes;  // the replicated centroid-sum table
+  float pair_sum[64];    // c[a] + c[b] at index a + 8b (fp32 codebook)
   int8_t group_kind[MAX_GROUPS];
   uint8_t pair_base[MAX_GROUPS];
   uint8_t owner0[MAX_GROUPS];  // epilogue half that processes the unit starting at group g (rotated tiles)
@@ -142,7 +163,12 @@ __device__ __forceinline__ int64_t item_tiles(const Params& p, int32_t i, Walker
   if (it.n_tokens < 0 || it.dst_pos < 0) { err |= KAMERA_EFLAG_LEN; return 0; }
   if (it.seq < 0 || it.seq >= p.n_seqs) { err |= KAMERA_EFLAG_PAGE_OOB; return 0; }
   const int64_t T = it.n_tokens;
-  if (!p.src_pool) {
+  if (p.comp_row_offset) {
+    if (it.chunk_id < 0 || it.chunk_id >= p.n_chunks) { err |= KAMERA_EFLAG_CHUNK_OOB; return 0; }
+    if (p.comp_len[it.chunk_id] != it.n_tokens) { err |= KAMERA_EFLAG_LEN; return 0; }
+    const int64_t r0 = p.comp_row_offset[it.chunk_id];
+    if (r0 < 0 || r0 + (int64_t)p.num_layers * T > p.comp_rows) { err |= KAMERA_EFLAG_CHUNK_OOB; return 0; }
+  } else if (!p.src_pool) {
     if (it.chunk_id < 0 || it.chunk_id >= p.n_chunks) { err |= KAMERA_EFLAG_CHUNK_OOB; return 0; }
     if (p.store_len[it.chunk_id] != it.n_tokens) { err |= KAMERA_EFLAG_LEN; return 0; }
     const int64_t off = p.store_off[it.chunk_id];
@@ -239,6 +265,7 @@ struct SmemMisc {
 struct Smem {
   uint8_t* stages;     // stage s at stages + s * stage_bytes
   uint8_t* uv;         // slot u at uv + u * (u_bytes + v_bytes): U tile then V tile
+  float* table;        // compressed V: pair_sum[e] for lane l at table[e * 32 + l]
   uint64_t* full;      // [stages] TMA loads landed
   uint64_t* uv_full;   // [uv_slots] patch factors landed
   uint64_t* uv_empty;  // [uv_slots] slot free (MMA done with it)
@@ -257,7 +284,8 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
   Smem s;
   s.stages = base;
   s.uv = base + (size_t)p.stages * p.stage_bytes;
-  uint8_t* q = s.uv + (size_t)p.uv_slots * (p.u_bytes + p.v_bytes);
+  s.table = reinterpret_cast<float*>(s.uv + (size_t)p.uv_slots * (p.u_bytes + p.v_bytes));
+  uint8_t* q = reinterpret_cast<uint8_t*>(s.table) + p.table_bytes;
   s.full = reinterpret_cast<uint64_t*>(q);
   s.empty = s.full + p.stages;
   s.computed = s.empty + p.stages;
@@ -354,12 +382,44 @@ __device__ __forceinline__ void put16(uint32_t a0, uint32_t a1, uint4 v0, uint4 
   }
 }
 
+// int8 codes -> fp32: a byte permute builds the float 2^23 + (q + 128), the
+// subtraction of 2^23 + 128 is exact, and the product with the scale is the
+// one rounding (the same value as (float)q * scale).
+__device__ __forceinline__ void dequant16(uint4 v, float scale, float* x) {
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      x[4 * k + b] = (__uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7540u | (uint32_t)b)) - 8388736.0f) * scale;
+}
+
+// Canonical values of this thread's row, 16 columns at a time.
+struct SrcTile {  // the bf16 tile itself (TMA-loaded canonical rows)
+  RowView rv;
+  __device__ __forceinline__ void load16(int c, float* x) const {
+    const uint4 v0 = lds128(rv.chunk(c)), v1 = lds128(rv.chunk(c + 8));
+    unpack8(v0, x);
+    unpack8(v1, x + 8);
+  }
+};
+struct SrcK8 {  // int8 K codes: 128-column boxes, 128B swizzle, one scale per (chunk, layer)
+  uint32_t base;  // staging + row * 128
+  uint32_t sw;    // row & 7
+  float scale;
+  __device__ __forceinline__ void load16(int c, float* x) const {
+    dequant16(lds128(base + (uint32_t)(c >> 7) * BOX_BYTES + ((((uint32_t)c >> 4) & 7u) ^ sw) * 16u), scale, x);
+  }
+};
+
 // 16 columns without rotation: out = x + P (patched); without a patch the
-// tile already holds the output and only a thread-stored row is copied out.
-template <bool kPatched>
-__device__ __forceinline__ void epi_plain16(const RowView& rv, int c0, uint32_t taddr, uint16_t* gdst) {
+// bf16 tile already holds the output and only a thread-stored row is copied
+// out (a compressed source is always decoded and written).
+template <bool kPatched, bool kComp, class Src>
+__device__ __forceinline__ void epi_plain16(const Src& src, const RowView& rv, int c0, uint32_t taddr,
+                                            uint16_t* gdst) {
   const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
-  if (!kPatched) {
+  if (!kPatched && !kComp) {
     if (gdst) {
       stg128_cs(gdst + c0, lds128(a0));
       stg128_cs(gdst + c0 + 8, lds128(a1));
@@ -367,34 +427,30 @@ __device__ __forceinline__ void epi_plain16(const RowView& rv, int c0, uint32_t 
     return;
   }
   uint32_t acc[16];
-  tmem_ld16(taddr + (uint32_t)c0, acc);
-  const uint4 v0 = lds128(a0), v1 = lds128(a1);
-  tmem_ld_wait();
+  if (kPatched) tmem_ld16(taddr + (uint32_t)c0, acc);
   float x[16];
-  unpack8(v0, x);
-  unpack8(v1, x + 8);
+  src.load16(c0, x);
+  if (kPatched) {
+    tmem_ld_wait();
 #pragma unroll
-  for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(acc[e]);
+    for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(acc[e]);
+  }
   put16(a0, a1, pack8(x), pack8(x + 8), gdst, c0);
 }
 
 // 16 rotate-half pairs (cA + e, cB + e), pair index pb + e.
-template <bool kPatched, bool kCanonicalFrame>
-__device__ __forceinline__ void epi_rotate16(const RowView& rv, int cA, int cB, int pb, uint32_t taddr,
-                                             const float2* cs, uint16_t* gdst) {
+template <bool kPatched, bool kCanonicalFrame, class Src>
+__device__ __forceinline__ void epi_rotate16(const Src& src, const RowView& rv, int cA, int cB, int pb,
+                                             uint32_t taddr, const float2* cs, uint16_t* gdst) {
   uint32_t accA[16], accB[16];
   if (kPatched) {
     tmem_ld16(taddr + (uint32_t)cA, accA);
     tmem_ld16(taddr + (uint32_t)cB, accB);
   }
-  const uint32_t a0 = rv.chunk(cA), a1 = rv.chunk(cA + 8), b0 = rv.chunk(cB), b1 = rv.chunk(cB + 8);
-  const uint4 va0 = lds128(a0), va1 = lds128(a1), vb0 = lds128(b0), vb1 = lds128(b1);
-  if (kPatched) tmem_ld_wait();
   float xa[16], xb[16];
-  unpack8(va0, xa);
-  unpack8(va1, xa + 8);
-  unpack8(vb0, xb);
-  unpack8(vb1, xb + 8);
+  src.load16(cA, xa);
+  src.load16(cB, xb);
+  if (kPatched) tmem_ld_wait();
   const float4* cs4 = reinterpret_cast<const float4*>(cs + pb);
 #pragma unroll
   for (int e2 = 0; e2 < 8; ++e2) {
@@ -418,22 +474,19 @@ __device__ __forceinline__ void epi_rotate16(const RowView& rv, int cA, int cB, 
       xb[e] = rb;
     }
   }
-  put16(a0, a1, pack8(xa), pack8(xa + 8), gdst, cA);
-  put16(b0, b1, pack8(xb), pack8(xb + 8), gdst, cB);
+  put16(rv.chunk(cA), rv.chunk(cA + 8), pack8(xa), pack8(xa + 8), gdst, cA);
+  put16(rv.chunk(cB), rv.chunk(cB + 8), pack8(xb), pack8(xb + 8), gdst, cB);
 }
 
 // 8 interleaved pairs (2e, 2e+1) in 16 columns, pair index pb + e.
-template <bool kPatched, bool kCanonicalFrame>
-__device__ __forceinline__ void epi_interleaved16(const RowView& rv, int c0, int pb, uint32_t taddr,
+template <bool kPatched, bool kCanonicalFrame, class Src>
+__device__ __forceinline__ void epi_interleaved16(const Src& src, const RowView& rv, int c0, int pb, uint32_t taddr,
                                                   const float2* cs, uint16_t* gdst) {
   uint32_t acc[16];
   if (kPatched) tmem_ld16(taddr + (uint32_t)c0, acc);
-  const uint32_t a0 = rv.chunk(c0), a1 = rv.chunk(c0 + 8);
-  const uint4 v0 = lds128(a0), v1 = lds128(a1);
-  if (kPatched) tmem_ld_wait();
   float x[16];
-  unpack8(v0, x);
-  unpack8(v1, x + 8);
+  src.load16(c0, x);
+  if (kPatched) tmem_ld_wait();
   const float4* cs4 = reinterpret_cast<const float4*>(cs + pb);
 #pragma unroll
   for (int e2 = 0; e2 < 4; ++e2) {
@@ -457,16 +510,16 @@ __device__ __forceinline__ void epi_interleaved16(const RowView& rv, int c0, int
       x[2 * e + 1] = rb;
     }
   }
-  put16(a0, a1, pack8(x), pack8(x + 8), gdst, c0);
+  put16(rv.chunk(c0), rv.chunk(c0 + 8), pack8(x), pack8(x + 8), gdst, c0);
 }
 
 // One tile row's share of the compute phase for epilogue half h.  gdst: the
 // pool row (at the tile's first column) when this row is stored by its
 // threads, else nullptr.
-template <bool kPatched, bool kCanonicalFrame>
-__device__ __forceinline__ void epi_row(const Params& p, const RowView& rv, int cb, bool rot, int h, uint32_t taddr,
-                                        const float2* cs, uint16_t* gdst) {
-  if (!kPatched && !rot && !gdst) return;  // bit copy of the whole tile: nothing to do
+template <bool kPatched, bool kCanonicalFrame, bool kComp, class Src>
+__device__ __forceinline__ void epi_row(const Params& p, const Src& src, const RowView& rv, int cb, bool rot, int h,
+                                        uint32_t taddr, const float2* cs, uint16_t* gdst) {
+  if (!kPatched && !kComp && !rot && !gdst) return;  // bit copy of the whole tile: nothing to do
   const int ng = p.BN / 32;
   const int g0 = cb * ng;
   for (int gl = 0; gl < ng; ++gl) {
@@ -477,24 +530,115 @@ __device__ __forceinline__ void epi_row(const Params& p, const RowView& rv, int 
     if (owner != h) continue;
     const int c0 = gl * 32;
     if (kind == GK_PLAIN) {
-      epi_plain16<kPatched>(rv, c0, taddr, gdst);
-      epi_plain16<kPatched>(rv, c0 + 16, taddr, gdst);
+      epi_plain16<kPatched, kComp>(src, rv, c0, taddr, gdst);
+      epi_plain16<kPatched, kComp>(src, rv, c0 + 16, taddr, gdst);
     } else if (kind == GK_INTERLEAVED) {
       const int pb = p.pair_base[g];
-      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0, pb, taddr, cs, gdst);
-      epi_interleaved16<kPatched, kCanonicalFrame>(rv, c0 + 16, pb + 8, taddr, cs, gdst);
+      epi_interleaved16<kPatched, kCanonicalFrame>(src, rv, c0, pb, taddr, cs, gdst);
+      epi_interleaved16<kPatched, kCanonicalFrame>(src, rv, c0 + 16, pb + 8, taddr, cs, gdst);
     } else {
       const int pb = p.pair_base[g];
       const int cB = (gl + kind) * 32;
-      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0, cB, pb, taddr, cs, gdst);
-      epi_rotate16<kPatched, kCanonicalFrame>(rv, c0 + 16, cB + 16, pb + 16, taddr, cs, gdst);
+      epi_rotate16<kPatched, kCanonicalFrame>(src, rv, c0, cB, pb, taddr, cs, gdst);
+      epi_rotate16<kPatched, kCanonicalFrame>(src, rv, c0 + 16, cB + 16, pb + 16, taddr, cs, gdst);
     }
+  }
+}
+
+// ---- compressed V: Walsh-Hadamard decode ----------------------------------------------------
+
+// In-place unnormalised Walsh-Hadamard transform of N values (Sylvester order).
+template <int N>
+__device__ __forceinline__ void fwht(float* u) {
+#pragma unroll
+  for (int h = 1; h < N; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < N; i += 2 * h)
+#pragma unroll
+      for (int j = i; j < i + h; ++j) {
+        const float a = u[j], b = u[j + h];
+        u[j] = a + b;
+        u[j + h] = a - b;
+      }
+}
+
+// Bit k of a head row's code stream is set in this mask iff it is one of the
+// upper three bits of its 6-bit field; XOR-ing it turns every field (a, b)
+// into (a, 7 - b), i.e. c[b] into c[7 - b] = -c[b].
+__host__ __device__ constexpr uint32_t upper_field_mask(int word) {
+  uint32_t m = 0;
+  for (int b = 0; b < 32; ++b)
+    if (((word * 32 + b) % 6) >= 3) m |= 1u << b;
+  return m;
+}
+
+// Half h of one head of this thread's row: outputs j = h*HD/2 + i, i < HD/2,
+//     v^_j = (||v|| / HD) * (H_{HD/2} (x_lo +- x_hi))_i,
+// where x_lo / x_hi are the centroids of codes i and i + HD/2 (field i) and
+// the sign is + for h = 0, - for h = 1 (the first butterfly of H_HD).
+//   codes: shared address of the head's packed codes (3*HD/8 bytes)
+//   scale: ||v|| / HD;   c_out: tile column of output i = 0
+//   tab_lane: shared address of the pair table + 4 * lane
+template <int HD, bool kPatched>
+__device__ __forceinline__ void epi_vhalf(const RowView& rv, uint32_t codes, float scale, int h, int c_out,
+                                          uint32_t taddr, uint32_t tab_lane, uint16_t* gdst) {
+  constexpr int NW = 3 * HD / 32;  // 32-bit code words per head row
+  constexpr int NF = HD / 2;       // fields = outputs of this half
+  uint32_t w[NW];
+  if (HD == 128) {
+#pragma unroll
+    for (int k = 0; k < NW / 4; ++k) {
+      const uint4 v = lds128(codes + 16u * k);
+      w[4 * k] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NW / 2; ++k) {
+      const uint2 v = lds64(codes + 8u * k);
+      w[2 * k] = v.x;
+      w[2 * k + 1] = v.y;
+    }
+  }
+  if (h) {
+#pragma unroll
+    for (int k = 0; k < NW; ++k) w[k] ^= upper_field_mask(k);
+  }
+  float u[NF];
+#pragma unroll
+  for (int i = 0; i < NF; ++i) {
+    const int bit = 6 * i, wi = bit >> 5, o = bit & 31;
+    // field i shifted to bit 7: table entry e of this lane is at e * 128 + lane * 4
+    uint32_t f;
+    if (o <= 26)
+      f = o >= 7 ? (w[wi] >> (o - 7)) : (w[wi] << (7 - o));
+    else
+      f = __funnelshift_r(w[wi], w[wi + 1], o - 7);
+    u[i] = lds_f32_const(tab_lane + (f & (63u << 7)));
+  }
+  fwht<NF>(u);
+#pragma unroll
+  for (int g = 0; g < NF; g += 16) {
+    float x[16];
+    if (kPatched) {
+      uint32_t acc[16];
+      tmem_ld16(taddr + (uint32_t)(c_out + g), acc);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = fmaf(u[g + e], scale, __uint_as_float(acc[e]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = u[g + e] * scale;
+    }
+    put16(rv.chunk(c_out + g), rv.chunk(c_out + g + 8), pack8(x), pack8(x + 8), gdst, c_out + g);
   }
 }
 
 // ---- the kernel ----------------------------------------------------------------------------------
 
-template <bool kPatch>
+template <bool kPatch, bool kComp>
 __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem sm = carve_smem(smem_raw, p);
@@ -563,6 +707,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       tmem_relinquish();
     }
   }
+  if (kComp)  // one copy of the centroid-sum table per lane: lane l reads only bank l
+    for (int i = threadIdx.x; i < 64 * 32; i += NUM_THREADS) sm.table[i] = p.pair_sum[i >> 5];
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -575,7 +721,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   if (warp == 0) {
     // ================= TMA producer: canonical tiles =================
     if (lane == 0) {
-      tma_prefetch_desc(p.src_pool ? &p.pool_map[0] : &p.src_map);
+      if (kComp) {
+        tma_prefetch_desc(&p.kc_map);
+        tma_prefetch_desc(&p.vc_map);
+      } else {
+        tma_prefetch_desc(p.src_pool ? &p.pool_map[0] : &p.src_map);
+      }
       Walker w;
       walker_init(w);
       uint32_t it = 0;
@@ -594,9 +745,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           }
         }
         const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
-        const int32_t src_row =
-            p.src_pool ? 0
-                       : (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
+        int32_t src_row = 0;
+        if (kComp) {
+          src_row = (int32_t)(p.comp_row_offset[w.chunk] + (int64_t)t.layer * w.T + t0);
+          bytes = t.ch == 0 ? (uint32_t)p.BN * (uint32_t)BM : (uint32_t)(3 * p.BN / 8) * (uint32_t)BM;
+        } else if (!p.src_pool) {
+          src_row = (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
+        }
         for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
           const int s = (int)(it % (uint32_t)p.stages);
           const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
@@ -604,7 +759,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
           const int col0 = (p.cb_first + cbi) * p.BN;
           mbar_arrive_expect_tx(&sm.full[s], bytes);
-          if (!p.src_pool) {
+          if (kComp) {
+            uint8_t* stg = st + p.out_bytes;
+            if (t.ch == 0) {
+              for (int b = 0; b < p.BN / 128; ++b)
+                tma_load_2d(stg + b * BOX_BYTES, &p.kc_map, &sm.full[s], col0 + b * 128, src_row);
+            } else {
+              tma_load_2d(stg, &p.vc_map, &sm.full[s], (p.cb_first + cbi) * (3 * p.BN / 8), src_row);
+            }
+          } else if (!p.src_pool) {
             for (int b = 0; b < nbox; ++b)
               tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, src_row);
           } else {
@@ -786,6 +949,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           }
         }
       }
+      // compressed store: this row's store row and the K scale of (chunk, layer)
+      int64_t crow = -1;
+      float kscale = 0.0f;
+      if (kComp) {
+        const int64_t tok = t.pos0 + r - w.dst_pos;
+        if (tok >= 0 && tok < w.T) crow = p.comp_row_offset[w.chunk] + (int64_t)t.layer * w.T + tok;
+        if (t.ch == 0) kscale = p.k_scale[(int64_t)w.chunk * p.num_layers + t.layer];
+      }
       // phase tables alternate by row-block parity: their previous readers
       // finished before the last joint barrier
       float2* cs = sm.cs + (rbi & 1u) * pairs_pad(p.n_pairs);
@@ -800,6 +971,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         const int s = (int)(it % (uint32_t)p.stages);
         const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
         const uint32_t buf = pt & 1u;
+        float nrm[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // compressed V: ||v|| of the tile's heads in this row
+        if (kComp && t.ch == 1 && crow >= 0) {
+          const int hpt = p.BN / p.head_dim, H = p.D / p.head_dim;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < hpt) nrm[j] = __ldg(p.v_norm + crow * H + t.cb * hpt + j);
+        }
         bool wok = ok && wait_bounded(&sm.full[s], ph, sm.misc, p.err_flag);
         if (wok && patched) wok = wait_bounded(&sm.tfull[buf], (pt >> 1) & 1u, sm.misc, p.err_flag);
         ok = __all_sync(0xFFFFFFFFu, wok);
@@ -809,14 +987,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           const RowView rv{smem_addr(sm.stages + (size_t)s * p.stage_bytes) + (uint32_t)r * 128u, (uint32_t)r & 7u};
           const uint32_t taddr = tmem_base + lane_addr + buf * (uint32_t)p.BN;
           uint16_t* gdst = dst >= 0 ? p.pool[t.ch] + dst * p.D + (int64_t)t.cb * p.BN : nullptr;
-          if (patched) {
-            tc_fence_after_sync();
-            if (p.frame == KAMERA_PATCH_CANONICAL_FRAME)
-              epi_row<true, true>(p, rv, t.cb, rot, h, taddr, cs, gdst);
+          if (patched) tc_fence_after_sync();
+          if (kComp && t.ch == 1) {
+            const uint32_t stg = smem_addr(sm.stages + (size_t)s * p.stage_bytes) + p.out_bytes;
+            const uint32_t tab = smem_addr(sm.table) + 4u * (uint32_t)lane;
+            const int hpt = p.BN / p.head_dim;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (j >= hpt) break;
+              if (p.head_dim == 128) {
+                const uint32_t codes = stg + (uint32_t)r * (3u * p.BN / 8u) + (uint32_t)j * 48u;
+                if (patched)
+                  epi_vhalf<128, true>(rv, codes, nrm[j] * (1.0f / 128), h, j * 128 + h * 64, taddr, tab, gdst);
+                else
+                  epi_vhalf<128, false>(rv, codes, nrm[j] * (1.0f / 128), h, j * 128 + h * 64, taddr, tab, gdst);
+              } else {
+                const uint32_t codes = stg + (uint32_t)r * (3u * p.BN / 8u) + (uint32_t)j * 24u;
+                if (patched)
+                  epi_vhalf<64, true>(rv, codes, nrm[j] * (1.0f / 64), h, j * 64 + h * 32, taddr, tab, gdst);
+                else
+                  epi_vhalf<64, false>(rv, codes, nrm[j] * (1.0f / 64), h, j * 64 + h * 32, taddr, tab, gdst);
+              }
+            }
+          } else if (kComp) {
+            const uint32_t stg = smem_addr(sm.stages + (size_t)s * p.stage_bytes) + p.out_bytes;
+            const SrcK8 src{stg + (uint32_t)r * 128u, (uint32_t)r & 7u, kscale};
+            if (patched && p.frame == KAMERA_PATCH_CANONICAL_FRAME)
+              epi_row<true, true, true>(p, src, rv, t.cb, rot, h, taddr, cs, gdst);
+            else if (patched)
+              epi_row<true, false, true>(p, src, rv, t.cb, rot, h, taddr, cs, gdst);
             else
-              epi_row<true, false>(p, rv, t.cb, rot, h, taddr, cs, gdst);
+              epi_row<false, false, true>(p, src, rv, t.cb, rot, h, taddr, cs, gdst);
           } else {
-            epi_row<false, false>(p, rv, t.cb, rot, h, taddr, cs, gdst);
+            const SrcTile src{rv};
+            if (patched && p.frame == KAMERA_PATCH_CANONICAL_FRAME)
+              epi_row<true, true, false>(p, src, rv, t.cb, rot, h, taddr, cs, gdst);
+            else if (patched)
+              epi_row<true, false, false>(p, src, rv, t.cb, rot, h, taddr, cs, gdst);
+            else
+              epi_row<false, false, false>(p, src, rv, t.cb, rot, h, taddr, cs, gdst);
           }
         }
         if (patched) {

@@ -26,10 +26,11 @@ def model_for(wl: W.Workload, t: dict | None = None):
                          section_delta=(t or {}).get("section_delta"))
 
 
-def device_inputs(wl: W.Workload, torch, device="cuda", pool_host=None) -> dict:
-    """All device tensors of one call; the pool is the sentinel / seeded initial pool."""
+def device_inputs(wl: W.Workload, torch, device="cuda", pool_host=None, with_store=True) -> dict:
+    """All device tensors of one call; the pool is the sentinel / seeded initial pool.
+    with_store=False leaves out the bf16 chunk store (a compressed store serves instead)."""
     t = {}
-    if wl.mode == "reuse":
+    if wl.mode == "reuse" and with_store:
         t["store"] = wl.device_store(torch, device)
         t["store_off"] = torch.tensor(wl.store_off, dtype=torch.int64, device=device)
         t["store_len"] = torch.tensor(np.array(wl.chunk_lens, np.int32), dtype=torch.int32, device=device)
@@ -130,3 +131,70 @@ def assert_report(rep: dict):
     assert rep["within_tol"], rep
     if "exact_cols_bit_exact" in rep:
         assert rep["exact_cols_bit_exact"], rep
+
+
+# ---- compressed canonical store (PolyKV §2B) ---------------------------------------------------
+
+COMP_KEYS = ("k_codes", "k_scale", "v_codes", "v_norm", "row_offset", "len")
+
+
+def comp_arrays(cs) -> dict:
+    """Host arrays of a compressed store: from the oracle's encoder
+    (``oracle.Compressed``) or from ``Workload.random_compressed()``."""
+    if isinstance(cs, dict):
+        return {k: cs[k] for k in COMP_KEYS}
+    return {"k_codes": cs.k_codes, "k_scale": cs.k_scale, "v_codes": cs.v_codes, "v_norm": cs.v_norm,
+            "row_offset": cs.row_offset, "len": cs.len}
+
+
+def oracle_store(arrs: dict):
+    """The same host arrays as the oracle's store object (with the oracle's codebook)."""
+    import oracle
+
+    c32, _ = oracle.v_codebook()
+    return oracle.Compressed(arrs["k_codes"], arrs["k_scale"], arrs["v_codes"], arrs["v_norm"], arrs["row_offset"],
+                             arrs["len"], c32)
+
+
+def device_compressed(arrs: dict, torch, device="cuda"):
+    """(kamera_compressed_store, device tensors) for host arrays."""
+    t = {k: torch.from_numpy(np.ascontiguousarray(arrs[k])).to(device) for k in COMP_KEYS}
+    return pk.compressed_store(t["k_codes"], t["k_scale"], t["v_codes"], t["v_norm"], t["row_offset"], t["len"]), t
+
+
+def empty_compressed(wl: W.Workload, torch, device="cuda"):
+    """A device compressed store of the workload's row layout, to be filled by the encoder."""
+    rows, D, H, n = wl.comp_rows, wl.D, wl.num_kv_heads, wl.head_dim
+    t = {"k_codes": torch.zeros((rows, D), dtype=torch.int8, device=device),
+         "k_scale": torch.zeros((len(wl.chunk_lens), wl.num_layers), dtype=torch.float32, device=device),
+         "v_codes": torch.zeros((rows, H, 3 * n // 8), dtype=torch.uint8, device=device),
+         "v_norm": torch.zeros((rows, H), dtype=torch.float32, device=device),
+         "row_offset": torch.from_numpy(wl.comp_row_offset).to(device),
+         "len": torch.from_numpy(np.array(wl.chunk_lens, np.int32)).to(device)}
+    return pk.compressed_store(t["k_codes"], t["k_scale"], t["v_codes"], t["v_norm"], t["row_offset"], t["len"]), t
+
+
+def call_compressed(wl: W.Workload, t: dict, cstore, stream=None, raise_on_error=True) -> int:
+    return pk.call_compressed(model_for(wl, t), cstore, items=t["items"], pool_k=t["pool_k"], pool_v=t["pool_v"],
+                              block_table=t["block_table"], page_size=wl.page_size, patch=t.get("patch"),
+                              patch_off=t.get("patch_off"), patch_len=t.get("patch_len"),
+                              rank=wl.rank if "patch" in t else 0, err_flag=t["err"], stream=stream,
+                              raise_on_error=raise_on_error)
+
+
+def oracle_reference_compressed(wl: W.Workload, ocs, pool_k_in=None, pool_v_in=None):
+    """fp64 oracle of the reuse operator reading the compressed store ``ocs``."""
+    import oracle
+
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
+                     wl.pairing, wl.patch_frame, wl.rope_sections)
+    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    kw = {}
+    if wl.rank:
+        kw.update(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
+                  rank=wl.rank)
+    return oracle.reuse_compressed(m, th, ocs, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
+                                   page_size=wl.page_size,
+                                   pool_k_in=wl.host_pool(0) if pool_k_in is None else pool_k_in,
+                                   pool_v_in=wl.host_pool(1) if pool_v_in is None else pool_v_in,
+                                   section_deltas=wl.section_deltas, **kw)

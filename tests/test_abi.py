@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert pk.abi_version() == 2
+    assert pk.abi_version() == 3
     assert pk.status_string(pk.KAMERA_OK) == "KAMERA_OK"
     assert pk.status_string(pk.KAMERA_ERR_CUDA) == "KAMERA_ERR_CUDA"
     assert pk.status_string(99) == "KAMERA_ERR_UNKNOWN"
@@ -60,6 +60,8 @@ int main(void) {
   printf("%zu %zu %zu %zu %zu\n", offsetof(kamera_model_desc, rope_base), offsetof(kamera_reuse_item, delta),
          offsetof(kamera_reuse_item, dst_pos), offsetof(kamera_paged_pool, block_table),
          offsetof(kamera_model_desc, section_delta));
+  printf("%zu %zu %zu\n", sizeof(kamera_compressed_store), offsetof(kamera_compressed_store, n_chunks),
+         offsetof(kamera_compressed_store, n_rows));
   return 0;
 }
 ''')
@@ -74,6 +76,9 @@ int main(void) {
     assert offs == [pk.kamera_model_desc.rope_base.offset, pk.REUSE_ITEM.fields["delta"][1],
                     pk.REUSE_ITEM.fields["dst_pos"][1], pk.kamera_paged_pool.block_table.offset,
                     pk.kamera_model_desc.section_delta.offset]
+    comp = [int(x) for x in lines[2].split()]
+    assert comp == [ctypes.sizeof(pk.kamera_compressed_store), pk.kamera_compressed_store.n_chunks.offset,
+                    pk.kamera_compressed_store.n_rows.offset]
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -185,3 +190,61 @@ def test_orbit_mean_validation(lib):
     assert pk.kamera_orbit_mean(FAKE, 3, 100, 100, FAKE + 4, None, False) == pk.KAMERA_ERR_INVALID_ARG  # overlap
     assert pk.kamera_orbit_mean(FAKE + 2, 3, 100, 100, FAKE + (1 << 20), None, False) == pk.KAMERA_ERR_ALIGNMENT
     assert pk.kamera_orbit_mean(FAKE, 3, 100, 0, FAKE, None, False) == pk.KAMERA_OK
+
+
+# ---- compressed canonical store ---------------------------------------------------------------------
+
+def test_v_codebook_matches_the_oracle_bit_for_bit(lib):
+    """The library's Lloyd-Max solver and the oracle's are written separately;
+    the fp32 codebook and thresholds (part of the store format) must agree."""
+    import numpy as np
+
+    import oracle
+
+    c_lib, t_lib = pk.kamera_v_codebook()
+    c_or, t_or = oracle.v_codebook()
+    np.testing.assert_array_equal(c_lib.view(np.uint32), c_or.view(np.uint32))
+    np.testing.assert_array_equal(t_lib.view(np.uint32), t_or.view(np.uint32))
+
+
+def _cstore(**kw):
+    c = pk.kamera_compressed_store(FAKE, FAKE + 1024, FAKE + 4096, FAKE + 8192, FAKE + 16384, FAKE + 20480, 4, 0,
+                                   1 << 16)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _reuse_c(model, pool, cs=None, n=1):
+    return pk.kamera_reuse_compressed(model, cs if cs is not None else _cstore(), None, FAKE, n, pool, None, None,
+                                      raise_on_error=False)
+
+
+def test_compressed_validation(lib):
+    assert pk.kamera_reuse_compressed(_gqa_model(), None, None, FAKE, 1, _pool(), None, None,
+                                      False) == pk.KAMERA_ERR_NULL
+    assert _reuse_c(_gqa_model(), _pool(), _cstore(v_norm=None)) == pk.KAMERA_ERR_NULL
+    assert _reuse_c(_gqa_model(), _pool(), _cstore(k_codes=FAKE + 8)) == pk.KAMERA_ERR_ALIGNMENT
+    assert _reuse_c(_gqa_model(), _pool(), _cstore(row_offset=FAKE + 4)) == pk.KAMERA_ERR_ALIGNMENT
+    assert _reuse_c(_gqa_model(), _pool(), _cstore(reserved=1)) == pk.KAMERA_ERR_INVALID_ARG
+    assert _reuse_c(_gqa_model(), _pool(), _cstore(n_rows=1 << 31)) == pk.KAMERA_ERR_UNSUPPORTED
+    mla = pk.model_desc(pk.KAMERA_MLA, 2, rope_dim=64, latent_dim=512)
+    assert _reuse_c(mla, _pool(v=None)) == pk.KAMERA_ERR_UNSUPPORTED
+    assert _reuse_c(_gqa_model(head_dim=256), _pool()) == pk.KAMERA_ERR_UNSUPPORTED
+    assert _reuse_c(_gqa_model(head_dim=64, num_kv_heads=1), _pool()) == pk.KAMERA_ERR_UNSUPPORTED  # D = 64
+    assert _reuse_c(_gqa_model(), _pool(), n=0) == pk.KAMERA_OK
+
+
+def test_compress_chunks_validation(lib):
+    def run(model, src, dst):
+        return pk.kamera_compress_chunks(model, src, dst, None, None, raise_on_error=False)
+
+    assert run(None, _store(), _cstore()) == pk.KAMERA_ERR_NULL
+    mla = pk.model_desc(pk.KAMERA_MLA, 2, rope_dim=64, latent_dim=512)
+    assert run(mla, _store(), _cstore()) == pk.KAMERA_ERR_UNSUPPORTED
+    assert run(_gqa_model(head_dim=192), _store(), _cstore()) == pk.KAMERA_ERR_UNSUPPORTED
+    assert run(_gqa_model(), _store(), _cstore(n_chunks=3)) == pk.KAMERA_ERR_INVALID_ARG
+    assert run(_gqa_model(), _store(), _cstore(v_codes=None)) == pk.KAMERA_ERR_NULL
+    assert run(_gqa_model(), _store(), _cstore(v_codes=FAKE + 8)) == pk.KAMERA_ERR_ALIGNMENT
+    empty = pk.kamera_chunk_store(None, 0, None, None, 0)
+    assert run(_gqa_model(), empty, _cstore(n_chunks=0)) == pk.KAMERA_OK

@@ -1,0 +1,229 @@
+"""GPU parity of the compressed canonical store (PolyKV, gist.science
+summary, §2B: int8 K with one scale per tensor; 3-bit V by Walsh-Hadamard
+rotation and the Lloyd-Max centroids of N(0,1)).
+
+- The encoder (kamera_compress_chunks) against the oracle's encoder: bit for
+  bit on every byte and scale, since the format fixes each fp32 decision.
+- Reuse from a compressed store (kamera_reuse_compressed) against the oracle
+  (decode in fp64, then the Kamera §2 operator), element by element, with the
+  tolerance of the other parity tests: one bf16 ulp of the oracle value +
+  1e-3.  Inputs come from the oracle's encoder or are seeded random contents.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import workloads as W
+from tests import harness as H
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import position_invariant_kv_kamera_gb300 as pk
+
+    pk.load()
+    torch.cuda.set_device(0)
+
+
+def _oracle_model(wl):
+    return oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
+                        wl.pairing, wl.patch_frame, wl.rope_sections)
+
+
+def _oracle_encode(wl):
+    return oracle.compress_store(_oracle_model(wl), wl.host_store(), wl.store_off, np.array(wl.chunk_lens, np.int32),
+                                 row_offset=wl.comp_row_offset, n_rows=wl.comp_rows)
+
+
+def _gpu_encode(wl):
+    import position_invariant_kv_kamera_gb300 as pk
+
+    t = H.device_inputs(wl, torch)
+    cstore, ct = H.empty_compressed(wl, torch)
+    src = pk.chunk_store(t["store"], t["store_off"], t["store_len"])
+    pk.kamera_compress_chunks(H.model_for(wl), src, cstore, t["err"].data_ptr(), pk.stream_handle())
+    torch.cuda.synchronize()
+    return int(t["err"].item()), {k: v.cpu().numpy() for k, v in ct.items()}
+
+
+# ---- the encoder -----------------------------------------------------------------------------------------
+
+ENCODE_CASES = {
+    "gqa128_ragged": lambda: W.gqa_video(num_layers=2, n_chunks=3, T=70, rank=0).replace(chunk_lens=[70, 129, 1]),
+    "gqa128_outliers": lambda: W.gqa_video(num_layers=3, n_chunks=2, T=300, rank=0),
+    "mha64": lambda: W.tiny_mha(),
+    "zero_chunk": lambda: W.gqa_video(num_layers=1, n_chunks=2, T=40, rank=0).replace(sigma_kv=0.0,
+                                                                                      outlier_permille=0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(ENCODE_CASES))
+def test_encoder_matches_oracle_bit_for_bit(case):
+    wl = ENCODE_CASES[case]()
+    err, got = _gpu_encode(wl)
+    assert err == 0
+    ref = H.comp_arrays(_oracle_encode(wl))
+    for k in ("k_scale", "v_norm"):
+        np.testing.assert_array_equal(got[k].view(np.uint32), ref[k].view(np.uint32), err_msg=k)
+    for k in ("k_codes", "v_codes"):
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+    if case == "zero_chunk":
+        assert not got["k_codes"].any() and not got["v_codes"].any() and not got["v_norm"].any()
+
+
+def test_encoder_skips_bad_chunks_with_error_bits():
+    import position_invariant_kv_kamera_gb300 as pk
+
+    wl = W.gqa_video(num_layers=2, n_chunks=3, T=64, rank=0)
+    t = H.device_inputs(wl, torch)
+    cstore, ct = H.empty_compressed(wl, torch)
+    ct["len"][1] = 63  # length mismatch for chunk 1
+    ct["row_offset"][2] = wl.comp_rows - 10  # chunk 2 runs past the store
+    src = pk.chunk_store(t["store"], t["store_off"], t["store_len"])
+    pk.kamera_compress_chunks(H.model_for(wl), src, cstore, t["err"].data_ptr(), pk.stream_handle())
+    torch.cuda.synchronize()
+    assert int(t["err"].item()) == (8 | 1)
+    ref = H.comp_arrays(_oracle_encode(wl))
+    rows0 = wl.num_layers * 64  # chunk 0 is still encoded
+    np.testing.assert_array_equal(ct["k_codes"][:rows0].cpu().numpy(), ref["k_codes"][:rows0])
+    np.testing.assert_array_equal(ct["v_codes"][:rows0].cpu().numpy(), ref["v_codes"][:rows0])
+    assert not ct["k_codes"][rows0:2 * rows0].cpu().numpy().any()  # chunk 1 skipped
+
+
+# ---- reuse from the compressed store ---------------------------------------------------------------------
+
+def run_compressed(wl, arrs):
+    cstore, _ct = H.device_compressed(arrs, torch)
+    t = H.device_inputs(wl, torch, with_store=False)
+    H.call_compressed(wl, t, cstore)
+    torch.cuda.synchronize()
+    err, ref_k, ref_v, wk, wv = H.oracle_reference_compressed(wl, H.oracle_store(arrs))
+    assert int(t["err"].item()) == err
+    rep_k = H.compare_pool(H.to_bits(t["pool_k"]), wl.host_pool(0), ref_k, wk)
+    rep_v = H.compare_pool(H.to_bits(t["pool_v"]), wl.host_pool(1), ref_v, wv)
+    H.assert_report(rep_k)
+    H.assert_report(rep_v)
+    return rep_k, rep_v, t
+
+
+def _shifted(wl, page_size):
+    """Chunks that start mid-page and leave gaps (row blocks with ragged heads and tails)."""
+    n = len(wl.items)
+    T = int(wl.items["n_tokens"][0])
+    wl.items["dst_pos"] = 5 + np.arange(n) * (T + 37)
+    end = int(wl.items["dst_pos"][-1]) + T
+    wl.block_table = W.shuffled_block_table(wl.seed, 1, -(-end // page_size))
+    wl.num_pages = wl.block_table.shape[1]
+    return wl
+
+
+def _contents(wl, how):
+    return H.comp_arrays(_oracle_encode(wl) if how == "encoded" else wl.random_compressed())
+
+
+@pytest.mark.parametrize("how", ["encoded", "random"])
+@pytest.mark.parametrize("rank", [0, 8, 16, 32, 64])
+def test_gqa_ranks(rank, how):
+    wl = _shifted(W.gqa_video(num_layers=2, n_chunks=3, T=200, rank=rank, page_size=16), 16)
+    run_compressed(wl, _contents(wl, how))
+
+
+@pytest.mark.parametrize("page_size", [8, 64, 256])
+def test_page_sizes(page_size):
+    wl = _shifted(W.gqa_video(num_layers=2, n_chunks=2, T=300, rank=16, page_size=page_size), page_size)
+    run_compressed(wl, _contents(wl, "encoded"))
+
+
+@pytest.mark.parametrize("T", [1, 63, 127, 129, 1296])
+def test_ragged_chunk_lengths(T):
+    wl = W.gqa_video(num_layers=1, n_chunks=2, T=T, rank=16, page_size=64)
+    run_compressed(wl, _contents(wl, "random"))
+
+
+def test_mha_head_dim_64():
+    wl = W.tiny_mha()
+    rep_k, _, _ = run_compressed(wl, _contents(wl, "encoded"))
+    assert rep_k["rows_written"] == 256
+
+
+def test_mha_head_dim_64_eight_heads_random():
+    wl = W.tiny_mha().replace(num_kv_heads=8, rank=0, patch_lens=[])
+    wl.items["patch_id"] = -1
+    run_compressed(wl, _contents(wl, "random"))
+
+
+@pytest.mark.parametrize("pairing", [W.ROTATE_HALF, W.INTERLEAVED])
+@pytest.mark.parametrize("frame", [W.AFTER_ROTATION, W.CANONICAL_FRAME])
+def test_pairing_and_frame(pairing, frame):
+    wl = W.gqa_video(num_layers=2, n_chunks=2, T=150, rank=16, page_size=64).replace(pairing=pairing,
+                                                                                    patch_frame=frame)
+    run_compressed(wl, _contents(wl, "encoded"))
+
+
+def test_partial_rotary():
+    wl = W.gqa_video(num_layers=2, n_chunks=2, T=150, rank=8, page_size=64).replace(rope_dim=64)
+    run_compressed(wl, _contents(wl, "random"))
+
+
+def test_mrope_sections():
+    wl = W.with_mrope(W.gqa_video(num_layers=2, n_chunks=2, T=150, rank=16, page_size=64))
+    run_compressed(wl, _contents(wl, "encoded"))
+
+
+def test_eight_heads_long_video_shape_small():
+    wl = W.long_video(num_layers=1, n_reorder=3, n_recall=1, T=300, rank=64, num_kv_heads=8)
+    run_compressed(wl, _contents(wl, "random"))
+
+
+def test_error_bits_and_skips():
+    wl = W.gqa_video(num_layers=2, n_chunks=4, T=64, rank=8, page_size=16)
+    arrs = _contents(wl, "random")
+    wl.items["chunk_id"][1] = 9          # chunk out of range
+    wl.items["n_tokens"][2] = 63         # length mismatch
+    arrs["row_offset"] = arrs["row_offset"].copy()
+    arrs["row_offset"][3] = wl.comp_rows - 5  # rows past the store
+    _, _, t = run_compressed(wl, arrs)
+    assert int(t["err"].item()) == (1 | 8)
+
+
+def test_gpu_encoder_then_gpu_reuse():
+    """The whole compressed path on the GPU: encode the bf16 store, then reuse
+    from it; the oracle encodes and decodes on its own (the two encoders agree
+    bit for bit, as tested above)."""
+    import position_invariant_kv_kamera_gb300 as pk
+
+    wl = _shifted(W.gqa_video(num_layers=2, n_chunks=3, T=200, rank=32, page_size=64), 64)
+    t = H.device_inputs(wl, torch)
+    cstore, _ct = H.empty_compressed(wl, torch)
+    pk.kamera_compress_chunks(H.model_for(wl), pk.chunk_store(t["store"], t["store_off"], t["store_len"]), cstore,
+                              t["err"].data_ptr(), pk.stream_handle())
+    H.call_compressed(wl, t, cstore)
+    torch.cuda.synchronize()
+    assert int(t["err"].item()) == 0
+    err, ref_k, ref_v, wk, wv = H.oracle_reference_compressed(wl, _oracle_encode(wl))
+    H.assert_report(H.compare_pool(H.to_bits(t["pool_k"]), wl.host_pool(0), ref_k, wk))
+    H.assert_report(H.compare_pool(H.to_bits(t["pool_v"]), wl.host_pool(1), ref_v, wv))
+
+
+def test_decoded_values_stay_close_to_the_bf16_reuse():
+    """Sanity of the scheme end to end: reuse from the compressed store and
+    from the bf16 store of the same chunks differ by the quantisation error
+    only (K within half an int8 step per element; V within a few times the
+    Lloyd-Max distortion of the row's energy)."""
+    wl = W.gqa_video(num_layers=1, n_chunks=2, T=256, rank=0, page_size=64)
+    arrs = _contents(wl, "encoded")
+    _, _, t_c = run_compressed(wl, arrs)
+    t_b = H.device_inputs(wl, torch)
+    H.call(wl, t_b)
+    torch.cuda.synchronize()
+    for ch in ("pool_k", "pool_v"):
+        a = H.bits_to_f64(H.to_bits(t_c[ch])).reshape(-1, wl.D)
+        b = H.bits_to_f64(H.to_bits(t_b[ch])).reshape(-1, wl.D)
+        rows = ~np.isnan(b).any(axis=1)
+        rel = np.sum((a[rows] - b[rows]) ** 2) / np.sum(b[rows] ** 2)
+        assert rel < (1e-3 if ch == "pool_k" else 0.06), (ch, rel)

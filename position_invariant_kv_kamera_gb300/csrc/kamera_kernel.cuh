@@ -275,7 +275,7 @@ struct Smem {
   uint64_t* tempty;    // [2] accumulator drained
   uint64_t* drain;     // [1]
   SmemMisc* misc;
-  float2* cs;        // [2][n_pairs_pad] (cos, sin) tables, one per row-block parity
+  float2* cs;        // [2][n_pairs_pad] phase tables, one per row-block parity: per two pairs (c, c', s, s')
 };
 
 __device__ __forceinline__ Smem carve_smem(uint8_t* raw, const Params& p) {
@@ -327,24 +327,9 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Sme
 
 // ---- epilogue helpers ----------------------------------------------------------------------
 
-__device__ __forceinline__ void unpack8(uint4 v, float* f) {
-  f[0] = __uint_as_float(v.x << 16);
-  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
-  f[2] = __uint_as_float(v.y << 16);
-  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
-  f[4] = __uint_as_float(v.z << 16);
-  f[5] = __uint_as_float(v.z & 0xFFFF0000u);
-  f[6] = __uint_as_float(v.w << 16);
-  f[7] = __uint_as_float(v.w & 0xFFFF0000u);
-}
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint4 pack8(const float* f) {
-  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
 // cos/sin of delta*theta_i: the angle is formed and reduced modulo 2*pi in fp64
@@ -382,32 +367,52 @@ __device__ __forceinline__ void put16(uint32_t a0, uint32_t a1, uint4 v0, uint4 
   }
 }
 
-// int8 codes -> fp32: a byte permute builds the float 2^23 + (q + 128), the
-// subtraction of 2^23 + 128 is exact, and the product with the scale is the
-// one rounding (the same value as (float)q * scale).
-__device__ __forceinline__ void dequant16(uint4 v, float scale, float* x) {
+// int8 codes -> fp32 pairs: a byte permute builds the float 2^23 + (q + 128),
+// the subtraction of 2^23 + 128 is exact, and the product with the scale is
+// the one rounding (the same value as (float)q * scale).
+__device__ __forceinline__ void dequant16(uint4 v, float scale, float2* x) {
   const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+  const float2 bias = make_float2(8388736.0f, 8388736.0f), sc = make_float2(scale, scale);
 #pragma unroll
   for (int k = 0; k < 4; ++k)
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-      x[4 * k + b] = (__uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7540u | (uint32_t)b)) - 8388736.0f) * scale;
+    for (int b = 0; b < 4; b += 2) {
+      const float2 f = make_float2(__uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7540u | (uint32_t)b)),
+                                   __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7540u | (uint32_t)(b + 1))));
+      x[2 * k + b / 2] = mul_f2(sub_f2(f, bias), sc);
+    }
 }
 
-// Canonical values of this thread's row, 16 columns at a time.
+__device__ __forceinline__ void unpack8_f2(uint4 v, float2* x) {
+  x[0] = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
+  x[1] = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  x[2] = make_float2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
+  x[3] = make_float2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint4 pack8_f2(const float2* x) {
+  return make_uint4(pack2(x[0].x, x[0].y), pack2(x[1].x, x[1].y), pack2(x[2].x, x[2].y), pack2(x[3].x, x[3].y));
+}
+
+__device__ __forceinline__ float2 acc_f2(const uint32_t* acc, int e) {
+  return make_float2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
+}
+
+// Canonical values of this thread's row, 16 columns at a time, as 8 pairs of
+// neighbouring columns.
 struct SrcTile {  // the bf16 tile itself (TMA-loaded canonical rows)
   RowView rv;
-  __device__ __forceinline__ void load16(int c, float* x) const {
+  __device__ __forceinline__ void load16(int c, float2* x) const {
     const uint4 v0 = lds128(rv.chunk(c)), v1 = lds128(rv.chunk(c + 8));
-    unpack8(v0, x);
-    unpack8(v1, x + 8);
+    unpack8_f2(v0, x);
+    unpack8_f2(v1, x + 4);
   }
 };
 struct SrcK8 {  // int8 K codes: 128-column boxes, 128B swizzle, one scale per (chunk, layer)
   uint32_t base;  // staging + row * 128
   uint32_t sw;    // row & 7
   float scale;
-  __device__ __forceinline__ void load16(int c, float* x) const {
+  __device__ __forceinline__ void load16(int c, float2* x) const {
     dequant16(lds128(base + (uint32_t)(c >> 7) * BOX_BYTES + ((((uint32_t)c >> 4) & 7u) ^ sw) * 16u), scale, x);
   }
 };
@@ -428,17 +433,18 @@ __device__ __forceinline__ void epi_plain16(const Src& src, const RowView& rv, i
   }
   uint32_t acc[16];
   if (kPatched) tmem_ld16(taddr + (uint32_t)c0, acc);
-  float x[16];
+  float2 x[8];
   src.load16(c0, x);
   if (kPatched) {
     tmem_ld_wait();
 #pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(acc[e]);
+    for (int e = 0; e < 8; ++e) x[e] = add_f2(x[e], acc_f2(acc, e));
   }
-  put16(a0, a1, pack8(x), pack8(x + 8), gdst, c0);
+  put16(a0, a1, pack8_f2(x), pack8_f2(x + 4), gdst, c0);
 }
 
-// 16 rotate-half pairs (cA + e, cB + e), pair index pb + e.
+// 16 rotate-half pairs (cA + e, cB + e), pair index pb + e, two pairs per
+// paired operation:  a' = a cos - b sin,  b' = b cos + a sin.
 template <bool kPatched, bool kCanonicalFrame, class Src>
 __device__ __forceinline__ void epi_rotate16(const Src& src, const RowView& rv, int cA, int cB, int pb,
                                              uint32_t taddr, const float2* cs, uint16_t* gdst) {
@@ -447,35 +453,31 @@ __device__ __forceinline__ void epi_rotate16(const Src& src, const RowView& rv, 
     tmem_ld16(taddr + (uint32_t)cA, accA);
     tmem_ld16(taddr + (uint32_t)cB, accB);
   }
-  float xa[16], xb[16];
+  float2 xa[8], xb[8];
   src.load16(cA, xa);
   src.load16(cB, xb);
   if (kPatched) tmem_ld_wait();
   const float4* cs4 = reinterpret_cast<const float4*>(cs + pb);
 #pragma unroll
-  for (int e2 = 0; e2 < 8; ++e2) {
-    const float4 t = cs4[e2];  // (cos, sin) of pairs pb + 2*e2 and pb + 2*e2 + 1
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = 2 * e2 + h;
-      const float c = h ? t.z : t.x, s = h ? t.w : t.y;
-      float a = xa[e], b = xb[e];
-      if (kPatched && kCanonicalFrame) {
-        a += __uint_as_float(accA[e]);
-        b += __uint_as_float(accB[e]);
-      }
-      float ra = fmaf(a, c, -b * s);
-      float rb = fmaf(b, c, a * s);
-      if (kPatched && !kCanonicalFrame) {
-        ra += __uint_as_float(accA[e]);
-        rb += __uint_as_float(accB[e]);
-      }
-      xa[e] = ra;
-      xb[e] = rb;
+  for (int e = 0; e < 8; ++e) {
+    const float4 t = cs4[e];  // (cos, cos', sin, sin') of pairs pb + 2e and pb + 2e + 1
+    const float2 c = make_float2(t.x, t.y), sn = make_float2(t.z, t.w);
+    float2 a = xa[e], b = xb[e];
+    if (kPatched && kCanonicalFrame) {
+      a = add_f2(a, acc_f2(accA, e));
+      b = add_f2(b, acc_f2(accB, e));
     }
+    float2 ra = sub_f2(mul_f2(a, c), mul_f2(b, sn));
+    float2 rb = fma_f2(a, sn, mul_f2(b, c));
+    if (kPatched && !kCanonicalFrame) {
+      ra = add_f2(ra, acc_f2(accA, e));
+      rb = add_f2(rb, acc_f2(accB, e));
+    }
+    xa[e] = ra;
+    xb[e] = rb;
   }
-  put16(rv.chunk(cA), rv.chunk(cA + 8), pack8(xa), pack8(xa + 8), gdst, cA);
-  put16(rv.chunk(cB), rv.chunk(cB + 8), pack8(xb), pack8(xb + 8), gdst, cB);
+  put16(rv.chunk(cA), rv.chunk(cA + 8), pack8_f2(xa), pack8_f2(xa + 4), gdst, cA);
+  put16(rv.chunk(cB), rv.chunk(cB + 8), pack8_f2(xb), pack8_f2(xb + 4), gdst, cB);
 }
 
 // 8 interleaved pairs (2e, 2e+1) in 16 columns, pair index pb + e.
@@ -484,18 +486,18 @@ __device__ __forceinline__ void epi_interleaved16(const Src& src, const RowView&
                                                   const float2* cs, uint16_t* gdst) {
   uint32_t acc[16];
   if (kPatched) tmem_ld16(taddr + (uint32_t)c0, acc);
-  float x[16];
+  float2 x[8];  // x[e] = (a, b) of pair pb + e
   src.load16(c0, x);
   if (kPatched) tmem_ld_wait();
   const float4* cs4 = reinterpret_cast<const float4*>(cs + pb);
 #pragma unroll
   for (int e2 = 0; e2 < 4; ++e2) {
-    const float4 t = cs4[e2];
+    const float4 t = cs4[e2];  // (cos, cos', sin, sin') of pairs pb + 2*e2 and pb + 2*e2 + 1
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int e = 2 * e2 + h;
-      const float c = h ? t.z : t.x, s = h ? t.w : t.y;
-      float a = x[2 * e], b = x[2 * e + 1];
+      const float c = h ? t.y : t.x, s = h ? t.w : t.z;
+      float a = x[e].x, b = x[e].y;
       if (kPatched && kCanonicalFrame) {
         a += __uint_as_float(acc[2 * e]);
         b += __uint_as_float(acc[2 * e + 1]);
@@ -506,11 +508,10 @@ __device__ __forceinline__ void epi_interleaved16(const Src& src, const RowView&
         ra += __uint_as_float(acc[2 * e]);
         rb += __uint_as_float(acc[2 * e + 1]);
       }
-      x[2 * e] = ra;
-      x[2 * e + 1] = rb;
+      x[e] = make_float2(ra, rb);
     }
   }
-  put16(rv.chunk(c0), rv.chunk(c0 + 8), pack8(x), pack8(x + 8), gdst, c0);
+  put16(rv.chunk(c0), rv.chunk(c0 + 8), pack8_f2(x), pack8_f2(x + 4), gdst, c0);
 }
 
 // One tile row's share of the compute phase for epilogue half h.  gdst: the
@@ -547,18 +548,22 @@ __device__ __forceinline__ void epi_row(const Params& p, const Src& src, const R
 
 // ---- compressed V: Walsh-Hadamard decode ----------------------------------------------------
 
-// In-place unnormalised Walsh-Hadamard transform of N values (Sylvester order).
+// In-place unnormalised Walsh-Hadamard transform of N values (Sylvester
+// order) held as N/2 pairs v[k] = (u[2k], u[2k+1]): the stride-1 butterflies
+// inside each pair, then every wider stride on whole pairs with paired adds.
 template <int N>
-__device__ __forceinline__ void fwht(float* u) {
+__device__ __forceinline__ void fwht_pairs(float2* v) {
 #pragma unroll
-  for (int h = 1; h < N; h <<= 1)
+  for (int k = 0; k < N / 2; ++k) v[k] = make_float2(v[k].x + v[k].y, v[k].x - v[k].y);
 #pragma unroll
-    for (int i = 0; i < N; i += 2 * h)
+  for (int h = 1; h < N / 2; h <<= 1)
 #pragma unroll
-      for (int j = i; j < i + h; ++j) {
-        const float a = u[j], b = u[j + h];
-        u[j] = a + b;
-        u[j + h] = a - b;
+    for (int i = 0; i < N / 2; i += 2 * h)
+#pragma unroll
+      for (int k = i; k < i + h; ++k) {
+        const float2 a = v[k], b = v[k + h];
+        v[k] = add_f2(a, b);
+        v[k + h] = sub_f2(a, b);
       }
 }
 
@@ -579,9 +584,10 @@ __host__ __device__ constexpr uint32_t upper_field_mask(int word) {
 //   codes: shared address of the head's packed codes (3*HD/8 bytes)
 //   scale: ||v|| / HD;   c_out: tile column of output i = 0
 //   tab_lane: shared address of the pair table + 4 * lane
-template <int HD, bool kPatched>
+//   patched: add the patch accumulator (warp-uniform)
+template <int HD>
 __device__ __forceinline__ void epi_vhalf(const RowView& rv, uint32_t codes, float scale, int h, int c_out,
-                                          uint32_t taddr, uint32_t tab_lane, uint16_t* gdst) {
+                                          uint32_t taddr, uint32_t tab_lane, uint16_t* gdst, bool patched) {
   constexpr int NW = 3 * HD / 32;  // 32-bit code words per head row
   constexpr int NF = HD / 2;       // fields = outputs of this half
   uint32_t w[NW];
@@ -606,7 +612,7 @@ __device__ __forceinline__ void epi_vhalf(const RowView& rv, uint32_t codes, flo
 #pragma unroll
     for (int k = 0; k < NW; ++k) w[k] ^= upper_field_mask(k);
   }
-  float u[NF];
+  float2 v[NF / 2];
 #pragma unroll
   for (int i = 0; i < NF; ++i) {
     const int bit = 6 * i, wi = bit >> 5, o = bit & 31;
@@ -616,23 +622,33 @@ __device__ __forceinline__ void epi_vhalf(const RowView& rv, uint32_t codes, flo
       f = o >= 7 ? (w[wi] >> (o - 7)) : (w[wi] << (7 - o));
     else
       f = __funnelshift_r(w[wi], w[wi + 1], o - 7);
-    u[i] = lds_f32_const(tab_lane + (f & (63u << 7)));
+    const float x = lds_f32_const(tab_lane + (f & (63u << 7)));
+    if (i & 1)
+      v[i >> 1].y = x;
+    else
+      v[i >> 1].x = x;
   }
-  fwht<NF>(u);
+  fwht_pairs<NF>(v);
+  const float2 sc = make_float2(scale, scale);
 #pragma unroll
   for (int g = 0; g < NF; g += 16) {
-    float x[16];
-    if (kPatched) {
+    float2 x[8];
+    if (patched) {
       uint32_t acc[16];
       tmem_ld16(taddr + (uint32_t)(c_out + g), acc);
       tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = fmaf(u[g + e], scale, __uint_as_float(acc[e]));
+      for (int e = 0; e < 8; ++e)
+        x[e] = fma_f2(v[g / 2 + e], sc, make_float2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1])));
     } else {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = u[g + e] * scale;
+      for (int e = 0; e < 8; ++e) x[e] = mul_f2(v[g / 2 + e], sc);
     }
-    put16(rv.chunk(c_out + g), rv.chunk(c_out + g + 8), pack8(x), pack8(x + 8), gdst, c_out + g);
+    const uint4 o0 = make_uint4(pack2(x[0].x, x[0].y), pack2(x[1].x, x[1].y), pack2(x[2].x, x[2].y),
+                                pack2(x[3].x, x[3].y));
+    const uint4 o1 = make_uint4(pack2(x[4].x, x[4].y), pack2(x[5].x, x[5].y), pack2(x[6].x, x[6].y),
+                                pack2(x[7].x, x[7].y));
+    put16(rv.chunk(c_out + g), rv.chunk(c_out + g + 8), o0, o1, gdst, c_out + g);
   }
 }
 
@@ -960,9 +976,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       // phase tables alternate by row-block parity: their previous readers
       // finished before the last joint barrier
       float2* cs = sm.cs + (rbi & 1u) * pairs_pad(p.n_pairs);
-      if (h == 1 && rot && w.item != table_item[rbi & 1u])
-        for (int i = et - 128; i < p.n_pairs; i += 128)
-          cs[i] = phase_cs(i < p.sec_end0 ? w.d0 : (i < p.sec_end1 ? w.d1 : w.d2), p.theta[i]);
+      if (h == 1 && rot && w.item != table_item[rbi & 1u]) {
+        float* csf = reinterpret_cast<float*>(cs);
+        for (int i = et - 128; i < p.n_pairs; i += 128) {
+          const float2 v = phase_cs(i < p.sec_end0 ? w.d0 : (i < p.sec_end1 ? w.d1 : w.d2), p.theta[i]);
+          csf[4 * (i >> 1) + (i & 1)] = v.x;
+          csf[4 * (i >> 1) + 2 + (i & 1)] = v.y;
+        }
+      }
       if (rot) table_item[rbi & 1u] = w.item;
       if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the table is ready
 
@@ -991,23 +1012,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           if (kComp && t.ch == 1) {
             const uint32_t stg = smem_addr(sm.stages + (size_t)s * p.stage_bytes) + p.out_bytes;
             const uint32_t tab = smem_addr(sm.table) + 4u * (uint32_t)lane;
-            const int hpt = p.BN / p.head_dim;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (j >= hpt) break;
-              if (p.head_dim == 128) {
-                const uint32_t codes = stg + (uint32_t)r * (3u * p.BN / 8u) + (uint32_t)j * 48u;
-                if (patched)
-                  epi_vhalf<128, true>(rv, codes, nrm[j] * (1.0f / 128), h, j * 128 + h * 64, taddr, tab, gdst);
-                else
-                  epi_vhalf<128, false>(rv, codes, nrm[j] * (1.0f / 128), h, j * 128 + h * 64, taddr, tab, gdst);
-              } else {
-                const uint32_t codes = stg + (uint32_t)r * (3u * p.BN / 8u) + (uint32_t)j * 24u;
-                if (patched)
-                  epi_vhalf<64, true>(rv, codes, nrm[j] * (1.0f / 64), h, j * 64 + h * 32, taddr, tab, gdst);
-                else
-                  epi_vhalf<64, false>(rv, codes, nrm[j] * (1.0f / 64), h, j * 64 + h * 32, taddr, tab, gdst);
-              }
+            const int hd = p.head_dim, hpt = p.BN / hd;
+            const uint32_t row_codes = stg + (uint32_t)r * (3u * p.BN / 8u);
+#pragma unroll 1
+            for (int j = 0; j < hpt; ++j) {
+              const float n = j == 0 ? nrm[0] : (j == 1 ? nrm[1] : (j == 2 ? nrm[2] : nrm[3]));
+              const uint32_t codes = row_codes + (uint32_t)(j * 3 * hd / 8);
+              if (hd == 128)
+                epi_vhalf<128>(rv, codes, n * (1.0f / 128), h, j * 128 + h * 64, taddr, tab, gdst, patched);
+              else
+                epi_vhalf<64>(rv, codes, n * (1.0f / 64), h, j * 64 + h * 32, taddr, tab, gdst, patched);
             }
           } else if (kComp) {
             const uint32_t stg = smem_addr(sm.stages + (size_t)s * p.stage_bytes) + p.out_bytes;

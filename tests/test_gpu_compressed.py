@@ -213,8 +213,10 @@ def test_gpu_encoder_then_gpu_reuse():
 def test_decoded_values_stay_close_to_the_bf16_reuse():
     """Sanity of the scheme end to end: reuse from the compressed store and
     from the bf16 store of the same chunks differ by the quantisation error
-    only (K within half an int8 step per element; V within a few times the
-    Lloyd-Max distortion of the row's energy)."""
+    only.  K: with 1 % outlier channels x8 the per-tensor step is about
+    max|x|/127 = 0.25 sigma, an error of step^2/12 against a mean square of
+    1.6 sigma^2, about 0.3 %; V: the Lloyd-Max distortion 3.5 % of the row's
+    energy."""
     wl = W.gqa_video(num_layers=1, n_chunks=2, T=256, rank=0, page_size=64)
     arrs = _contents(wl, "encoded")
     _, _, t_c = run_compressed(wl, arrs)
@@ -226,4 +228,4 @@ def test_decoded_values_stay_close_to_the_bf16_reuse():
         b = H.bits_to_f64(H.to_bits(t_b[ch])).reshape(-1, wl.D)
         rows = ~np.isnan(b).any(axis=1)
         rel = np.sum((a[rows] - b[rows]) ** 2) / np.sum(b[rows] ** 2)
-        assert rel < (1e-3 if ch == "pool_k" else 0.06), (ch, rel)
+        assert rel < (0.01 if ch == "pool_k" else 0.06), (ch, rel)

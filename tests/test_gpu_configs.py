@@ -73,3 +73,37 @@ def test_all_launch_configurations_agree_bitwise(name):
     H.assert_report(H.compare_pool(base[1], pool[0], ref_k, wk))
     if wl.n_ch == 2:
         H.assert_report(H.compare_pool(base[2], pool[1], ref_v, wv))
+
+
+COMPRESSED = {
+    "gqa_r32_compressed": lambda: W.gqa_video(num_layers=2, n_chunks=3, T=300, rank=32, page_size=16),
+    "mha64_r8_compressed": lambda: W.gqa_video(num_layers=2, n_chunks=2, T=200, rank=8,
+                                               page_size=64).replace(num_kv_heads=8, head_dim=64, rope_dim=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(COMPRESSED))
+def test_compressed_launch_configurations_agree_bitwise(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    wl = COMPRESSED[name]()
+    arrs = H.comp_arrays(wl.random_compressed())
+    results = []
+    for cfg in CONFIGS:
+        for k in KEYS:
+            os.environ.pop(k, None)
+        os.environ.update(cfg)
+        cstore, _ct = H.device_compressed(arrs, torch)
+        t = H.device_inputs(wl, torch, with_store=False)
+        if H.call_compressed(wl, t, cstore, raise_on_error=False) != 0:
+            continue  # a forced shape the compressed path does not serve (BN 64)
+        torch.cuda.synchronize()
+        assert int(t["err"].item()) == 0, cfg
+        results.append((cfg, H.to_bits(t["pool_k"]), H.to_bits(t["pool_v"])))
+    assert len(results) >= 3
+    for cfg, k, v in results[1:]:
+        np.testing.assert_array_equal(k, results[0][1], err_msg=str(cfg))
+        np.testing.assert_array_equal(v, results[0][2], err_msg=str(cfg))
+    err, ref_k, ref_v, wk, wv = H.oracle_reference_compressed(wl, H.oracle_store(arrs))
+    H.assert_report(H.compare_pool(results[0][1], wl.host_pool(0), ref_k, wk))
+    H.assert_report(H.compare_pool(results[0][2], wl.host_pool(1), ref_v, wv))

@@ -175,3 +175,33 @@ def test_full_long_video():
     _check_samples(wl, t)
     del t
     torch.cuda.empty_cache()
+
+
+def test_full_gqa_video_compressed():
+    """The headline batch reused from a compressed store at full size (458,752
+    store rows, 0.33 GB of codes) in the bench's launch configuration, with
+    seeded random contents; sampled rows are decoded and recomputed by the
+    oracle one by one."""
+    wl = W.gqa_video()
+    arrs = H.comp_arrays(wl.random_compressed())
+    cstore, _ct = H.device_compressed(arrs, torch)
+    t = H.device_inputs(wl, torch, with_store=False)
+    H.call_compressed(wl, t, cstore)
+    torch.cuda.synchronize()
+    assert int(t["err"].item()) == 0
+    _check_sentinel_coverage(wl, t["pool_k"])
+    _check_sentinel_coverage(wl, t["pool_v"])
+    m = _oracle_model(wl)
+    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    ocs = H.oracle_store(arrs)
+    rng = np.random.default_rng(11)
+    for (i, layer, ch, tok) in _samples(wl, rng):
+        it = wl.items[i]
+        page, slot = _slot_rows(wl, it, tok)
+        src = oracle.decode_row(m, ocs, int(it["chunk_id"]), layer, ch, tok)
+        u = H.bits_to_f64(wl.u_rows(int(it["patch_id"]), layer, ch, tok, tok + 1)[0])
+        v = H.bits_to_f64(wl.v_rows(int(it["patch_id"]), layer, ch))
+        ref = oracle.row(m, th, ch, int(it["delta"]), src, u, v)
+        got = H.to_bits((t["pool_k"] if ch == 0 else t["pool_v"])[layer, page, slot])
+        ok = H.within_tol(H.bits_to_f64(got), ref)
+        assert ok.all(), (i, layer, ch, tok, np.abs(H.bits_to_f64(got) - ref).max())

@@ -20,15 +20,19 @@ def _cuda():
     torch.cuda.set_device(0)
 
 
-def random_workload(seed: int) -> W.Workload:
+def random_workload(seed: int, compressed: bool = False) -> W.Workload:
+    """compressed: shapes the compressed store serves (MHA/GQA, head_dim 64 or
+    128, D a multiple of 128)."""
     rng = np.random.default_rng(seed)
-    family = int(rng.choice([W.MHA, W.GQA, W.MLA]))
+    family = int(rng.choice([W.MHA, W.GQA] if compressed else [W.MHA, W.GQA, W.MLA]))
     kw = {}
     if family == W.MLA:
         kw.update(latent_dim=int(rng.choice([128, 256, 512])), rope_dim=64)
     else:
-        hd = int(rng.choice([64, 128, 256]))
+        hd = int(rng.choice([64, 128] if compressed else [64, 128, 256]))
         heads = int(rng.integers(1, max(2, min(5, 1024 // hd + 1))))
+        if compressed and hd == 64 and heads % 2:
+            heads += 1
         rope = hd if rng.random() < 0.7 or hd == 64 else 64
         kw.update(num_kv_heads=heads, head_dim=hd, rope_dim=rope)
     L = int(rng.integers(1, 4))
@@ -103,3 +107,27 @@ def test_fuzz_in_place_modes(seed):
     H.assert_report(H.compare_pool(H.to_bits(t["pool_k"]), pool[0], ref_k, wk, exact))
     if wl.n_ch == 2:
         H.assert_report(H.compare_pool(H.to_bits(t["pool_v"]), pool[1], ref_v, wv))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_compressed_store(seed):
+    """kamera_reuse_compressed on random shapes; the store is the oracle's
+    encoding of the bf16 store (even seeds) or seeded random contents (odd)."""
+    import oracle
+
+    wl = random_workload(3000 + seed, compressed=True)
+    if seed % 2 == 0:
+        m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim)
+        arrs = H.comp_arrays(oracle.compress_store(m, wl.host_store(), wl.store_off,
+                                                   np.array(wl.chunk_lens, np.int32),
+                                                   row_offset=wl.comp_row_offset, n_rows=wl.comp_rows))
+    else:
+        arrs = H.comp_arrays(wl.random_compressed())
+    cstore, _ct = H.device_compressed(arrs, torch)
+    t = H.device_inputs(wl, torch, with_store=False)
+    H.call_compressed(wl, t, cstore)
+    torch.cuda.synchronize()
+    err, ref_k, ref_v, wk, wv = H.oracle_reference_compressed(wl, H.oracle_store(arrs))
+    assert int(t["err"].item()) == err
+    H.assert_report(H.compare_pool(H.to_bits(t["pool_k"]), wl.host_pool(0), ref_k, wk))
+    H.assert_report(H.compare_pool(H.to_bits(t["pool_v"]), wl.host_pool(1), ref_v, wv))

@@ -60,17 +60,38 @@ struct FParams {
 // tx + 16y (K-contiguous B) or 4tx..4tx+3; the next K step is fetched into
 // registers while the current one multiplies.  Out-of-range elements read as 0.
 constexpr int KS = GK + 4;  // row stride of K-contiguous tiles (16-byte aligned rows)
-constexpr int TILE_FLOATS = GT * KS;
+constexpr int GP = GT + 8;  // row stride of M/N-contiguous tiles (tensor-core fragment reads free of bank conflicts)
+constexpr int TILE_FLOATS = GK * GP > GT * KS ? GK * GP : GT * KS;
 
-template <typename OutT, bool kAcc, bool kAK, bool kBK>
+// fp32 -> tf32 (round to nearest, ties away), kept in a 32-bit register
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// D += A B on a 16x8x8 tile: tf32 operands, fp32 accumulation (warp-level tensor-core MMA)
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+template <typename OutT, bool kAcc, bool kAK, bool kBK, bool kTC = false>
 __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t a_cs, const float* B, int64_t b_rs,
                      int64_t b_cs, OutT* C, int64_t c_rs, int64_t c_cs, float* sA, float* sB, float alpha = 1.f) {
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
+  // tensor-core layout: warp w owns rows 32*(w&1) .. +31 and columns 16*(w>>1) .. +15 of the tile
+  const int lane = tid & 31, warp = tid >> 5;
+  const int wm = 32 * (warp & 1), wn = 16 * (warp >> 1);
+  const int g = lane >> 2, t4 = lane & 3;
   constexpr int PER = GK * GT / THREADS;  // 4 elements of each operand per thread and K step
   for (int i0 = 0; i0 < M; i0 += GT) {
     for (int j0 = 0; j0 < N; j0 += GT) {
-      float acc[4][4];
+      float acc[4][4];  // SIMT: [row][column]; tensor cores: [m16 tile * 2 + n8 tile][fragment element]
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -83,9 +104,11 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
           const int i = kAK ? e / GK : e % GT, l = kAK ? e % GK : e / GT;
           const int gi = i0 + i, gl = l0 + l;
           ra[r] = (gi < M && gl < K) ? A[gi * a_rs + gl * a_cs] : 0.f;
+          if (kTC) ra[r] = to_tf32(ra[r]);
           const int j = kBK ? e / GK : e % GT, l2 = kBK ? e % GK : e / GT;
           const int gj = j0 + j, gl2 = l0 + l2;
           rb[r] = (gj < N && gl2 < K) ? B[gl2 * b_rs + gj * b_cs] : 0.f;
+          if (kTC) rb[r] = to_tf32(rb[r]);
         }
       };
       auto stash = [&]() {
@@ -93,9 +116,9 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
         for (int r = 0; r < PER; ++r) {
           const int e = tid + r * THREADS;
           if (kAK) sA[(e / GK) * KS + e % GK] = ra[r];
-          else sA[(e / GT) * GT + e % GT] = ra[r];
+          else sA[(e / GT) * GP + e % GT] = ra[r];
           if (kBK) sB[(e / GK) * KS + e % GK] = rb[r];
-          else sB[(e / GT) * GT + e % GT] = rb[r];
+          else sB[(e / GT) * GP + e % GT] = rb[r];
         }
       };
       fetch(0);
@@ -104,8 +127,35 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
       for (int l0 = 0; l0 < K; l0 += GK) {
         const bool more = l0 + GK < K;
         if (more) fetch(l0 + GK);
+        if (kTC) {
+          // element (i, l) of the A tile and (l, j) of the B tile, in their shared layouts
+          auto at = [&](int i, int l) { return __float_as_uint(kAK ? sA[i * KS + l] : sA[l * GP + i]); };
+          auto bt = [&](int l, int j) { return __float_as_uint(kBK ? sB[j * KS + l] : sB[l * GP + j]); };
 #pragma unroll
-        for (int l4 = 0; l4 < GK; l4 += 4) {
+          for (int k8 = 0; k8 < GK; k8 += 8) {
+            uint32_t af[2][4], bf[2][2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const int r0 = wm + 16 * mt + g;
+              af[mt][0] = at(r0, k8 + t4);
+              af[mt][1] = at(r0 + 8, k8 + t4);
+              af[mt][2] = at(r0, k8 + t4 + 4);
+              af[mt][3] = at(r0 + 8, k8 + t4 + 4);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const int c0 = wn + 8 * nt + g;
+              bf[nt][0] = bt(k8 + t4, c0);
+              bf[nt][1] = bt(k8 + t4 + 4, c0);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[2 * mt + nt], af[mt], bf[nt]);
+          }
+        }
+#pragma unroll
+        for (int l4 = 0; l4 < (kTC ? 0 : GK); l4 += 4) {
           float a[4][4], b[4][4];  // [row or column][k]
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
@@ -113,14 +163,14 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
               const float4 v = *reinterpret_cast<const float4*>(sA + (ty * 4 + x) * KS + l4);
               a[x][0] = v.x; a[x][1] = v.y; a[x][2] = v.z; a[x][3] = v.w;
             } else {
-              const float4 v = *reinterpret_cast<const float4*>(sA + (l4 + x) * GT + ty * 4);
+              const float4 v = *reinterpret_cast<const float4*>(sA + (l4 + x) * GP + ty * 4);
               a[0][x] = v.x; a[1][x] = v.y; a[2][x] = v.z; a[3][x] = v.w;
             }
             if (kBK) {
               const float4 v = *reinterpret_cast<const float4*>(sB + (tx + 16 * x) * KS + l4);
               b[x][0] = v.x; b[x][1] = v.y; b[x][2] = v.z; b[x][3] = v.w;
             } else {
-              const float4 v = *reinterpret_cast<const float4*>(sB + (l4 + x) * GT + tx * 4);
+              const float4 v = *reinterpret_cast<const float4*>(sB + (l4 + x) * GP + tx * 4);
               b[0][x] = v.x; b[1][x] = v.y; b[2][x] = v.z; b[3][x] = v.w;
             }
           }
@@ -141,7 +191,10 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
       for (int x = 0; x < 4; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
-          const int gi = i0 + ty * 4 + x, gj = j0 + (kBK ? tx + 16 * y : tx * 4 + y);
+          // SIMT: row ty*4+x, column tx+16y / 4tx+y.  Tensor cores: fragment element y of
+          // (m16 tile x>>1, n8 tile x&1): row g (+8 for y >= 2), column 2*t4 + (y & 1)
+          const int gi = kTC ? i0 + wm + 16 * (x >> 1) + g + 8 * (y >> 1) : i0 + ty * 4 + x;
+          const int gj = kTC ? j0 + wn + 8 * (x & 1) + 2 * t4 + (y & 1) : j0 + (kBK ? tx + 16 * y : tx * 4 + y);
           if (gi < M && gj < N) {
             float v = alpha * acc[x][y];
             if constexpr (kAcc) v += C[gi * c_rs + gj * c_cs];
@@ -320,15 +373,15 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
     // Y = Delta Omega (columns k..kp-1 stay zero)
     for (int64_t e = threadIdx.x; e < (int64_t)kp * T; e += THREADS) Y[e] = 0.f;
     __syncthreads();
-    gemm<float, false, true, false>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
+    gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
     orth_block(Y, T, k, cblk, norms, red, sA, sB);
     for (int it = 0; it < p.power_iters; ++it) {
-      gemm<float, false, false, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);  // Z = Delta^T Q
+      gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);  // Z = Delta^T Q
       orth_block(Z, D, k, cblk, norms, red, sA, sB);
-      gemm<float, false, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);  // Y = Delta Z
+      gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);  // Y = Delta Z
       orth_block(Y, T, k, cblk, norms, red, sA, sB);
     }
-    gemm<float, false, true, false>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);    // B = Q^T Delta
+    gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);    // B = Q^T Delta
     for (int e = threadIdx.x; e < kp * kp; e += THREADS) C[e] = 0.f;
     __syncthreads();
     gemm<float, false, true, true>(k, k, D, B, D, 1, B, 1, D, C, kp, 1, sA, sB);   // C = B B^T

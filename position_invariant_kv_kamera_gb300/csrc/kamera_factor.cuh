@@ -30,6 +30,10 @@
 namespace kamera {
 namespace factor {
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 constexpr int THREADS = 256;
 constexpr int KMAX = 96;   // k = m + oversampling, padded to a multiple of 16
 constexpr int GT = 64;     // GEMM tile (rows and columns)
@@ -211,6 +215,117 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
   __syncthreads();
 }
 
+// ---- tensor-core GEMM with a cp.async ring ---------------------------------------------------
+// C = alpha * A B with tf32 operands and fp32 accumulation, the operand tiles
+// streamed through TC_STAGES shared-memory stages by 16-byte cp.async copies
+// (zero-filled past the edges).  kAK: A(i,l) = A[i*a_ld + l], else A[i + l*a_ld];
+// kBK: B(l,j) = B[l + j*b_ld], else B[l*b_ld + j].  Requires 16-byte aligned
+// operand bases, leading dimensions that are multiples of 4, and M, N, K
+// multiples of 4 (a 16-byte chunk never straddles an edge).  Warp layout and
+// fragments as in gemm<..., kTC = true>.
+constexpr int TC_STAGES = 4;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename OutT, bool kAK, bool kBK>
+__device__ void gemm_tc(int M, int N, int K, const float* A, int64_t a_ld, const float* B, int64_t b_ld, OutT* C,
+                        int64_t c_rs, int64_t c_cs, float* ring, float alpha = 1.f) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = 32 * (warp & 1), wn = 16 * (warp >> 1);
+  const int g = lane >> 2, t4 = lane & 3;
+  const int nsteps = (K + GK - 1) / GK;
+  for (int i0 = 0; i0 < M; i0 += GT) {
+    for (int j0 = 0; j0 < N; j0 += GT) {
+      // one 16-byte chunk of each operand tile per thread and stage
+      auto load_stage = [&](int slot, int l0) {
+        float* sA = ring + (2 * slot) * TILE_FLOATS;
+        float* sB = sA + TILE_FLOATS;
+        int i, l, soff;
+        if (kAK) { i = tid >> 2; l = 4 * (tid & 3); soff = i * KS + l; }
+        else     { l = tid >> 4; i = 4 * (tid & 15); soff = l * GP + i; }
+        bool ok = i0 + i < M && l0 + l < K;
+        const float* src = ok ? (kAK ? A + (int64_t)(i0 + i) * a_ld + l0 + l : A + (i0 + i) + (int64_t)(l0 + l) * a_ld) : A;
+        cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u);
+        int j;
+        if (kBK) { j = tid >> 2; l = 4 * (tid & 3); soff = j * KS + l; }
+        else     { l = tid >> 4; j = 4 * (tid & 15); soff = l * GP + j; }
+        ok = j0 + j < N && l0 + l < K;
+        src = ok ? (kBK ? B + (int64_t)(j0 + j) * b_ld + l0 + l : B + (int64_t)(l0 + l) * b_ld + j0 + j) : B;
+        cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u);
+      };
+      float acc[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll
+      for (int st = 0; st < TC_STAGES - 1; ++st) {
+        if (st < nsteps) load_stage(st, st * GK);
+        cp_async_commit();
+      }
+      for (int st = 0; st < nsteps; ++st) {
+        cp_async_wait<TC_STAGES - 2>();
+        __syncthreads();  // stage st landed for every thread; stage st-1 is no longer read
+        const int nx = st + TC_STAGES - 1;
+        if (nx < nsteps) load_stage(nx % TC_STAGES, nx * GK);
+        cp_async_commit();
+        const float* sA = ring + (2 * (st % TC_STAGES)) * TILE_FLOATS;
+        const float* sB = sA + TILE_FLOATS;
+        auto at = [&](int i, int l) { return __float_as_uint(to_tf32(kAK ? sA[i * KS + l] : sA[l * GP + i])); };
+        auto bt = [&](int l, int j) { return __float_as_uint(to_tf32(kBK ? sB[j * KS + l] : sB[l * GP + j])); };
+#pragma unroll
+        for (int k8 = 0; k8 < GK; k8 += 8) {
+          uint32_t af[2][4], bf[2][2];
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const int r0 = wm + 16 * mt + g;
+            af[mt][0] = at(r0, k8 + t4);
+            af[mt][1] = at(r0 + 8, k8 + t4);
+            af[mt][2] = at(r0, k8 + t4 + 4);
+            af[mt][3] = at(r0 + 8, k8 + t4 + 4);
+          }
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int c0 = wn + 8 * nt + g;
+            bf[nt][0] = bt(k8 + t4, c0);
+            bf[nt][1] = bt(k8 + t4 + 4, c0);
+          }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[2 * mt + nt], af[mt], bf[nt]);
+        }
+      }
+      cp_async_wait<0>();
+      __syncthreads();  // the ring is reused by the next output tile
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int gi = i0 + wm + 16 * (x >> 1) + g + 8 * (y >> 1);
+          const int gj = j0 + wn + 8 * (x & 1) + 2 * t4 + (y & 1);
+          if (gi < M && gj < N) {
+            const float v = alpha * acc[x][y];
+            if constexpr (sizeof(OutT) == 2) {
+              __nv_bfloat16 h = __float2bfloat16_rn(v);
+              C[gi * c_rs + gj * c_cs] = *reinterpret_cast<uint16_t*>(&h);
+            } else {
+              C[gi * c_rs + gj * c_cs] = v;
+            }
+          }
+        }
+    }
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ float block_sum(float v, float* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -345,15 +460,16 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return 2 * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + OB + 2 * kp + 32 + kp;
+  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + OB + 2 * kp + 32 + kp;
 }
 
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
   extern __shared__ __align__(16) float fsm[];
   const int T = p.T, D = p.D, k = p.k, kp = p.kp, m = p.m;
-  float* sA = fsm;                    // TILE_FLOATS
-  float* sB = sA + TILE_FLOATS;       // TILE_FLOATS
-  float* C = sB + TILE_FLOATS;        // kp*kp
+  float* ring = fsm;                  // 2*TC_STAGES*TILE_FLOATS: the tensor-core GEMM's stages
+  float* sA = ring;                   // the first two tiles serve the fp32 GEMMs
+  float* sB = sA + TILE_FLOATS;
+  float* C = ring + 2 * TC_STAGES * TILE_FLOATS;  // kp*kp
   float* W = C + kp * kp;             // kp*kp
   float* Ws = W + kp * kp;            // kp*m: sorted leading eigenvectors
   float* cblk = Ws + kp * m;          // kp*OB: block Gram-Schmidt coefficients
@@ -368,20 +484,35 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
 
   // rows k..kp-1 of B are never written: keep them zero for the V_m product
   for (int64_t e = (int64_t)k * D + threadIdx.x; e < (int64_t)kp * D; e += THREADS) B[e] = 0.f;
+  // the cp.async path needs 16-byte chunks that never straddle an edge
+  const bool ring_ok = ((T | D | k) & 3) == 0 && (p.delta_stride & 3) == 0 &&
+                       ((reinterpret_cast<uintptr_t>(p.delta) | reinterpret_cast<uintptr_t>(p.omega)) & 15u) == 0;
   for (int s = blockIdx.x; s < p.n_slabs; s += gridDim.x) {
     const float* A = p.delta + (int64_t)s * p.delta_stride;  // [T][D]
     // Y = Delta Omega (columns k..kp-1 stay zero)
     for (int64_t e = threadIdx.x; e < (int64_t)kp * T; e += THREADS) Y[e] = 0.f;
     __syncthreads();
-    gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
+    if (ring_ok)
+      gemm_tc<float, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
+    else
+      gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
     orth_block(Y, T, k, cblk, norms, red, sA, sB);
     for (int it = 0; it < p.power_iters; ++it) {
-      gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);  // Z = Delta^T Q
+      if (ring_ok)  // Z = Delta^T Q
+        gemm_tc<float, false, true>(D, k, T, A, D, Y, T, Z, 1, D, ring);
+      else
+        gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);
       orth_block(Z, D, k, cblk, norms, red, sA, sB);
-      gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);  // Y = Delta Z
+      if (ring_ok)  // Y = Delta Z
+        gemm_tc<float, true, true>(T, k, D, A, D, Z, D, Y, 1, T, ring);
+      else
+        gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);
       orth_block(Y, T, k, cblk, norms, red, sA, sB);
     }
-    gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);    // B = Q^T Delta
+    if (ring_ok)  // B = Q^T Delta
+      gemm_tc<float, true, false>(k, D, T, Y, T, A, D, B, D, 1, ring);
+    else
+      gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);
     for (int e = threadIdx.x; e < kp * kp; e += THREADS) C[e] = 0.f;
     __syncthreads();
     gemm<float, false, true, true>(k, k, D, B, D, 1, B, 1, D, C, kp, 1, sA, sB);   // C = B B^T

@@ -337,54 +337,143 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-constexpr int OB = 16;  // column block of the block Gram-Schmidt
+constexpr int OB = 16;  // column block of the orthonormalisation
 
-// Orthonormalise the k columns (length n, column j at X + j*n) in place by
-// block classical Gram-Schmidt with reorthogonalisation: each block of 16
-// columns is projected off the finished columns twice (two GEMMs per pass),
-// then orthonormalised column by column inside the block (classical
-// Gram-Schmidt, twice).  A column whose remainder falls below 1e-4 of its
-// original norm is dependent and becomes zero.
-__device__ void orth_block(float* X, int n, int k, float* cblk, float* norms, float* red, float* sA, float* sB) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// ---- tall-skinny primitives over panels of n rows (column j of a panel at P + j*n) ----------
+
+// ts_tn for a <= 48
+__device__ void ts_tn48(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[6][OB];
+#pragma unroll
+  for (int i = 0; i < 6; ++i)
+#pragma unroll
+    for (int q = 0; q < OB; ++q) acc[i][q] = 0.f;
+  for (int r = lane; r < n; r += 32) {
+    float qv[OB];
+#pragma unroll
+    for (int q = 0; q < OB; ++q) qv[q] = q < b ? Q[(int64_t)q * n + r] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+      const int p = warp + 8 * i;
+      if (p < a) {
+        const float pv = P[(int64_t)p * n + r];
+#pragma unroll
+        for (int q = 0; q < OB; ++q) acc[i][q] = fmaf(pv, qv[q], acc[i][q]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    const int p = warp + 8 * i;
+    if (p >= a) break;  // warp-uniform
+#pragma unroll
+    for (int q = 0; q < OB; ++q) {
+      float v = acc[i][q];
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      if (lane == 0 && q < b) C[p * ldc + q] = v;
+    }
+  }
+}
+
+// C[p][q] = sum_r P[p][r] Q[q][r] for p < a, q < b (b <= 16), C row-major with row
+// stride ldc.  In chunks of 48 rows of C: warp w takes rows p = w, w+8, ...; its
+// lanes split the n rows of the panels and the partial sums meet by shuffles.
+__device__ void ts_tn(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
+  for (int p0 = 0; p0 < a; p0 += 48) ts_tn48(C + p0 * ldc, ldc, P + (int64_t)p0 * n, min(48, a - p0), Q, b, n);
+}
+
+// X[q][r] -= sum_{p < a} P[p][r] C[p][q] for q < b: one row r per thread.
+__device__ void ts_update(float* X, int b, const float* P, int a, const float* C, int ldc, int n) {
+  for (int r = threadIdx.x; r < n; r += THREADS) {
+    float x[OB];
+#pragma unroll
+    for (int q = 0; q < OB; ++q) x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
+    for (int p = 0; p < a; ++p) {
+      const float pv = P[(int64_t)p * n + r];
+#pragma unroll
+      for (int q = 0; q < OB; ++q) x[q] = fmaf(-pv, C[p * ldc + q], x[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < OB; ++q)
+      if (q < b) X[(int64_t)q * n + r] = x[q];
+  }
+}
+
+// Cholesky G = R^T R of a b x b Gram matrix (b <= 16, row stride OB) by one warp,
+// dropping column j (row j of R zero, inv_diag[j] = 0) when its pivot -- the
+// squared norm of what remains of column j after the columns before it -- is at
+// most thr[j].
+__device__ void chol_drop(const float* G, float* R, float* inv_diag, const float* thr, int b) {
+  const int lane = threadIdx.x & 31;
+  for (int j = 0; j < b; ++j) {
+    float sv = 0.f;
+    if (lane < b && lane >= j) {
+      sv = G[j * OB + lane];
+      for (int l = 0; l < j; ++l) sv -= R[l * OB + j] * R[l * OB + lane];
+    }
+    const float d = __shfl_sync(0xFFFFFFFFu, sv, j);
+    const bool keep = d > thr[j];
+    const float rjj = keep ? sqrtf(d) : 0.f;
+    if (lane < b) R[j * OB + lane] = (keep && lane >= j) ? (lane == j ? rjj : sv / rjj) : 0.f;
+    if (lane == 0) inv_diag[j] = keep ? 1.f / rjj : 0.f;
+    __syncwarp();
+  }
+}
+
+// X <- X R^{-1} row by row (forward substitution), R upper triangular, dropped
+// columns become zero.
+__device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, int n) {
+  for (int r = threadIdx.x; r < n; r += THREADS) {
+    float x[OB];
+#pragma unroll
+    for (int q = 0; q < OB; ++q) x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
+#pragma unroll
+    for (int j = 0; j < OB; ++j) {
+      float v = x[j];
+#pragma unroll
+      for (int l = 0; l < j; ++l) v = fmaf(-x[l], R[l * OB + j], v);
+      x[j] = v * inv_diag[j < b ? j : 0] * (j < b ? 1.f : 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < OB; ++q)
+      if (q < b) X[(int64_t)q * n + r] = x[q];
+  }
+}
+
+// Orthonormalise the k columns (length n, column j at X + j*n) in place, one
+// block of 16 columns at a time: the block is projected off the finished
+// columns twice (classical block Gram-Schmidt with reorthogonalisation), then
+// orthonormalised by Cholesky QR twice (Gram matrix, Cholesky, triangular
+// solve).  A column whose remainder falls below 1e-4 of its original norm is
+// dependent and becomes zero (its Cholesky pivot is dropped).
+// Scratch (shared): cblk [kp][OB], gram [OB][OB], rmat [OB][OB], inv_diag [OB], thr [OB].
+__device__ void orth_block(float* X, int n, int k, float* cblk, float* gram, float* rmat, float* inv_diag,
+                           float* thr) {
   for (int J0 = 0; J0 < k; J0 += OB) {
     const int b = min(OB, k - J0);
     float* XJ = X + (int64_t)J0 * n;
-    for (int j = 0; j < b; ++j) {
-      float s = 0.f;
-      for (int t = tid; t < n; t += THREADS) s += XJ[(int64_t)j * n + t] * XJ[(int64_t)j * n + t];
-      s = block_sum(s, red);
-      if (tid == 0) norms[j] = sqrtf(s);
-    }
+    // squared original norms -> drop thresholds (1e-4 of the norm)
+    ts_tn(gram, OB, XJ, b, XJ, b, n);
+    __syncthreads();
+    if (threadIdx.x < b) thr[threadIdx.x] = 1e-8f * gram[threadIdx.x * OB + threadIdx.x];
     __syncthreads();
     for (int pass = 0; pass < 2 && J0 > 0; ++pass) {
-      // cblk [J0][b] = Q_<J0^T X_J ;  X_J -= Q_<J0 cblk
-      gemm<float, false, true, true>(J0, b, n, X, n, 1, XJ, 1, n, cblk, b, 1, sA, sB);
-      gemm<float, true, false, false>(n, b, J0, X, 1, n, cblk, b, 1, XJ, 1, n, sA, sB, -1.f);
+      ts_tn(cblk, OB, X, J0, XJ, b, n);  // cblk [J0][b] = Q_<^T X_J
+      __syncthreads();
+      ts_update(XJ, b, X, J0, cblk, OB, n);  // X_J -= Q_< cblk
+      __syncthreads();
     }
-    for (int j = 0; j < b; ++j) {
-      float* v = XJ + (int64_t)j * n;
-      for (int pass = 0; pass < 2 && j > 0; ++pass) {
-        for (int l = warp; l < j; l += THREADS / 32) {
-          const float* ql = XJ + (int64_t)l * n;
-          float s = 0.f;
-          for (int t = lane; t < n; t += 32) s += ql[t] * v[t];
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-          if (lane == 0) cblk[l] = s;
-        }
-        __syncthreads();
-        for (int t = tid; t < n; t += THREADS) {
-          float s = v[t];
-          for (int l = 0; l < j; ++l) s -= cblk[l] * XJ[(int64_t)l * n + t];
-          v[t] = s;
-        }
-        __syncthreads();
+    for (int pass = 0; pass < 2; ++pass) {
+      ts_tn(gram, OB, XJ, b, XJ, b, n);
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        if (pass == 1 && threadIdx.x < b) thr[threadIdx.x] = 1e-8f * gram[threadIdx.x * OB + threadIdx.x];
+        __syncwarp();
+        chol_drop(gram, rmat, inv_diag, thr, b);
       }
-      float nr = 0.f;
-      for (int t = tid; t < n; t += THREADS) nr += v[t] * v[t];
-      nr = sqrtf(block_sum(nr, red));
-      const float scale = (nr > 1e-4f * norms[j] && nr > 0.f) ? 1.f / nr : 0.f;
-      for (int t = tid; t < n; t += THREADS) v[t] *= scale;
+      __syncthreads();
+      ts_trsm(XJ, b, rmat, inv_diag, n);
       __syncthreads();
     }
   }
@@ -460,7 +549,7 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + OB + 2 * kp + 32 + kp;
+  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + OB + 2 * kp + 32 + kp + 2 * OB * OB + 2 * OB;
 }
 
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
@@ -477,6 +566,10 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   float* rot = norms + OB;            // 2*kp
   float* red = rot + 2 * kp;          // 32
   int* perm = reinterpret_cast<int*>(red + 32);  // kp
+  float* gram = red + 32 + kp;        // OB*OB
+  float* rmat = gram + OB * OB;       // OB*OB
+  float* inv_diag = rmat + OB * OB;   // OB
+  float* thr = inv_diag + OB;         // OB
 
   float* Y = p.work + blockIdx.x * p.work_per_cta;  // [kp][T] column-major
   float* Z = Y + (int64_t)kp * T;                   // [kp][D]
@@ -496,18 +589,18 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
       gemm_tc<float, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
     else
       gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
-    orth_block(Y, T, k, cblk, norms, red, sA, sB);
+    orth_block(Y, T, k, cblk, gram, rmat, inv_diag, thr);
     for (int it = 0; it < p.power_iters; ++it) {
       if (ring_ok)  // Z = Delta^T Q
         gemm_tc<float, false, true>(D, k, T, A, D, Y, T, Z, 1, D, ring);
       else
         gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);
-      orth_block(Z, D, k, cblk, norms, red, sA, sB);
+      orth_block(Z, D, k, cblk, gram, rmat, inv_diag, thr);
       if (ring_ok)  // Y = Delta Z
         gemm_tc<float, true, true>(T, k, D, A, D, Z, D, Y, 1, T, ring);
       else
         gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);
-      orth_block(Y, T, k, cblk, norms, red, sA, sB);
+      orth_block(Y, T, k, cblk, gram, rmat, inv_diag, thr);
     }
     if (ring_ok)  // B = Q^T Delta
       gemm_tc<float, true, false>(k, D, T, Y, T, A, D, B, D, 1, ring);

@@ -341,20 +341,23 @@ constexpr int OB = 16;  // column block of the orthonormalisation
 
 // ---- tall-skinny primitives over panels of n rows (column j of a panel at P + j*n) ----------
 
-// ts_tn for a <= 48
-__device__ void ts_tn48(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
+// ts_tn for a <= 24: warp w takes rows p = w, w+8, w+16 of C; each lane keeps
+// four panel rows in flight.
+__device__ void ts_tn24(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float acc[6][OB];
+  if (warp >= a) return;  // no row of C for this warp (warp-uniform)
+  float acc[3][OB];
 #pragma unroll
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 3; ++i)
 #pragma unroll
     for (int q = 0; q < OB; ++q) acc[i][q] = 0.f;
+#pragma unroll 4
   for (int r = lane; r < n; r += 32) {
     float qv[OB];
 #pragma unroll
     for (int q = 0; q < OB; ++q) qv[q] = q < b ? Q[(int64_t)q * n + r] : 0.f;
 #pragma unroll
-    for (int i = 0; i < 6; ++i) {
+    for (int i = 0; i < 3; ++i) {
       const int p = warp + 8 * i;
       if (p < a) {
         const float pv = P[(int64_t)p * n + r];
@@ -364,7 +367,7 @@ __device__ void ts_tn48(float* C, int ldc, const float* P, int a, const float* Q
     }
   }
 #pragma unroll
-  for (int i = 0; i < 6; ++i) {
+  for (int i = 0; i < 3; ++i) {
     const int p = warp + 8 * i;
     if (p >= a) break;  // warp-uniform
 #pragma unroll
@@ -377,10 +380,10 @@ __device__ void ts_tn48(float* C, int ldc, const float* P, int a, const float* Q
 }
 
 // C[p][q] = sum_r P[p][r] Q[q][r] for p < a, q < b (b <= 16), C row-major with row
-// stride ldc.  In chunks of 48 rows of C: warp w takes rows p = w, w+8, ...; its
-// lanes split the n rows of the panels and the partial sums meet by shuffles.
+// stride ldc, in chunks of 24 rows of C; the lanes of a warp split the n rows of
+// the panels and the partial sums meet by shuffles.
 __device__ void ts_tn(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
-  for (int p0 = 0; p0 < a; p0 += 48) ts_tn48(C + p0 * ldc, ldc, P + (int64_t)p0 * n, min(48, a - p0), Q, b, n);
+  for (int p0 = 0; p0 < a; p0 += 24) ts_tn24(C + p0 * ldc, ldc, P + (int64_t)p0 * n, min(24, a - p0), Q, b, n);
 }
 
 // X[q][r] -= sum_{p < a} P[p][r] C[p][q] for q < b: one row r per thread.
@@ -389,6 +392,7 @@ __device__ void ts_update(float* X, int b, const float* P, int a, const float* C
     float x[OB];
 #pragma unroll
     for (int q = 0; q < OB; ++q) x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
+#pragma unroll 8
     for (int p = 0; p < a; ++p) {
       const float pv = P[(int64_t)p * n + r];
 #pragma unroll

@@ -83,11 +83,16 @@ def profile_traffic(workload: str) -> float | None:
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != kernel_hash():
+    if not h or h.group(1) != kernel_hash():
         return None
-    return float(m.group(1))
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if m:
+        return float(m.group(1))
+    # a reduced capture of a workload too large to profile: scaled by the units processed
+    m = re.search(r"dram_bytes_per_launch_reduced:\s*([0-9.eE+]+)", txt)
+    f = re.search(r"traffic_scale_to_full:\s*([0-9.eE+]+)", txt)
+    return float(m.group(1)) * float(f.group(1)) if m and f else None
 
 
 class ClockSampler:

@@ -204,46 +204,48 @@ def oracle_sample_workload(name: str, n_items: int, n_tokens: int | None = None)
     return wl
 
 
-def time_oracle(wl: W.Workload) -> tuple[float, int]:
-    """Seconds of one oracle call over wl (inputs generated outside the timing)."""
+def oracle_call(wl: W.Workload, compressed: bool = False):
+    """The oracle over wl as a ready-to-run closure: every input (the bf16 or
+    the compressed store, patches, pools) is generated here, once."""
     import oracle
-    from tests import harness as H
 
     m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
                      wl.pairing, wl.patch_frame)
     th = oracle.theta(wl.rope_base, wl.rope_dim)
     kw = {}
-    if wl.mode == "reuse":
-        kw.update(store=wl.host_store(), store_off=wl.store_off, store_len=np.array(wl.chunk_lens, np.int32))
     if wl.rank and wl.mode != "relocate_in_place":
         kw.update(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
                   rank=wl.rank)
-    mode = {"reuse": oracle.MODE_REUSE, "relocate_in_place": oracle.MODE_RELOCATE_IN_PLACE,
-            "apply_patch": oracle.MODE_PATCH_IN_PLACE}[wl.mode]
     pk_in = wl.host_pool(0)
     pv_in = wl.host_pool(1) if wl.n_ch == 2 else None
-    del H
+    if compressed:
+        cs = oracle.compress_store(m, wl.host_store(), wl.store_off, np.array(wl.chunk_lens, np.int32))
+        return lambda: oracle.reuse_compressed(m, th, cs, items=wl.items, block_table=wl.block_table,
+                                               num_pages=wl.num_pages, page_size=wl.page_size, pool_k_in=pk_in,
+                                               pool_v_in=pv_in, **kw)
+    if wl.mode == "reuse":
+        kw.update(store=wl.host_store(), store_off=wl.store_off, store_len=np.array(wl.chunk_lens, np.int32))
+    mode = {"reuse": oracle.MODE_REUSE, "relocate_in_place": oracle.MODE_RELOCATE_IN_PLACE,
+            "apply_patch": oracle.MODE_PATCH_IN_PLACE}[wl.mode]
+    return lambda: oracle.reuse(m, th, mode, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
+                                page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, **kw)
+
+
+def timed(fn) -> float:
     t0 = time.perf_counter()
-    oracle.reuse(m, th, mode, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
-                 page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, **kw)
-    return time.perf_counter() - t0, wl.tokens
+    fn()
+    return time.perf_counter() - t0
+
+
+def time_oracle(wl: W.Workload) -> tuple[float, int]:
+    """Seconds of one oracle call over wl (inputs generated outside the timing)."""
+    return timed(oracle_call(wl)), wl.tokens
 
 
 def time_oracle_compressed(wl: W.Workload) -> tuple[float, int]:
     """Seconds of one oracle reuse from a compressed store (encoded by the
     oracle, outside the timing) over wl."""
-    import oracle
-
-    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim)
-    cs = oracle.compress_store(m, wl.host_store(), wl.store_off, np.array(wl.chunk_lens, np.int32))
-    th = oracle.theta(wl.rope_base, wl.rope_dim)
-    kw = dict(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
-              rank=wl.rank) if wl.rank else {}
-    pk_in, pv_in = wl.host_pool(0), wl.host_pool(1)
-    t0 = time.perf_counter()
-    oracle.reuse_compressed(m, th, cs, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
-                            page_size=wl.page_size, pool_k_in=pk_in, pool_v_in=pv_in, **kw)
-    return time.perf_counter() - t0, wl.tokens
+    return timed(oracle_call(wl, compressed=True)), wl.tokens
 
 
 def cpu_baseline(name: str, budget_s: float = 15.0) -> dict:
@@ -284,13 +286,13 @@ def run_reference(args) -> None:
     budget = 120.0 / (args.steps + args.warmup)
     n_tok = max(1, min(full_T or tok_probe, int(budget / max(per_tok, 1e-9))))
     sample = oracle_sample_workload(base, 1, n_tok if full_T else None)
+    call = oracle_call(sample, compressed=comp)  # inputs generated once, outside the timing
     for _ in range(args.warmup):
-        timer(sample)
+        call()
     total, toks = 0.0, 0
     for _ in range(args.steps):
-        dt, tok = timer(sample)
-        total += dt
-        toks += tok
+        total += timed(call)
+        toks += sample.tokens
     value = toks / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,

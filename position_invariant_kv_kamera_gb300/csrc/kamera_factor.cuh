@@ -11,14 +11,17 @@
 //
 // Method: the randomized range finder with subspace iteration of Halko,
 // Martinsson & Tropp ("Finding structure with randomness", SIAM Review 2011,
-// Algorithms 4.4 and 5.1), all in fp32:
+// Algorithms 4.4 and 5.1):
 //   Y = Delta Omega (Omega [D][k] Gaussian, k = m + oversampling, an input);
 //   Q = orth(Y);  q times: Z = orth(Delta^T Q), Q = orth(Delta Z);
 //   B = Q^T Delta  [k][D];  C = B B^T = W Lambda W^T (cyclic Jacobi);
 //   U_m = Q W_m (orthonormal columns),  V_m = B^T W_m (carries Sigma).
-// orth() is block classical Gram-Schmidt with reorthogonalisation; a column
-// whose remainder falls below 1e-4 of its norm is dropped (set to zero), so
-// deficits of rank below k are handled exactly.
+// The four products with Delta run on tensor cores (tf32 operands, fp32
+// accumulation); everything else is fp32 on the CUDA cores.  orth() works on
+// blocks of 16 columns: each block is projected off the finished columns
+// twice, then orthonormalised by Cholesky QR twice; a column whose remainder
+// falls below 1e-4 of its norm is dropped (set to zero), so deficits of rank
+// below k are handled exactly.
 //
 // One CTA (256 threads, two per SM) per slab at a time; each CTA owns a
 // workspace region (Y [k][T], Z [k][D], B [k][D], column-major panels) in
@@ -553,7 +556,7 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + OB + 2 * kp + 32 + kp + 2 * OB * OB + 2 * OB;
+  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 2 * OB;
 }
 
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
@@ -565,9 +568,8 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   float* C = ring + 2 * TC_STAGES * TILE_FLOATS;  // kp*kp
   float* W = C + kp * kp;             // kp*kp
   float* Ws = W + kp * kp;            // kp*m: sorted leading eigenvectors
-  float* cblk = Ws + kp * m;          // kp*OB: block Gram-Schmidt coefficients
-  float* norms = cblk + kp * OB;      // OB
-  float* rot = norms + OB;            // 2*kp
+  float* cblk = Ws + kp * m;          // kp*OB: projection coefficients of a column block
+  float* rot = cblk + kp * OB;        // 2*kp
   float* red = rot + 2 * kp;          // 32
   int* perm = reinterpret_cast<int*>(red + 32);  // kp
   float* gram = red + 32 + kp;        // OB*OB

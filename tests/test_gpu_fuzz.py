@@ -5,7 +5,6 @@ and unpatched items mixed in one batch, several sequences."""
 import numpy as np
 import pytest
 
-from synth import gen
 from synth import workloads as W
 from tests import harness as H
 

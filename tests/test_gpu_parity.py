@@ -9,7 +9,6 @@ patched values; bit-exact for untouched slots, unpatched c_KV and copies.
 import numpy as np
 import pytest
 
-from synth import gen
 from synth import workloads as W
 from tests import harness as H
 

@@ -411,8 +411,9 @@ __device__ void ts_update(float* X, int b, const float* P, int a, const float* C
 // dropping column j (row j of R zero, inv_diag[j] = 0) when its pivot -- the
 // squared norm of what remains of column j after the columns before it -- is at
 // most thr[j].
-__device__ void chol_drop(const float* G, float* R, float* inv_diag, const float* thr, int b) {
+__device__ void chol_drop(const float* G, float* R, float* inv_diag, const float* thr, int b, float* cond) {
   const int lane = threadIdx.x & 31;
+  float rmax = 0.f, rmin = INFINITY;
   for (int j = 0; j < b; ++j) {
     float sv = 0.f;
     if (lane < b && lane >= j) {
@@ -424,8 +425,13 @@ __device__ void chol_drop(const float* G, float* R, float* inv_diag, const float
     const float rjj = keep ? sqrtf(d) : 0.f;
     if (lane < b) R[j * OB + lane] = (keep && lane >= j) ? (lane == j ? rjj : sv / rjj) : 0.f;
     if (lane == 0) inv_diag[j] = keep ? 1.f / rjj : 0.f;
+    if (keep) {
+      rmax = fmaxf(rmax, rjj);
+      rmin = fminf(rmin, rjj);
+    }
     __syncwarp();
   }
+  if (lane == 0) *cond = rmax > 0.f ? rmax / rmin : 1.f;  // ratio of the largest to the smallest kept pivot
 }
 
 // X <- X R^{-1} row by row (forward substitution), R upper triangular, dropped
@@ -450,38 +456,59 @@ __device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, 
 
 // Orthonormalise the k columns (length n, column j at X + j*n) in place, one
 // block of 16 columns at a time: the block is projected off the finished
-// columns twice (classical block Gram-Schmidt with reorthogonalisation), then
-// orthonormalised by Cholesky QR twice (Gram matrix, Cholesky, triangular
-// solve).  A column whose remainder falls below 1e-4 of its original norm is
-// dependent and becomes zero (its Cholesky pivot is dropped).
-// Scratch (shared): cblk [kp][OB], gram [OB][OB], rmat [OB][OB], inv_diag [OB], thr [OB].
+// columns (classical block Gram-Schmidt), a second time when a column lost
+// more than half of its squared norm in the first projection ("twice is
+// enough", Giraud, Langou & Rozloznik 2005), then orthonormalised by Cholesky
+// QR (Gram matrix, Cholesky, triangular solve), a second time when the first
+// Cholesky factor is ill-conditioned (largest / smallest pivot above 16).  A
+// column whose remainder falls below 1e-4 of its original norm is dependent
+// and becomes zero (its Cholesky pivot is dropped).
+// Scratch (shared): cblk [kp][OB], gram [OB][OB], rmat [OB][OB], inv_diag [OB],
+// thr [OB], orig [OB] (squared original norms), cond [1].
 __device__ void orth_block(float* X, int n, int k, float* cblk, float* gram, float* rmat, float* inv_diag,
                            float* thr) {
+  float* orig = thr + OB;
+  float* cond = orig + OB;
   for (int J0 = 0; J0 < k; J0 += OB) {
     const int b = min(OB, k - J0);
     float* XJ = X + (int64_t)J0 * n;
     // squared original norms -> drop thresholds (1e-4 of the norm)
     ts_tn(gram, OB, XJ, b, XJ, b, n);
     __syncthreads();
-    if (threadIdx.x < b) thr[threadIdx.x] = 1e-8f * gram[threadIdx.x * OB + threadIdx.x];
+    if (threadIdx.x < b) {
+      orig[threadIdx.x] = gram[threadIdx.x * OB + threadIdx.x];
+      thr[threadIdx.x] = 1e-8f * orig[threadIdx.x];
+    }
     __syncthreads();
+    bool fresh_gram = true;  // gram holds the Gram matrix of the current X_J
     for (int pass = 0; pass < 2 && J0 > 0; ++pass) {
       ts_tn(cblk, OB, X, J0, XJ, b, n);  // cblk [J0][b] = Q_<^T X_J
       __syncthreads();
       ts_update(XJ, b, X, J0, cblk, OB, n);  // X_J -= Q_< cblk
       __syncthreads();
-    }
-    for (int pass = 0; pass < 2; ++pass) {
       ts_tn(gram, OB, XJ, b, XJ, b, n);
       __syncthreads();
+      bool again = false;
+      for (int j = 0; j < b; ++j) again |= gram[j * OB + j] < 0.5f * orig[j];
+      if (!again) break;  // block-uniform: every thread reads the same shared values
+      __syncthreads();    // the next pass rewrites cblk and gram
+    }
+    for (int pass = 0; pass < 2; ++pass) {
+      if (!fresh_gram) {
+        ts_tn(gram, OB, XJ, b, XJ, b, n);
+        __syncthreads();
+      }
       if (threadIdx.x < 32) {
         if (pass == 1 && threadIdx.x < b) thr[threadIdx.x] = 1e-8f * gram[threadIdx.x * OB + threadIdx.x];
         __syncwarp();
-        chol_drop(gram, rmat, inv_diag, thr, b);
+        chol_drop(gram, rmat, inv_diag, thr, b, cond);
       }
       __syncthreads();
       ts_trsm(XJ, b, rmat, inv_diag, n);
+      const bool again = *cond > 16.f;
       __syncthreads();
+      fresh_gram = false;
+      if (!again) break;
     }
   }
 }
@@ -556,7 +583,7 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 2 * OB;
+  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
 }
 
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   float* gram = red + 32 + kp;        // OB*OB
   float* rmat = gram + OB * OB;       // OB*OB
   float* inv_diag = rmat + OB * OB;   // OB
-  float* thr = inv_diag + OB;         // OB
+  float* thr = inv_diag + OB;         // OB, then orig (OB) and cond (1) for orth_block
 
   float* Y = p.work + blockIdx.x * p.work_per_cta;  // [kp][T] column-major
   float* Z = Y + (int64_t)kp * T;                   // [kp][D]

@@ -227,6 +227,9 @@ __device__ void gemm(int M, int N, int K, const float* A, int64_t a_rs, int64_t 
 // multiples of 4 (a 16-byte chunk never straddles an edge).  Warp layout and
 // fragments as in gemm<..., kTC = true>.
 constexpr int TC_STAGES = 4;
+constexpr int TK = 32;                                // K per stage of the tensor-core GEMM
+constexpr int TKS = TK + 4;                           // row stride of its K-contiguous tiles
+constexpr int TC_TILE = GT * TKS > TK * GP ? GT * TKS : TK * GP;  // floats per operand tile
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -243,25 +246,30 @@ __device__ void gemm_tc(int M, int N, int K, const float* A, int64_t a_ld, const
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wm = 32 * (warp & 1), wn = 16 * (warp >> 1);
   const int g = lane >> 2, t4 = lane & 3;
-  const int nsteps = (K + GK - 1) / GK;
+  const int nsteps = (K + TK - 1) / TK;
   for (int i0 = 0; i0 < M; i0 += GT) {
     for (int j0 = 0; j0 < N; j0 += GT) {
-      // one 16-byte chunk of each operand tile per thread and stage
+      // two 16-byte chunks of each operand tile per thread and stage
       auto load_stage = [&](int slot, int l0) {
-        float* sA = ring + (2 * slot) * TILE_FLOATS;
-        float* sB = sA + TILE_FLOATS;
-        int i, l, soff;
-        if (kAK) { i = tid >> 2; l = 4 * (tid & 3); soff = i * KS + l; }
-        else     { l = tid >> 4; i = 4 * (tid & 15); soff = l * GP + i; }
-        bool ok = i0 + i < M && l0 + l < K;
-        const float* src = ok ? (kAK ? A + (int64_t)(i0 + i) * a_ld + l0 + l : A + (i0 + i) + (int64_t)(l0 + l) * a_ld) : A;
-        cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u);
-        int j;
-        if (kBK) { j = tid >> 2; l = 4 * (tid & 3); soff = j * KS + l; }
-        else     { l = tid >> 4; j = 4 * (tid & 15); soff = l * GP + j; }
-        ok = j0 + j < N && l0 + l < K;
-        src = ok ? (kBK ? B + (int64_t)(j0 + j) * b_ld + l0 + l : B + (int64_t)(l0 + l) * b_ld + j0 + j) : B;
-        cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u);
+        float* sA = ring + (2 * slot) * TC_TILE;
+        float* sB = sA + TC_TILE;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = tid + THREADS * h;  // chunk 0 .. 511
+          int i, l, soff;
+          if (kAK) { i = c >> 3; l = 4 * (c & 7); soff = i * TKS + l; }
+          else     { l = c >> 4; i = 4 * (c & 15); soff = l * GP + i; }
+          bool ok = i0 + i < M && l0 + l < K;
+          const float* src =
+              ok ? (kAK ? A + (int64_t)(i0 + i) * a_ld + l0 + l : A + (i0 + i) + (int64_t)(l0 + l) * a_ld) : A;
+          cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u);
+          int j;
+          if (kBK) { j = c >> 3; l = 4 * (c & 7); soff = j * TKS + l; }
+          else     { l = c >> 4; j = 4 * (c & 15); soff = l * GP + j; }
+          ok = j0 + j < N && l0 + l < K;
+          src = ok ? (kBK ? B + (int64_t)(j0 + j) * b_ld + l0 + l : B + (int64_t)(l0 + l) * b_ld + j0 + j) : B;
+          cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u);
+        }
       };
       float acc[4][4];
 #pragma unroll
@@ -270,21 +278,21 @@ __device__ void gemm_tc(int M, int N, int K, const float* A, int64_t a_ld, const
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 #pragma unroll
       for (int st = 0; st < TC_STAGES - 1; ++st) {
-        if (st < nsteps) load_stage(st, st * GK);
+        if (st < nsteps) load_stage(st, st * TK);
         cp_async_commit();
       }
       for (int st = 0; st < nsteps; ++st) {
         cp_async_wait<TC_STAGES - 2>();
         __syncthreads();  // stage st landed for every thread; stage st-1 is no longer read
         const int nx = st + TC_STAGES - 1;
-        if (nx < nsteps) load_stage(nx % TC_STAGES, nx * GK);
+        if (nx < nsteps) load_stage(nx % TC_STAGES, nx * TK);
         cp_async_commit();
-        const float* sA = ring + (2 * (st % TC_STAGES)) * TILE_FLOATS;
-        const float* sB = sA + TILE_FLOATS;
-        auto at = [&](int i, int l) { return __float_as_uint(to_tf32(kAK ? sA[i * KS + l] : sA[l * GP + i])); };
-        auto bt = [&](int l, int j) { return __float_as_uint(to_tf32(kBK ? sB[j * KS + l] : sB[l * GP + j])); };
+        const float* sA = ring + (2 * (st % TC_STAGES)) * TC_TILE;
+        const float* sB = sA + TC_TILE;
+        auto at = [&](int i, int l) { return __float_as_uint(to_tf32(kAK ? sA[i * TKS + l] : sA[l * GP + i])); };
+        auto bt = [&](int l, int j) { return __float_as_uint(to_tf32(kBK ? sB[j * TKS + l] : sB[l * GP + j])); };
 #pragma unroll
-        for (int k8 = 0; k8 < GK; k8 += 8) {
+        for (int k8 = 0; k8 < TK; k8 += 8) {
           uint32_t af[2][4], bf[2][2];
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
@@ -583,16 +591,16 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return 2 * TC_STAGES * TILE_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
+  return 2 * TC_STAGES * TC_TILE + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
 }
 
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
   extern __shared__ __align__(16) float fsm[];
   const int T = p.T, D = p.D, k = p.k, kp = p.kp, m = p.m;
-  float* ring = fsm;                  // 2*TC_STAGES*TILE_FLOATS: the tensor-core GEMM's stages
-  float* sA = ring;                   // the first two tiles serve the fp32 GEMMs
+  float* ring = fsm;                  // 2*TC_STAGES*TC_TILE: the tensor-core GEMM's stages
+  float* sA = ring;                   // the first two fp32-GEMM tiles overlay the ring
   float* sB = sA + TILE_FLOATS;
-  float* C = ring + 2 * TC_STAGES * TILE_FLOATS;  // kp*kp
+  float* C = ring + 2 * TC_STAGES * TC_TILE;  // kp*kp
   float* W = C + kp * kp;             // kp*kp
   float* Ws = W + kp * kp;            // kp*m: sorted leading eigenvectors
   float* cblk = Ws + kp * m;          // kp*OB: projection coefficients of a column block

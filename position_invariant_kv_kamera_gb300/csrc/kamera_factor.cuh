@@ -289,8 +289,11 @@ __device__ void gemm_tc(int M, int N, int K, const float* A, int64_t a_ld, const
         cp_async_commit();
         const float* sA = ring + (2 * (st % TC_STAGES)) * TC_TILE;
         const float* sB = sA + TC_TILE;
-        auto at = [&](int i, int l) { return __float_as_uint(to_tf32(kAK ? sA[i * TKS + l] : sA[l * GP + i])); };
-        auto bt = [&](int l, int j) { return __float_as_uint(to_tf32(kBK ? sB[j * TKS + l] : sB[l * GP + j])); };
+        // the tf32 MMA reads the upper 19 bits of each fp32 operand; adding half a
+        // tf32 ulp (bit 12) first rounds the magnitude to nearest, ties away, in
+        // one integer add instead of a conversion
+        auto at = [&](int i, int l) { return __float_as_uint(kAK ? sA[i * TKS + l] : sA[l * GP + i]) + 0x1000u; };
+        auto bt = [&](int l, int j) { return __float_as_uint(kBK ? sB[j * TKS + l] : sB[l * GP + j]) + 0x1000u; };
 #pragma unroll
         for (int k8 = 0; k8 < TK; k8 += 8) {
           uint32_t af[2][4], bf[2][2];

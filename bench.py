@@ -487,10 +487,11 @@ FACTOR_SHAPE = dict(n_slabs=16 * 28 * 2, T=1024, D=512, rank=32, oversample=16, 
 
 def factor_flops(T: int, D: int, k: int, m: int, q: int) -> int:
     """Algorithmic flops of one slab: the GEMMs (Delta Omega, 2q subspace
-    products, Q^T Delta, B B^T, the two output products) and classical
-    the orthonormalisation of each of the 2q+1 panels, done twice (4 k^2 n per panel)."""
+    products, Q^T Delta, B B^T, the two output products) and one QR of each
+    of the 2q+1 panels (2 k^2 n for an n x k panel; a reorthogonalisation
+    pass is overhead and not counted)."""
     gemm = 2 * T * D * k * (2 + 2 * q) + 2 * D * k * k + 2 * (T + D) * k * m
-    orth = 4 * k * k * (T + q * (T + D))
+    orth = 2 * k * k * (T + q * (T + D))
     return gemm + orth
 
 

@@ -234,16 +234,31 @@ constexpr int TC_TILE = GT * TKS > TK * GP ? GT * TKS : TK * GP;  // floats per 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// the same with an L2 eviction policy (createpolicy)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src), "r"(src_bytes),
+               "l"(policy)
+               : "memory");
+}
+// Delta streams through L2 once per product (no slab fits alongside the others), so
+// its lines go first and the CTAs' panels (Y, Z, B) stay resident between the steps
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename OutT, bool kAK, bool kBK>
+// kStreamA / kStreamB: that operand is Delta (loaded with the evict-first policy).
+template <typename OutT, bool kAK, bool kBK, bool kStreamA, bool kStreamB>
 __device__ void gemm_tc(int M, int N, int K, const float* A, int64_t a_ld, const float* B, int64_t b_ld, OutT* C,
                         int64_t c_rs, int64_t c_cs, float* ring, float alpha = 1.f) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint64_t pol = evict_first_policy();
   const int wm = 32 * (warp & 1), wn = 16 * (warp >> 1);
   const int g = lane >> 2, t4 = lane & 3;
   const int nsteps = (K + TK - 1) / TK;
@@ -262,13 +277,19 @@ __device__ void gemm_tc(int M, int N, int K, const float* A, int64_t a_ld, const
           bool ok = i0 + i < M && l0 + l < K;
           const float* src =
               ok ? (kAK ? A + (int64_t)(i0 + i) * a_ld + l0 + l : A + (i0 + i) + (int64_t)(l0 + l) * a_ld) : A;
-          cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u);
+          if (kStreamA)
+            cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u, pol);
+          else
+            cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u);
           int j;
           if (kBK) { j = c >> 3; l = 4 * (c & 7); soff = j * TKS + l; }
           else     { l = c >> 4; j = 4 * (c & 15); soff = l * GP + j; }
           ok = j0 + j < N && l0 + l < K;
           src = ok ? (kBK ? B + (int64_t)(j0 + j) * b_ld + l0 + l : B + (int64_t)(l0 + l) * b_ld + j0 + j) : B;
-          cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u);
+          if (kStreamB)
+            cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u, pol);
+          else
+            cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u);
         }
       };
       float acc[4][4];
@@ -419,30 +440,35 @@ __device__ void ts_update(float* X, int b, const float* P, int a, const float* C
 }
 
 // Cholesky G = R^T R of a b x b Gram matrix (b <= 16, row stride OB) by one warp,
-// dropping column j (row j of R zero, inv_diag[j] = 0) when its pivot -- the
-// squared norm of what remains of column j after the columns before it -- is at
-// most thr[j].
+// right-looking: lane c keeps column c of the partly eliminated matrix in registers
+// and row j of R reaches the other lanes by shuffles.  Column j is dropped (row j
+// of R zero, inv_diag[j] = 0) when its pivot -- the squared norm of what remains
+// of column j after the columns before it -- is at most thr[j].  cond receives the
+// ratio of the largest to the smallest kept pivot.
 __device__ void chol_drop(const float* G, float* R, float* inv_diag, const float* thr, int b, float* cond) {
   const int lane = threadIdx.x & 31;
+  float col[OB];
+#pragma unroll
+  for (int i = 0; i < OB; ++i) col[i] = (lane < b && i < b) ? G[i * OB + lane] : 0.f;
   float rmax = 0.f, rmin = INFINITY;
-  for (int j = 0; j < b; ++j) {
-    float sv = 0.f;
-    if (lane < b && lane >= j) {
-      sv = G[j * OB + lane];
-      for (int l = 0; l < j; ++l) sv -= R[l * OB + j] * R[l * OB + lane];
-    }
-    const float d = __shfl_sync(0xFFFFFFFFu, sv, j);
+#pragma unroll
+  for (int j = 0; j < OB; ++j) {
+    if (j >= b) break;  // warp-uniform
+    const float d = __shfl_sync(0xFFFFFFFFu, col[j], j);
     const bool keep = d > thr[j];
     const float rjj = keep ? sqrtf(d) : 0.f;
-    if (lane < b) R[j * OB + lane] = (keep && lane >= j) ? (lane == j ? rjj : sv / rjj) : 0.f;
+    const float r = (keep && lane >= j) ? (lane == j ? rjj : col[j] / rjj) : 0.f;  // R(j, lane)
+    if (lane < b) R[j * OB + lane] = r;
     if (lane == 0) inv_diag[j] = keep ? 1.f / rjj : 0.f;
     if (keep) {
       rmax = fmaxf(rmax, rjj);
       rmin = fminf(rmin, rjj);
     }
-    __syncwarp();
+#pragma unroll
+    for (int i = j + 1; i < OB; ++i) col[i] = fmaf(-__shfl_sync(0xFFFFFFFFu, r, i), r, col[i]);
   }
-  if (lane == 0) *cond = rmax > 0.f ? rmax / rmin : 1.f;  // ratio of the largest to the smallest kept pivot
+  __syncwarp();
+  if (lane == 0) *cond = rmax > 0.f ? rmax / rmin : 1.f;
 }
 
 // X <- X R^{-1} row by row (forward substitution), R upper triangular, dropped
@@ -465,6 +491,195 @@ __device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, 
   }
 }
 
+// ---- tall-skinny primitives on the tensor cores (3xTF32) -------------------------------------
+// x = hi + lo with hi = x rounded to tf32 (half an ulp added to the bits, the low 13
+// cleared) and lo = x - hi (exact in fp32), rounded to tf32 the same way when the MMA
+// reads it.  A product a b is taken as lo_a hi_b + hi_a lo_b + hi_a hi_b: only
+// lo_a lo_b and the rounding of the lo parts are lost (below 2^-21 of |a b|), so the
+// sums keep close to fp32 accuracy -- enough for the drop rule at 1e-8 of a squared
+// norm -- at tensor-core speed.
+__device__ __forceinline__ void split3(float x, uint32_t& hi, uint32_t& lo) {
+  const uint32_t h = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+  hi = h;
+  lo = __float_as_uint(x - __uint_as_float(h)) + 0x1000u;
+}
+
+__device__ __forceinline__ void mma3(float* d, const uint32_t* ah, const uint32_t* al, const uint32_t* bh,
+                                     const uint32_t* bl) {
+  mma_tf32(d, al, bh);
+  mma_tf32(d, ah, bl);
+  mma_tf32(d, ah, bh);
+}
+
+__device__ __forceinline__ float4 ld4_or0(const float* p, bool ok) {
+  return ok ? *reinterpret_cast<const float4*>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ float2 ld2_or0(const float* p, bool ok) {
+  return ok ? *reinterpret_cast<const float2*>(p) : make_float2(0.f, 0.f);
+}
+__device__ __forceinline__ float f4_at(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+constexpr int TN_P = 48;  // columns of P per pass of tn_mma
+
+// C[p][q] = sum_r P(r, p) Q(r, q) for p < a, q < b (b <= 16): P and Q column-major
+// panels of n rows (column j at P + j*n; n a multiple of 4, columns 16-byte
+// aligned), C row-major with row stride ldc.  Rows go to the warps in chunks of 16;
+// in a chunk lane (g, t4) loads rows 4t4 .. 4t4+3 of each of its columns as one
+// float4, and the chunk's two MMA K steps s = 0, 1 give K indexes t4 and t4 + 4 to
+// rows 4t4 + 2s and 4t4 + 2s + 1 (a permutation of the rows, which the sum does not
+// see).  The warps' partial sums meet in scr (8 x TN_P x 16 floats of shared
+// memory) and are added in warp order.
+__device__ void tn_mma(float* C, int ldc, const float* P, int a, const float* Q, int b, int n, float* scr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
+  const int nch = (n + 15) >> 4;
+  for (int p0 = 0; p0 < a; p0 += TN_P) {
+    const int ap = min(TN_P, a - p0);
+    float acc[3][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 3; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+#pragma unroll 1
+    for (int ch = warp; ch < nch; ch += 8) {
+      const int r = 16 * ch + 4 * t4;
+      const bool rok = r < n;  // n % 4 == 0: a float4 is wholly inside or wholly outside
+      float4 pv[3][2], qv[2];
+#pragma unroll
+      for (int mt = 0; mt < 3; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = p0 + 16 * mt + 8 * h + g;
+          pv[mt][h] = ld4_or0(P + (int64_t)c * n + r, rok && 16 * mt < ap && c < a);
+        }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 8 * nt + g;
+        qv[nt] = ld4_or0(Q + (int64_t)c * n + r, rok && c < b);
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          split3(f4_at(qv[nt], 2 * s2), bh[nt][0], bl[nt][0]);
+          split3(f4_at(qv[nt], 2 * s2 + 1), bh[nt][1], bl[nt][1]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 3; ++mt) {
+          if (16 * mt >= ap) break;  // warp-uniform
+          uint32_t ah[4], al[4];
+          split3(f4_at(pv[mt][0], 2 * s2), ah[0], al[0]);      // (g, t4)
+          split3(f4_at(pv[mt][1], 2 * s2), ah[1], al[1]);      // (g + 8, t4)
+          split3(f4_at(pv[mt][0], 2 * s2 + 1), ah[2], al[2]);  // (g, t4 + 4)
+          split3(f4_at(pv[mt][1], 2 * s2 + 1), ah[3], al[3]);  // (g + 8, t4 + 4)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+            if (8 * nt < b) mma3(acc[mt][nt], ah, al, bh[nt], bl[nt]);
+        }
+      }
+    }
+    float* sw = scr + warp * (TN_P * OB);
+#pragma unroll
+    for (int mt = 0; mt < 3; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sw[(16 * mt + g + 8 * (e >> 1)) * OB + 8 * nt + 2 * t4 + (e & 1)] = acc[mt][nt][e];
+    __syncthreads();
+    for (int e = threadIdx.x; e < ap * OB; e += THREADS) {
+      const int pp = e / OB, q = e % OB;
+      if (q < b) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < THREADS / 32; ++w) sum += scr[w * (TN_P * OB) + e];
+        C[(p0 + pp) * ldc + q] = sum;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// X(r, q) = (kAcc ? X(r, q) : 0) + sum_{p < a} P(r, p) sgn M[p][q] for q < b (b <= 16):
+// X and P column-major panels of n rows (n a multiple of 4, columns 16-byte aligned),
+// M row-major in shared memory with row stride ldm.  Rows go to the warps in tiles
+// of 16; MMA row g of a tile is row 2g and MMA row g + 8 is row 2g + 1, so a lane's
+// A values of one column, and its accumulator pairs, are one float2 each.  P may
+// be X itself when kAcc is false: a tile is read in full (every lane's values
+// enter the warp's MMAs) before any of it is written.
+template <bool kAcc>
+__device__ void mm_mma(float* X, int b, const float* P, int a, const float* M, int ldm, float sgn, int n) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
+  const int ntile = (n + 15) >> 4;
+#pragma unroll 1
+  for (int tile = warp; tile < ntile; tile += 8) {
+    const int r = 16 * tile + 2 * g;
+    const bool rok = r < n;  // n even: rows r and r + 1 are both inside or both outside
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int c = 8 * nt + 2 * t4;
+      const float2 u = ld2_or0(X + (int64_t)c * n + r, kAcc && rok && c < b);
+      const float2 v = ld2_or0(X + (int64_t)(c + 1) * n + r, kAcc && rok && c + 1 < b);
+      acc[nt][0] = u.x;  // (g, 2t4)
+      acc[nt][1] = v.x;  // (g, 2t4 + 1)
+      acc[nt][2] = u.y;  // (g + 8, 2t4)
+      acc[nt][3] = v.y;  // (g + 8, 2t4 + 1)
+    }
+#pragma unroll 4
+    for (int k0 = 0; k0 < a; k0 += 8) {
+      const int c0 = k0 + t4, c1 = k0 + t4 + 4;
+      const float2 v0 = ld2_or0(P + (int64_t)c0 * n + r, rok && c0 < a);
+      const float2 v1 = ld2_or0(P + (int64_t)c1 * n + r, rok && c1 < a);
+      uint32_t ah[4], al[4];
+      split3(v0.x, ah[0], al[0]);  // (g, t4)
+      split3(v0.y, ah[1], al[1]);  // (g + 8, t4)
+      split3(v1.x, ah[2], al[2]);  // (g, t4 + 4)
+      split3(v1.y, ah[3], al[3]);  // (g + 8, t4 + 4)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        if (8 * nt >= b) break;  // warp-uniform
+        const int j = 8 * nt + g;
+        uint32_t bh[2], bl[2];
+        split3(c0 < a && j < b ? sgn * M[c0 * ldm + j] : 0.f, bh[0], bl[0]);
+        split3(c1 < a && j < b ? sgn * M[c1 * ldm + j] : 0.f, bh[1], bl[1]);
+        mma3(acc[nt], ah, al, bh, bl);
+      }
+    }
+    if (rok) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 8 * nt + 2 * t4;
+        if (c < b) *reinterpret_cast<float2*>(X + (int64_t)c * n + r) = make_float2(acc[nt][0], acc[nt][2]);
+        if (c + 1 < b) *reinterpret_cast<float2*>(X + (int64_t)(c + 1) * n + r) = make_float2(acc[nt][1], acc[nt][3]);
+      }
+    }
+  }
+}
+
+// M with X R^{-1} = X M in the sense of ts_trsm's forward substitution (a dropped
+// column j, inv_diag[j] = 0, gives a zero column of M): row i of M is that
+// substitution applied to the unit row e_i, computed by lane i of one warp.
+// M row-major with row stride OB; rows and columns from b on are left unwritten.
+__device__ void tri_inv(const float* R, const float* inv_diag, float* M, int b) {
+  const int lane = threadIdx.x & 31;
+  float x[OB];
+#pragma unroll
+  for (int j = 0; j < OB; ++j) {
+    float v = j == lane ? 1.f : 0.f;
+#pragma unroll
+    for (int l = 0; l < j; ++l) v = fmaf(-x[l], R[l * OB + j], v);
+    x[j] = j < b ? v * inv_diag[j < b ? j : 0] : 0.f;
+  }
+  if (lane < b)
+#pragma unroll
+    for (int j = 0; j < OB; ++j)
+      if (j < b) M[lane * OB + j] = x[j];
+}
+
 // Orthonormalise the k columns (length n, column j at X + j*n) in place, one
 // block of 16 columns at a time: the block is projected off the finished
 // columns (classical block Gram-Schmidt), a second time when a column lost
@@ -473,31 +688,48 @@ __device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, 
 // QR (Gram matrix, Cholesky, triangular solve), a second time when the first
 // Cholesky factor is ill-conditioned (largest / smallest pivot above 16).  A
 // column whose remainder falls below 1e-4 of its original norm is dependent
-// and becomes zero (its Cholesky pivot is dropped).
-// Scratch (shared): cblk [kp][OB], gram [OB][OB], rmat [OB][OB], inv_diag [OB],
-// thr [OB], orig [OB] (squared original norms), cond [1].
-__device__ void orth_block(float* X, int n, int k, float* cblk, float* gram, float* rmat, float* inv_diag,
-                           float* thr) {
+// and becomes zero (its Cholesky pivot is dropped).  One pass over the first
+// J0 + 16 columns gives both the first projection coefficients and the block's
+// original Gram matrix.  kTC: the panel products on the tensor cores (3xTF32;
+// n a multiple of 4, columns 16-byte aligned) and the solve as a product with
+// the inverse factor; else the fp32 warp primitives.
+// Scratch (shared): cblk [kp][OB] (coefficients above row J0, the block's Gram
+// matrix from row J0), minv [OB][OB], rmat [OB][OB], inv_diag [OB], thr [OB],
+// orig [OB] (squared original norms), cond [1]; scr 8*TN_P*OB floats (kTC).
+template <bool kTC>
+__device__ void orth_block(float* X, int n, int k, float* cblk, float* minv, float* rmat, float* inv_diag, float* thr,
+                           float* scr) {
   float* orig = thr + OB;
   float* cond = orig + OB;
+  auto tn = [&](float* C, const float* P, int a, const float* Q, int b) {
+    if constexpr (kTC)
+      tn_mma(C, OB, P, a, Q, b, n, scr);
+    else
+      ts_tn(C, OB, P, a, Q, b, n);
+  };
   for (int J0 = 0; J0 < k; J0 += OB) {
     const int b = min(OB, k - J0);
     float* XJ = X + (int64_t)J0 * n;
-    // squared original norms -> drop thresholds (1e-4 of the norm)
-    ts_tn(gram, OB, XJ, b, XJ, b, n);
+    float* gram = cblk + J0 * OB;
+    tn(cblk, X, J0 + b, XJ, b);  // [Q_< | X_J]^T X_J
     __syncthreads();
-    if (threadIdx.x < b) {
+    if (threadIdx.x < b) {  // squared original norms -> drop thresholds (1e-4 of the norm)
       orig[threadIdx.x] = gram[threadIdx.x * OB + threadIdx.x];
       thr[threadIdx.x] = 1e-8f * orig[threadIdx.x];
     }
     __syncthreads();
     bool fresh_gram = true;  // gram holds the Gram matrix of the current X_J
     for (int pass = 0; pass < 2 && J0 > 0; ++pass) {
-      ts_tn(cblk, OB, X, J0, XJ, b, n);  // cblk [J0][b] = Q_<^T X_J
+      if (pass == 1) {
+        tn(cblk, X, J0, XJ, b);  // cblk [J0][b] = Q_<^T X_J
+        __syncthreads();
+      }
+      if constexpr (kTC)  // X_J -= Q_< cblk
+        mm_mma<true>(XJ, b, X, J0, cblk, OB, -1.f, n);
+      else
+        ts_update(XJ, b, X, J0, cblk, OB, n);
       __syncthreads();
-      ts_update(XJ, b, X, J0, cblk, OB, n);  // X_J -= Q_< cblk
-      __syncthreads();
-      ts_tn(gram, OB, XJ, b, XJ, b, n);
+      tn(gram, XJ, b, XJ, b);
       __syncthreads();
       bool again = false;
       for (int j = 0; j < b; ++j) again |= gram[j * OB + j] < 0.5f * orig[j];
@@ -506,16 +738,23 @@ __device__ void orth_block(float* X, int n, int k, float* cblk, float* gram, flo
     }
     for (int pass = 0; pass < 2; ++pass) {
       if (!fresh_gram) {
-        ts_tn(gram, OB, XJ, b, XJ, b, n);
+        tn(gram, XJ, b, XJ, b);
         __syncthreads();
       }
       if (threadIdx.x < 32) {
         if (pass == 1 && threadIdx.x < b) thr[threadIdx.x] = 1e-8f * gram[threadIdx.x * OB + threadIdx.x];
         __syncwarp();
         chol_drop(gram, rmat, inv_diag, thr, b, cond);
+        if constexpr (kTC) {
+          __syncwarp();
+          tri_inv(rmat, inv_diag, minv, b);
+        }
       }
       __syncthreads();
-      ts_trsm(XJ, b, rmat, inv_diag, n);
+      if constexpr (kTC)
+        mm_mma<false>(XJ, b, XJ, b, minv, OB, 1.f, n);
+      else
+        ts_trsm(XJ, b, rmat, inv_diag, n);
       const bool again = *cond > 16.f;
       __syncthreads();
       fresh_gram = false;
@@ -610,8 +849,8 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   float* rot = cblk + kp * OB;        // 2*kp
   float* red = rot + 2 * kp;          // 32
   int* perm = reinterpret_cast<int*>(red + 32);  // kp
-  float* gram = red + 32 + kp;        // OB*OB
-  float* rmat = gram + OB * OB;       // OB*OB
+  float* minv = red + 32 + kp;        // OB*OB
+  float* rmat = minv + OB * OB;       // OB*OB
   float* inv_diag = rmat + OB * OB;   // OB
   float* thr = inv_diag + OB;         // OB, then orig (OB) and cond (1) for orth_block
 
@@ -624,30 +863,38 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   // the cp.async path needs 16-byte chunks that never straddle an edge
   const bool ring_ok = ((T | D | k) & 3) == 0 && (p.delta_stride & 3) == 0 &&
                        ((reinterpret_cast<uintptr_t>(p.delta) | reinterpret_cast<uintptr_t>(p.omega)) & 15u) == 0;
+  // the tensor-core panel primitives need 16-byte aligned panel columns
+  const bool panel_ok = ((T | D) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.work) & 15u) == 0;
+  auto orth = [&](float* X, int n) {
+    if (panel_ok)
+      orth_block<true>(X, n, k, cblk, minv, rmat, inv_diag, thr, ring);
+    else
+      orth_block<false>(X, n, k, cblk, minv, rmat, inv_diag, thr, ring);
+  };
   for (int s = blockIdx.x; s < p.n_slabs; s += gridDim.x) {
     const float* A = p.delta + (int64_t)s * p.delta_stride;  // [T][D]
     // Y = Delta Omega (columns k..kp-1 stay zero)
     for (int64_t e = threadIdx.x; e < (int64_t)kp * T; e += THREADS) Y[e] = 0.f;
     __syncthreads();
     if (ring_ok)
-      gemm_tc<float, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
+      gemm_tc<float, true, false, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
     else
       gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
-    orth_block(Y, T, k, cblk, gram, rmat, inv_diag, thr);
+    orth(Y, T);
     for (int it = 0; it < p.power_iters; ++it) {
       if (ring_ok)  // Z = Delta^T Q
-        gemm_tc<float, false, true>(D, k, T, A, D, Y, T, Z, 1, D, ring);
+        gemm_tc<float, false, true, true, false>(D, k, T, A, D, Y, T, Z, 1, D, ring);
       else
         gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);
-      orth_block(Z, D, k, cblk, gram, rmat, inv_diag, thr);
+      orth(Z, D);
       if (ring_ok)  // Y = Delta Z
-        gemm_tc<float, true, true>(T, k, D, A, D, Z, D, Y, 1, T, ring);
+        gemm_tc<float, true, true, true, false>(T, k, D, A, D, Z, D, Y, 1, T, ring);
       else
         gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);
-      orth_block(Y, T, k, cblk, gram, rmat, inv_diag, thr);
+      orth(Y, T);
     }
     if (ring_ok)  // B = Q^T Delta
-      gemm_tc<float, true, false>(k, D, T, Y, T, A, D, B, D, 1, ring);
+      gemm_tc<float, true, false, false, true>(k, D, T, Y, T, A, D, B, D, 1, ring);
     else
       gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);
     for (int e = threadIdx.x; e < kp * kp; e += THREADS) C[e] = 0.f;

@@ -782,12 +782,12 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
     off = block_sum(off, red);
     tot = block_sum(tot, red);
     if (off <= 1e-10f * tot || tot == 0.f) break;
+    // pair tid of round r: players a = 1 + (tid - 1 + r) mod (kp - 1) (0 for tid 0) and
+    // b = 1 + (kp - 2 - tid + r) mod (kp - 1) of the rotated ring, stepped without division
+    int pa = tid == 0 ? 0 : tid, pb = kp - 1 - tid;
     for (int round = 0; round < kp - 1; ++round) {
-      // pair i: players (i, kp-1-i) of the rotated ring; player 0 stays fixed
       if (tid < half) {
-        int a = tid == 0 ? 0 : 1 + (tid - 1 + round) % (kp - 1);
-        int b = 1 + (kp - 2 - tid + round) % (kp - 1);
-        int p = min(a, b), q = max(a, b);
+        const int p = min(pa, pb), q = max(pa, pb);
         const float app = C[p * kp + p], aqq = C[q * kp + q], apq = C[p * kp + q];
         float c = 1.f, s = 0.f;
         if (apq != 0.f && fabsf(apq) > 1e-30f) {
@@ -796,35 +796,41 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
           c = rsqrtf(1.f + t * t);
           s = c * t;
         }
-        rot[4 * tid + 0] = (float)p;
-        rot[4 * tid + 1] = (float)q;
-        rot[4 * tid + 2] = c;
-        rot[4 * tid + 3] = s;
+        *reinterpret_cast<float4*>(rot + 4 * tid) = make_float4(__int_as_float(p), __int_as_float(q), c, s);
+        if (tid > 0) pa = pa == kp - 1 ? 1 : pa + 1;
+        pb = pb == kp - 1 ? 1 : pb + 1;
       }
       __syncthreads();
-      // rows p, q of C  (C <- J^T C)
-      for (int e = tid; e < half * kp; e += THREADS) {
-        const int i = e / kp, j = e % kp;
-        const int p = (int)rot[4 * i], q = (int)rot[4 * i + 1];
-        const float c = rot[4 * i + 2], s = rot[4 * i + 3];
-        const float xp = C[p * kp + j], xq = C[q * kp + j];
-        C[p * kp + j] = c * xp - s * xq;
-        C[q * kp + j] = s * xp + c * xq;
+      // The pairs are disjoint and cover every index, so C splits into 2x2 blocks
+      // B_ij (rows p_i, q_i; columns p_j, q_j), each of which becomes G_i B_ij G_j^T
+      // with G = [c -s; s c]; W <- W G^T on the column pairs.  One step, each
+      // element read and written once.
+      for (int i = tid >> 3; i < half; i += THREADS / 8) {
+        const float4 ri = *reinterpret_cast<const float4*>(rot + 4 * i);
+        const int pi = __float_as_int(ri.x), qi = __float_as_int(ri.y);
+        for (int j = tid & 7; j < half; j += 8) {
+          const float4 rj = *reinterpret_cast<const float4*>(rot + 4 * j);
+          const int pj = __float_as_int(rj.x), qj = __float_as_int(rj.y);
+          const float b00 = C[pi * kp + pj], b01 = C[pi * kp + qj], b10 = C[qi * kp + pj], b11 = C[qi * kp + qj];
+          // rows: G_i B
+          const float u00 = ri.z * b00 - ri.w * b10, u01 = ri.z * b01 - ri.w * b11;
+          const float u10 = ri.w * b00 + ri.z * b10, u11 = ri.w * b01 + ri.z * b11;
+          // columns: (G_i B) G_j^T
+          C[pi * kp + pj] = rj.z * u00 - rj.w * u01;
+          C[pi * kp + qj] = rj.w * u00 + rj.z * u01;
+          C[qi * kp + pj] = rj.z * u10 - rj.w * u11;
+          C[qi * kp + qj] = rj.w * u10 + rj.z * u11;
+        }
       }
-      __syncthreads();
-      // columns p, q of C and of W  (C <- C J, W <- W J); consecutive threads
-      // take different planes so that the column accesses spread over banks
-      for (int e = tid; e < half * kp; e += THREADS) {
-        const int i = e % half, j = e / half;
-        const int p = (int)rot[4 * i], q = (int)rot[4 * i + 1];
-        const float c = rot[4 * i + 2], s = rot[4 * i + 3];
-        float xp = C[j * kp + p], xq = C[j * kp + q];
-        C[j * kp + p] = c * xp - s * xq;
-        C[j * kp + q] = s * xp + c * xq;
-        xp = W[j * kp + p];
-        xq = W[j * kp + q];
-        W[j * kp + p] = c * xp - s * xq;
-        W[j * kp + q] = s * xp + c * xq;
+      for (int jr = tid >> 2; jr < kp; jr += THREADS / 4) {
+        float* w = W + jr * kp;
+        for (int i = tid & 3; i < half; i += 4) {
+          const float4 ri = *reinterpret_cast<const float4*>(rot + 4 * i);
+          const int pi = __float_as_int(ri.x), qi = __float_as_int(ri.y);
+          const float xp = w[pi], xq = w[qi];
+          w[pi] = ri.z * xp - ri.w * xq;
+          w[qi] = ri.w * xp + ri.z * xq;
+        }
       }
       __syncthreads();
     }

@@ -44,6 +44,8 @@ UNIT = "tokens/s"
 KERNEL_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_kernel.cuh",
                   "position_invariant_kv_kamera_gb300/csrc/ptx.cuh",
                   "position_invariant_kv_kamera_gb300/csrc/kamera_api.cu"]
+FACTOR_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_factor.cuh",
+                  "position_invariant_kv_kamera_gb300/csrc/kamera_api.cu"]
 DESCRIPTIONS = {
     "gqa_video": "GQA Qwen2.5-VL-7B-shaped: 28 layers, 4 KV heads x 128, base 1e6, 16 chunks x 1024 tokens, "
                  "1% outlier channels x8, rank-32 patch per layer per K/V, delta in [-32768, 32768], "
@@ -61,9 +63,9 @@ DESCRIPTIONS = {
 COMPRESSED = {"gqa_video_compressed": "gqa_video"}
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources: list[str] = KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -76,15 +78,15 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profile_traffic(workload: str) -> float | None:
+def profile_traffic(workload: str, kernel: str = "reuse_kernel", sources: list[str] = KERNEL_SOURCES) -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, if it was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"reuse_kernel_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", txt)
-    if not h or h.group(1) != kernel_hash():
+    if not h or h.group(1) != kernel_hash(sources):
         return None
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if m:
@@ -552,12 +554,20 @@ def run_factor(args) -> None:
             "config": {"workload": f"{n} slabs of {T}x{D} (16 patches x 28 layers x K/V of the GQA video shape), "
                                    f"rank {m}, oversample {p}, {q} subspace iterations, deficit rank {r}"},
             "roofline": {"bound": "alu", "achieved": flops / sec / 1e12, "peak": peak, "unit": "TFLOP/s",
-                         "frac": flops / sec / 1e12 / peak, "traffic": None,
+                         "frac": flops / sec / 1e12 / peak,
+                         "traffic": profile_traffic("patch_formation", "factor_kernel", FACTOR_SOURCES),
                          "peak_source": f"derived: {sms} SMs x 128 fp32 FMA lanes x 2 flops x 2.07 GHz"},
             "cpu_baseline": {"value": 1.0 / cpu_s, "unit": "slabs/s", "cores": 1, "kind": "oracle",
                              "sample": f"one {T}x{D} slab, exact one-sided Jacobi SVD ({cpu_s:.1f} s)"},
             "gpu_launches": steps, "clocks": clocks.summary()}
     print(_json.dumps(line), flush=True)
+
+
+def orbit_traffic(slabs: int) -> float | None:
+    """DRAM bytes per launch of the orbit mean over `slabs` slabs: the committed
+    capture (scaled to 896 slabs) scaled by the slabs processed."""
+    t = profile_traffic("orbit_mean", "orbit_mean_kernel", FACTOR_SOURCES)
+    return t * slabs / 896 if t is not None else None
 
 
 def run_orbit(args) -> None:
@@ -603,7 +613,8 @@ def run_orbit(args) -> None:
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"{n_ord} orderings x {slabs} slabs of 1024x512 fp32 deficits"},
             "roofline": {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": nbytes / sec / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                         "frac": nbytes / sec / 1e9 / peaks["hbm_gbs"],
+                         "traffic": orbit_traffic(slabs),
                          "frac_of_nominal": nbytes / sec / 1e9 / NOMINAL_HBM_GBS,
                          "peak_source": peaks["source"] + " (burst copy)"},
             "cpu_baseline": {"value": (1 << 24) / (1024 * 512) / cpu_s, "unit": "slabs/s", "cores": 1,

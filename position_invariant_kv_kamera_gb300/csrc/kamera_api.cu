@@ -643,6 +643,31 @@ kamera_status factor_shape(const kamera_factor_desc* d, FactorShape* fs) {
   return KAMERA_OK;
 }
 
+// The aligned instance when the shapes and pointers allow it (the conditions of
+// factor_kernel<true>), else the one with run-time fallbacks.
+kamera_status launch_factor(const factor::FParams& fp, int grid, uint32_t smem, kamera_stream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    const int most = (int)factor::factor_smem_bytes(factor::KMAX, 64);
+    attr_err = cudaFuncSetAttribute(factor::factor_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(factor::factor_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+  });
+  if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  const bool aligned = ((fp.T | fp.D | fp.k) & 3) == 0 && (fp.delta_stride & 3) == 0 &&
+                       ((reinterpret_cast<uintptr_t>(fp.delta) | reinterpret_cast<uintptr_t>(fp.omega) |
+                         reinterpret_cast<uintptr_t>(fp.work)) & 15u) == 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (aligned)
+    factor::factor_kernel<true><<<grid, factor::THREADS, smem, s>>>(fp);
+  else
+    factor::factor_kernel<false><<<grid, factor::THREADS, smem, s>>>(fp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return KAMERA_OK;
+}
+
 kamera_status factor_workspace_size(const kamera_factor_desc* d, size_t* bytes) {
   g_last_error.clear();
   if (!bytes) return fail(KAMERA_ERR_NULL, "bytes is NULL");
@@ -685,19 +710,7 @@ kamera_status factor_patches(const kamera_factor_desc* d, void* u_out, void* v_o
   fp.work = static_cast<float*>(workspace);
   fp.work_per_cta = fs.work_per_cta;
   const uint32_t smem = factor::factor_smem_bytes(fs.kp, d->rank);
-  {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)factor::factor_smem_bytes(factor::KMAX, 64));
-    });
-    if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  }
-  factor::factor_kernel<<<fs.grid, factor::THREADS, smem, reinterpret_cast<cudaStream_t>(stream)>>>(fp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-  return KAMERA_OK;
+  return launch_factor(fp, fs.grid, smem, stream);
 }
 
 kamera_status orbit_mean(const float* deltas, int32_t n, int64_t stride, int64_t n_elems, float* out,
@@ -789,19 +802,7 @@ kamera_status factor_patches_noalloc(const kamera_factor_desc* d, void* u_out, v
   fp.work = scratch;
   fp.work_per_cta = fs.work_per_cta;
   const uint32_t smem = factor::factor_smem_bytes(fs.kp, d->rank);
-  {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-      attr_err = cudaFuncSetAttribute(factor::factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)factor::factor_smem_bytes(factor::KMAX, 64));
-    });
-    if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  }
-  factor::factor_kernel<<<grid, factor::THREADS, smem, reinterpret_cast<cudaStream_t>(stream)>>>(fp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-  return KAMERA_OK;
+  return launch_factor(fp, grid, smem, stream);
 }
 
 }  // namespace

@@ -842,6 +842,11 @@ __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
   return 2 * TC_STAGES * TC_TILE + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
 }
 
+// kAligned: T, D, k and the slab stride are multiples of 4 and Delta, Omega and the
+// workspace are 16-byte aligned (the host checks it), so every product takes the
+// tensor-core path and the fp32 fallbacks are not compiled in -- they would set the
+// register budget of the whole kernel.
+template <bool kAligned>
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
   extern __shared__ __align__(16) float fsm[];
   const int T = p.T, D = p.D, k = p.k, kp = p.kp, m = p.m;
@@ -867,10 +872,11 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   // rows k..kp-1 of B are never written: keep them zero for the V_m product
   for (int64_t e = (int64_t)k * D + threadIdx.x; e < (int64_t)kp * D; e += THREADS) B[e] = 0.f;
   // the cp.async path needs 16-byte chunks that never straddle an edge
-  const bool ring_ok = ((T | D | k) & 3) == 0 && (p.delta_stride & 3) == 0 &&
-                       ((reinterpret_cast<uintptr_t>(p.delta) | reinterpret_cast<uintptr_t>(p.omega)) & 15u) == 0;
+  const bool ring_ok = kAligned || (((T | D | k) & 3) == 0 && (p.delta_stride & 3) == 0 &&
+                                    ((reinterpret_cast<uintptr_t>(p.delta) | reinterpret_cast<uintptr_t>(p.omega)) &
+                                     15u) == 0);
   // the tensor-core panel primitives need 16-byte aligned panel columns
-  const bool panel_ok = ((T | D) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.work) & 15u) == 0;
+  const bool panel_ok = kAligned || (((T | D) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.work) & 15u) == 0);
   auto orth = [&](float* X, int n) {
     if (panel_ok)
       orth_block<true>(X, n, k, cblk, minv, rmat, inv_diag, thr, ring);

@@ -837,9 +837,137 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
   }
 }
 
+// ---- tall-skinny tensor-core GEMM: all of N (<= 48) in one tile ------------------------------
+// C = alpha * A B for N <= TN: output tiles of TM x TN, warp w owns rows 32 (w & 3) .. +31
+// and columns 24 (w >> 2) .. +23 (two m16 x three n8 fragments), so that no warp idles at
+// N = 48 and the skinny operand is re-read once per 128 rows.  Operands stream through
+// TALL_STAGES stages of K = TK as in gemm_tc, with its layouts, edge rules and rounding.
+constexpr int TM = 128, TN = 48;
+constexpr int GPA = TM + 8, GPB = TN + 8;  // row strides of M/N-contiguous tiles (conflict-free fragment reads)
+constexpr int TALL_STAGES = 3;
+constexpr int TALL_A = TM * TKS > TK * GPA ? TM * TKS : TK * GPA;
+constexpr int TALL_B = TN * TKS > TK * GPB ? TN * TKS : TK * GPB;
+constexpr int TALL_STAGE = TALL_A + TALL_B;
+constexpr int RING_FLOATS =
+    2 * TC_STAGES * TC_TILE > TALL_STAGES * TALL_STAGE ? 2 * TC_STAGES * TC_TILE : TALL_STAGES * TALL_STAGE;
+
+template <typename OutT, bool kAK, bool kBK, bool kStreamA, bool kStreamB>
+__device__ void gemm_tall(int M, int N, int K, const float* A, int64_t a_ld, const float* B, int64_t b_ld, OutT* C,
+                          int64_t c_rs, int64_t c_cs, float* ring, float alpha = 1.f) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = 32 * (warp & 3), wn = 24 * (warp >> 2);
+  const int g = lane >> 2, t4 = lane & 3;
+  const uint64_t pol = evict_first_policy();
+  const int nsteps = (K + TK - 1) / TK;
+  for (int i0 = 0; i0 < M; i0 += TM) {
+    auto load_stage = [&](int slot, int l0) {
+      float* sA = ring + slot * TALL_STAGE;
+      float* sB = sA + TALL_A;
+#pragma unroll
+      for (int h = 0; h < TM * TK / 4 / THREADS; ++h) {  // four 16-byte chunks of A per thread
+        const int c = tid + THREADS * h;
+        int i, l, soff;
+        if (kAK) { i = c >> 3; l = 4 * (c & 7); soff = i * TKS + l; }
+        else     { l = c >> 5; i = 4 * (c & 31); soff = l * GPA + i; }
+        const bool ok = i0 + i < M && l0 + l < K;
+        const float* src =
+            ok ? (kAK ? A + (int64_t)(i0 + i) * a_ld + l0 + l : A + (i0 + i) + (int64_t)(l0 + l) * a_ld) : A;
+        if (kStreamA)
+          cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u, pol);
+        else
+          cp_async16(smem_u32(sA + soff), src, ok ? 16u : 0u);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // 384 chunks of B
+        const int c = tid + THREADS * h;
+        if (c < TN * TK / 4) {
+          int j, l, soff;
+          if (kBK) { j = c >> 3; l = 4 * (c & 7); soff = j * TKS + l; }
+          else     { l = c / (TN / 4); j = 4 * (c % (TN / 4)); soff = l * GPB + j; }
+          const bool ok = j < N && l0 + l < K;
+          const float* src = ok ? (kBK ? B + (int64_t)j * b_ld + l0 + l : B + (int64_t)(l0 + l) * b_ld + j) : B;
+          if (kStreamB)
+            cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u, pol);
+          else
+            cp_async16(smem_u32(sB + soff), src, ok ? 16u : 0u);
+        }
+      }
+    };
+    float acc[2][3][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 3; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[a][b][e] = 0.f;
+#pragma unroll
+    for (int st = 0; st < TALL_STAGES - 1; ++st) {
+      if (st < nsteps) load_stage(st, st * TK);
+      cp_async_commit();
+    }
+    for (int st = 0; st < nsteps; ++st) {
+      cp_async_wait<TALL_STAGES - 2>();
+      __syncthreads();  // stage st landed for every thread; stage st-1 is no longer read
+      const int nx = st + TALL_STAGES - 1;
+      if (nx < nsteps) load_stage(nx % TALL_STAGES, nx * TK);
+      cp_async_commit();
+      const float* sA = ring + (st % TALL_STAGES) * TALL_STAGE;
+      const float* sB = sA + TALL_A;
+      // tf32 rounding by half an ulp added to the bits, as in gemm_tc
+      auto at = [&](int i, int l) { return __float_as_uint(kAK ? sA[i * TKS + l] : sA[l * GPA + i]) + 0x1000u; };
+      auto bt = [&](int l, int j) { return __float_as_uint(kBK ? sB[j * TKS + l] : sB[l * GPB + j]) + 0x1000u; };
+#pragma unroll
+      for (int k8 = 0; k8 < TK; k8 += 8) {
+        uint32_t af[2][4], bf[3][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int r0 = wm + 16 * mt + g;
+          af[mt][0] = at(r0, k8 + t4);
+          af[mt][1] = at(r0 + 8, k8 + t4);
+          af[mt][2] = at(r0, k8 + t4 + 4);
+          af[mt][3] = at(r0 + 8, k8 + t4 + 4);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 3; ++nt) {
+          const int c0 = wn + 8 * nt + g;
+          bf[nt][0] = bt(k8 + t4, c0);
+          bf[nt][1] = bt(k8 + t4 + 4, c0);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 3; ++nt) {
+          if (wn + 8 * nt >= N) break;  // warp-uniform: columns past N are zero
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) mma_tf32(acc[mt][nt], af[mt], bf[nt]);
+        }
+      }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // the ring is reused by the next output tile
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int gi = i0 + wm + 16 * mt + g + 8 * (e >> 1);
+          const int gj = wn + 8 * nt + 2 * t4 + (e & 1);
+          if (gi < M && gj < N) {
+            const float v = alpha * acc[mt][nt][e];
+            if constexpr (sizeof(OutT) == 2) {
+              __nv_bfloat16 hv = __float2bfloat16_rn(v);
+              C[gi * c_rs + gj * c_cs] = *reinterpret_cast<uint16_t*>(&hv);
+            } else {
+              C[gi * c_rs + gj * c_cs] = v;
+            }
+          }
+        }
+  }
+  __syncthreads();
+}
+
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return 2 * TC_STAGES * TC_TILE + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
+  return RING_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
 }
 
 // kAligned: T, D, k and the slab stride are multiples of 4 and Delta, Omega and the
@@ -850,10 +978,10 @@ template <bool kAligned>
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
   extern __shared__ __align__(16) float fsm[];
   const int T = p.T, D = p.D, k = p.k, kp = p.kp, m = p.m;
-  float* ring = fsm;                  // 2*TC_STAGES*TC_TILE: the tensor-core GEMM's stages
+  float* ring = fsm;                  // RING_FLOATS: the tensor-core GEMMs' stages
   float* sA = ring;                   // the first two fp32-GEMM tiles overlay the ring
   float* sB = sA + TILE_FLOATS;
-  float* C = ring + 2 * TC_STAGES * TC_TILE;  // kp*kp
+  float* C = ring + RING_FLOATS;      // kp*kp
   float* W = C + kp * kp;             // kp*kp
   float* Ws = W + kp * kp;            // kp*m: sorted leading eigenvectors
   float* cblk = Ws + kp * m;          // kp*OB: projection coefficients of a column block
@@ -877,6 +1005,7 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
                                      15u) == 0);
   // the tensor-core panel primitives need 16-byte aligned panel columns
   const bool panel_ok = kAligned || (((T | D) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.work) & 15u) == 0);
+  const bool tall = ring_ok && kp <= TN;  // every product in one column tile
   auto orth = [&](float* X, int n) {
     if (panel_ok)
       orth_block<true>(X, n, k, cblk, minv, rmat, inv_diag, thr, ring);
@@ -888,24 +1017,32 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
     // Y = Delta Omega (columns k..kp-1 stay zero)
     for (int64_t e = threadIdx.x; e < (int64_t)kp * T; e += THREADS) Y[e] = 0.f;
     __syncthreads();
-    if (ring_ok)
+    if (tall)
+      gemm_tall<float, true, false, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
+    else if (ring_ok)
       gemm_tc<float, true, false, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
     else
       gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
     orth(Y, T);
     for (int it = 0; it < p.power_iters; ++it) {
-      if (ring_ok)  // Z = Delta^T Q
+      if (tall)  // Z = Delta^T Q
+        gemm_tall<float, false, true, true, false>(D, k, T, A, D, Y, T, Z, 1, D, ring);
+      else if (ring_ok)
         gemm_tc<float, false, true, true, false>(D, k, T, A, D, Y, T, Z, 1, D, ring);
       else
         gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);
       orth(Z, D);
-      if (ring_ok)  // Y = Delta Z
+      if (tall)  // Y = Delta Z
+        gemm_tall<float, true, true, true, false>(T, k, D, A, D, Z, D, Y, 1, T, ring);
+      else if (ring_ok)
         gemm_tc<float, true, true, true, false>(T, k, D, A, D, Z, D, Y, 1, T, ring);
       else
         gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);
       orth(Y, T);
     }
-    if (ring_ok)  // B = Q^T Delta
+    if (tall)  // B = Q^T Delta, formed as B^T = Delta^T Q (D x k, column j = row j of B)
+      gemm_tall<float, false, true, true, false>(D, k, T, A, D, Y, T, B, 1, D, ring);
+    else if (ring_ok)  // B = Q^T Delta
       gemm_tc<float, true, false, false, true>(k, D, T, Y, T, A, D, B, D, 1, ring);
     else
       gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);

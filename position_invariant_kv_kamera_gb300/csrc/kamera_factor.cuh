@@ -17,11 +17,13 @@
 //   B = Q^T Delta  [k][D];  C = B B^T = W Lambda W^T (cyclic Jacobi);
 //   U_m = Q W_m (orthonormal columns),  V_m = B^T W_m (carries Sigma).
 // The four products with Delta run on tensor cores (tf32 operands, fp32
-// accumulation); everything else is fp32 on the CUDA cores.  orth() works on
-// blocks of 16 columns: each block is projected off the finished columns
-// twice, then orthonormalised by Cholesky QR twice; a column whose remainder
-// falls below 1e-4 of its norm is dropped (set to zero), so deficits of rank
-// below k are handled exactly.
+// accumulation), and so do the panel products of orth() (3xTF32, about fp32
+// accuracy); the rest is fp32 on the CUDA cores.  orth() works on blocks of
+// 16 columns: each block is projected off the finished columns (again when a
+// column lost more than half its norm), then orthonormalised by Cholesky QR
+// (again when the factor is ill-conditioned); a column whose remainder falls
+// below 1e-4 of its norm is dropped (set to zero), so deficits of rank below
+// k are handled exactly.
 //
 // One CTA (256 threads, two per SM) per slab at a time; each CTA owns a
 // workspace region (Y [k][T], Z [k][D], B [k][D], column-major panels) in
@@ -514,9 +516,6 @@ __device__ __forceinline__ void mma3(float* d, const uint32_t* ah, const uint32_
 __device__ __forceinline__ float4 ld4_or0(const float* p, bool ok) {
   return ok ? *reinterpret_cast<const float4*>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
-__device__ __forceinline__ float2 ld2_or0(const float* p, bool ok) {
-  return ok ? *reinterpret_cast<const float2*>(p) : make_float2(0.f, 0.f);
-}
 __device__ __forceinline__ float f4_at(const float4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -603,83 +602,6 @@ __device__ void tn_mma(float* C, int ldc, const float* P, int a, const float* Q,
   }
 }
 
-// X(r, q) = (kAcc ? X(r, q) : 0) + sum_{p < a} P(r, p) sgn M[p][q] for q < b (b <= 16):
-// X and P column-major panels of n rows (n a multiple of 4, columns 16-byte aligned),
-// M row-major in shared memory with row stride ldm.  Rows go to the warps in tiles
-// of 16; MMA row g of a tile is row 2g and MMA row g + 8 is row 2g + 1, so a lane's
-// A values of one column, and its accumulator pairs, are one float2 each.  P may
-// be X itself when kAcc is false: a tile is read in full (every lane's values
-// enter the warp's MMAs) before any of it is written.
-template <bool kAcc>
-__device__ void mm_mma(float* X, int b, const float* P, int a, const float* M, int ldm, float sgn, int n) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
-  const int ntile = (n + 15) >> 4;
-#pragma unroll 1
-  for (int tile = warp; tile < ntile; tile += 8) {
-    const int r = 16 * tile + 2 * g;
-    const bool rok = r < n;  // n even: rows r and r + 1 are both inside or both outside
-    float acc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int c = 8 * nt + 2 * t4;
-      const float2 u = ld2_or0(X + (int64_t)c * n + r, kAcc && rok && c < b);
-      const float2 v = ld2_or0(X + (int64_t)(c + 1) * n + r, kAcc && rok && c + 1 < b);
-      acc[nt][0] = u.x;  // (g, 2t4)
-      acc[nt][1] = v.x;  // (g, 2t4 + 1)
-      acc[nt][2] = u.y;  // (g + 8, 2t4)
-      acc[nt][3] = v.y;  // (g + 8, 2t4 + 1)
-    }
-#pragma unroll 4
-    for (int k0 = 0; k0 < a; k0 += 8) {
-      const int c0 = k0 + t4, c1 = k0 + t4 + 4;
-      const float2 v0 = ld2_or0(P + (int64_t)c0 * n + r, rok && c0 < a);
-      const float2 v1 = ld2_or0(P + (int64_t)c1 * n + r, rok && c1 < a);
-      uint32_t ah[4], al[4];
-      split3(v0.x, ah[0], al[0]);  // (g, t4)
-      split3(v0.y, ah[1], al[1]);  // (g + 8, t4)
-      split3(v1.x, ah[2], al[2]);  // (g, t4 + 4)
-      split3(v1.y, ah[3], al[3]);  // (g + 8, t4 + 4)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        if (8 * nt >= b) break;  // warp-uniform
-        const int j = 8 * nt + g;
-        uint32_t bh[2], bl[2];
-        split3(c0 < a && j < b ? sgn * M[c0 * ldm + j] : 0.f, bh[0], bl[0]);
-        split3(c1 < a && j < b ? sgn * M[c1 * ldm + j] : 0.f, bh[1], bl[1]);
-        mma3(acc[nt], ah, al, bh, bl);
-      }
-    }
-    if (rok) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int c = 8 * nt + 2 * t4;
-        if (c < b) *reinterpret_cast<float2*>(X + (int64_t)c * n + r) = make_float2(acc[nt][0], acc[nt][2]);
-        if (c + 1 < b) *reinterpret_cast<float2*>(X + (int64_t)(c + 1) * n + r) = make_float2(acc[nt][1], acc[nt][3]);
-      }
-    }
-  }
-}
-
-// M with X R^{-1} = X M in the sense of ts_trsm's forward substitution (a dropped
-// column j, inv_diag[j] = 0, gives a zero column of M): row i of M is that
-// substitution applied to the unit row e_i, computed by lane i of one warp.
-// M row-major with row stride OB; rows and columns from b on are left unwritten.
-__device__ void tri_inv(const float* R, const float* inv_diag, float* M, int b) {
-  const int lane = threadIdx.x & 31;
-  float x[OB];
-#pragma unroll
-  for (int j = 0; j < OB; ++j) {
-    float v = j == lane ? 1.f : 0.f;
-#pragma unroll
-    for (int l = 0; l < j; ++l) v = fmaf(-x[l], R[l * OB + j], v);
-    x[j] = j < b ? v * inv_diag[j < b ? j : 0] : 0.f;
-  }
-  if (lane < b)
-#pragma unroll
-    for (int j = 0; j < OB; ++j)
-      if (j < b) M[lane * OB + j] = x[j];
-}
-
 // Orthonormalise the k columns (length n, column j at X + j*n) in place, one
 // block of 16 columns at a time: the block is projected off the finished
 // columns (classical block Gram-Schmidt), a second time when a column lost
@@ -690,15 +612,16 @@ __device__ void tri_inv(const float* R, const float* inv_diag, float* M, int b) 
 // column whose remainder falls below 1e-4 of its original norm is dependent
 // and becomes zero (its Cholesky pivot is dropped).  One pass over the first
 // J0 + 16 columns gives both the first projection coefficients and the block's
-// original Gram matrix.  kTC: the panel products on the tensor cores (3xTF32;
-// n a multiple of 4, columns 16-byte aligned) and the solve as a product with
-// the inverse factor; else the fp32 warp primitives.
+// original Gram matrix.  kTC: the coefficient and Gram products on the tensor
+// cores (3xTF32; n a multiple of 4, columns 16-byte aligned), else the fp32
+// warp primitives; the projection update and the triangular solve are fp32
+// row-per-thread loops either way (they keep more loads in flight than a warp
+// tile of MMAs does).
 // Scratch (shared): cblk [kp][OB] (coefficients above row J0, the block's Gram
-// matrix from row J0), minv [OB][OB], rmat [OB][OB], inv_diag [OB], thr [OB],
-// orig [OB] (squared original norms), cond [1]; scr 8*TN_P*OB floats (kTC).
+// matrix from row J0), rmat [OB][OB], inv_diag [OB], thr [OB], orig [OB]
+// (squared original norms), cond [1]; scr 8*TN_P*OB floats (kTC).
 template <bool kTC>
-__device__ void orth_block(float* X, int n, int k, float* cblk, float* minv, float* rmat, float* inv_diag, float* thr,
-                           float* scr) {
+__device__ void orth_block(float* X, int n, int k, float* cblk, float* rmat, float* inv_diag, float* thr, float* scr) {
   float* orig = thr + OB;
   float* cond = orig + OB;
   auto tn = [&](float* C, const float* P, int a, const float* Q, int b) {
@@ -724,10 +647,7 @@ __device__ void orth_block(float* X, int n, int k, float* cblk, float* minv, flo
         tn(cblk, X, J0, XJ, b);  // cblk [J0][b] = Q_<^T X_J
         __syncthreads();
       }
-      if constexpr (kTC)  // X_J -= Q_< cblk
-        mm_mma<true>(XJ, b, X, J0, cblk, OB, -1.f, n);
-      else
-        ts_update(XJ, b, X, J0, cblk, OB, n);
+      ts_update(XJ, b, X, J0, cblk, OB, n);  // X_J -= Q_< cblk
       __syncthreads();
       tn(gram, XJ, b, XJ, b);
       __syncthreads();
@@ -745,16 +665,9 @@ __device__ void orth_block(float* X, int n, int k, float* cblk, float* minv, flo
         if (pass == 1 && threadIdx.x < b) thr[threadIdx.x] = 1e-8f * gram[threadIdx.x * OB + threadIdx.x];
         __syncwarp();
         chol_drop(gram, rmat, inv_diag, thr, b, cond);
-        if constexpr (kTC) {
-          __syncwarp();
-          tri_inv(rmat, inv_diag, minv, b);
-        }
       }
       __syncthreads();
-      if constexpr (kTC)
-        mm_mma<false>(XJ, b, XJ, b, minv, OB, 1.f, n);
-      else
-        ts_trsm(XJ, b, rmat, inv_diag, n);
+      ts_trsm(XJ, b, rmat, inv_diag, n);
       const bool again = *cond > 16.f;
       __syncthreads();
       fresh_gram = false;
@@ -967,7 +880,7 @@ __device__ void gemm_tall(int M, int N, int K, const float* A, int64_t a_ld, con
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return RING_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + 2 * OB * OB + 3 * OB + 4;
+  return RING_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + OB * OB + 3 * OB + 4;
 }
 
 // kAligned: T, D, k and the slab stride are multiples of 4 and Delta, Omega and the
@@ -988,8 +901,7 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   float* rot = cblk + kp * OB;        // 2*kp
   float* red = rot + 2 * kp;          // 32
   int* perm = reinterpret_cast<int*>(red + 32);  // kp
-  float* minv = red + 32 + kp;        // OB*OB
-  float* rmat = minv + OB * OB;       // OB*OB
+  float* rmat = red + 32 + kp;        // OB*OB
   float* inv_diag = rmat + OB * OB;   // OB
   float* thr = inv_diag + OB;         // OB, then orig (OB) and cond (1) for orth_block
 
@@ -1008,9 +920,9 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   const bool tall = ring_ok && kp <= TN;  // every product in one column tile
   auto orth = [&](float* X, int n) {
     if (panel_ok)
-      orth_block<true>(X, n, k, cblk, minv, rmat, inv_diag, thr, ring);
+      orth_block<true>(X, n, k, cblk, rmat, inv_diag, thr, ring);
     else
-      orth_block<false>(X, n, k, cblk, minv, rmat, inv_diag, thr, ring);
+      orth_block<false>(X, n, k, cblk, rmat, inv_diag, thr, ring);
   };
   for (int s = blockIdx.x; s < p.n_slabs; s += gridDim.x) {
     const float* A = p.delta + (int64_t)s * p.delta_stride;  // [T][D]

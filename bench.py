@@ -41,11 +41,11 @@ from synth import workloads as W  # noqa: E402
 METRIC = "reused KV tokens/sec (rotate + rank-m patch), achieved HBM GB/s vs roofline"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth (the "~8 TB/s" figure); the roofline uses the measured copy
 UNIT = "tokens/s"
+# the device sources of each profiled kernel: a committed capture counts only while they are unchanged
 KERNEL_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_kernel.cuh",
-                  "position_invariant_kv_kamera_gb300/csrc/ptx.cuh",
-                  "position_invariant_kv_kamera_gb300/csrc/kamera_api.cu"]
-FACTOR_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_factor.cuh",
-                  "position_invariant_kv_kamera_gb300/csrc/kamera_api.cu"]
+                  "position_invariant_kv_kamera_gb300/csrc/ptx.cuh"]
+FACTOR_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_factor.cuh"]
+ORBIT_SOURCES = ["position_invariant_kv_kamera_gb300/csrc/kamera_orbit.cuh"]
 DESCRIPTIONS = {
     "gqa_video": "GQA Qwen2.5-VL-7B-shaped: 28 layers, 4 KV heads x 128, base 1e6, 16 chunks x 1024 tokens, "
                  "1% outlier channels x8, rank-32 patch per layer per K/V, delta in [-32768, 32768], "
@@ -566,7 +566,7 @@ def run_factor(args) -> None:
 def orbit_traffic(slabs: int) -> float | None:
     """DRAM bytes per launch of the orbit mean over `slabs` slabs: the committed
     capture (scaled to 896 slabs) scaled by the slabs processed."""
-    t = profile_traffic("orbit_mean", "orbit_mean_kernel", FACTOR_SOURCES)
+    t = profile_traffic("orbit_mean", "orbit_mean_kernel", ORBIT_SOURCES)
     return t * slabs / 896 if t is not None else None
 
 

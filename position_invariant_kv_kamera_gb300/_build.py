@@ -10,7 +10,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkamera.so")
 SOURCES = [os.path.join(CSRC, "kamera_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kamera_kernel.cuh", "kamera_factor.cuh", "kamera_compress.cuh", "ptx.cuh")] + [os.path.join(INCLUDE, "kamera.h")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kamera_kernel.cuh", "kamera_factor.cuh", "kamera_orbit.cuh", "kamera_compress.cuh", "ptx.cuh")] + [os.path.join(INCLUDE, "kamera.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-shared"]

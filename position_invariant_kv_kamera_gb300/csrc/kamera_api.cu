@@ -19,6 +19,7 @@
 #include "kamera.h"
 #include "kamera_compress.cuh"
 #include "kamera_factor.cuh"
+#include "kamera_orbit.cuh"
 #include "kamera_kernel.cuh"
 
 namespace kamera {

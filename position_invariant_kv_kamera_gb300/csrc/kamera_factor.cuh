@@ -985,43 +985,6 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   }
 }
 
-// Mean of n sampled deficits, element-wise, fp32, terms added in index order.
-// Streaming: 16-byte loads when every row start is 16-byte aligned.
-__global__ void orbit_mean_kernel(const float* __restrict__ d, int n, int64_t stride, int64_t n_elems,
-                                  float* __restrict__ out) {
-  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool vec = ((reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0 &&
-                   (stride & 3) == 0;
-  const float fn = (float)n;
-  if (vec) {
-    const int64_t n4 = n_elems / 4;
-    for (int64_t e = t0; e < n4; e += nthreads) {
-      float4 s = __ldcs(reinterpret_cast<const float4*>(d) + e);
-      for (int j = 1; j < n; ++j) {
-        const float4 x = __ldcs(reinterpret_cast<const float4*>(d + (int64_t)j * stride) + e);
-        s.x += x.x;
-        s.y += x.y;
-        s.z += x.z;
-        s.w += x.w;
-      }
-      __stcs(reinterpret_cast<float4*>(out) + e, make_float4(__fdiv_rn(s.x, fn), __fdiv_rn(s.y, fn),
-                                                            __fdiv_rn(s.z, fn), __fdiv_rn(s.w, fn)));
-    }
-    for (int64_t e = n4 * 4 + t0; e < n_elems; e += nthreads) {
-      float s = d[e];
-      for (int j = 1; j < n; ++j) s += d[(int64_t)j * stride + e];
-      out[e] = __fdiv_rn(s, fn);
-    }
-  } else {
-    for (int64_t e = t0; e < n_elems; e += nthreads) {
-      float s = d[e];
-      for (int j = 1; j < n; ++j) s += d[(int64_t)j * stride + e];
-      out[e] = __fdiv_rn(s, fn);
-    }
-  }
-}
-
 __host__ __device__ constexpr uint32_t factor_smem_bytes(int kp, int m) {
   return (uint32_t)sizeof(float) * (uint32_t)factor_smem_floats(kp, m);
 }

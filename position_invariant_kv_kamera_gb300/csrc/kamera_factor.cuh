@@ -980,8 +980,15 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
     __syncthreads();
     uint16_t* uo = p.u_out + (int64_t)s * p.out_stride;
     uint16_t* vo = p.v_out + (int64_t)s * p.out_stride;
-    gemm<uint16_t, false, false, false>(T, m, kp, Y, 1, T, Ws, m, 1, uo, m, 1, sA, sB);  // U_m = Q W_m
-    gemm<uint16_t, false, false, false>(D, m, kp, B, 1, D, Ws, m, 1, vo, m, 1, sA, sB);  // V_m = B^T W_m
+    if (tall && D >= m) {  // W_m through the free Z region, and both products on the tensor cores
+      for (int e = threadIdx.x; e < kp * m; e += THREADS) Z[e] = Ws[e];
+      __syncthreads();
+      gemm_tall<uint16_t, false, false, false, false>(T, m, kp, Y, T, Z, m, uo, m, 1, ring);  // U_m = Q W_m
+      gemm_tall<uint16_t, false, false, false, false>(D, m, kp, B, D, Z, m, vo, m, 1, ring);  // V_m = B^T W_m
+    } else {
+      gemm<uint16_t, false, false, false>(T, m, kp, Y, 1, T, Ws, m, 1, uo, m, 1, sA, sB);  // U_m = Q W_m
+      gemm<uint16_t, false, false, false>(D, m, kp, B, 1, D, Ws, m, 1, vo, m, 1, sA, sB);  // V_m = B^T W_m
+    }
   }
 }
 

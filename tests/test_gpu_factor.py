@@ -85,6 +85,19 @@ def test_leading_subspace_matches_oracle_truncation(T, D):
         assert rel(U[s] @ V[s].T, P_ref) < 1e-2
 
 
+@pytest.mark.parametrize("m,p,T,D", [(8, 12, 260, 196), (16, 20, 132, 516), (32, 4, 388, 100), (8, 40, 64, 64)])
+def test_oversampling_that_leaves_partial_tiles(m, p, T, D):
+    """k = m + p not a multiple of 8 or 16 (k = 20, 36, 36, 48) and T, D off
+    the 128-row tile: the last output tile and the last column tile are
+    partial; the rank-m product still matches the oracle's truncation."""
+    spec = np.concatenate([np.linspace(9, 3, m), np.full(6, 0.02)])
+    deltas = np.stack([gen.low_rank_deficit(17, s, T, D, spec, noise=1e-3) for s in range(2)])
+    U, V = gpu_factor(deltas, m, p=p, q=2)
+    for s in range(2):
+        assert np.isfinite(U[s]).all() and np.isfinite(V[s]).all()
+        assert rel(U[s] @ V[s].T, oracle_truncation(deltas[s], m)) < 1e-2
+
+
 def test_near_optimal_without_a_gap():
     """Slowly decaying spectrum: the error is within 2 % of Eckart-Young."""
     T, D, m = 256, 192, 16

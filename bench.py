@@ -178,7 +178,7 @@ def rank_workload(name: str, rank: int, world: int, chunks: int = 0) -> W.Worklo
     seed); there is no data exchange between ranks.  chunks > 0 selects a
     reduced batch of that many chunks (profiling captures only)."""
     name = COMPRESSED.get(name, name)
-    base = SCALED[name](chunks) if chunks and name in SCALED else W.CONFIGS[name]()
+    base = SCALED[name](chunks) if chunks and name in SCALED else W.WORKLOADS[name]()
     return base.replace(seed=base.seed + 1000 * rank) if world > 1 else base
 
 
@@ -192,7 +192,7 @@ def aggregate(tokens_per_rank: int, world: int, max_elapsed_s: float, steps: int
 def oracle_sample_workload(name: str, n_items: int, n_tokens: int | None = None) -> W.Workload:
     """A bounded sample of the workload with the same shapes: the first n_items
     chunks (optionally truncated to n_tokens tokens each)."""
-    full = W.CONFIGS[name]()
+    full = W.WORKLOADS[name]()
     if name == "gqa_video":
         wl = W.gqa_video(n_chunks=n_items, T=n_tokens or 1024)
     elif name == "mla_lite":
@@ -262,7 +262,7 @@ def cpu_baseline(name: str, budget_s: float = 15.0) -> dict:
                 "sample": f"one chunk truncated to {T} tokens, all layers and channels ({tok} tokens, {dt:.1f} s, "
                           f"single-threaded fp64 C oracle decoding the compressed store)"}
     dt1, tok1 = time_oracle(oracle_sample_workload(name, 1))
-    n = max(1, min(len(W.CONFIGS[name]().items), int(budget_s / max(dt1, 1e-3))))
+    n = max(1, min(len(W.WORKLOADS[name]().items), int(budget_s / max(dt1, 1e-3))))
     if n > 1:
         dt, tok = time_oracle(oracle_sample_workload(name, n))
     else:
@@ -629,7 +629,7 @@ def main(argv=None) -> None:
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="gqa_video",
-                    choices=sorted(W.CONFIGS) + sorted(COMPRESSED) + ["patch_formation", "orbit_mean"])
+                    choices=sorted(W.WORKLOADS) + sorted(COMPRESSED) + ["patch_formation", "orbit_mean"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--chunks", type=int, default=0,

@@ -25,7 +25,7 @@
  *       deficit; oracle_jacobi_svd below is a one-sided (Hestenes) Jacobi SVD
  *       used to build exact-rank test cases.
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent (taken as follows):
  *   - RoPE pairs are rotate-half (i, i + d_r/2) unless interleaved (2i, 2i+1)
  *     is requested; theta_i = base^(-2i/d_r) unless a table is given.
  *   - delta is an integer position shift, the same for every token of a chunk.

@@ -401,7 +401,7 @@ def long_video(seed: int = 0x4B414D45 + 5, num_layers: int = 32, n_reorder: int 
                     num_pages=ppseq, block_table=shuffled_block_table(seed, 1, ppseq), seed=seed)
 
 
-CONFIGS = {
+WORKLOADS = {
     "tiny_mha": tiny_mha,
     "gqa_video": gqa_video,
     "mla_lite": mla_lite,

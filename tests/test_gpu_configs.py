@@ -14,7 +14,7 @@ from tests import harness as H
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [
+LAUNCHES = [
     {},
     {"KAMERA_BN": "128"},
     {"KAMERA_STAGES": "2"},
@@ -52,7 +52,7 @@ def test_all_launch_configurations_agree_bitwise(name):
     wl = WORKLOADS[name]()
     pool = (wl.host_pool(0), wl.host_pool(1) if wl.n_ch == 2 else None)
     results = []
-    for cfg in CONFIGS:
+    for cfg in LAUNCHES:
         for k in KEYS:
             os.environ.pop(k, None)
         os.environ.update(cfg)
@@ -89,7 +89,7 @@ def test_compressed_launch_configurations_agree_bitwise(name):
     wl = COMPRESSED[name]()
     arrs = H.comp_arrays(wl.random_compressed())
     results = []
-    for cfg in CONFIGS:
+    for cfg in LAUNCHES:
         for k in KEYS:
             os.environ.pop(k, None)
         os.environ.update(cfg)

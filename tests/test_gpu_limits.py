@@ -115,10 +115,12 @@ def test_factor_largest_slab():
     assert rel < 1e-2, rel
 
 
-@pytest.mark.parametrize("T,D", [(5, 3), (3, 40), (1, 64), (64, 1)])
+@pytest.mark.parametrize("T,D", [(5, 3), (3, 40), (1, 64), (64, 1), (64, 4), (4, 64), (8, 8)])
 def test_factor_slabs_smaller_than_k(T, D):
     """Slabs whose rank min(T, D) is below k: every dependent direction is
-    dropped and the factors reproduce the slab exactly (to bf16 rounding)."""
+    dropped and the factors reproduce the slab exactly (to bf16 rounding).
+    The last three are aligned (tensor-core path with tiny tiles; at D = 4 < m
+    the output products take the fp32 fallback)."""
     rng = np.random.default_rng(T * 100 + D)
     delta = rng.standard_normal((2, T, D)).astype(np.float32)
     U, V = _factor(delta, m=8, p=16, q=2)

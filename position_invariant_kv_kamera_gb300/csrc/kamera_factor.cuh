@@ -680,15 +680,15 @@ __device__ void orth_block(float* X, int n, int k, float* cblk, float* rmat, flo
 // major, in shared memory) with the parallel (round-robin tournament) order:
 // each round rotates kp/2 disjoint planes at once.  On return the diagonal of
 // C holds the eigenvalues and the columns of W the eigenvectors.
-__device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
+__device__ void jacobi_eig(float* C, float* W, int kp, int ld, float* rot, float* red) {
   const int tid = threadIdx.x;
-  for (int e = tid; e < kp * kp; e += THREADS) W[e] = (e / kp == e % kp) ? 1.f : 0.f;
+  for (int e = tid; e < kp * kp; e += THREADS) W[(e / kp) * ld + e % kp] = (e / kp == e % kp) ? 1.f : 0.f;
   __syncthreads();
   const int half = kp / 2;
   for (int sweep = 0; sweep < MAX_SWEEPS; ++sweep) {
     float off = 0.f, tot = 0.f;
     for (int e = tid; e < kp * kp; e += THREADS) {
-      const float x = C[e];
+      const float x = C[(e / kp) * ld + e % kp];
       tot += x * x;
       if (e / kp != e % kp) off += x * x;
     }
@@ -701,7 +701,7 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
     for (int round = 0; round < kp - 1; ++round) {
       if (tid < half) {
         const int p = min(pa, pb), q = max(pa, pb);
-        const float app = C[p * kp + p], aqq = C[q * kp + q], apq = C[p * kp + q];
+        const float app = C[p * ld + p], aqq = C[q * ld + q], apq = C[p * ld + q];
         float c = 1.f, s = 0.f;
         if (apq != 0.f && fabsf(apq) > 1e-30f) {
           const float zeta = (aqq - app) / (2.f * apq);
@@ -724,19 +724,19 @@ __device__ void jacobi_eig(float* C, float* W, int kp, float* rot, float* red) {
         for (int j = tid & 7; j < half; j += 8) {
           const float4 rj = *reinterpret_cast<const float4*>(rot + 4 * j);
           const int pj = __float_as_int(rj.x), qj = __float_as_int(rj.y);
-          const float b00 = C[pi * kp + pj], b01 = C[pi * kp + qj], b10 = C[qi * kp + pj], b11 = C[qi * kp + qj];
+          const float b00 = C[pi * ld + pj], b01 = C[pi * ld + qj], b10 = C[qi * ld + pj], b11 = C[qi * ld + qj];
           // rows: G_i B
           const float u00 = ri.z * b00 - ri.w * b10, u01 = ri.z * b01 - ri.w * b11;
           const float u10 = ri.w * b00 + ri.z * b10, u11 = ri.w * b01 + ri.z * b11;
           // columns: (G_i B) G_j^T
-          C[pi * kp + pj] = rj.z * u00 - rj.w * u01;
-          C[pi * kp + qj] = rj.w * u00 + rj.z * u01;
-          C[qi * kp + pj] = rj.z * u10 - rj.w * u11;
-          C[qi * kp + qj] = rj.w * u10 + rj.z * u11;
+          C[pi * ld + pj] = rj.z * u00 - rj.w * u01;
+          C[pi * ld + qj] = rj.w * u00 + rj.z * u01;
+          C[qi * ld + pj] = rj.z * u10 - rj.w * u11;
+          C[qi * ld + qj] = rj.w * u10 + rj.z * u11;
         }
       }
       for (int jr = tid >> 2; jr < kp; jr += THREADS / 4) {
-        float* w = W + jr * kp;
+        float* w = W + jr * ld;
         for (int i = tid & 3; i < half; i += 4) {
           const float4 ri = *reinterpret_cast<const float4*>(rot + 4 * i);
           const int pi = __float_as_int(ri.x), qi = __float_as_int(ri.y);
@@ -880,7 +880,7 @@ __device__ void gemm_tall(int M, int N, int K, const float* A, int64_t a_ld, con
 
 // Shared memory of one CTA, in floats, for a given kp and m.
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return RING_FLOATS + 2 * kp * kp + kp * m + kp * OB + 2 * kp + 32 + kp + OB * OB + 3 * OB + 4;
+  return RING_FLOATS + 2 * kp * (kp + 1) + kp * m + kp * OB + 2 * kp + 32 + kp + OB * OB + 3 * OB + 4;
 }
 
 // kAligned: T, D, k and the slab stride are multiples of 4 and Delta, Omega and the
@@ -894,9 +894,10 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
   float* ring = fsm;                  // RING_FLOATS: the tensor-core GEMMs' stages
   float* sA = ring;                   // the first two fp32-GEMM tiles overlay the ring
   float* sB = sA + TILE_FLOATS;
-  float* C = ring + RING_FLOATS;      // kp*kp
-  float* W = C + kp * kp;             // kp*kp
-  float* Ws = W + kp * kp;            // kp*m: sorted leading eigenvectors
+  float* C = ring + RING_FLOATS;      // kp*(kp+1)
+  const int ld = kp + 1;              // row stride of C and W: rows fall on different banks
+  float* W = C + kp * ld;             // kp*ld
+  float* Ws = W + kp * ld;            // kp*m: sorted leading eigenvectors
   float* cblk = Ws + kp * m;          // kp*OB: projection coefficients of a column block
   float* rot = cblk + kp * OB;        // 2*kp
   float* red = rot + 2 * kp;          // 32
@@ -958,16 +959,16 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
       gemm_tc<float, true, false, false, true>(k, D, T, Y, T, A, D, B, D, 1, ring);
     else
       gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);
-    for (int e = threadIdx.x; e < kp * kp; e += THREADS) C[e] = 0.f;
+    for (int e = threadIdx.x; e < kp * ld; e += THREADS) C[e] = 0.f;
     __syncthreads();
-    gemm<float, false, true, true>(k, k, D, B, D, 1, B, 1, D, C, kp, 1, sA, sB);   // C = B B^T
-    jacobi_eig(C, W, kp, rot, red);
+    gemm<float, false, true, true>(k, k, D, B, D, 1, B, 1, D, C, ld, 1, sA, sB);   // C = B B^T
+    jacobi_eig(C, W, kp, ld, rot, red);
     // order the eigenpairs by decreasing eigenvalue (ties by index)
     for (int i = threadIdx.x; i < kp; i += THREADS) {
-      const float li = C[i * kp + i];
+      const float li = C[i * ld + i];
       int r = 0;
       for (int j = 0; j < kp; ++j) {
-        const float lj = C[j * kp + j];
+        const float lj = C[j * ld + j];
         r += (lj > li) || (lj == li && j < i);
       }
       perm[r] = i;
@@ -975,7 +976,7 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
     __syncthreads();
     for (int e = threadIdx.x; e < kp * m; e += THREADS) {
       const int i = e / m, r = e % m;
-      Ws[e] = W[i * kp + perm[r]];
+      Ws[e] = W[i * ld + perm[r]];
     }
     __syncthreads();
     uint16_t* uo = p.u_out + (int64_t)s * p.out_stride;

@@ -423,21 +423,35 @@ __device__ void ts_tn(float* C, int ldc, const float* P, int a, const float* Q, 
   for (int p0 = 0; p0 < a; p0 += 24) ts_tn24(C + p0 * ldc, ldc, P + (int64_t)p0 * n, min(24, a - p0), Q, b, n);
 }
 
-// X[q][r] -= sum_{p < a} P[p][r] C[p][q] for q < b: one row r per thread.
+// X[q][r] -= sum_{p < a} P[p][r] C[p][q] for q < b: rows r and r + THREADS per
+// thread, so that each coefficient read from shared memory serves two rows.
 __device__ void ts_update(float* X, int b, const float* P, int a, const float* C, int ldc, int n) {
-  for (int r = threadIdx.x; r < n; r += THREADS) {
-    float x[OB];
+  for (int r = threadIdx.x; r < n; r += 2 * THREADS) {
+    const int r2 = r + THREADS;
+    const bool two = r2 < n;
+    float x[OB], y[OB];
 #pragma unroll
-    for (int q = 0; q < OB; ++q) x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
-#pragma unroll 8
+    for (int q = 0; q < OB; ++q) {
+      x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
+      y[q] = q < b && two ? X[(int64_t)q * n + r2] : 0.f;
+    }
+#pragma unroll 4
     for (int p = 0; p < a; ++p) {
       const float pv = P[(int64_t)p * n + r];
+      const float pw = two ? P[(int64_t)p * n + r2] : 0.f;
 #pragma unroll
-      for (int q = 0; q < OB; ++q) x[q] = fmaf(-pv, C[p * ldc + q], x[q]);
+      for (int q = 0; q < OB; ++q) {
+        const float c = C[p * ldc + q];
+        x[q] = fmaf(-pv, c, x[q]);
+        y[q] = fmaf(-pw, c, y[q]);
+      }
     }
 #pragma unroll
     for (int q = 0; q < OB; ++q)
-      if (q < b) X[(int64_t)q * n + r] = x[q];
+      if (q < b) {
+        X[(int64_t)q * n + r] = x[q];
+        if (two) X[(int64_t)q * n + r2] = y[q];
+      }
   }
 }
 

@@ -488,22 +488,37 @@ __device__ void chol_drop(const float* G, float* R, float* inv_diag, const float
 }
 
 // X <- X R^{-1} row by row (forward substitution), R upper triangular, dropped
-// columns become zero.
+// columns become zero; rows r and r + THREADS per thread, so that each entry of
+// R read from shared memory serves two rows.
 __device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, int n) {
-  for (int r = threadIdx.x; r < n; r += THREADS) {
-    float x[OB];
+  for (int r = threadIdx.x; r < n; r += 2 * THREADS) {
+    const int r2 = r + THREADS;
+    const bool two = r2 < n;
+    float x[OB], y[OB];
 #pragma unroll
-    for (int q = 0; q < OB; ++q) x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
+    for (int q = 0; q < OB; ++q) {
+      x[q] = q < b ? X[(int64_t)q * n + r] : 0.f;
+      y[q] = q < b && two ? X[(int64_t)q * n + r2] : 0.f;
+    }
 #pragma unroll
     for (int j = 0; j < OB; ++j) {
-      float v = x[j];
+      float v = x[j], w = y[j];
 #pragma unroll
-      for (int l = 0; l < j; ++l) v = fmaf(-x[l], R[l * OB + j], v);
-      x[j] = v * inv_diag[j < b ? j : 0] * (j < b ? 1.f : 0.f);
+      for (int l = 0; l < j; ++l) {
+        const float rl = R[l * OB + j];
+        v = fmaf(-x[l], rl, v);
+        w = fmaf(-y[l], rl, w);
+      }
+      const float d = inv_diag[j < b ? j : 0] * (j < b ? 1.f : 0.f);
+      x[j] = v * d;
+      y[j] = w * d;
     }
 #pragma unroll
     for (int q = 0; q < OB; ++q)
-      if (q < b) X[(int64_t)q * n + r] = x[q];
+      if (q < b) {
+        X[(int64_t)q * n + r] = x[q];
+        if (two) X[(int64_t)q * n + r2] = y[q];
+      }
   }
 }
 

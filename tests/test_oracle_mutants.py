@@ -5,7 +5,8 @@ a dropped term, a transposed operand, an off-by-one -- into a copy of the
 oracle's C source, builds it, and runs the independent checks below (complex
 RoPE, M-RoPE, library matmul, brute-force page map, the vectorised whole-batch
 formulation, library SVD, library mean, Max's quantiser table, the int8 error
-bound, scipy's Hadamard matrix, the nearest-centroid rule).  Every mutant must fail at least one.
+bound, scipy's Hadamard matrix, the nearest-centroid rule, the error bits of
+items that disagree with the stores).  Every mutant must fail at least one.
 """
 
 import json
@@ -19,7 +20,7 @@ import oracle
 from synth import gen
 from synth import workloads as W
 from tests.test_oracle_compressed import _independent_reuse_compressed, _pack, _unpack
-from tests.test_oracle_operator import CASES, _independent_reuse, _oracle_model
+from tests.test_oracle_operator import CASES, _independent_reuse, _oracle_model, _run_oracle, _small_gqa
 from tests.test_oracle_pins import _theta_np, mrope_complex, rope_complex
 
 SRC = open(oracle._SRC).read()
@@ -64,6 +65,38 @@ MUTANTS = [
     ("K scale index transposed", "cs->k_scale[(int64_t)c * m->num_layers + l]", "cs->k_scale[(int64_t)l * cs->n_chunks + c]"),
     ("compressed row order token-major", "const int64_t row = cs->row_offset[c] + (int64_t)l * cs->len[c] + t;",
      "const int64_t row = cs->row_offset[c] + (int64_t)t * m->num_layers + l;"),
+    ("interleaved partner taken as rotate-half",
+     "int32_t ib = (pairing == OR_INTERLEAVED) ? 2 * i + 1 : i + half;\n    double phi = (double)deltas[s] * theta[i];",
+     "int32_t ib = i + half;\n    double phi = (double)deltas[s] * theta[i];"),
+    ("head offset by rope_dim", "oracle_rotate_region_sections(row + (int64_t)h * m->head_dim,",
+     "oracle_rotate_region_sections(row + (int64_t)h * m->rope_dim,"),
+    ("third section boundary", "if (i >= sections[0] + sections[1]) s = 2;", "if (i >= sections[1]) s = 2;"),
+    ("theta exponent from a wider row", "theta[i] = pow(base, -2.0 * (double)i / (double)rope_dim);",
+     "theta[i] = pow(base, -2.0 * (double)i / (double)(rope_dim + 2));"),
+    ("page bound off by one", "if (page < 0 || page >= num_pages) return -1;",
+     "if (page < 0 || page > num_pages) return -1;"),
+    ("block index bound off by one", "if (blk >= max_pages_per_seq) return -1;",
+     "if (blk > max_pages_per_seq) return -1;"),
+    ("block-table row stride", "int64_t page = block_table[(int64_t)seq * max_pages_per_seq + blk];",
+     "int64_t page = block_table[(int64_t)seq * num_pages + blk];"),
+    ("destination offset ignored", "const int64_t pos = item->dst_pos + t;", "const int64_t pos = t;"),
+    ("pool layer stride", "const int64_t dst_row = (int64_t)l * num_pages * page_size + dst;",
+     "const int64_t dst_row = (int64_t)l * num_pages + dst;"),
+    ("V factor read at U's offset",
+     "vmat[j * rank + r] = bf16_bits_to_f64(patch[base + ((int64_t)T + j) * rank + r]);",
+     "vmat[j * rank + r] = bf16_bits_to_f64(patch[base + ((int64_t)j) * rank + r]);"),
+    ("patch layer/channel order",
+     "const int64_t base = patch_off[item->patch_id] + ((int64_t)l * n_ch + ch) * (int64_t)(T + D) * rank;",
+     "const int64_t base = patch_off[item->patch_id] + ((int64_t)ch * L + l) * (int64_t)(T + D) * rank;"),
+    ("chunk length unchecked", "if (store_len[item->chunk_id] != T) { err |= OR_EFLAG_LEN; continue; }", ""),
+    ("patch length unchecked", "if (patch_len[item->patch_id] != T) { err |= OR_EFLAG_LEN; continue; }", ""),
+    ("patch id bound off by one", "if (item->patch_id >= n_patches) { err |= OR_EFLAG_PATCH_OOB; continue; }",
+     "if (item->patch_id > n_patches) { err |= OR_EFLAG_PATCH_OOB; continue; }"),
+    ("Jacobi sine not scaled by the cosine", "double s = c * t;", "double s = t;"),
+    ("Jacobi stops after one sweep", "if (!rotated) break;", "break;"),
+    ("orbit ordering stride", "s += (double)deltas[(int64_t)j * stride + e];",
+     "s += (double)deltas[(int64_t)j * n_elems + e];"),
+    ("V decode without the norm", "out[i] = (double)norm / (double)n * acc;", "out[i] = 1.0 / (double)n * acc;"),
 ]
 
 
@@ -136,11 +169,63 @@ def c_frame(lib):
                                atol=1e-11)
 
 
+def c_partial(lib):
+    m = oracle.model(oracle.GQA, 1, num_kv_heads=2, head_dim=128, rope_dim=64)
+    th = _theta_np(1e4, 64)
+    x = rng.standard_normal(256)
+    k = oracle.rotate_row(m, th, 0, 99, x, lib=lib)
+    for h in range(2):
+        np.testing.assert_allclose(k[h * 128:h * 128 + 64], rope_complex(x[h * 128:h * 128 + 64], 99, th), atol=1e-11)
+        np.testing.assert_array_equal(k[h * 128 + 64:(h + 1) * 128], x[h * 128 + 64:(h + 1) * 128])
+
+
 def c_slot(lib):
-    P, mp, num_pages = 16, 5, 12
-    bt = rng.permutation(num_pages)[:mp].reshape(1, mp).astype(np.int32)
-    for pos in range(mp * P):
-        assert oracle.slot(bt, mp, num_pages, P, 0, pos, lib=lib) == int(bt[0, pos // P]) * P + pos % P
+    # several sequences, page ids on and past the bound; the table is the head
+    # of a larger array of valid page ids, so that a mutant reading past it
+    # reads defined memory and shows up as a wrong slot
+    P, n_seqs, mp, num_pages = 16, 3, 5, 20
+    full = np.stack([rng.permutation(num_pages)[:mp] for _ in range(40)]).astype(np.int32)
+    bt = full[:n_seqs]
+    bt[1, 4] = num_pages
+    bt[2, 0] = -1
+    for seq in range(n_seqs):
+        for pos in range(-2, mp * P + 3):
+            want = -1
+            if 0 <= pos < mp * P:
+                page = int(bt[seq, pos // P])
+                if 0 <= page < num_pages:
+                    want = page * P + pos % P
+            assert oracle.slot(bt, mp, num_pages, P, seq, pos, lib=lib) == want
+
+
+def c_errors(lib):
+    wl = _small_gqa()
+    n_p = len(wl.patch_lens)
+
+    def run(items, patch_len=None, patch_off=None):
+        m = _oracle_model(wl)
+        th = oracle.theta(wl.rope_base, wl.rope_dim, lib=lib)
+        return oracle.reuse(
+            m, th, oracle.MODE_REUSE, store=wl.host_store(), store_off=wl.store_off,
+            store_len=np.array(wl.chunk_lens, np.int32), patch=wl.host_patch(),
+            patch_off=wl.patch_off if patch_off is None else patch_off,
+            patch_len=np.array(wl.patch_lens, np.int32) if patch_len is None else patch_len, rank=wl.rank,
+            items=items, block_table=wl.block_table, num_pages=wl.num_pages, page_size=wl.page_size,
+            pool_k_in=wl.host_pool(0), pool_v_in=wl.host_pool(1), lib=lib)[0]
+
+    items = wl.items.copy()
+    items[0]["n_tokens"] = 69                      # length disagrees with the chunk store only
+    plen = np.array(wl.patch_lens, np.int32)
+    plen[int(wl.items[0]["patch_id"])] = 69
+    assert run(items, patch_len=plen) == oracle.EFLAG_LEN
+    plen = np.array(wl.patch_lens, np.int32)
+    plen[int(wl.items[0]["patch_id"])] = 71          # length disagrees with the patch store
+    assert run(wl.items, patch_len=plen) == oracle.EFLAG_LEN
+    items = wl.items.copy()
+    items[1]["patch_id"] = n_p                     # one past the last patch; the arrays are views into
+    plen = np.append(np.array(wl.patch_lens, np.int32), np.int32(wl.patch_lens[0]))[:n_p]  # longer ones
+    poff = np.append(np.asarray(wl.patch_off, np.int64), np.int64(wl.patch_off[0]))[:n_p]
+    assert run(items, patch_len=plen, patch_off=poff) == oracle.EFLAG_PATCH_OOB
 
 
 def c_reuse(lib):
@@ -171,6 +256,11 @@ def c_svd(lib):
 def c_orbit(lib):
     d = rng.standard_normal((4, 50)).astype(np.float32)
     np.testing.assert_allclose(oracle.orbit_mean(d, lib=lib), d.astype(np.float64).mean(axis=0), atol=1e-15)
+    # orderings further apart than the elements averaged (stride 40, 25 elements)
+    full = rng.standard_normal((3, 40)).astype(np.float32)
+    out = np.zeros(25, np.float64)
+    lib.oracle_orbit_mean(oracle._ptr(full), 3, 40, 25, oracle._ptr(out))
+    np.testing.assert_allclose(out, full[:, :25].astype(np.float64).mean(axis=0), atol=1e-15)
 
 
 def c_codebook(lib):
@@ -223,8 +313,8 @@ def c_reuse_comp(lib):
     np.testing.assert_allclose(pv[iwv], iv[iwv], atol=1e-10)
 
 
-CHECKS = [c_theta, c_rope, c_row, c_mla, c_mrope, c_patch, c_frame, c_slot, c_reuse, c_svd, c_orbit, c_codebook,
-          c_kquant, c_vcodec, c_reuse_comp]
+CHECKS = [c_theta, c_rope, c_row, c_partial, c_mla, c_mrope, c_patch, c_frame, c_slot, c_errors, c_reuse, c_svd,
+          c_orbit, c_codebook, c_kquant, c_vcodec, c_reuse_comp]
 
 
 def test_unmutated_oracle_passes_every_check(tmp_path):

@@ -205,6 +205,55 @@ def test_byte_budget_gives_the_pages_ratio(oracle_lib):
     assert abs(g["baseline_bits"] / ((g["k_bits"] + g["v_bits"]) / 2) - g["ratio"]) < g["abs_tol"]
 
 
+def check_store_encoding(wl, cs):
+    """Every (chunk, layer) K tensor and every V head row of the bf16 store
+    against its place in the compressed store, by properties of the codecs
+    computed here with numpy and scipy: the K scale is max|x| / 127, every K
+    code lies within half a step of its value and the largest |x| takes
+    +-127; each V norm is the row's Euclidean norm, each V code the nearest
+    centroid of (H x) / ||x|| (either neighbour within fp32 rounding of a
+    threshold)."""
+    T_all, D, H, n, L = wl.chunk_lens, wl.D, wl.num_kv_heads, wl.head_dim, wl.num_layers
+    store = wl.host_store()
+    Hm = linalg.hadamard(n).astype(np.float64)
+    c64 = cs.codebook.astype(np.float64)
+    for c, T in enumerate(T_all):
+        for l in range(L):
+            base = int(wl.store_off[c]) + 2 * l * T * D
+            k = _bits_to_f64(store[base:base + T * D]).reshape(T, D)
+            v = _bits_to_f64(store[base + T * D:base + 2 * T * D]).reshape(T, D)
+            r0 = int(cs.row_offset[c]) + l * T
+            s = float(cs.k_scale[c, l])
+            assert abs(s - np.abs(k).max() / 127) <= 1e-6 * s
+            q = cs.k_codes[r0:r0 + T].astype(np.float64)
+            assert np.all(np.abs(k - q * s) <= 0.5 * s * (1 + 1e-5))
+            i = np.unravel_index(np.abs(k).argmax(), k.shape)
+            assert abs(q[i]) == 127
+            for t in range(T):
+                for h in range(H):
+                    x = v[t, h * n:(h + 1) * n]
+                    nx = np.linalg.norm(x)
+                    assert abs(float(cs.v_norm[r0 + t, h]) - nx) <= 1e-6 * nx
+                    z = Hm @ x / nx
+                    near = np.abs(z[:, None] - c64[None, :]).argmin(axis=1)
+                    dist = np.abs(z[:, None] - (c64[1:] + c64[:-1])[None, :] / 2).min(axis=1)
+                    codes = _unpack(cs.v_codes[r0 + t, h], n)
+                    assert np.all((codes == near) | ((dist < 1e-5) & (np.abs(codes - near) == 1)))
+
+
+def test_compressed_store_holds_each_tensor_and_head_row_in_place(oracle_lib):
+    """The store layout (row_offset[c] + l*T + t; K scale per (chunk, layer);
+    V head rows in order) and the codecs, for two chunks of three layers
+    whose rows start after a gap and leave another gap between them."""
+    wl = W.gqa_video(num_layers=3, n_chunks=2, T=24, rank=0, page_size=16)
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim)
+    lens = np.array(wl.chunk_lens, np.int32)
+    row_offset = np.array([5, 5 + wl.num_layers * int(lens[0]) + 7], np.int64)
+    cs = oracle.compress_store(m, wl.host_store(), wl.store_off, lens, row_offset=row_offset)
+    check_store_encoding(wl, cs)
+    assert not cs.k_codes[:5].any() and not cs.v_norm[:5].any()
+
+
 # ---- the reuse operator reading a compressed store -----------------------------------------------------
 
 def _decode_np(wl, cs, chunk, layer, ch):

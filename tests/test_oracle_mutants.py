@@ -19,7 +19,7 @@ from scipy import linalg
 import oracle
 from synth import gen
 from synth import workloads as W
-from tests.test_oracle_compressed import _independent_reuse_compressed, _pack, _unpack
+from tests.test_oracle_compressed import _independent_reuse_compressed, _pack, _unpack, check_store_encoding
 from tests.test_oracle_operator import CASES, _independent_reuse, _oracle_model, _run_oracle, _small_gqa
 from tests.test_oracle_pins import _theta_np, mrope_complex, rope_complex
 
@@ -97,6 +97,13 @@ MUTANTS = [
     ("orbit ordering stride", "s += (double)deltas[(int64_t)j * stride + e];",
      "s += (double)deltas[(int64_t)j * n_elems + e];"),
     ("V decode without the norm", "out[i] = (double)norm / (double)n * acc;", "out[i] = 1.0 / (double)n * acc;"),
+    ("compressed K taken from V", "const uint16_t* k = store + store_off[c] + ((int64_t)l * 2 + 0) * T * D;",
+     "const uint16_t* k = store + store_off[c] + ((int64_t)l * 2 + 1) * T * D;"),
+    ("compressed K scale index transposed", "&k_scale[(int64_t)c * L + l]", "&k_scale[(int64_t)l * n_chunks + c]"),
+    ("compressed V head offset halved", "oracle_encode_v(v + t * D + (int64_t)h * n, n,",
+     "oracle_encode_v(v + t * D + (int64_t)h * (n / 2), n,"),
+    ("compressed rows of a layer overlap", "const int64_t row0 = row_offset[c] + (int64_t)l * T;",
+     "const int64_t row0 = row_offset[c] + (int64_t)l;"),
 ]
 
 
@@ -313,8 +320,15 @@ def c_reuse_comp(lib):
     np.testing.assert_allclose(pv[iwv], iv[iwv], atol=1e-10)
 
 
+def c_compress(lib):
+    wl = W.gqa_video(num_layers=2, n_chunks=2, T=12, rank=0, page_size=16)
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim)
+    check_store_encoding(wl, oracle.compress_store(m, wl.host_store(), wl.store_off,
+                                                    np.array(wl.chunk_lens, np.int32), lib=lib))
+
+
 CHECKS = [c_theta, c_rope, c_row, c_partial, c_mla, c_mrope, c_patch, c_frame, c_slot, c_errors, c_reuse, c_svd,
-          c_orbit, c_codebook, c_kquant, c_vcodec, c_reuse_comp]
+          c_orbit, c_codebook, c_kquant, c_vcodec, c_compress, c_reuse_comp]
 
 
 def test_unmutated_oracle_passes_every_check(tmp_path):

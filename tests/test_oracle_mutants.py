@@ -20,7 +20,8 @@ import oracle
 from synth import gen
 from synth import workloads as W
 from tests.test_oracle_compressed import _independent_reuse_compressed, _pack, _unpack, check_store_encoding
-from tests.test_oracle_operator import CASES, _independent_reuse, _oracle_model, _run_oracle, _small_gqa
+from tests.test_oracle_operator import (CASES, _complex_rotate_rows, _independent_reuse, _oracle_model, _run_oracle,
+                                        _small_gqa)
 from tests.test_oracle_pins import _theta_np, mrope_complex, rope_complex
 
 SRC = open(oracle._SRC).read()
@@ -104,6 +105,13 @@ MUTANTS = [
      "oracle_encode_v(v + t * D + (int64_t)h * (n / 2), n,"),
     ("compressed rows of a layer overlap", "const int64_t row0 = row_offset[c] + (int64_t)l * T;",
      "const int64_t row0 = row_offset[c] + (int64_t)l;"),
+    ("in-place relocation writes V too", "const int32_t ch_count = (mode == OR_MODE_RELOCATE_IN_PLACE) ? 1 : n_ch;",
+     "const int32_t ch_count = n_ch;"),
+    ("in-place patch also rotates", "const int32_t rotate = (mode != OR_MODE_PATCH_IN_PLACE);",
+     "const int32_t rotate = 1;"),
+    ("in-place patch rewrites unpatched items", "if (mode == OR_MODE_PATCH_IN_PLACE && !use_patch) continue;", ""),
+    ("in-place source row without its layer", "src[j] = bf16_bits_to_f64(pin[dst_row * D + j]);",
+     "src[j] = bf16_bits_to_f64(pin[dst * D + j]);"),
 ]
 
 
@@ -253,6 +261,44 @@ def c_reuse(lib):
             np.testing.assert_allclose(pv[iwv], iv[iwv], atol=1e-10)
 
 
+def c_inplace(lib):
+    # sliding-window survival: K of the survivors' pages turned by delta, V and other pages untouched
+    wl = W.sliding_window(num_layers=2, n_resident=6, n_evict=2, T=32, page_size=16, num_kv_heads=2)
+    k_in, v_in = wl.host_pool(0), wl.host_pool(1)
+    err, pk, pv, wk, wv = _run_oracle(wl, k_in, v_in, lib=lib)
+    assert err == 0 and not wv.any()
+    np.testing.assert_array_equal(pv, oracle.bf16_bits_to_f64(v_in))
+    kin = oracle.bf16_bits_to_f64(k_in)
+    surv = set(wl.block_table[0].tolist())
+    theta = _theta_np(wl.rope_base, 128)
+    for layer in range(2):
+        for page in range(wl.num_pages):
+            if page in surv:
+                want = _complex_rotate_rows(kin[layer, page], 2, 128, 128, 0, -64, theta, W.ROTATE_HALF)
+                np.testing.assert_allclose(pk[layer, page], want, atol=1e-10)
+            else:
+                np.testing.assert_array_equal(pk[layer, page], kin[layer, page])
+    # patch in place: U V^T added with no rotation; an item without a patch is not written
+    wl = _small_gqa().replace(mode="apply_patch", pool_init="random", chunk_lens=[])
+    wl.items["patch_id"][0] = -1
+    k_in, v_in = wl.host_pool(0), wl.host_pool(1)
+    err, pk, pv, wk, wv = _run_oracle(wl, k_in, v_in, lib=lib)
+    assert err == 0
+    for it_i, it in enumerate(wl.items):
+        pos = int(it["dst_pos"]) + np.arange(int(it["n_tokens"]))
+        pages, slots = wl.block_table[0, pos // 16], pos % 16
+        assert wk[:, pages, slots].all() == (it_i != 0) and wv[:, pages, slots].all() == (it_i != 0)
+        if it_i == 0:
+            continue
+        p = int(it["patch_id"])
+        for layer in range(wl.num_layers):
+            for ch, img, src in ((0, pk, k_in), (1, pv, v_in)):
+                U = oracle.bf16_bits_to_f64(wl.u_rows(p, layer, ch))
+                V = oracle.bf16_bits_to_f64(wl.v_rows(p, layer, ch))
+                want = oracle.bf16_bits_to_f64(src[layer, pages, slots]) + U @ V.T
+                np.testing.assert_allclose(img[layer, pages, slots], want, atol=1e-12)
+
+
 def c_svd(lib):
     a = rng.standard_normal((30, 10))
     us, v, sig = oracle.jacobi_svd(a, lib=lib)
@@ -327,7 +373,7 @@ def c_compress(lib):
                                                     np.array(wl.chunk_lens, np.int32), lib=lib))
 
 
-CHECKS = [c_theta, c_rope, c_row, c_partial, c_mla, c_mrope, c_patch, c_frame, c_slot, c_errors, c_reuse, c_svd,
+CHECKS = [c_theta, c_rope, c_row, c_partial, c_mla, c_mrope, c_patch, c_frame, c_slot, c_errors, c_reuse, c_inplace, c_svd,
           c_orbit, c_codebook, c_kquant, c_vcodec, c_compress, c_reuse_comp]
 
 

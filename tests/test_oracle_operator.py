@@ -25,9 +25,9 @@ def _oracle_model(wl):
                         wl.pairing, wl.patch_frame)
 
 
-def _run_oracle(wl, pool_k=None, pool_v=None):
+def _run_oracle(wl, pool_k=None, pool_v=None, lib=None):
     m = _oracle_model(wl)
-    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    th = oracle.theta(wl.rope_base, wl.rope_dim, lib=lib)
     mode = {"reuse": oracle.MODE_REUSE, "relocate_in_place": oracle.MODE_RELOCATE_IN_PLACE,
             "apply_patch": oracle.MODE_PATCH_IN_PLACE}[wl.mode]
     pool_k = wl.host_pool(0) if pool_k is None else pool_k
@@ -39,7 +39,7 @@ def _run_oracle(wl, pool_k=None, pool_v=None):
         kw.update(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),
                   rank=wl.rank)
     return oracle.reuse(m, th, mode, items=wl.items, block_table=wl.block_table, num_pages=wl.num_pages,
-                        page_size=wl.page_size, pool_k_in=pool_k, pool_v_in=pool_v, **kw)
+                        page_size=wl.page_size, pool_k_in=pool_k, pool_v_in=pool_v, lib=lib, **kw)
 
 
 def _complex_rotate_rows(x, heads, rope, stride, col0, delta, theta, pairing):

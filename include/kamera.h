@@ -20,8 +20,10 @@
  * R(delta) only (kamera_relocate, in place).
  *
  * Conventions for every entry point:
- *   - Ownership: the caller owns every buffer.  The library keeps no state
- *     between calls and allocates no memory, host or device.
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     memory, host or device, on any call.  Between calls it keeps only a
+ *     per-device cache of launch facts (SM count, shared-memory limit) and
+ *     the static scratch array of kamera_factor_patches_noalloc.
  *   - Pointers marked "device" must be device (or managed) memory of the
  *     current device; "host" pointers are read during the call only.
  *   - Asynchrony: work is enqueued on `stream`; KAMERA_OK means "validated and
@@ -46,6 +48,13 @@
  *     not overlap, except for the in-place modes, where each slot is read and
  *     written by the same item.  Two items writing the same slot is a caller
  *     error (the result is one of the two).
+ *   - Launch-shape overrides (for tuning sweeps and tests; results do not
+ *     depend on them): the reuse entry points read the environment variables
+ *     KAMERA_BN (tile width, 64/128/192/256), KAMERA_STAGES (canonical
+ *     stages, 2..6), KAMERA_UV_SLOTS (patch-factor slots, 1 or 2),
+ *     KAMERA_KSPLIT (patch factors staged in 1, 2 or 4 parts of the rank) and
+ *     KAMERA_NO_PDL (non-zero: no programmatic dependent launch).  Unset, the
+ *     library picks the widest tile and the deepest pipeline that fit.
  */
 #ifndef KAMERA_H_
 #define KAMERA_H_

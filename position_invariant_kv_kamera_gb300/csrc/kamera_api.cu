@@ -149,7 +149,8 @@ const Codebook& codebook() {
 
 enum Mode { MODE_REUSE = 0, MODE_RELOCATE_IN_PLACE = 1, MODE_PATCH_IN_PLACE = 2 };
 
-// Optional tuning overrides (for sweeps): KAMERA_BN, KAMERA_STAGES.
+// Optional launch-shape overrides (tuning sweeps, configuration-invariance tests):
+// KAMERA_BN, KAMERA_STAGES, KAMERA_UV_SLOTS, KAMERA_KSPLIT, KAMERA_NO_PDL.
 int env_int(const char* name) {
   const char* s = getenv(name);
   return s ? atoi(s) : 0;

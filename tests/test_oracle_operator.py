@@ -59,15 +59,19 @@ def _complex_rotate_rows(x, heads, rope, stride, col0, delta, theta, pairing):
 
 
 def _independent_reuse(wl):
-    """The same operator as matrix algebra over whole slabs + explicit page map."""
+    """The same operator as matrix algebra over whole slabs + explicit page map
+    (M-RoPE: a per-pair shift vector from the sections)."""
     D, L = wl.D, wl.num_layers
     theta = _theta_np(wl.rope_base, wl.rope_dim)
     pk = _bits_to_f64(wl.host_pool(0))
     pv = _bits_to_f64(wl.host_pool(1)) if wl.n_ch == 2 else None
     wk = np.zeros(pk.shape[:-1], bool)
     wv = np.zeros(pk.shape[:-1], bool)
-    for it in wl.items:
+    for i_it, it in enumerate(wl.items):
         T, c, p, delta = int(it["n_tokens"]), int(it["chunk_id"]), int(it["patch_id"]), int(it["delta"])
+        if sum(wl.rope_sections) and wl.section_deltas is not None:
+            # M-RoPE: pair i turns by the shift of the section it falls in
+            delta = np.repeat(np.asarray(wl.section_deltas[i_it], np.float64), wl.rope_sections)
         pos = int(it["dst_pos"]) + np.arange(T)
         pages = wl.block_table[int(it["seq"]), pos // wl.page_size]
         slots = pos % wl.page_size
@@ -205,3 +209,25 @@ def test_error_bits_and_skips(oracle_lib):
     items[0]["n_tokens"] = 69        # length disagrees with the store
     err, *_ = _run_oracle(wl.replace(items=items))
     assert err == oracle.EFLAG_LEN
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_workloads_match_independent_formulation(oracle_lib, seed):
+    """The seeded random batches of the GPU fuzz (family, head size, partial
+    rotary, rank, page size, pairing, frame, M-RoPE sections, ragged chunks
+    reused at several positions, several sequences, patched and unpatched
+    items) through the oracle and through the independent formulation."""
+    from tests.harness import oracle_reference
+    from tests.test_gpu_fuzz import random_workload
+
+    wl = random_workload(1000 + seed)
+    err, pk, pv, wk, wv = oracle_reference(wl)
+    assert err == 0
+    ik, iv, iwk, iwv = _independent_reuse(wl)
+    np.testing.assert_array_equal(wk.astype(bool), iwk)
+    np.testing.assert_allclose(pk[iwk], ik[iwk], rtol=0, atol=1e-9)
+    np.testing.assert_array_equal(pk[~iwk], ik[~iwk])
+    if wl.n_ch == 2:
+        np.testing.assert_array_equal(wv.astype(bool), iwv)
+        np.testing.assert_allclose(pv[iwv], iv[iwv], rtol=0, atol=1e-9)
+        np.testing.assert_array_equal(pv[~iwv], iv[~iwv])

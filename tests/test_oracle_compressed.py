@@ -277,8 +277,10 @@ def _independent_reuse_compressed(wl, cs):
     pv = _bits_to_f64(wl.host_pool(1))
     wk = np.zeros(pk.shape[:-1], bool)
     wv = np.zeros(pk.shape[:-1], bool)
-    for it in wl.items:
+    for i_it, it in enumerate(wl.items):
         T, c, p, delta = int(it["n_tokens"]), int(it["chunk_id"]), int(it["patch_id"]), int(it["delta"])
+        if sum(wl.rope_sections) and wl.section_deltas is not None:
+            delta = np.repeat(np.asarray(wl.section_deltas[i_it], np.float64), wl.rope_sections)
         pos = int(it["dst_pos"]) + np.arange(T)
         pages, slots = wl.block_table[int(it["seq"]), pos // wl.page_size], pos % wl.page_size
         for layer in range(wl.num_layers):
@@ -287,7 +289,10 @@ def _independent_reuse_compressed(wl, cs):
                 patch = 0.0
                 if wl.rank and p >= 0:
                     patch = _bits_to_f64(wl.u_rows(p, layer, ch)) @ _bits_to_f64(wl.v_rows(p, layer, ch)).T
-                if ch == 0:
+                if ch == 0 and wl.patch_frame == W.CANONICAL_FRAME:
+                    y = _complex_rotate_rows(x + patch, wl.num_kv_heads, wl.rope_dim, wl.head_dim, 0, delta, theta,
+                                             wl.pairing)
+                elif ch == 0:
                     y = _complex_rotate_rows(x, wl.num_kv_heads, wl.rope_dim, wl.head_dim, 0, delta, theta,
                                              wl.pairing) + patch
                 else:
@@ -357,3 +362,27 @@ def test_reuse_compressed_error_bits(oracle_lib):
     short = oracle.Compressed(cs.k_codes[:-1], cs.k_scale, cs.v_codes[:-1], cs.v_norm[:-1], cs.row_offset, cs.len,
                               cs.codebook)
     assert run(wl.items, short) == oracle.EFLAG_CHUNK_OOB  # the last chunk's rows run past the store
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_compressed_workloads_match_independent_formulation(oracle_lib, seed):
+    """The seeded random batches of the GPU fuzz of the compressed store (the
+    oracle's encoding for even seeds, random contents for odd ones) through
+    the oracle and through the independent formulation."""
+    from tests import harness as H
+    from tests.test_gpu_fuzz import random_workload
+
+    wl = random_workload(3000 + seed, compressed=True)
+    if seed % 2 == 0:
+        m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim)
+        cs = oracle.compress_store(m, wl.host_store(), wl.store_off, np.array(wl.chunk_lens, np.int32),
+                                   row_offset=wl.comp_row_offset, n_rows=wl.comp_rows)
+    else:
+        cs = H.oracle_store(H.comp_arrays(wl.random_compressed()))
+    err, pk, pv, wk, wv = H.oracle_reference_compressed(wl, cs)
+    assert err == 0
+    ik, iv, iwk, iwv = _independent_reuse_compressed(wl, cs)
+    for got, want, w, iw in ((pk, ik, wk, iwk), (pv, iv, wv, iwv)):
+        np.testing.assert_array_equal(w.astype(bool), iw)
+        np.testing.assert_allclose(got[iw], want[iw], rtol=0, atol=1e-9)
+        np.testing.assert_array_equal(got[~iw], want[~iw])

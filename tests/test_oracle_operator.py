@@ -231,3 +231,68 @@ def test_fuzz_workloads_match_independent_formulation(oracle_lib, seed):
         np.testing.assert_array_equal(wv.astype(bool), iwv)
         np.testing.assert_allclose(pv[iwv], iv[iwv], rtol=0, atol=1e-9)
         np.testing.assert_array_equal(pv[~iwv], iv[~iwv])
+
+
+def _independent_in_place(wl, pool_k, pool_v):
+    """The in-place modes as matrix algebra: relocation turns the K rows at
+    each item's slots by its shift (V untouched); the patch mode adds U V^T to
+    the K and V rows at the slots of each patched item, with no rotation."""
+    theta = _theta_np(wl.rope_base, wl.rope_dim)
+    pk = _bits_to_f64(pool_k)
+    pv = _bits_to_f64(pool_v) if pool_v is not None else None
+    wk = np.zeros(pk.shape[:-1], bool)
+    wv = np.zeros(pk.shape[:-1], bool)
+    for i_it, it in enumerate(wl.items):
+        T, p, delta = int(it["n_tokens"]), int(it["patch_id"]), int(it["delta"])
+        if sum(wl.rope_sections) and wl.section_deltas is not None:
+            delta = np.repeat(np.asarray(wl.section_deltas[i_it], np.float64), wl.rope_sections)
+        pos = int(it["dst_pos"]) + np.arange(T)
+        pages, slots = wl.block_table[int(it["seq"]), pos // wl.page_size], pos % wl.page_size
+        for layer in range(wl.num_layers):
+            if wl.mode == "relocate_in_place":
+                if wl.family == W.MLA:
+                    heads, stride, col0 = 1, 0, wl.latent_dim
+                else:
+                    heads, stride, col0 = wl.num_kv_heads, wl.head_dim, 0
+                x = pk[layer, pages, slots]
+                pk[layer, pages, slots] = _complex_rotate_rows(x, heads, wl.rope_dim, stride, col0, delta, theta,
+                                                               wl.pairing)
+                wk[layer, pages, slots] = True
+            elif p >= 0:
+                for ch in range(wl.n_ch):
+                    img, w = (pk, wk) if ch == 0 else (pv, wv)
+                    U = _bits_to_f64(wl.u_rows(p, layer, ch))
+                    V = _bits_to_f64(wl.v_rows(p, layer, ch))
+                    img[layer, pages, slots] = img[layer, pages, slots] + U @ V.T
+                    w[layer, pages, slots] = True
+    return pk, pv, wk, wv
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_in_place_modes_match_independent_formulation(oracle_lib, seed):
+    """The seeded random batches of the GPU fuzz of the in-place modes
+    (sliding-window relocation for even seeds, patch in place for odd ones)
+    through the oracle and through the independent formulation."""
+    from tests.harness import oracle_reference
+    from tests.test_gpu_fuzz import random_workload
+
+    base = random_workload(2000 + seed)
+    mode = "relocate_in_place" if seed % 2 == 0 else "apply_patch"
+    if mode == "apply_patch" and base.rank == 0:
+        base = base.replace(rank=16, patch_lens=base.chunk_lens)
+        base.items["patch_id"] = base.items["chunk_id"]
+    wl = base.replace(mode=mode, pool_init="random")
+    if mode == "apply_patch":
+        _, first = np.unique(wl.items["chunk_id"], return_index=True)
+        wl = wl.replace(items=wl.items[np.sort(first)].copy())
+    pool_k, pool_v = wl.host_pool(0), wl.host_pool(1) if wl.n_ch == 2 else None
+    err, pk, pv, wk, wv = oracle_reference(wl, pool_k, pool_v)
+    assert err == 0
+    ik, iv, iwk, iwv = _independent_in_place(wl, pool_k, pool_v)
+    np.testing.assert_array_equal(wk.astype(bool), iwk)
+    np.testing.assert_allclose(pk[iwk], ik[iwk], rtol=0, atol=1e-9)
+    np.testing.assert_array_equal(pk[~iwk], ik[~iwk])
+    if wl.n_ch == 2:
+        np.testing.assert_array_equal(wv.astype(bool), iwv)
+        np.testing.assert_allclose(pv[iwv], iv[iwv], rtol=0, atol=1e-9)
+        np.testing.assert_array_equal(pv[~iwv], iv[~iwv])

@@ -73,7 +73,8 @@ kamera_status encode(CUtensorMap* map, const void* base, int rank, const cuuint6
 struct DeviceFacts {
   int sms = 0;
   int smem_optin = 0;
-  bool attr_set[4] = {false, false, false, false};
+  bool attr_set[4] = {false, false, false, false};  // reuse kernel variants: shared-memory limit raised
+  bool factor_attr_set = false;                     // both patch-formation instances
 };
 constexpr int kMaxDevices = 64;
 DeviceFacts g_dev[kMaxDevices];
@@ -648,15 +649,22 @@ kamera_status factor_shape(const kamera_factor_desc* d, FactorShape* fs) {
 // The aligned instance when the shapes and pointers allow it (the conditions of
 // factor_kernel<true>), else the one with run-time fallbacks.
 kamera_status launch_factor(const factor::FParams& fp, int grid, uint32_t smem, kamera_stream_t stream) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    const int most = (int)factor::factor_smem_bytes(factor::KMAX, 64);
-    attr_err = cudaFuncSetAttribute(factor::factor_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(factor::factor_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-  });
-  if (attr_err != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  int dev = 0;
+  DeviceFacts* facts = nullptr;
+  if (kamera_status st = device_facts(&dev, &facts)) return st;
+  {
+    // the shared-memory limit is a function attribute of each device: raise it once per device
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!facts->factor_attr_set) {
+      const int most = (int)factor::factor_smem_bytes(factor::KMAX, 64);
+      cudaError_t e =
+          cudaFuncSetAttribute(factor::factor_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(factor::factor_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      facts->factor_attr_set = true;
+    }
+  }
   const bool aligned = ((fp.T | fp.D | fp.k) & 3) == 0 && (fp.delta_stride & 3) == 0 &&
                        ((reinterpret_cast<uintptr_t>(fp.delta) | reinterpret_cast<uintptr_t>(fp.omega) |
                          reinterpret_cast<uintptr_t>(fp.work)) & 15u) == 0;

@@ -644,8 +644,9 @@ __device__ void tn_mma(float* C, int ldc, const float* P, int a, const float* Q,
 // original Gram matrix.  kTC: the coefficient and Gram products on the tensor
 // cores (3xTF32; n a multiple of 4, columns 16-byte aligned), else the fp32
 // warp primitives; the projection update and the triangular solve are fp32
-// row-per-thread loops either way (they keep more loads in flight than a warp
-// tile of MMAs does).
+// loops over rows, two rows per thread, either way (they keep more loads in
+// flight than a warp tile of MMAs does, and each shared-memory coefficient
+// read serves both rows).
 // Scratch (shared): cblk [kp][OB] (coefficients above row J0, the block's Gram
 // matrix from row J0), rmat [OB][OB], inv_diag [OB], thr [OB], orig [OB]
 // (squared original norms), cond [1]; scr 8*TN_P*OB floats (kTC).

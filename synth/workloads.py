@@ -63,6 +63,7 @@ class Workload:
     pool_init: str = "sentinel"  # "sentinel" | "random"
     rope_sections: tuple = (0, 0, 0)  # M-RoPE pairs per (temporal, height, width) section; zeros = plain RoPE
     section_deltas: np.ndarray = None  # [n_items][3] per-section shifts (None: the item's delta everywhere)
+    inv_freq: np.ndarray = None  # explicit fp64 frequency table [rope_dim/2] (None: rope_base^(-2i/rope_dim))
 
     # ---- derived shapes ----------------------------------------------------
     def __post_init__(self):

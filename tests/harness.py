@@ -22,8 +22,8 @@ ABS_TOL = 1e-3
 
 def model_for(wl: W.Workload, t: dict | None = None):
     return pk.model_desc(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
-                         wl.pairing, wl.patch_frame, wl.rope_base, rope_sections=wl.rope_sections,
-                         section_delta=(t or {}).get("section_delta"))
+                         wl.pairing, wl.patch_frame, wl.rope_base, inv_freq=wl.inv_freq,
+                         rope_sections=wl.rope_sections, section_delta=(t or {}).get("section_delta"))
 
 
 def device_inputs(wl: W.Workload, torch, device="cuda", pool_host=None, with_store=True) -> dict:
@@ -83,13 +83,23 @@ def within_tol(gpu_f64: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return np.abs(gpu_f64 - ref) <= ulp_bf16(ref) + ABS_TOL
 
 
+def oracle_theta(wl: W.Workload) -> np.ndarray:
+    """The frequency table both sides use: the workload's explicit table, or
+    the oracle's ladder rope_base^(-2i/rope_dim)."""
+    import oracle
+
+    if wl.inv_freq is not None:
+        return np.ascontiguousarray(wl.inv_freq, np.float64)
+    return oracle.theta(wl.rope_base, wl.rope_dim)
+
+
 def oracle_reference(wl: W.Workload, pool_k_in=None, pool_v_in=None):
     """fp64 oracle over the whole workload (small workloads only)."""
     import oracle
 
     m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
                      wl.pairing, wl.patch_frame, wl.rope_sections)
-    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    th = oracle_theta(wl)
     mode = {"reuse": oracle.MODE_REUSE, "relocate": oracle.MODE_REUSE,
             "relocate_in_place": oracle.MODE_RELOCATE_IN_PLACE, "apply_patch": oracle.MODE_PATCH_IN_PLACE}[wl.mode]
     pk_in = wl.host_pool(0) if pool_k_in is None else pool_k_in
@@ -188,7 +198,7 @@ def oracle_reference_compressed(wl: W.Workload, ocs, pool_k_in=None, pool_v_in=N
 
     m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
                      wl.pairing, wl.patch_frame, wl.rope_sections)
-    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    th = oracle_theta(wl)
     kw = {}
     if wl.rank:
         kw.update(patch=wl.host_patch(), patch_off=wl.patch_off, patch_len=np.array(wl.patch_lens, np.int32),

@@ -195,3 +195,29 @@ def test_mrope_equal_section_shifts_match_plain_rope_bitwise():
     H.call(wl, t1)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(H.to_bits(t0["pool_k"]), H.to_bits(t1["pool_k"]))
+
+
+def scaled_inv_freq(base: float, rope_dim: int, factor: float = 8.0, ctx: float = 8192.0, lo: float = 1.0,
+                    hi: float = 4.0) -> np.ndarray:
+    """A long-context scaled frequency table (the frequency-dependent scaling
+    of Llama 3.1's RoPE): pairs whose wavelength 2 pi / theta is longer than
+    ctx / lo turn `factor` times slower, pairs shorter than ctx / hi keep their
+    frequency, and the band between blends the two linearly in ctx / wavelength."""
+    th = base ** (-2.0 * np.arange(rope_dim // 2) / rope_dim)
+    wl = 2 * np.pi / th
+    smooth = np.clip((ctx / wl - lo) / (hi - lo), 0.0, 1.0)
+    return (1 - smooth) * th / factor + smooth * th
+
+
+@pytest.mark.parametrize("family", [W.GQA, W.MLA])
+@pytest.mark.parametrize("pairing", [W.ROTATE_HALF, W.INTERLEAVED])
+def test_explicit_frequency_table(family, pairing):
+    """R(delta) with an explicit frequency table (kamera_model_desc.inv_freq)
+    in place of the base ladder: the same table drives the oracle."""
+    if family == W.GQA:
+        base = W.gqa_video(num_layers=2, n_chunks=3, T=200, rank=32, page_size=16)
+    else:
+        base = W.mla_lite(num_layers=2, n_chunks=2, T=150, rank=16, page_size=16)
+    th = scaled_inv_freq(base.rope_base, base.rope_dim)
+    assert not np.allclose(th, base.rope_base ** (-2.0 * np.arange(base.rope_dim // 2) / base.rope_dim))
+    run_and_compare(base.replace(inv_freq=th, pairing=pairing))

@@ -248,3 +248,24 @@ def test_compress_chunks_validation(lib):
     assert run(_gqa_model(), _store(), _cstore(v_codes=FAKE + 8)) == pk.KAMERA_ERR_ALIGNMENT
     empty = pk.kamera_chunk_store(None, 0, None, None, 0)
     assert run(_gqa_model(), empty, _cstore(n_chunks=0)) == pk.KAMERA_OK
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """With no built library there is no other path: loading and every call
+    raise ImportError (checked in a fresh interpreter so that this process's
+    loaded library is not disturbed)."""
+    code = (
+        "import sys\n"
+        f"sys.path.insert(0, {os.path.dirname(_build.PKG)!r})\n"
+        "import position_invariant_kv_kamera_gb300 as pk\n"
+        "from position_invariant_kv_kamera_gb300 import _build\n"
+        f"_build.LIB = {str(tmp_path / 'libkamera.so')!r}\n"
+        "for f in (pk.load, pk.abi_version, pk.kamera_v_codebook):\n"
+        "    try:\n"
+        "        f()\n"
+        "    except ImportError:\n"
+        "        continue\n"
+        "    sys.exit('no error from ' + f.__name__)\n"
+    )
+    r = subprocess.run([os.sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr

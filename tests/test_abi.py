@@ -269,3 +269,31 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     )
     r = subprocess.run([os.sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_callable_from_plain_c(lib, tmp_path):
+    """A C program (gcc, no CUDA headers) links against the library and calls
+    it through the header alone: version, codebook, and a validation error
+    with its message (no GPU needed: the call returns before any CUDA call)."""
+    prog = tmp_path / "client.c"
+    prog.write_text(r'''
+#include <stdio.h>
+#include "kamera.h"
+int main(void) {
+  float c[8], t[7];
+  if (kamera_abi_version() != KAMERA_ABI_VERSION) return 1;
+  if (kamera_v_codebook(c, t) != KAMERA_OK) return 2;
+  for (int k = 0; k < 4; ++k) if (c[7 - k] != -c[k] || !(c[k] < c[k + 1])) return 3;
+  kamera_status s = kamera_reuse_batched(NULL, NULL, NULL, NULL, 0, NULL, NULL, NULL);
+  printf("%s|%s|%.4f\n", kamera_status_string(s), kamera_last_error(), c[7]);
+  return s == KAMERA_ERR_NULL ? 0 : 4;
+}
+''')
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(_build.LIB)
+    subprocess.run(["gcc", "-std=c11", "-I" + _build.INCLUDE, "-o", str(exe), str(prog), "-L" + libdir, "-lkamera",
+                    "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    status, msg, c7 = r.stdout.strip().split("|")
+    assert status == "KAMERA_ERR_NULL" and "NULL" in msg and abs(float(c7) - 2.152) < 1e-3

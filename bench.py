@@ -539,7 +539,6 @@ def run_factor(args) -> None:
         torch.cuda.synchronize()
     sec = b.elapsed_time(e) / 1e3 / steps
     flops = n * factor_flops(T, D, m + p, m, q)
-    import json as _json
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     peak = sms * 128 * 2 * 2.07e9 / 1e12  # fp32 FMA lanes x 2 flops x max SM clock
     # CPU: the oracle's exact Jacobi SVD of one slab
@@ -560,7 +559,7 @@ def run_factor(args) -> None:
             "cpu_baseline": {"value": 1.0 / cpu_s, "unit": "slabs/s", "cores": 1, "kind": "oracle",
                              "sample": f"one {T}x{D} slab, exact one-sided Jacobi SVD ({cpu_s:.1f} s)"},
             "gpu_launches": steps, "clocks": clocks.summary()}
-    print(_json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
 
 
 def orbit_traffic(slabs: int) -> float | None:

@@ -18,7 +18,7 @@
 
 #include "kamera.h"
 #include "kamera_compress.cuh"
-#include "kamera_factor.cuh"
+#include "kamera_factor_launch.h"
 #include "kamera_orbit.cuh"
 #include "kamera_kernel.cuh"
 
@@ -657,10 +657,8 @@ kamera_status launch_factor(const factor::FParams& fp, int grid, uint32_t smem, 
     std::lock_guard<std::mutex> lk(g_dev_mu);
     if (!facts->factor_attr_set) {
       const int most = (int)factor::factor_smem_bytes(factor::KMAX, 64);
-      cudaError_t e =
-          cudaFuncSetAttribute(factor::factor_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(factor::factor_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      cudaError_t e = factor::set_smem_limit_aligned(most);
+      if (e == cudaSuccess) e = factor::set_smem_limit_general(most);
       if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
       facts->factor_attr_set = true;
     }
@@ -669,11 +667,7 @@ kamera_status launch_factor(const factor::FParams& fp, int grid, uint32_t smem, 
                        ((reinterpret_cast<uintptr_t>(fp.delta) | reinterpret_cast<uintptr_t>(fp.omega) |
                          reinterpret_cast<uintptr_t>(fp.work)) & 15u) == 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (aligned)
-    factor::factor_kernel<true><<<grid, factor::THREADS, smem, s>>>(fp);
-  else
-    factor::factor_kernel<false><<<grid, factor::THREADS, smem, s>>>(fp);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = aligned ? factor::launch_aligned(fp, grid, smem, s) : factor::launch_general(fp, grid, smem, s);
   if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   return KAMERA_OK;
 }

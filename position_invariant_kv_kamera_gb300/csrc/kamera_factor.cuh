@@ -380,7 +380,7 @@ constexpr int OB = 16;  // column block of the orthonormalisation
 
 // ts_tn for a <= 24: warp w takes rows p = w, w+8, w+16 of C; each lane keeps
 // four panel rows in flight.
-__device__ void ts_tn24(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
+static __device__ void ts_tn24(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp >= a) return;  // no row of C for this warp (warp-uniform)
   float acc[3][OB];
@@ -419,13 +419,13 @@ __device__ void ts_tn24(float* C, int ldc, const float* P, int a, const float* Q
 // C[p][q] = sum_r P[p][r] Q[q][r] for p < a, q < b (b <= 16), C row-major with row
 // stride ldc, in chunks of 24 rows of C; the lanes of a warp split the n rows of
 // the panels and the partial sums meet by shuffles.
-__device__ void ts_tn(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
+static __device__ void ts_tn(float* C, int ldc, const float* P, int a, const float* Q, int b, int n) {
   for (int p0 = 0; p0 < a; p0 += 24) ts_tn24(C + p0 * ldc, ldc, P + (int64_t)p0 * n, min(24, a - p0), Q, b, n);
 }
 
 // X[q][r] -= sum_{p < a} P[p][r] C[p][q] for q < b: rows r and r + THREADS per
 // thread, so that each coefficient read from shared memory serves two rows.
-__device__ void ts_update(float* X, int b, const float* P, int a, const float* C, int ldc, int n) {
+static __device__ void ts_update(float* X, int b, const float* P, int a, const float* C, int ldc, int n) {
   for (int r = threadIdx.x; r < n; r += 2 * THREADS) {
     const int r2 = r + THREADS;
     const bool two = r2 < n;
@@ -461,7 +461,7 @@ __device__ void ts_update(float* X, int b, const float* P, int a, const float* C
 // of R zero, inv_diag[j] = 0) when its pivot -- the squared norm of what remains
 // of column j after the columns before it -- is at most thr[j].  cond receives the
 // ratio of the largest to the smallest kept pivot.
-__device__ void chol_drop(const float* G, float* R, float* inv_diag, const float* thr, int b, float* cond) {
+static __device__ void chol_drop(const float* G, float* R, float* inv_diag, const float* thr, int b, float* cond) {
   const int lane = threadIdx.x & 31;
   float col[OB];
 #pragma unroll
@@ -490,7 +490,7 @@ __device__ void chol_drop(const float* G, float* R, float* inv_diag, const float
 // X <- X R^{-1} row by row (forward substitution), R upper triangular, dropped
 // columns become zero; rows r and r + THREADS per thread, so that each entry of
 // R read from shared memory serves two rows.
-__device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, int n) {
+static __device__ void ts_trsm(float* X, int b, const float* R, const float* inv_diag, int n) {
   for (int r = threadIdx.x; r < n; r += 2 * THREADS) {
     const int r2 = r + THREADS;
     const bool two = r2 < n;
@@ -559,7 +559,7 @@ constexpr int TN_P = 48;  // columns of P per pass of tn_mma
 // rows 4t4 + 2s and 4t4 + 2s + 1 (a permutation of the rows, which the sum does not
 // see).  The warps' partial sums meet in scr (8 x TN_P x 16 floats of shared
 // memory) and are added in warp order.
-__device__ void tn_mma(float* C, int ldc, const float* P, int a, const float* Q, int b, int n, float* scr) {
+static __device__ void tn_mma(float* C, int ldc, const float* P, int a, const float* Q, int b, int n, float* scr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
   const int nch = (n + 15) >> 4;
   for (int p0 = 0; p0 < a; p0 += TN_P) {
@@ -710,7 +710,7 @@ __device__ void orth_block(float* X, int n, int k, float* cblk, float* rmat, flo
 // major, in shared memory) with the parallel (round-robin tournament) order:
 // each round rotates kp/2 disjoint planes at once.  On return the diagonal of
 // C holds the eigenvalues and the columns of W the eigenvectors.
-__device__ void jacobi_eig(float* C, float* W, int kp, int ld, float* rot, float* red) {
+static __device__ void jacobi_eig(float* C, float* W, int kp, int ld, float* rot, float* red) {
   const int tid = threadIdx.x;
   for (int e = tid; e < kp * kp; e += THREADS) W[(e / kp) * ld + e % kp] = (e / kp == e % kp) ? 1.f : 0.f;
   __syncthreads();

@@ -297,3 +297,17 @@ int main(void) {
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     status, msg, c7 = r.stdout.strip().split("|")
     assert status == "KAMERA_ERR_NULL" and "NULL" in msg and abs(float(c7) - 2.152) < 1e-3
+
+
+def test_every_cuda_build_targets_sm_103a_only():
+    """The library's units, its link and the generator's device twin are
+    built for sm_103a alone (one -gencode, no PTX for other targets)."""
+    from synth import device as synth_device
+
+    cmds = [_build.compile_cmd(s) for s in _build.SOURCES] + [_build.link_cmd(), synth_device.build_cmd()]
+    for cmd in cmds:
+        gencodes = [cmd[i + 1] for i, a in enumerate(cmd) if a == "-gencode"]
+        assert gencodes == ["arch=compute_103a,code=sm_103a"], cmd
+        assert not any(a.startswith(("-arch", "--gpu-architecture", "-code")) for a in cmd), cmd
+    for cmd in cmds[:-2]:
+        assert "-lineinfo" in cmd and "-O3" in cmd

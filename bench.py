@@ -279,12 +279,14 @@ def run_reference(args) -> None:
     name = args.workload
     comp = name in COMPRESSED
     base = COMPRESSED.get(name, name)
-    timer = time_oracle_compressed if comp else time_oracle
     # one step = the oracle over a token sample of one chunk, all layers, sized so
-    # that warm-up + timed steps take about two minutes in total
+    # that warm-up + timed steps take about two minutes in total; the size comes
+    # from a warm probe (a cold first call overstates the cost per token)
     full_T = {"gqa_video": 1024, "mla_lite": 2048, "long_video": 1296}.get(base)
-    dt_probe, tok_probe = timer(oracle_sample_workload(base, 1, 16 if full_T else None))
-    per_tok = dt_probe / max(tok_probe, 1)
+    probe = oracle_sample_workload(base, 1, 16 if full_T else None)
+    probe_call = oracle_call(probe, compressed=comp)
+    probe_call()
+    per_tok = timed(probe_call) / max(probe.tokens, 1)
     budget = 120.0 / (args.steps + args.warmup)
     n_tok = max(1, min(full_T or tok_probe, int(budget / max(per_tok, 1e-9))))
     sample = oracle_sample_workload(base, 1, n_tok if full_T else None)

@@ -48,13 +48,10 @@
  *     not overlap, except for the in-place modes, where each slot is read and
  *     written by the same item.  Two items writing the same slot is a caller
  *     error (the result is one of the two).
- *   - Launch-shape overrides (for tuning sweeps and tests; results do not
- *     depend on them): the reuse entry points read the environment variables
- *     KAMERA_BN (tile width, 64/128/192/256), KAMERA_STAGES (canonical
- *     stages, 2..6), KAMERA_UV_SLOTS (patch-factor slots, 1 or 2),
- *     KAMERA_KSPLIT (patch factors staged in 1, 2 or 4 parts of the rank) and
- *     KAMERA_NO_PDL (non-zero: no programmatic dependent launch).  Unset, the
- *     library picks the widest tile and the deepest pipeline that fit.
+ *   - Launch shape: the reuse entry points pick the widest tile and the
+ *     deepest pipeline that fit; kamera_set_launch_tuning (below) overrides
+ *     that process-wide for tuning sweeps and tests.  Results do not depend
+ *     on the launch shape.
  */
 #ifndef KAMERA_H_
 #define KAMERA_H_
@@ -68,7 +65,7 @@ extern "C" {
 /* The CUDA stream type (cudaStream_t), declared without the CUDA headers. */
 typedef struct CUstream_st* kamera_stream_t;
 
-#define KAMERA_ABI_VERSION 3
+#define KAMERA_ABI_VERSION 4
 
 typedef enum {
   KAMERA_OK = 0,
@@ -270,7 +267,9 @@ kamera_status kamera_orbit_mean(const float* deltas, int32_t n_orderings, int64_
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the array and it keeps the last
+ * before any stream capture.  The address is kept for the life of the process:
+ * after cudaDeviceReset of a device the kept address is stale, so a process
+ * that resets a device must not call this entry point on that device again.  All calls share the array and it keeps the last
  * call's contents; the kernel clears what it needs, so no caller action is
  * required -- but calls that overlap on the GPU (different streams, no
  * ordering between them) race on the array and must not be issued.
@@ -352,6 +351,41 @@ kamera_status kamera_reuse_compressed(const kamera_model_desc* model, const kame
                                       const kamera_patch_store* patches, const kamera_reuse_item* items,
                                       int32_t n_items, const kamera_paged_pool* pool, int32_t* err_flag,
                                       kamera_stream_t stream);
+
+/*
+ * Launch tuning (no counterpart on the pages: a knob of this library).  One
+ * process-wide setting, read by every later call of the reuse entry points
+ * (kamera_reuse_batched, kamera_relocate, kamera_apply_patch,
+ * kamera_reuse_compressed); a field left 0 keeps the library's own choice.
+ * It exists for tuning sweeps and tests: the output bits do not depend on
+ * bn, stages, uv_slots, ksplit, no_pdl or grid.  A shape that does not fit
+ * a call (e.g. bn not dividing D) makes that call return
+ * KAMERA_ERR_UNSUPPORTED.  Thread-safe; calls already enqueued keep the
+ * setting they were launched with.
+ */
+typedef struct {
+  int32_t bn;             /* tile width in columns: 64, 128, 192 or 256 */
+  int32_t stages;         /* canonical tile stages in shared memory: 2..6 */
+  int32_t uv_slots;       /* patch-factor slots: 1 or 2 */
+  int32_t ksplit;         /* patch factors staged in 1, 2 or 4 parts of the rank */
+  int32_t no_pdl;         /* non-zero: launch without programmatic dependent launch */
+  int32_t grid;           /* CTAs of the persistent grid, 1..65535; 0 = one per SM */
+  int64_t wait_limit_ns;  /* bound on every wait inside the kernel, 1 us .. 60 s; 0 = 2 s */
+  /* TEST ONLY.  Non-zero: in every CTA the producer leaves the first canonical
+   * stage unfilled and its barrier unarmed, so the waits on it run out after
+   * wait_limit_ns.  The call then sets KAMERA_EFLAG_TIMEOUT, and each CTA
+   * stops, waits (bounded) for its own copies and tensor-core work in flight,
+   * releases its tensor memory and exits; the pool rows of the call are
+   * incomplete.  This exercises the expiry path without any fault. */
+  int32_t test_unarm_first_stage;
+  int32_t reserved;       /* 0 */
+} kamera_launch_tuning;
+
+/* Set the process-wide tuning (NULL: back to the defaults, all fields 0).
+ * KAMERA_ERR_INVALID_ARG for a field out of the ranges above. */
+kamera_status kamera_set_launch_tuning(const kamera_launch_tuning* tuning);
+/* Read the current setting. */
+kamera_status kamera_get_launch_tuning(kamera_launch_tuning* tuning);
 
 /* Human-readable name of a status code (static storage). */
 const char* kamera_status_string(kamera_status status);

@@ -27,8 +27,8 @@ KAMERA_EFLAG_CHUNK_OOB, KAMERA_EFLAG_PAGE_OOB, KAMERA_EFLAG_PATCH_OOB, KAMERA_EF
 
 EXPORTS = ("kamera_reuse_batched", "kamera_relocate", "kamera_apply_patch", "kamera_factor_workspace_size",
            "kamera_factor_patches", "kamera_factor_patches_noalloc", "kamera_orbit_mean", "kamera_v_codebook",
-           "kamera_compress_chunks", "kamera_reuse_compressed", "kamera_status_string", "kamera_last_error",
-           "kamera_abi_version")
+           "kamera_compress_chunks", "kamera_reuse_compressed", "kamera_set_launch_tuning",
+           "kamera_get_launch_tuning", "kamera_status_string", "kamera_last_error", "kamera_abi_version")
 FACTOR_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -66,6 +66,13 @@ class kamera_compressed_store(ctypes.Structure):
     _fields_ = [("k_codes", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
                 ("v_norm", ctypes.c_void_p), ("row_offset", ctypes.c_void_p), ("len", ctypes.c_void_p),
                 ("n_chunks", ctypes.c_int32), ("reserved", ctypes.c_int32), ("n_rows", ctypes.c_int64)]
+
+
+class kamera_launch_tuning(ctypes.Structure):
+    _fields_ = [("bn", ctypes.c_int32), ("stages", ctypes.c_int32), ("uv_slots", ctypes.c_int32),
+                ("ksplit", ctypes.c_int32), ("no_pdl", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64), ("test_unarm_first_stage", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 # kamera_reuse_item as a numpy record (32 bytes, naturally aligned)
@@ -117,6 +124,10 @@ def load(build_if_missing: bool = False):
         lib.kamera_compress_chunks.restype = ctypes.c_int
         lib.kamera_reuse_compressed.argtypes = [P, P, P, P, ctypes.c_int32, P, P, P]
         lib.kamera_reuse_compressed.restype = ctypes.c_int
+        lib.kamera_set_launch_tuning.argtypes = [P]
+        lib.kamera_set_launch_tuning.restype = ctypes.c_int
+        lib.kamera_get_launch_tuning.argtypes = [P]
+        lib.kamera_get_launch_tuning.restype = ctypes.c_int
         lib.kamera_status_string.argtypes = [ctypes.c_int]
         lib.kamera_status_string.restype = ctypes.c_char_p
         lib.kamera_last_error.argtypes = []
@@ -141,6 +152,20 @@ def abi_version() -> int:
 
 def _ref(s):
     return None if s is None else ctypes.byref(s)
+
+
+def kamera_set_launch_tuning(tuning=None, raise_on_error=True, **fields) -> int:
+    """Process-wide launch tuning of the reuse entry points (a
+    kamera_launch_tuning, or its fields as keywords; neither = defaults)."""
+    if tuning is None and fields:
+        tuning = kamera_launch_tuning(**fields)
+    return _check(load().kamera_set_launch_tuning(_ref(tuning)), raise_on_error)
+
+
+def kamera_get_launch_tuning() -> kamera_launch_tuning:
+    t = kamera_launch_tuning()
+    _check(load().kamera_get_launch_tuning(ctypes.byref(t)), True)
+    return t
 
 
 def _check(status: int, raise_on_error: bool) -> int:

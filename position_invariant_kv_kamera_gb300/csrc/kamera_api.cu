@@ -150,11 +150,37 @@ const Codebook& codebook() {
 
 enum Mode { MODE_REUSE = 0, MODE_RELOCATE_IN_PLACE = 1, MODE_PATCH_IN_PLACE = 2 };
 
-// Optional launch-shape overrides (tuning sweeps, configuration-invariance tests):
-// KAMERA_BN, KAMERA_STAGES, KAMERA_UV_SLOTS, KAMERA_KSPLIT, KAMERA_NO_PDL.
-int env_int(const char* name) {
-  const char* s = getenv(name);
-  return s ? atoi(s) : 0;
+// Process-wide launch tuning (kamera_set_launch_tuning): copied under the lock
+// at each call, so a call never sees a half-written setting.
+kamera_launch_tuning g_tuning = {};
+std::mutex g_tuning_mu;
+
+kamera_launch_tuning current_tuning() {
+  std::lock_guard<std::mutex> lk(g_tuning_mu);
+  return g_tuning;
+}
+
+kamera_status set_tuning(const kamera_launch_tuning* t) {
+  g_last_error.clear();
+  kamera_launch_tuning v = {};
+  if (t) {
+    v = *t;
+    if (v.bn != 0 && v.bn != 64 && v.bn != 128 && v.bn != 192 && v.bn != 256)
+      return fail(KAMERA_ERR_INVALID_ARG, "tuning: bn = %d (0, 64, 128, 192 or 256)", v.bn);
+    if (v.stages != 0 && (v.stages < 2 || v.stages > 6))
+      return fail(KAMERA_ERR_INVALID_ARG, "tuning: stages = %d (0 or 2..6)", v.stages);
+    if (v.uv_slots < 0 || v.uv_slots > 2) return fail(KAMERA_ERR_INVALID_ARG, "tuning: uv_slots = %d", v.uv_slots);
+    if (v.ksplit != 0 && v.ksplit != 1 && v.ksplit != 2 && v.ksplit != 4)
+      return fail(KAMERA_ERR_INVALID_ARG, "tuning: ksplit = %d (0, 1, 2 or 4)", v.ksplit);
+    if (v.grid < 0 || v.grid > 65535) return fail(KAMERA_ERR_INVALID_ARG, "tuning: grid = %d", v.grid);
+    if (v.wait_limit_ns != 0 && (v.wait_limit_ns < 1000 || v.wait_limit_ns > 60000000000ll))
+      return fail(KAMERA_ERR_INVALID_ARG, "tuning: wait_limit_ns = %lld (0 or 1e3 .. 6e10)",
+                  (long long)v.wait_limit_ns);
+    if (v.reserved != 0) return fail(KAMERA_ERR_INVALID_ARG, "tuning: reserved must be 0");
+  }
+  std::lock_guard<std::mutex> lk(g_tuning_mu);
+  g_tuning = v;
+  return KAMERA_OK;
 }
 
 kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chunk_store* store,
@@ -329,16 +355,22 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   int dev = 0;
   DeviceFacts* facts = nullptr;
   if (kamera_status st = device_facts(&dev, &facts)) return st;
-  const int bn_env = env_int("KAMERA_BN"), st_env = env_int("KAMERA_STAGES"), uv_env = env_int("KAMERA_UV_SLOTS"),
-            ks_env = env_int("KAMERA_KSPLIT");
+  const kamera_launch_tuning tune = current_tuning();
+  const int bn_env = tune.bn, st_env = tune.stages, uv_env = tune.uv_slots, ks_env = tune.ksplit;
   int BN = 0, stages = 0, uv_slots = 0, ksplit = 1, kg_alloc = 0;
   uint32_t stage_bytes = 0, uv_slot_bytes = 0;
   // compressed: the stage also holds the codes (BN*128 bytes for K, more than
   // the 3BN/8 * 128 of V), plus the replicated centroid-sum table
   const uint32_t table_bytes = comp ? 64u * 32u * 4u : 0u;
+  // Widest tile first (fewer, longer TMA boxes per byte moved), except for
+  // calls with fewer (item, layer, channel) slabs than SMs: their tiles are
+  // the only parallelism, so the narrowest tile that keeps rotation pairs
+  // whole spreads them over the most SMs.
+  const int n_ch_work = mode == MODE_RELOCATE_IN_PLACE ? 1 : n_ch_layout;
+  const bool small_call = (int64_t)n_items * model->num_layers * n_ch_work < (int64_t)facts->sms;
   const int cands[4] = {256, 192, 128, 64};
   for (int ci = 0; ci < 4 && BN == 0; ++ci) {
-    const int bn = cands[ci];
+    const int bn = cands[small_call ? 3 - ci : ci];
     if (bn_env && bn != bn_env) continue;
     if (D % bn != 0) continue;
     if (comp && bn % 128 != 0) continue;  // 128-column K boxes; 16-byte V code boxes
@@ -398,7 +430,7 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   p.num_layers = model->num_layers;
   p.D = D;
   p.n_ch_layout = n_ch_layout;
-  p.n_ch_work = mode == MODE_RELOCATE_IN_PLACE ? 1 : n_ch_layout;
+  p.n_ch_work = n_ch_work;
   p.BN = BN;
   p.stages = stages;
   p.uv_slots = uv_slots;
@@ -417,6 +449,8 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   while (tc < 2u * (uint32_t)BN) tc <<= 1;
   p.tmem_cols = tc;
   p.err_flag = err_flag;
+  p.wait_limit_ns = tune.wait_limit_ns > 0 ? (uint64_t)tune.wait_limit_ns : WAIT_LIMIT_NS;
+  p.test_unarm = tune.test_unarm_first_stage ? 1 : 0;
   if (mode == MODE_RELOCATE_IN_PLACE) {
     // only the column blocks that hold rotated groups change
     int lo = D / BN, hi = -1;
@@ -520,13 +554,13 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   // previous kernel on the stream drains; the kernel waits for it
   // (griddepcontrol.wait) before touching global memory.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)facts->sms);
+  cfg.gridDim = dim3((unsigned)(tune.grid > 0 ? tune.grid : facts->sms));
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = env_int("KAMERA_NO_PDL") ? 0 : 1;
+  attr[0].val.programmaticStreamSerializationAllowed = tune.no_pdl ? 0 : 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
@@ -890,6 +924,17 @@ const char* kamera_status_string(kamera_status status) {
 }
 
 const char* kamera_last_error(void) { return kamera::g_last_error.c_str(); }
+
+kamera_status kamera_set_launch_tuning(const kamera_launch_tuning* tuning) { return kamera::set_tuning(tuning); }
+
+kamera_status kamera_get_launch_tuning(kamera_launch_tuning* tuning) {
+  if (!tuning) {
+    kamera::g_last_error = "tuning is NULL";
+    return KAMERA_ERR_NULL;
+  }
+  *tuning = kamera::current_tuning();
+  return KAMERA_OK;
+}
 
 int32_t kamera_abi_version(void) { return KAMERA_ABI_VERSION; }
 

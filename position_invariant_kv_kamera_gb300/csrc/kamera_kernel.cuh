@@ -6,10 +6,12 @@
 //
 //     out = R(delta) . KV(B|empty) + U_m V_m^T        -> bf16 -> paged pool slot
 //
-// Work unit ("row block"): 128 destination positions (aligned to 128 in
-// position space) of one (item, layer, channel); it is processed as tiles of
-// BN columns.  CTAs take row blocks round-robin.  Per CTA (384 threads, one
-// CTA per SM):
+// Row block: 128 destination positions (aligned to 128 in position space) of
+// one (item, layer, channel); it splits into tiles of BN columns.  The work
+// unit is one tile; CTAs take tiles round-robin (tile g is column block
+// g mod n_cb of row block g / n_cb), so the last round is at most one tile
+// deep and small calls spread over as many SMs as they have tiles.  Per CTA
+// (384 threads, one CTA per SM):
 //   warp 0      TMA producer: the canonical tile (64-column boxes, 128B
 //               swizzle; from the chunk store, or page by page from the pool
 //               for the in-place modes) and, for patched items, the U tile
@@ -36,7 +38,8 @@
 // length d/2 in registers and the scale ||v|| / d.  Each epilogue half decodes
 // its half of every head.  The decoded row then takes the same rotation,
 // patch and store as a bf16 canonical row.
-// Every wait on an mbarrier is bounded (about 2 s): on expiry the kernel sets
+// Every wait on an mbarrier is bounded (2 s unless the call sets another
+// limit): on expiry the kernel sets
 // KAMERA_EFLAG_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #pragma once
 #include <cuda_bf16.h>
@@ -58,7 +61,7 @@ constexpr int MAX_GROUPS = 64;      // 32-column groups per row (D <= 2048)
 constexpr int MAX_PAIRS = 128;      // rope_dim / 2
 constexpr int BOX_COLS = 64;        // 64 bf16 = one 128-byte swizzle row
 constexpr uint32_t BOX_BYTES = BM * 128;  // one 64-column box of 128 rows
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // default bound of every wait (the call may set another)
 
 // group kinds (per 32-column group of a key row); a positive value is a
 // rotate-half first half whose partner group is that many groups to the right
@@ -114,6 +117,8 @@ struct Params {
   const int64_t* section_delta;    // [n_items][3] per-section shifts, or nullptr (every section: item delta)
   uint32_t stage_bytes, u_bytes, v_bytes, tmem_cols;  // stage_bytes = one canonical tile
   int32_t* err_flag;
+  uint64_t wait_limit_ns;  // bound of every wait
+  int32_t test_unarm;      // test only: the producer leaves its first stage unfilled (the waits on it run out)
   // compressed canonical store (kComp)
   CUtensorMap kc_map;  // K codes as rows [rows][D] uint8: box 128 x 128, 128B swizzle
   CUtensorMap vc_map;  // V codes as rows [rows][3D/8] uint8: box 3BN/8 x 128, no swizzle
@@ -260,6 +265,7 @@ struct SmemMisc {
   uint32_t tmem_base;
   int32_t abort_flag;
   int64_t total_tiles;
+  uint64_t wait_limit;  // ns
 };
 
 struct Smem {
@@ -317,7 +323,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Sme
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && *reinterpret_cast<volatile int32_t*>(&misc->abort_flag)) return false;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (global_timer_ns() - t0 > misc->wait_limit) {
       *reinterpret_cast<volatile int32_t*>(&misc->abort_flag) = 1;
       if (err_flag) atomicOr(err_flag, KAMERA_EFLAG_TIMEOUT);
       return false;
@@ -678,12 +684,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       err |= __shfl_xor_sync(0xFFFFFFFFu, err, o);
     }
     if (lane == 0) {
-      sm.misc->total_tiles = n;
+      sm.misc->total_tiles = n * p.n_cb;
       if (blockIdx.x == 0 && err && p.err_flag) atomicOr(p.err_flag, err);
     }
   }
   __syncthreads();
-  if ((int64_t)blockIdx.x >= sm.misc->total_tiles) return;  // no row block for this CTA
+  if ((int64_t)blockIdx.x >= sm.misc->total_tiles) return;  // no tile for this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -701,6 +707,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     }
     mbar_init(sm.drain, 1);
     sm.misc->abort_flag = 0;
+    sm.misc->wait_limit = p.wait_limit_ns;
     fence_mbar_init();
   }
   if (kPatch) {
@@ -746,10 +753,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t it = 0;
-      bool go = true;
-      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
-        walk_to(p, w, g);
-        Tile t = decode(p, w, g);
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+        const int64_t rb = g / p.n_cb;
+        const int cbi = (int)(g - rb * p.n_cb);
+        walk_to(p, w, rb);
+        const Tile t = decode(p, w, rb);
         // pool rows of the row block's page segments (in-place source)
         int32_t seg_y[BM / 8];
         uint32_t bytes = (uint32_t)nbox * BOX_BYTES;
@@ -768,31 +776,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         } else if (!p.src_pool) {
           src_row = (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
         }
-        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
-          const int s = (int)(it % (uint32_t)p.stages);
-          const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
-          if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-          uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
-          const int col0 = (p.cb_first + cbi) * p.BN;
-          mbar_arrive_expect_tx(&sm.full[s], bytes);
-          if (kComp) {
-            uint8_t* stg = st + p.out_bytes;
-            if (t.ch == 0) {
-              for (int b = 0; b < p.BN / 128; ++b)
-                tma_load_2d(stg + b * BOX_BYTES, &p.kc_map, &sm.full[s], col0 + b * 128, src_row);
-            } else {
-              tma_load_2d(stg, &p.vc_map, &sm.full[s], (p.cb_first + cbi) * (3 * p.BN / 8), src_row);
-            }
-          } else if (!p.src_pool) {
-            for (int b = 0; b < nbox; ++b)
-              tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, src_row);
+        const int s = (int)(it % (uint32_t)p.stages);
+        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) break;
+        if (p.test_unarm && it == 0) continue;  // test only: this stage's barrier is never armed
+        uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+        const int col0 = (p.cb_first + cbi) * p.BN;
+        mbar_arrive_expect_tx(&sm.full[s], bytes);
+        if (kComp) {
+          uint8_t* stg = st + p.out_bytes;
+          if (t.ch == 0) {
+            for (int b = 0; b < p.BN / 128; ++b)
+              tma_load_2d(stg + b * BOX_BYTES, &p.kc_map, &sm.full[s], col0 + b * 128, src_row);
           } else {
-            for (int sg = 0; sg < nseg; ++sg) {
-              if (seg_y[sg] < 0) continue;
-              for (int b = 0; b < nbox; ++b)
-                tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
-                            col0 + b * BOX_COLS, seg_y[sg]);
-            }
+            tma_load_2d(stg, &p.vc_map, &sm.full[s], (p.cb_first + cbi) * (3 * p.BN / 8), src_row);
+          }
+        } else if (!p.src_pool) {
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, src_row);
+        } else {
+          for (int sg = 0; sg < nseg; ++sg) {
+            if (seg_y[sg] < 0) continue;
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
+                          col0 + b * BOX_COLS, seg_y[sg]);
           }
         }
       }
@@ -813,24 +820,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       uint32_t pu = 0;
       bool go = true;
       for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
-        walk_to(p, w, g);
+        const int64_t rb = g / p.n_cb;
+        const int cbi = (int)(g - rb * p.n_cb);
+        walk_to(p, w, rb);
         if (w.patch < 0) continue;
-        const Tile t = decode(p, w, g);
+        const Tile t = decode(p, w, rb);
         const int64_t prow = p.patch_off[w.patch] / p.rank +
                              ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
         const int32_t u_row = (int32_t)(prow + (t.pos0 - w.dst_pos));
         const int kg_chunk = p.rank / 8 / p.ksplit;  // K groups per chunk
-        for (int cbi = 0; cbi < p.n_cb && go; ++cbi) {
-          for (int kc = 0; kc < p.ksplit; ++kc, ++pu) {
-            const int u = (int)(pu % (uint32_t)p.uv_slots);
-            const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
-            if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-            uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
-            mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
-            tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, u_row, kc * kg_chunk);
-            tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0,
-                        (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), kc * kg_chunk);
-          }
+        for (int kc = 0; kc < p.ksplit; ++kc, ++pu) {
+          const int u = (int)(pu % (uint32_t)p.uv_slots);
+          const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
+          if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+          uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
+          mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
+          tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, u_row, kc * kg_chunk);
+          tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0,
+                      (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), kc * kg_chunk);
         }
       }
       const uint32_t S = (uint32_t)p.uv_slots;
@@ -849,28 +856,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       uint32_t pt = 0, pc = 0;  // patched tiles, patch-factor chunks
       bool issued = false, go = true;
       for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
-        walk_to(p, w, g);
+        walk_to(p, w, g / p.n_cb);
         if (w.patch < 0) continue;
-        for (int cbi = 0; cbi < p.n_cb && go; ++cbi, ++pt) {
-          const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
-          if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-          for (int kc = 0; kc < p.ksplit; ++kc, ++pc) {
-            const int u = (int)(pc % (uint32_t)p.uv_slots);
-            const uint32_t uph = (pc / (uint32_t)p.uv_slots) & 1u;
-            if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) { go = false; break; }
-            tc_fence_after_sync();
-            const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
-            for (int k = 0; k < p.ksteps; ++k) {
-              const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
-              const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
-              umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
-            }
-            umma_commit(&sm.uv_empty[u]);
-            issued = true;
+        const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
+        if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) break;
+        for (int kc = 0; kc < p.ksplit; ++kc, ++pc) {
+          const int u = (int)(pc % (uint32_t)p.uv_slots);
+          const uint32_t uph = (pc / (uint32_t)p.uv_slots) & 1u;
+          if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) { go = false; break; }
+          tc_fence_after_sync();
+          const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
+          for (int k = 0; k < p.ksteps; ++k) {
+            const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
+            const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+            umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
           }
-          if (!go) break;
-          umma_commit(&sm.tfull[buf]);
+          umma_commit(&sm.uv_empty[u]);
+          issued = true;
         }
+        if (!go) break;
+        umma_commit(&sm.tfull[buf]);
+        ++pt;
       }
       if (issued) {
         umma_commit(sm.drain);
@@ -883,10 +889,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t it = 0;
-      bool go = true;
-      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
-        walk_to(p, w, g);
-        const Tile t = decode(p, w, g);
+      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+        const int64_t rb = g / p.n_cb;
+        const int cbi = (int)(g - rb * p.n_cb);
+        walk_to(p, w, rb);
+        const Tile t = decode(p, w, rb);
         int32_t seg_y[BM / 8];  // pool row of each valid page segment, else -1
         bool seg_full[BM / 8];
         int lo8 = 0, hi8 = 0;   // 8-row sub-blocks of the row block inside the item: [lo8, hi8)
@@ -900,33 +907,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           seg_y[sg] = seg.y;
           seg_full[sg] = seg.full;
         }
-        for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
-          const int s = (int)(it % (uint32_t)p.stages);
-          const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
-          if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) { go = false; break; }
-          const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
-          const int col0 = (p.cb_first + cbi) * p.BN;
-          for (int sg = 0; sg < nseg; ++sg) {
-            if (seg_y[sg] < 0) continue;
-            if (seg_full[sg]) {
-              for (int b = 0; b < nbox; ++b)
-                tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
-                             col0 + b * BOX_COLS, seg_y[sg]);
-              continue;
-            }
-            // partly covered page: its 8-row sub-blocks that lie inside the item
-            const int r0 = sg * p.seg_rows;
-            for (int k8 = r0 >> 3; k8 < ((r0 + p.seg_rows) >> 3); ++k8) {
-              if (k8 < lo8 || k8 >= hi8) continue;
-              for (int b = 0; b < nbox; ++b)
-                tma_store_2d(&p.pool_map8[t.ch], st + b * BOX_BYTES + (uint32_t)k8 * 1024u, col0 + b * BOX_COLS,
-                             seg_y[sg] + (k8 * 8 - r0));
-            }
+        const int s = (int)(it % (uint32_t)p.stages);
+        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+        if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) break;
+        // after a wait gave up, tiles may be marked computed without being so: store nothing more
+        if (*reinterpret_cast<volatile int32_t*>(&sm.misc->abort_flag)) break;
+        const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+        const int col0 = (p.cb_first + cbi) * p.BN;
+        for (int sg = 0; sg < nseg; ++sg) {
+          if (seg_y[sg] < 0) continue;
+          if (seg_full[sg]) {
+            for (int b = 0; b < nbox; ++b)
+              tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
+                           col0 + b * BOX_COLS, seg_y[sg]);
+            continue;
           }
-          bulk_commit_group();
-          bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
-          mbar_arrive(&sm.empty[s]);
+          // partly covered page: its 8-row sub-blocks that lie inside the item
+          const int r0 = sg * p.seg_rows;
+          for (int k8 = r0 >> 3; k8 < ((r0 + p.seg_rows) >> 3); ++k8) {
+            if (k8 < lo8 || k8 >= hi8) continue;
+            for (int b = 0; b < nbox; ++b)
+              tma_store_2d(&p.pool_map8[t.ch], st + b * BOX_BYTES + (uint32_t)k8 * 1024u, col0 + b * BOX_COLS,
+                           seg_y[sg] + (k8 * 8 - r0));
+          }
         }
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
+        mbar_arrive(&sm.empty[s]);
       }
       bulk_wait_group0();
     }
@@ -941,11 +948,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     Walker w;
     walker_init(w);
     int32_t table_item[2] = {-1, -1};  // item whose phases each table holds
-    uint32_t it = 0, pt = 0, rbi = 0;
+    uint32_t it = 0, pt = 0;  // tiles of this CTA, patched tiles
     bool ok = true;  // warp-uniform: every wait of this warp so far succeeded
-    for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++rbi) {
-      walk_to(p, w, g);
-      Tile t = decode(p, w, g);
+    for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+      const int64_t rb = g / p.n_cb;
+      walk_to(p, w, rb);
+      Tile t = decode(p, w, rb);
+      t.cb = p.cb_first + (int)(g - rb * p.n_cb);
       const bool patched = kPatch && w.patch >= 0;
       const bool rot = p.rotate && t.ch == 0;
       // destination of row r: rows of whole page segments go out with the TMA
@@ -973,10 +982,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         if (tok >= 0 && tok < w.T) crow = p.comp_row_offset[w.chunk] + (int64_t)t.layer * w.T + tok;
         if (t.ch == 0) kscale = p.k_scale[(int64_t)w.chunk * p.num_layers + t.layer];
       }
-      // phase tables alternate by row-block parity: their previous readers
+      // phase tables alternate by tile parity: their previous readers
       // finished before the last joint barrier
-      float2* cs = sm.cs + (rbi & 1u) * pairs_pad(p.n_pairs);
-      if (h == 1 && rot && w.item != table_item[rbi & 1u]) {
+      float2* cs = sm.cs + (it & 1u) * pairs_pad(p.n_pairs);
+      if (h == 1 && rot && w.item != table_item[it & 1u]) {
         float* csf = reinterpret_cast<float*>(cs);
         for (int i = et - 128; i < p.n_pairs; i += 128) {
           const float2 v = phase_cs(i < p.sec_end0 ? w.d0 : (i < p.sec_end1 ? w.d1 : w.d2), p.theta[i]);
@@ -984,11 +993,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           csf[4 * (i >> 1) + 2 + (i & 1)] = v.y;
         }
       }
-      if (rot) table_item[rbi & 1u] = w.item;
+      if (rot) table_item[it & 1u] = w.item;
       if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the table is ready
 
-      for (int cbi = 0; cbi < p.n_cb; ++cbi, ++it) {
-        t.cb = p.cb_first + cbi;
+      {
         const int s = (int)(it % (uint32_t)p.stages);
         const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
         const uint32_t buf = pt & 1u;

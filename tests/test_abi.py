@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert pk.abi_version() == 3
+    assert pk.abi_version() == 4
     assert pk.status_string(pk.KAMERA_OK) == "KAMERA_OK"
     assert pk.status_string(pk.KAMERA_ERR_CUDA) == "KAMERA_ERR_CUDA"
     assert pk.status_string(99) == "KAMERA_ERR_UNKNOWN"
@@ -181,6 +181,28 @@ def test_factor_validation(lib):
     assert pk.kamera_factor_patches(d, FAKE, FAKE, 1 << 20, FAKE + 16, 1 << 30, None, False) == pk.KAMERA_ERR_ALIGNMENT
     empty = pk.kamera_factor_desc(None, 0, 0, 300, 256, 16, 16, 1, None)
     assert pk.kamera_factor_patches(empty, None, None, 0, None, 0, None, False) == pk.KAMERA_OK
+
+
+def test_launch_tuning_set_get_and_validation(lib):
+    """The process-wide launch tuning round-trips, rejects out-of-range fields
+    and resets to the defaults (all zero: the library's own choice, a 2 s wait
+    bound) with NULL.  Host-only calls."""
+    try:
+        pk.kamera_set_launch_tuning(bn=128, stages=3, uv_slots=1, ksplit=2, no_pdl=1, grid=40,
+                                    wait_limit_ns=1_000_000, test_unarm_first_stage=1)
+        t = pk.kamera_get_launch_tuning()
+        assert (t.bn, t.stages, t.uv_slots, t.ksplit, t.no_pdl, t.grid, t.wait_limit_ns,
+                t.test_unarm_first_stage) == (128, 3, 1, 2, 1, 40, 1_000_000, 1)
+        for bad in ({"bn": 96}, {"stages": 1}, {"stages": 7}, {"uv_slots": 3}, {"ksplit": 3}, {"grid": -1},
+                    {"grid": 70000}, {"wait_limit_ns": 10}, {"wait_limit_ns": 61_000_000_000}, {"reserved": 1}):
+            assert pk.kamera_set_launch_tuning(raise_on_error=False, **bad) == pk.KAMERA_ERR_INVALID_ARG, bad
+        # a rejected setting leaves the previous one in place
+        assert pk.kamera_get_launch_tuning().bn == 128
+        assert lib.kamera_get_launch_tuning(None) == pk.KAMERA_ERR_NULL
+    finally:
+        pk.kamera_set_launch_tuning()
+    t = pk.kamera_get_launch_tuning()
+    assert all(getattr(t, f) == 0 for f, _ in t._fields_)
 
 
 def test_orbit_mean_validation(lib):

@@ -3,8 +3,6 @@ output element does not depend on the tile width, the number of stages or
 patch-factor slots, or on staging the patch factors in K chunks (the MMA
 accumulates the same K=16 steps in the same order), so the pools must be
 bit-identical across them -- and equal to the oracle within tolerance."""
-import os
-
 import numpy as np
 import pytest
 
@@ -14,16 +12,20 @@ from tests import harness as H
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+import position_invariant_kv_kamera_gb300 as pk  # noqa: E402
+
 LAUNCHES = [
     {},
-    {"KAMERA_BN": "128"},
-    {"KAMERA_STAGES": "2"},
-    {"KAMERA_STAGES": "2", "KAMERA_UV_SLOTS": "1"},
-    {"KAMERA_KSPLIT": "2"},
-    {"KAMERA_KSPLIT": "4", "KAMERA_UV_SLOTS": "2"},
-    {"KAMERA_BN": "64", "KAMERA_STAGES": "5"},
+    {"bn": 128},
+    {"stages": 2},
+    {"stages": 2, "uv_slots": 1},
+    {"ksplit": 2},
+    {"ksplit": 4, "uv_slots": 2},
+    {"bn": 64, "stages": 5},
+    {"grid": 7},             # fewer CTAs than tiles: every CTA walks many tiles
+    {"bn": 64, "grid": 300},  # more CTAs than SMs
+    {"no_pdl": 1},
 ]
-KEYS = ("KAMERA_BN", "KAMERA_STAGES", "KAMERA_UV_SLOTS", "KAMERA_KSPLIT")
 
 WORKLOADS = {
     "gqa_r64": lambda: W.gqa_video(num_layers=2, n_chunks=3, T=300, rank=64, page_size=16),
@@ -36,13 +38,10 @@ WORKLOADS = {
 
 
 @pytest.fixture(autouse=True)
-def _clean_env():
-    saved = {k: os.environ.pop(k, None) for k in KEYS}
+def _default_tuning():
+    pk.kamera_set_launch_tuning()
     yield
-    for k, v in saved.items():
-        os.environ.pop(k, None)
-        if v is not None:
-            os.environ[k] = v
+    pk.kamera_set_launch_tuning()
 
 
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
@@ -53,9 +52,7 @@ def test_all_launch_configurations_agree_bitwise(name):
     pool = (wl.host_pool(0), wl.host_pool(1) if wl.n_ch == 2 else None)
     results = []
     for cfg in LAUNCHES:
-        for k in KEYS:
-            os.environ.pop(k, None)
-        os.environ.update(cfg)
+        pk.kamera_set_launch_tuning(**cfg)
         t = H.device_inputs(wl, torch, pool_host=pool)
         st = H.call(wl, t, raise_on_error=False)
         if st != 0:  # a forced shape that does not fit this workload
@@ -90,9 +87,7 @@ def test_compressed_launch_configurations_agree_bitwise(name):
     arrs = H.comp_arrays(wl.random_compressed())
     results = []
     for cfg in LAUNCHES:
-        for k in KEYS:
-            os.environ.pop(k, None)
-        os.environ.update(cfg)
+        pk.kamera_set_launch_tuning(**cfg)
         cstore, _ct = H.device_compressed(arrs, torch)
         t = H.device_inputs(wl, torch, with_store=False)
         if H.call_compressed(wl, t, cstore, raise_on_error=False) != 0:

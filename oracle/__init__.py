@@ -118,6 +118,8 @@ def _declare(lib):
     lib.oracle_rotate_row.restype = None
     lib.oracle_row.argtypes = [ctypes.POINTER(Model), P, i32, P, i32, P, P, P, i32, P]
     lib.oracle_row.restype = None
+    lib.oracle_check_rows.argtypes = [ctypes.POINTER(Model), P, i32, P, i32, i32, P, P, P, i32, P, i32, f64, P, P]
+    lib.oracle_check_rows.restype = i64
     lib.oracle_slot.argtypes = [P, i32, i64, i32, i32, i64]
     lib.oracle_slot.restype = i64
     lib.oracle_reuse.argtypes = [ctypes.POINTER(Model), P, i32] + [P, P, P, i32] + [P, P, P, i32, i32] + [
@@ -227,6 +229,34 @@ def row(m: Model, th, channel: int, delta, src, u=None, vmat=None, rotate=True, 
     lib.oracle_row(ctypes.byref(m), _ptr(th), int(channel), _ptr(d), int(bool(rotate)), _ptr(src), _ptr(u),
                    _ptr(vmat), rank, _ptr(out))
     return out
+
+
+def check_rows(m: Model, th, channel: int, delta, src_bits, got_bits, u_bits=None, v_bits=None, rotate=True,
+               n_exact: int = 0, abs_tol: float = 1e-3, lib=None):
+    """Parity of a block of rows against the operator's definition (see
+    oracle_check_rows): src_bits, got_bits [n][D] bf16 bits; u_bits [n][rank]
+    and v_bits [D][rank] (or None for no patch).  Returns (n_bad, max_err,
+    first_bad).  Safe to call from several threads at once (the call releases
+    the GIL)."""
+    lib = lib or load()
+    src = np.ascontiguousarray(src_bits, dtype=np.uint16)
+    got = np.ascontiguousarray(got_bits, dtype=np.uint16)
+    n, D = src.shape
+    assert got.shape == src.shape and D == row_dim(m)
+    rank = 0
+    if u_bits is not None:
+        u_bits = np.ascontiguousarray(u_bits, dtype=np.uint16)
+        v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+        rank = int(u_bits.shape[1])
+        assert u_bits.shape == (n, rank) and v_bits.shape == (D, rank)
+    th = _c(th, np.float64)
+    d = _deltas(delta)
+    mx = ctypes.c_double(0.0)
+    first = ctypes.c_int64(-1)
+    bad = lib.oracle_check_rows(ctypes.byref(m), _ptr(th), int(channel), _ptr(d), int(bool(rotate)), int(n),
+                                _ptr(src), _ptr(u_bits), _ptr(v_bits), rank, _ptr(got), int(n_exact), float(abs_tol),
+                                ctypes.byref(mx), ctypes.byref(first))
+    return int(bad), float(mx.value), int(first.value)
 
 
 def slot(block_table, max_pages_per_seq, num_pages, page_size, seq, pos, lib=None) -> int:

@@ -647,3 +647,63 @@ void oracle_orbit_mean(const float* deltas, int32_t n, int64_t stride, int64_t n
     out[e] = s / (double)n;
   }
 }
+
+/* ---- parity driver (tests only) ------------------------------------------------
+ *
+ * Checks a block of rows computed elsewhere (e.g. by the GPU) against the
+ * operator's definition, row by row: for each row i of one (item, layer,
+ * channel), the reference is oracle_row() of the canonical row src[i], the
+ * patch row u[i] (NULL: no patch) and V (vmat, [D][rank]), and the row got[i]
+ * (bf16 bits) must satisfy, element by element,
+ *     |got - ref| <= ulp_bf16(ref) + abs_tol,
+ *     ulp_bf16(x) = 2^(floor(log2(max(|x|, 2^-126))) - 7)
+ * (one unit in the last place of bf16, which has 8 significant bits, plus an
+ * absolute allowance near zero).  Columns [0, n_exact) must moreover equal
+ * src bit for bit (MLA c_KV without a patch).  A NaN in got fails.
+ * Returns the number of failing elements; *max_err is the largest |got - ref|
+ * seen, *first_bad the index i*D + j of the first failure (or -1).  No state
+ * outside its arguments, so callers may run blocks on several threads. */
+int64_t oracle_check_rows(const oracle_model* m, const double* theta, int32_t channel, const int64_t* deltas,
+                          int32_t rotate, int32_t n_rows, const uint16_t* src, const uint16_t* u,
+                          const uint16_t* vmat, int32_t rank, const uint16_t* got, int32_t n_exact, double abs_tol,
+                          double* max_err, int64_t* first_bad) {
+  int32_t D = oracle_row_dim(m);
+  double* v = (double*)calloc((size_t)D * (size_t)(rank > 0 ? rank : 1), sizeof(double));
+  double* s = (double*)malloc((size_t)D * sizeof(double));
+  double* ur = (double*)malloc((size_t)(rank > 0 ? rank : 1) * sizeof(double));
+  double* ref = (double*)malloc((size_t)D * sizeof(double));
+  int64_t bad = 0;
+  double worst = 0.0;
+  *first_bad = -1;
+  if (u != NULL)
+    for (int64_t e = 0; e < (int64_t)D * rank; ++e) v[e] = bf16_bits_to_f64(vmat[e]);
+  for (int32_t i = 0; i < n_rows; ++i) {
+    const uint16_t* srow = src + (int64_t)i * D;
+    const uint16_t* grow = got + (int64_t)i * D;
+    for (int32_t j = 0; j < D; ++j) s[j] = bf16_bits_to_f64(srow[j]);
+    if (u != NULL)
+      for (int32_t r = 0; r < rank; ++r) ur[r] = bf16_bits_to_f64(u[(int64_t)i * rank + r]);
+    oracle_row(m, theta, channel, deltas, rotate, s, u != NULL ? ur : NULL, v, rank, ref);
+    for (int32_t j = 0; j < D; ++j) {
+      double g = bf16_bits_to_f64(grow[j]);
+      double err = fabs(g - ref[j]);
+      int e2 = 0;
+      double a = fabs(ref[j]);
+      frexp(a > 0x1p-126 ? a : 0x1p-126, &e2); /* a = f * 2^e2, f in [0.5, 1): floor(log2 a) = e2 - 1 */
+      double tol = ldexp(1.0, e2 - 1 - 7) + abs_tol;
+      int ok = err <= tol; /* false for NaN */
+      if (j < n_exact && grow[j] != srow[j]) ok = 0;
+      if (err > worst) worst = err;
+      if (!ok) {
+        if (*first_bad < 0) *first_bad = (int64_t)i * D + j;
+        ++bad;
+      }
+    }
+  }
+  free(v);
+  free(s);
+  free(ur);
+  free(ref);
+  *max_err = worst;
+  return bad;
+}

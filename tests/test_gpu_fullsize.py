@@ -1,9 +1,20 @@
 """Full-size parity: the five workload shapes at their real sizes (up to the
 57 GB long-video reorder + recall), launched exactly as the benchmark
-launches them.  Sampled output rows are recomputed one by one by the fp64
-oracle from regenerated inputs; properties that hold at any size (which
-slots are written, sentinel slots untouched, bit-exact copies) are checked
-over the whole pool on the device."""
+launches them, compared with the fp64 oracle on EVERY written row.
+
+Layer by layer and channel by channel, the rows each item wrote are gathered
+from the pool (destinations found by brute force on the block table), with
+the canonical rows and patch factors they were computed from (the device
+copies of the seeded generator's output, which the kernels read), and
+``oracle.check_rows`` recomputes each row with the oracle's row function and
+applies the comparison rule -- on all host cores, one item block per task.
+Properties that hold at any size (which slots are written, sentinel slots
+untouched, bit-exact copies) are checked over the whole pool on the device.
+The compressed-store case decodes rows with the oracle's O(d^2) decoder and
+stays sampled."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 
@@ -46,6 +57,85 @@ def _samples(wl, rng):
         t = int(rng.choice([0, T - 1, int(rng.integers(0, T)), min(T - 1, 127), min(T - 1, 128)]))
         out.append((i, int(rng.integers(0, wl.num_layers)), int(rng.integers(0, chans)), t))
     return out
+
+
+def _dest_rows(wl, item) -> np.ndarray:
+    """Pool rows (page * P + slot) of an item's tokens, by brute force on the block table."""
+    pos = int(item["dst_pos"]) + np.arange(int(item["n_tokens"]))
+    return (wl.block_table[int(item["seq"]), pos // wl.page_size].astype(np.int64) * wl.page_size
+            + pos % wl.page_size)
+
+
+def _gather(buf2d, rows: np.ndarray) -> np.ndarray:
+    """Rows of a 2-D device tensor (any 16-bit dtype) as host uint16 bits."""
+    idx = torch.from_numpy(rows).to(buf2d.device)
+    return buf2d.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _check_every_row(wl, t, fresh_pool=None):
+    """Every row every item wrote, against the oracle; fresh_pool: the initial
+    pool per channel (the in-place sources)."""
+    m = _oracle_model(wl)
+    th = H.oracle_theta(wl)
+    L, D, P = wl.num_layers, wl.D, wl.page_size
+    in_place = wl.mode == "relocate_in_place"
+    chans = 1 if in_place else wl.n_ch
+    patched = bool(wl.rank) and not in_place and "patch" in t
+    rotate = wl.mode != "apply_patch"
+    items = [it for it in wl.items if int(it["n_tokens"]) > 0]
+    dst = [_dest_rows(wl, it) for it in items]
+    bounds = np.cumsum([0] + [len(d) for d in dst])
+    all_dst = np.concatenate(dst)
+    deltas = [wl.section_deltas[i] if wl.section_deltas is not None else int(it["delta"])
+              for i, it in enumerate(wl.items) if int(it["n_tokens"]) > 0]
+    n_exact = wl.latent_dim if (wl.family == W.MLA and not patched) else 0
+    store2d = t["store"].view(-1, D) if "store" in t else None
+    patch2d = t["patch"].view(-1, wl.rank) if patched else None
+    failures, rows_checked = [], 0
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        for layer in range(L):
+            for ch in range(chans):
+                pool = t["pool_k"] if ch == 0 else t["pool_v"]
+                got = _gather(pool.view(L, -1, D)[layer], all_dst)
+                if in_place:
+                    src = _gather(fresh_pool[ch].view(L, -1, D)[layer], all_dst)
+                else:
+                    srows = np.concatenate([
+                        int(wl.store_off[int(it["chunk_id"])]) // D
+                        + (layer * wl.n_ch + ch) * int(it["n_tokens"]) + np.arange(int(it["n_tokens"]))
+                        for it in items])
+                    src = _gather(store2d, srows)
+                u_all = v_all = None
+                if patched:
+                    urows, vrows = [], []
+                    for it in items:
+                        T = int(it["n_tokens"])
+                        pid = int(it["patch_id"])
+                        if pid < 0:
+                            continue
+                        base = int(wl.patch_off[pid]) // wl.rank + (layer * wl.n_ch + ch) * (T + D)
+                        urows.append(base + np.arange(T))
+                        vrows.append(base + T + np.arange(D))
+                    u_all = _gather(patch2d, np.concatenate(urows)) if urows else None
+                    v_all = _gather(patch2d, np.concatenate(vrows)) if vrows else None
+                futs, ui, vi = [], 0, 0
+                for k, it in enumerate(items):
+                    a, b = bounds[k], bounds[k + 1]
+                    u = v = None
+                    if patched and int(it["patch_id"]) >= 0:
+                        u = u_all[ui:ui + (b - a)]
+                        v = v_all[vi:vi + D]
+                        ui += b - a
+                        vi += D
+                    futs.append((k, ex.submit(oracle.check_rows, m, th, ch, deltas[k], src[a:b], got[a:b], u, v,
+                                              rotate, n_exact if ch == 0 else 0)))
+                for k, f in futs:
+                    n_bad, max_err, first = f.result()
+                    if n_bad:
+                        failures.append((layer, ch, k, n_bad, max_err, divmod(first, D)))
+                rows_checked += len(all_dst)
+    assert not failures, (wl.name, failures[:10])
+    assert rows_checked == len(all_dst) * L * chans
 
 
 def _check_samples(wl, t, pool_init_rows=None):
@@ -115,6 +205,7 @@ def test_full_tiny_mha():
     t = _run(wl)
     _check_sentinel_coverage(wl, t["pool_k"])
     _check_sentinel_coverage(wl, t["pool_v"])
+    _check_every_row(wl, t)
     _check_samples(wl, t)
 
 
@@ -123,6 +214,7 @@ def test_full_gqa_video():
     t = _run(wl)
     _check_sentinel_coverage(wl, t["pool_k"])
     _check_sentinel_coverage(wl, t["pool_v"])
+    _check_every_row(wl, t)
     _check_samples(wl, t)
 
 
@@ -132,6 +224,7 @@ def test_full_gqa_video_mrope():
     wl = W.with_mrope(W.gqa_video())
     t = _run(wl)
     _check_sentinel_coverage(wl, t["pool_k"])
+    _check_every_row(wl, t)
     _check_samples(wl, t)
 
 
@@ -140,6 +233,7 @@ def test_full_mla_lite(rank):
     wl = W.mla_lite(rank=rank)
     t = _run(wl)
     _check_sentinel_coverage(wl, t["pool_k"])
+    _check_every_row(wl, t)  # rank 0: c_KV columns bit-exact on every row
     _check_samples(wl, t)
     if rank == 0:
         # c_KV byte for byte, over every reused row of every layer
@@ -163,6 +257,7 @@ def test_full_sliding_window():
     evicted = torch.ones(wl.num_pages, dtype=torch.bool, device="cuda")
     evicted[surv] = False
     assert torch.equal(t["pool_k"][:, evicted].view(torch.int16), fresh_k[:, evicted].view(torch.int16))
+    _check_every_row(wl, t, fresh_pool=[fresh_k])
     del fresh_k
     _check_samples(wl, t, pool_init_rows=wl.pool_rows)
 
@@ -172,6 +267,7 @@ def test_full_long_video():
     t = _run(wl)
     _check_sentinel_coverage(wl, t["pool_k"])
     _check_sentinel_coverage(wl, t["pool_v"])
+    _check_every_row(wl, t)
     _check_samples(wl, t)
     del t
     torch.cuda.empty_cache()

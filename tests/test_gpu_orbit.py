@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 from synth import gen
-from tests.test_gpu_factor import gpu_factor, oracle_truncation, rel
+from tests.test_gpu_factor import assert_product_matches, gpu_factor, oracle_truncation
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -51,13 +51,15 @@ def test_orbit_mean_matches_oracle(n, shape, pad):
 
 
 def test_orbit_patch_is_the_truncation_of_the_mean_deficit():
-    """Deficits under 6 orderings share a rank-8 core and differ by
-    ordering-specific low-rank terms; the orbit patch (rank 16) is the rank-16
-    truncation of their mean."""
-    n_ord, T, D, m = 6, 256, 256, 16
+    """Deficits under 6 orderings share a rank-8 core (singular values 10..4)
+    and differ by ordering-specific rank-2 terms, which average to singular
+    values near 0.25 and below; the orbit patch of rank 8 -- the shared core,
+    after a 16x gap, so the product is unique -- is the rank-8 truncation of
+    their mean, element by element."""
+    n_ord, T, D, m = 6, 256, 256, 8
     core = gen.low_rank_deficit(41, 0, T, D, np.linspace(10, 4, 8))
     samples = np.stack([core + gen.low_rank_deficit(42, j, T, D, [1.5, 0.5]) for j in range(n_ord)])
     mean = gpu_mean(samples).astype(np.float32)
     U, V = gpu_factor(mean[None], m, p=16, q=2)
     P_ref = oracle_truncation(oracle.orbit_mean(samples), m)
-    assert rel(U[0] @ V[0].T, P_ref) < 1e-2
+    assert_product_matches(U[0], V[0], P_ref, "orbit patch")

@@ -3,20 +3,26 @@
 
 One step = one kamera_reuse_batched call over the whole batch (every layer,
 K and V): gather the canonical chunks, re-rotate the keys by delta, add the
-rank-m patch, scatter into the paged pool.  Default workload: GQA shaped like
-Qwen2.5-VL-7B (28 layers, 4 KV heads x 128, base 1e6), 16 chunks x 1024
-tokens, rank-32 patch per layer per K/V, page 64, shuffled block table.
+rank-m patch, scatter into the paged pool.  Default workload (the largest
+single-GPU one): long-video reorder + recall on a GQA 8B-shaped backbone
+(32 layers, 8 KV heads x 128, base 5e5): 128 permuted chunks x 1296 tokens
+with rank-64 orbit patches plus 32 recalled chunks with fresh rank-64
+patches, page 64, shuffled block table -- 57.4 GB moved per call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints one JSON line.  ``value`` = reused tokens/s with inputs resident in
 HBM (device time, CUDA events on the launching stream, max over ranks);
 ``e2e`` = the same metric with the step's inputs copied host->device from
-pinned memory and the call's status read back inside the timed region.  Inputs
-(1.97 GB per step) are larger than L2, so no flush is needed between steps.
-``--impl reference`` times the fp64 CPU oracle on a bounded sample.
-``--workload gqa_video_compressed`` times kamera_reuse_compressed on the same
-batch read from a compressed canonical store (int8 K, 3-bit V).
+pinned memory and the call's status read back inside the timed region.  The
+headline inputs are far larger than L2, so no flush is needed between steps.
+With one GPU the line also carries ``configs``: the device-timed figures of
+the other four workloads (tiny MHA, GQA video, MLA, sliding window), each
+timed in the same process (those smaller than 4x L2 with an L2 flush
+between launches).  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample.  ``--workload gqa_video_compressed`` times
+kamera_reuse_compressed on the GQA video batch read from a compressed
+canonical store (int8 K, 3-bit V).
 """
 from __future__ import annotations
 
@@ -189,21 +195,23 @@ def aggregate(tokens_per_rank: int, world: int, max_elapsed_s: float, steps: int
 
 # ---- CPU oracle timing (cpu_baseline and the reference arm) -----------------------------------
 
+FULL_T = {"gqa_video": 1024, "mla_lite": 2048, "long_video": 1296, "sliding_window": 1024, "tiny_mha": 256}
+
+
 def oracle_sample_workload(name: str, n_items: int, n_tokens: int | None = None) -> W.Workload:
-    """A bounded sample of the workload with the same shapes: the first n_items
-    chunks (optionally truncated to n_tokens tokens each)."""
-    full = W.WORKLOADS[name]()
+    """A bounded sample of the workload with the same shapes (layers, row
+    width, rank, page size): its first n_items chunks, optionally truncated
+    to n_tokens tokens each."""
     if name == "gqa_video":
-        wl = W.gqa_video(n_chunks=n_items, T=n_tokens or 1024)
-    elif name == "mla_lite":
-        wl = W.mla_lite(n_chunks=n_items, T=n_tokens or 2048)
-    elif name == "long_video":
-        wl = W.long_video(n_reorder=n_items, n_recall=0, T=n_tokens or 1296)
-    elif name == "sliding_window":
-        wl = W.sliding_window(n_resident=n_items + 1, n_evict=1)
-    else:
-        wl = full
-    return wl
+        return W.gqa_video(n_chunks=n_items, T=n_tokens or 1024)
+    if name == "mla_lite":
+        return W.mla_lite(n_chunks=n_items, T=n_tokens or 2048)
+    if name == "long_video":
+        return W.long_video(n_reorder=n_items, n_recall=0, T=n_tokens or 1296)
+    if name == "sliding_window":
+        T = 1024 if not n_tokens else max(64, n_tokens // 64 * 64)  # whole pages: the relocation is in place
+        return W.sliding_window(n_resident=n_items + 1, n_evict=1, T=T)
+    return W.WORKLOADS[name]()
 
 
 def oracle_call(wl: W.Workload, compressed: bool = False):
@@ -239,99 +247,111 @@ def timed(fn) -> float:
     return time.perf_counter() - t0
 
 
-def time_oracle(wl: W.Workload) -> tuple[float, int]:
-    """Seconds of one oracle call over wl (inputs generated outside the timing)."""
-    return timed(oracle_call(wl)), wl.tokens
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
-def time_oracle_compressed(wl: W.Workload) -> tuple[float, int]:
-    """Seconds of one oracle reuse from a compressed store (encoded by the
-    oracle, outside the timing) over wl."""
-    return timed(oracle_call(wl, compressed=True)), wl.tokens
+def run_parallel(call, workers: int) -> float:
+    """Wall seconds of `workers` concurrent runs of the same oracle closure.
+    The oracle is C behind ctypes, which releases the GIL for the call, so
+    threads run on separate cores; inputs are shared read-only, every run
+    writes its own output images."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(lambda _: call(), range(workers)))
+        return time.perf_counter() - t0
 
 
-def cpu_baseline(name: str, budget_s: float = 15.0) -> dict:
-    """The oracle as it stands (single-threaded C, fp64) on a bounded sample."""
-    if name in COMPRESSED:
-        # the fp64 decode costs head_dim^2 operations per head row: a token sample of one chunk
-        probe = W.gqa_video(n_chunks=1, T=16)
-        dt1, tok1 = time_oracle_compressed(probe)
-        T = max(16, min(1024, int(16 * budget_s / max(dt1, 1e-3)) // 16 * 16))
-        dt, tok = time_oracle_compressed(W.gqa_video(n_chunks=1, T=T)) if T > 16 else (dt1, tok1)
-        return {"value": tok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"one chunk truncated to {T} tokens, all layers and channels ({tok} tokens, {dt:.1f} s, "
-                          f"single-threaded fp64 C oracle decoding the compressed store)"}
-    dt1, tok1 = time_oracle(oracle_sample_workload(name, 1))
-    n = max(1, min(len(W.WORKLOADS[name]().items), int(budget_s / max(dt1, 1e-3))))
-    if n > 1:
-        dt, tok = time_oracle(oracle_sample_workload(name, n))
-    else:
-        dt, tok = dt1, tok1
-    return {"value": tok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} of the workload's chunks, all layers and channels ({tok} tokens, {dt:.1f} s, "
-                      f"single-threaded fp64 C oracle)"}
+def oracle_sample(name: str, seconds: float) -> tuple[W.Workload, bool]:
+    """One chunk of the workload, truncated so that one single-threaded oracle
+    call over it takes about `seconds` (sized from a warm probe: a cold first
+    call overstates the cost per token)."""
+    comp = name in COMPRESSED
+    base = COMPRESSED.get(name, name)
+    full_T = FULL_T.get(base)
+    if not full_T:  # patch formation / orbit mean have their own baselines
+        raise ValueError(name)
+    probe = oracle_sample_workload(base, 1, 64)
+    call = oracle_call(probe, compressed=comp)
+    call()
+    per_tok = timed(call) / max(probe.tokens, 1)
+    n_tok = max(64, min(full_T, int(seconds / max(per_tok, 1e-9))))
+    return oracle_sample_workload(base, 1, n_tok if n_tok < full_T else None), comp
+
+
+def cpu_baseline(name: str, budget_s: float = 10.0) -> dict:
+    """The oracle as it stands (plain fp64 C, unchanged) on a bounded sample of
+    the workload: one chunk, all layers and channels, truncated to about
+    budget_s of single-core work; timed once on one core and once as one
+    independent run per host core at the same time."""
+    wl, comp = oracle_sample(name, budget_s)
+    call = oracle_call(wl, compressed=comp)
+    dt1 = timed(call)
+    cores = host_cores()
+    dtn = run_parallel(call, cores)
+    what = "decoding the compressed store" if comp else "bf16 store"
+    return {"value": cores * wl.tokens / dtn, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one chunk truncated to {wl.tokens} tokens, all {wl.num_layers} layers and channels "
+                      f"({what}); {cores} concurrent single-threaded runs of the fp64 C oracle, one per host core, "
+                      f"in {dtn:.1f} s",
+            "single_core": {"value": wl.tokens / dt1, "unit": UNIT, "cores": 1, "seconds": dt1}}
 
 
 def run_reference(args) -> None:
+    """The reference arm: the fp64 oracle (the method's plain definition; the
+    pages publish no code to install) timed on the host cores.  Each step runs
+    one single-threaded oracle call per host core concurrently, each over the
+    same token sample of one chunk (all layers and channels), sized so that
+    warm-up plus timed steps take about two minutes."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     name = args.workload
-    comp = name in COMPRESSED
-    base = COMPRESSED.get(name, name)
-    # one step = the oracle over a token sample of one chunk, all layers, sized so
-    # that warm-up + timed steps take about two minutes in total; the size comes
-    # from a warm probe (a cold first call overstates the cost per token)
-    full_T = {"gqa_video": 1024, "mla_lite": 2048, "long_video": 1296}.get(base)
-    probe = oracle_sample_workload(base, 1, 16 if full_T else None)
-    probe_call = oracle_call(probe, compressed=comp)
-    probe_call()
-    per_tok = timed(probe_call) / max(probe.tokens, 1)
+    if name not in FULL_T and COMPRESSED.get(name) not in FULL_T:
+        print(json.dumps({"impl": "reference", "unavailable": f"no CPU reference for workload {name}"}), flush=True)
+        return
+    cores = host_cores()
     budget = 120.0 / (args.steps + args.warmup)
-    n_tok = max(1, min(full_T or tok_probe, int(budget / max(per_tok, 1e-9))))
-    sample = oracle_sample_workload(base, 1, n_tok if full_T else None)
-    call = oracle_call(sample, compressed=comp)  # inputs generated once, outside the timing
+    wl, comp = oracle_sample(name, budget)
+    call = oracle_call(wl, compressed=comp)  # inputs generated once, outside the timing
     for _ in range(args.warmup):
-        call()
-    total, toks = 0.0, 0
+        run_parallel(call, cores)
+    total = 0.0
     for _ in range(args.steps):
-        total += timed(call)
-        toks += sample.tokens
+        total += run_parallel(call, cores)
+    toks = cores * wl.tokens * args.steps
     value = toks / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": f"{name}: {DESCRIPTIONS.get(name, '')}",
-                       "sample_per_step": f"{sample.tokens} tokens of one chunk, all layers"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"each step: {sample.tokens} tokens x {sample.num_layers} layers"},
+                       "sample_per_step": f"{cores} concurrent oracle runs over {wl.tokens} tokens of one chunk, "
+                                          f"all {wl.num_layers} layers"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {cores} x {wl.tokens} tokens x {wl.num_layers} layers"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ---- GPU arm ----------------------------------------------------------------------------------
 
-def run_gpu(args) -> None:
-    import torch
+L2_BYTES = 129 * 10**6  # GB300 L2
 
+
+def make_call(name: str, wl: W.Workload, torch, device, stream):
+    """(device inputs, one_call(inputs, stream)) for a workload; the compressed
+    variant encodes its store on the GPU first (write-once, off the timed path)."""
     import position_invariant_kv_kamera_gb300 as pk
     from tests import harness as H
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    pk.load()
-
-    wl = rank_workload(args.workload, rank, world, args.chunks)
-    comp = args.workload in COMPRESSED
-    stream = torch.cuda.current_stream(device)
-    if comp:
-        # the bf16 store is encoded once on the GPU (write-once, off the timed path), then dropped
+    if name in COMPRESSED:
         t = H.device_inputs(wl, torch, device)
         cstore, ct = H.empty_compressed(wl, torch, device)
         pk.kamera_compress_chunks(H.model_for(wl), pk.chunk_store(t["store"], t["store_off"], t["store_len"]),
@@ -351,6 +371,91 @@ def run_gpu(args) -> None:
         def one_call(d, s):
             return H.call(wl, d, stream=s)
     torch.cuda.synchronize(device)
+    return t, one_call
+
+
+def device_time(one_call, t, torch, device, stream, steps: int, warmup: int, flush: bool) -> dict:
+    """Device time of `steps` launches on the launching stream after `warmup`
+    untimed ones.  Inputs larger than L2: the launches run back to back
+    between two events.  Otherwise (flush=True) every launch is bracketed by
+    its own events, with a write of twice the L2 size between launches so
+    that each starts with a cold L2; the flush writes are outside the timed
+    intervals."""
+    for _ in range(warmup):
+        one_call(t, stream)
+    torch.cuda.synchronize(device)
+    if int(t["err"].item()) != 0:
+        raise RuntimeError(f"device error flag {int(t['err'].item())}")
+    if not flush:
+        b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b.record(stream)
+        for _ in range(steps):
+            one_call(t, stream)
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        total = b.elapsed_time(e) / 1e3
+    else:
+        scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for b, e in ev:
+                scrub.fill_(1.0)
+                b.record(stream)
+                one_call(t, stream)
+                e.record(stream)
+        torch.cuda.synchronize(device)
+        total = sum(b.elapsed_time(e) for b, e in ev) / 1e3
+        del scrub
+    if int(t["err"].item()) != 0:
+        raise RuntimeError(f"device error flag {int(t['err'].item())}")
+    return {"elapsed": total, "per_launch": total / steps, "steps": steps}
+
+
+CONFIG_ORDER = ["tiny_mha", "gqa_video", "mla_lite", "sliding_window"]
+
+
+def time_configs(names, torch, device, stream, steps: int, warmup: int, peak_gbs: float) -> dict:
+    """Device-timed figures of other workloads in this process (one at a time,
+    freeing each before the next)."""
+    out = {}
+    for name in names:
+        wl = W.WORKLOADS[name]()
+        t, one_call = make_call(name, wl, torch, device, stream)
+        nbytes = wl.algorithmic_bytes()
+        flush = nbytes < 4 * L2_BYTES
+        n = max(steps, 100) if flush else steps
+        r = device_time(one_call, t, torch, device, stream, n, warmup, flush)
+        gbs = nbytes / r["per_launch"] / 1e9
+        out[name] = {"description": DESCRIPTIONS[name], "ms_per_call": 1e3 * r["per_launch"],
+                     "tokens_per_s": wl.tokens / r["per_launch"], "algorithmic_bytes": nbytes, "gbs": gbs,
+                     "frac_of_measured_peak": gbs / peak_gbs, "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
+                     "launches": n, "l2": "flushed before every launch" if flush else "inputs larger than L2",
+                     "traffic": profile_traffic(name)}
+        del t
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args) -> None:
+    import torch
+
+    import position_invariant_kv_kamera_gb300 as pk
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pk.load()
+
+    wl = rank_workload(args.workload, rank, world, args.chunks)
+    comp = args.workload in COMPRESSED
+    stream = torch.cuda.current_stream(device)
+    t, one_call = make_call(args.workload, wl, torch, device, stream)
+    alg_bytes = wl.compressed_bytes() if comp else wl.algorithmic_bytes()
+    flush = alg_bytes < 4 * L2_BYTES
 
     for _ in range(args.warmup):
         one_call(t, stream)
@@ -358,36 +463,35 @@ def run_gpu(args) -> None:
     if int(t["err"].item()) != 0:
         raise RuntimeError(f"device error flag {int(t['err'].item())}")
 
-    # timed region: K back-to-back launches between two events on the launching stream
+    # timed region: K launches on the launching stream, bracketed by a barrier and a synchronize
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(local) as clocks:
         time.sleep(0.25)  # let the sampler start before the timed region
-        t_begin = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_begin.record(stream)
-        for _ in range(args.steps):
-            one_call(t, stream)
-        t_end.record(stream)
-        torch.cuda.synchronize(device)
+        r = device_time(one_call, t, torch, device, stream, args.steps, 0, flush)
     if world > 1:
         torch.distributed.barrier()
-    elapsed = t_begin.elapsed_time(t_end) / 1e3
+    elapsed = r["elapsed"]
     max_elapsed = reduce_max(elapsed, torch, device)
     value = aggregate(wl.tokens, world, max_elapsed, args.steps)
 
-    # end to end: the step's inputs from pinned host memory, the pool read back
+    # end to end: the step's inputs from pinned host memory, the status read back
     e2e = run_e2e(wl, t, torch, device, stream, min(args.steps, args.e2e_steps), one_call)
     e2e_value = reduce_max_time_value(e2e, wl.tokens, world, torch, device)
+    del t
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
     peaks = measured_peaks()
-    alg_bytes = wl.compressed_bytes() if comp else wl.algorithmic_bytes()
-    avg_launch_s = elapsed / args.steps  # one launch per step; consecutive launches may overlap their edges
+    configs = None
+    if world == 1 and args.configs and not args.chunks:
+        names = [n for n in CONFIG_ORDER if n != args.workload]
+        configs = time_configs(names, torch, device, stream, args.steps, args.warmup, peaks["hbm_gbs"])
+    avg_launch_s = r["per_launch"]
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = profile_traffic(args.workload)
     cpu = cpu_baseline(args.workload) if world == 1 or rank == 0 else None
@@ -400,8 +504,7 @@ def run_gpu(args) -> None:
                                + (f" [reduced to {args.chunks} chunks]" if args.chunks else ""),
                    "tokens_per_step": wl.tokens, "algorithmic_bytes_per_step": alg_bytes,
                    "patch_flops_per_step": wl.patch_flops(),
-                   "l2": "inputs larger than L2 (no flush needed)" if alg_bytes > 4 * 129e6
-                   else "inputs smaller than L2 (warm-cache steps)",
+                   "l2": "L2 flushed before every launch" if flush else "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -415,6 +518,8 @@ def run_gpu(args) -> None:
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -430,7 +535,8 @@ def run_e2e(wl, t, torch, device, stream, steps: int, one_call) -> dict:
     i+1's upload overlap step i."""
     names = [n for n in ("store", "store_off", "store_len", "k_codes", "k_scale", "v_codes", "v_norm", "row_offset",
                          "len", "patch", "patch_off", "patch_len", "items", "block_table", "section_delta") if n in t]
-    host_in = {n: t[n].cpu().pin_memory() for n in names}
+    # pinned host copies, allocated pinned (no pageable intermediate: the long-video inputs are 30 GB)
+    host_in = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True).copy_(t[n]) for n in names}
     host_err = [torch.empty(1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
     sets = [t, {**{n: torch.empty_like(t[n]) for n in names}, "pool_k": t["pool_k"], "pool_v": t.get("pool_v"),
                 "err": torch.zeros_like(t["err"])}]
@@ -629,10 +735,12 @@ def main(argv=None) -> None:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gqa_video",
+    ap.add_argument("--workload", default="long_video",
                     choices=sorted(W.WORKLOADS) + sorted(COMPRESSED) + ["patch_formation", "orbit_mean"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="time only the selected workload (no configs object)")
     ap.add_argument("--chunks", type=int, default=0,
                     help="reduced batch of this many chunks (profiler captures); 0 = the full workload")
     args = ap.parse_args(argv)

@@ -7,10 +7,12 @@
 //     out = R(delta) . KV(B|empty) + U_m V_m^T        -> bf16 -> paged pool slot
 //
 // Row block: 128 destination positions (aligned to 128 in position space) of
-// one (item, layer, channel); it splits into tiles of BN columns.  The work
-// unit is one tile; CTAs take tiles round-robin (tile g is column block
-// g mod n_cb of row block g / n_cb), so the last round is at most one tile
-// deep and small calls spread over as many SMs as they have tiles.  Per CTA
+// one (item, layer, channel); it splits into n_cb tiles of BN columns.  CTAs
+// take work units round-robin: whole row blocks for as many full rounds as
+// the grid allows (their per-row-block set-up -- page segments, phase table --
+// serves all n_cb tiles), then the row blocks of the partial last round split
+// into single tiles, so that round is one tile deep and calls with fewer row
+// blocks than CTAs spread over as many SMs as they have tiles.  Per CTA
 // (384 threads, one CTA per SM):
 //   warp 0      TMA producer: the canonical tile (64-column boxes, 128B
 //               swizzle; from the chunk store, or page by page from the pool
@@ -119,6 +121,8 @@ struct Params {
   int32_t* err_flag;
   uint64_t wait_limit_ns;  // bound of every wait
   int32_t test_unarm;      // test only: the producer leaves its first stage unfilled (the waits on it run out)
+  int32_t cache_hints;     // L2 eviction hints: 1 canonical loads evict-first, 2 pool stores evict-first,
+                           // 4 patch factors evict-last
   // compressed canonical store (kComp)
   CUtensorMap kc_map;  // K codes as rows [rows][D] uint8: box 128 x 128, 128B swizzle
   CUtensorMap vc_map;  // V codes as rows [rows][3D/8] uint8: box 3BN/8 x 128, no swizzle
@@ -237,6 +241,29 @@ __device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t
   return t;
 }
 
+// Work unit u of the schedule: units [0, full_rb) are whole row blocks, the
+// rest single tiles of the remaining row blocks (tile tt of them is column
+// block tt mod n_cb of row block full_rb + tt / n_cb).  False past the end.
+struct Unit {
+  int64_t rb;
+  int cb0, cb1;  // column blocks [cb0, cb1) relative to cb_first
+};
+
+__device__ __forceinline__ bool unit_at(int64_t u, int64_t full_rb, int64_t tail_tiles, int n_cb, Unit& x) {
+  if (u < full_rb) {
+    x.rb = u;
+    x.cb0 = 0;
+    x.cb1 = n_cb;
+    return true;
+  }
+  const int64_t tt = u - full_rb;
+  if (tt >= tail_tiles) return false;
+  x.rb = full_rb + tt / n_cb;
+  x.cb0 = (int)(tt - (tt / n_cb) * n_cb);
+  x.cb1 = x.cb0 + 1;
+  return true;
+}
+
 // A page segment of a tile (rows [sg*S, sg*S + S)): its pool row, or -1 when
 // its page is out of range.  `full` = every row of the segment belongs to the item.
 struct Segment {
@@ -264,7 +291,8 @@ __device__ __forceinline__ Segment segment(const Params& p, const Walker& w, con
 struct SmemMisc {
   uint32_t tmem_base;
   int32_t abort_flag;
-  int64_t total_tiles;
+  int64_t full_rb;     // row blocks dealt whole: the full rounds of the grid
+  int64_t tail_tiles;  // tiles of the remaining row blocks, dealt one by one
   uint64_t wait_limit;  // ns
 };
 
@@ -658,6 +686,64 @@ __device__ __forceinline__ void epi_vhalf(const RowView& rv, uint32_t codes, flo
   }
 }
 
+// ---- canonical-tile copies -----------------------------------------------------------------------
+
+// Where the canonical rows of one row block come from.
+struct SrcRB {
+  Tile t;
+  int32_t src_row;        // store (or code) row of tile row 0
+  int32_t seg_y[BM / 8];  // in place: pool row of each page segment, -1 = none
+  uint32_t bytes;         // bytes the loads of one tile deliver
+};
+
+template <bool kComp>
+__device__ __forceinline__ void rb_source(const Params& p, Walker& w, int64_t rb, int nbox, int nseg, SrcRB& c) {
+  walk_to(p, w, rb);
+  c.t = decode(p, w, rb);
+  c.bytes = (uint32_t)nbox * BOX_BYTES;
+  if (p.src_pool && !kComp) {
+    c.bytes = 0;
+    for (int sg = 0; sg < nseg; ++sg) {
+      c.seg_y[sg] = segment(p, w, c.t, sg).y;
+      if (c.seg_y[sg] >= 0) c.bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
+    }
+  }
+  const int64_t t0 = c.t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
+  c.src_row = 0;
+  if (kComp) {
+    c.src_row = (int32_t)(p.comp_row_offset[w.chunk] + (int64_t)c.t.layer * w.T + t0);
+    c.bytes = c.t.ch == 0 ? (uint32_t)p.BN * (uint32_t)BM : (uint32_t)(3 * p.BN / 8) * (uint32_t)BM;
+  } else if (!p.src_pool) {
+    c.src_row = (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)c.t.layer * p.n_ch_layout + c.t.ch) * w.T + t0);
+  }
+}
+
+// The TMA loads of column block cbi of a row block into stage st, with the
+// L2 eviction policy pol (0: none).
+template <bool kComp>
+__device__ __forceinline__ void tile_copy(const Params& p, const SrcRB& c, int cbi, int nbox, int nseg, uint8_t* st,
+                                          uint64_t* bar, uint64_t pol) {
+  const int col0 = (p.cb_first + cbi) * p.BN;
+  if (kComp) {
+    if (c.t.ch == 0) {
+      for (int b = 0; b < p.BN / 128; ++b)
+        tma_load_2d(st + p.out_bytes + b * BOX_BYTES, &p.kc_map, bar, col0 + b * 128, c.src_row, pol);
+    } else {
+      tma_load_2d(st + p.out_bytes, &p.vc_map, bar, (p.cb_first + cbi) * (3 * p.BN / 8), c.src_row, pol);
+    }
+  } else if (!p.src_pool) {
+    for (int b = 0; b < nbox; ++b)
+      tma_load_2d(st + b * BOX_BYTES, &p.src_map, bar, col0 + b * BOX_COLS, c.src_row, pol);
+  } else {
+    for (int sg = 0; sg < nseg; ++sg) {
+      if (c.seg_y[sg] < 0) continue;
+      for (int b = 0; b < nbox; ++b)
+        tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[c.t.ch], bar,
+                    col0 + b * BOX_COLS, c.seg_y[sg], pol);
+    }
+  }
+}
+
 // ---- the kernel ----------------------------------------------------------------------------------
 
 template <bool kPatch, bool kComp>
@@ -684,12 +770,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       err |= __shfl_xor_sync(0xFFFFFFFFu, err, o);
     }
     if (lane == 0) {
-      sm.misc->total_tiles = n * p.n_cb;
+      sm.misc->full_rb = n / gridDim.x * gridDim.x;
+      sm.misc->tail_tiles = (n - sm.misc->full_rb) * p.n_cb;
       if (blockIdx.x == 0 && err && p.err_flag) atomicOr(p.err_flag, err);
     }
   }
   __syncthreads();
-  if ((int64_t)blockIdx.x >= sm.misc->total_tiles) return;  // no tile for this CTA
+  if ((int64_t)blockIdx.x >= sm.misc->full_rb + sm.misc->tail_tiles) return;  // no work for this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -735,7 +822,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const int64_t total = sm.misc->total_tiles;
+  const int64_t full_rb = sm.misc->full_rb, tail_tiles = sm.misc->tail_tiles;
   const uint32_t tmem_base = kPatch ? sm.misc->tmem_base : 0u;
   const int nbox = p.BN / BOX_COLS;
   const int nseg = BM / p.seg_rows;
@@ -750,57 +837,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       } else {
         tma_prefetch_desc(p.src_pool ? &p.pool_map[0] : &p.src_map);
       }
+      const uint64_t pol_src = (p.cache_hints & 1) ? l2_policy_evict_first() : 0ull;
       Walker w;
       walker_init(w);
-      uint32_t it = 0;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
-        const int64_t rb = g / p.n_cb;
-        const int cbi = (int)(g - rb * p.n_cb);
-        walk_to(p, w, rb);
-        const Tile t = decode(p, w, rb);
-        // pool rows of the row block's page segments (in-place source)
-        int32_t seg_y[BM / 8];
-        uint32_t bytes = (uint32_t)nbox * BOX_BYTES;
-        if (p.src_pool) {
-          bytes = 0;
-          for (int sg = 0; sg < nseg; ++sg) {
-            seg_y[sg] = segment(p, w, t, sg).y;
-            if (seg_y[sg] >= 0) bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
-          }
-        }
-        const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
-        int32_t src_row = 0;
-        if (kComp) {
-          src_row = (int32_t)(p.comp_row_offset[w.chunk] + (int64_t)t.layer * w.T + t0);
-          bytes = t.ch == 0 ? (uint32_t)p.BN * (uint32_t)BM : (uint32_t)(3 * p.BN / 8) * (uint32_t)BM;
-        } else if (!p.src_pool) {
-          src_row = (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
-        }
-        const int s = (int)(it % (uint32_t)p.stages);
-        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
-        if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) break;
-        if (p.test_unarm && it == 0) continue;  // test only: this stage's barrier is never armed
-        uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
-        const int col0 = (p.cb_first + cbi) * p.BN;
-        mbar_arrive_expect_tx(&sm.full[s], bytes);
-        if (kComp) {
-          uint8_t* stg = st + p.out_bytes;
-          if (t.ch == 0) {
-            for (int b = 0; b < p.BN / 128; ++b)
-              tma_load_2d(stg + b * BOX_BYTES, &p.kc_map, &sm.full[s], col0 + b * 128, src_row);
-          } else {
-            tma_load_2d(stg, &p.vc_map, &sm.full[s], (p.cb_first + cbi) * (3 * p.BN / 8), src_row);
-          }
-        } else if (!p.src_pool) {
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(st + b * BOX_BYTES, &p.src_map, &sm.full[s], col0 + b * BOX_COLS, src_row);
-        } else {
-          for (int sg = 0; sg < nseg; ++sg) {
-            if (seg_y[sg] < 0) continue;
-            for (int b = 0; b < nbox; ++b)
-              tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[t.ch], &sm.full[s],
-                          col0 + b * BOX_COLS, seg_y[sg]);
-          }
+      uint32_t it = 0;  // tiles loaded (stage fills)
+      bool go = true;
+      Unit un;
+      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+        SrcRB c;
+        rb_source<kComp>(p, w, un.rb, nbox, nseg, c);
+        for (int cbi = un.cb0; cbi < un.cb1; ++cbi, ++it) {
+          const int s = (int)(it % (uint32_t)p.stages);
+          const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+          if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+          if (p.test_unarm && it == 0) continue;  // test only: this stage's barrier is never armed
+          mbar_arrive_expect_tx(&sm.full[s], c.bytes);
+          tile_copy<kComp>(p, c, cbi, nbox, nseg, sm.stages + (size_t)s * p.stage_bytes, &sm.full[s], pol_src);
         }
       }
       // drain: every stage's last fill must have landed before the CTA exits
@@ -817,27 +869,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       tma_prefetch_desc(&p.v_map);
       Walker w;
       walker_init(w);
+      const uint64_t pol_uv = (p.cache_hints & 4) ? l2_policy_evict_last() : 0ull;
       uint32_t pu = 0;
       bool go = true;
-      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
-        const int64_t rb = g / p.n_cb;
-        const int cbi = (int)(g - rb * p.n_cb);
-        walk_to(p, w, rb);
+      Unit un;
+      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+        walk_to(p, w, un.rb);
         if (w.patch < 0) continue;
-        const Tile t = decode(p, w, rb);
+        const Tile t = decode(p, w, un.rb);
         const int64_t prow = p.patch_off[w.patch] / p.rank +
                              ((int64_t)t.layer * p.n_ch_layout + t.ch) * (int64_t)(w.T + p.D);
         const int32_t u_row = (int32_t)(prow + (t.pos0 - w.dst_pos));
         const int kg_chunk = p.rank / 8 / p.ksplit;  // K groups per chunk
-        for (int kc = 0; kc < p.ksplit; ++kc, ++pu) {
-          const int u = (int)(pu % (uint32_t)p.uv_slots);
-          const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
-          if (!wait_bounded(&sm.uv_empty[u], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-          uint8_t* slot = sm.uv + (size_t)u * uv_bytes;
-          mbar_arrive_expect_tx(&sm.uv_full[u], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
-          tma_load_3d(slot, &p.u_map, &sm.uv_full[u], 0, u_row, kc * kg_chunk);
-          tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[u], 0,
-                      (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), kc * kg_chunk);
+        for (int cbi = un.cb0; cbi < un.cb1 && go; ++cbi) {
+          for (int kc = 0; kc < p.ksplit; ++kc, ++pu) {
+            const int ui = (int)(pu % (uint32_t)p.uv_slots);
+            const uint32_t ph = (pu / (uint32_t)p.uv_slots) & 1u;
+            if (!wait_bounded(&sm.uv_empty[ui], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+            uint8_t* slot = sm.uv + (size_t)ui * uv_bytes;
+            mbar_arrive_expect_tx(&sm.uv_full[ui], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
+            tma_load_3d(slot, &p.u_map, &sm.uv_full[ui], 0, u_row, kc * kg_chunk, pol_uv);
+            tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], 0,
+                        (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), kc * kg_chunk, pol_uv);
+          }
         }
       }
       const uint32_t S = (uint32_t)p.uv_slots;
@@ -855,28 +909,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       walker_init(w);
       uint32_t pt = 0, pc = 0;  // patched tiles, patch-factor chunks
       bool issued = false, go = true;
-      for (int64_t g = blockIdx.x; g < total && go; g += gridDim.x) {
-        walk_to(p, w, g / p.n_cb);
+      Unit un;
+      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+        walk_to(p, w, un.rb);
         if (w.patch < 0) continue;
-        const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
-        if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) break;
-        for (int kc = 0; kc < p.ksplit; ++kc, ++pc) {
-          const int u = (int)(pc % (uint32_t)p.uv_slots);
-          const uint32_t uph = (pc / (uint32_t)p.uv_slots) & 1u;
-          if (!wait_bounded(&sm.uv_full[u], uph, sm.misc, p.err_flag)) { go = false; break; }
-          tc_fence_after_sync();
-          const uint32_t ua = smem_addr(sm.uv + (size_t)u * uv_bytes), va = ua + p.u_bytes;
-          for (int k = 0; k < p.ksteps; ++k) {
-            const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
-            const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
-            umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
+        for (int cbi = un.cb0; cbi < un.cb1 && go; ++cbi, ++pt) {
+          const uint32_t buf = pt & 1u, tph = (pt >> 1) & 1u;
+          if (!wait_bounded(&sm.tempty[buf], tph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
+          for (int kc = 0; kc < p.ksplit; ++kc, ++pc) {
+            const int ui = (int)(pc % (uint32_t)p.uv_slots);
+            const uint32_t uph = (pc / (uint32_t)p.uv_slots) & 1u;
+            if (!wait_bounded(&sm.uv_full[ui], uph, sm.misc, p.err_flag)) { go = false; break; }
+            tc_fence_after_sync();
+            const uint32_t ua = smem_addr(sm.uv + (size_t)ui * uv_bytes), va = ua + p.u_bytes;
+            for (int k = 0; k < p.ksteps; ++k) {
+              const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
+              const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+              umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(&sm.uv_empty[ui]);
+            issued = true;
           }
-          umma_commit(&sm.uv_empty[u]);
-          issued = true;
+          if (!go) break;
+          umma_commit(&sm.tfull[buf]);
         }
-        if (!go) break;
-        umma_commit(&sm.tfull[buf]);
-        ++pt;
       }
       if (issued) {
         umma_commit(sm.drain);
@@ -888,12 +944,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     if (lane == 0) {
       Walker w;
       walker_init(w);
+      const uint64_t pol_dst = (p.cache_hints & 2) ? l2_policy_evict_first() : 0ull;
       uint32_t it = 0;
-      for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
-        const int64_t rb = g / p.n_cb;
-        const int cbi = (int)(g - rb * p.n_cb);
-        walk_to(p, w, rb);
-        const Tile t = decode(p, w, rb);
+      bool go = true;
+      Unit un;
+      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+        walk_to(p, w, un.rb);
+        const Tile t = decode(p, w, un.rb);
         int32_t seg_y[BM / 8];  // pool row of each valid page segment, else -1
         bool seg_full[BM / 8];
         int lo8 = 0, hi8 = 0;   // 8-row sub-blocks of the row block inside the item: [lo8, hi8)
@@ -907,35 +964,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           seg_y[sg] = seg.y;
           seg_full[sg] = seg.full;
         }
-        const int s = (int)(it % (uint32_t)p.stages);
-        const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
-        if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) break;
-        // after a wait gave up, tiles may be marked computed without being so: store nothing more
-        if (*reinterpret_cast<volatile int32_t*>(&sm.misc->abort_flag)) break;
-        const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
-        const int col0 = (p.cb_first + cbi) * p.BN;
-        for (int sg = 0; sg < nseg; ++sg) {
-          if (seg_y[sg] < 0) continue;
-          if (seg_full[sg]) {
-            for (int b = 0; b < nbox; ++b)
-              tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
-                           col0 + b * BOX_COLS, seg_y[sg]);
-            continue;
+        for (int cbi = un.cb0; cbi < un.cb1; ++cbi, ++it) {
+          const int s = (int)(it % (uint32_t)p.stages);
+          const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
+          if (!wait_bounded(&sm.computed[s], ph, sm.misc, p.err_flag)) { go = false; break; }
+          // after a wait gave up, tiles may be marked computed without being so: store nothing more
+          if (*reinterpret_cast<volatile int32_t*>(&sm.misc->abort_flag)) { go = false; break; }
+          const uint8_t* st = sm.stages + (size_t)s * p.stage_bytes;
+          const int col0 = (p.cb_first + cbi) * p.BN;
+          for (int sg = 0; sg < nseg; ++sg) {
+            if (seg_y[sg] < 0) continue;
+            if (seg_full[sg]) {
+              for (int b = 0; b < nbox; ++b)
+                tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
+                             col0 + b * BOX_COLS, seg_y[sg], pol_dst);
+              continue;
+            }
+            // partly covered page: its 8-row sub-blocks that lie inside the item
+            const int r0 = sg * p.seg_rows;
+            for (int k8 = r0 >> 3; k8 < ((r0 + p.seg_rows) >> 3); ++k8) {
+              if (k8 < lo8 || k8 >= hi8) continue;
+              for (int b = 0; b < nbox; ++b)
+                tma_store_2d(&p.pool_map8[t.ch], st + b * BOX_BYTES + (uint32_t)k8 * 1024u, col0 + b * BOX_COLS,
+                             seg_y[sg] + (k8 * 8 - r0), pol_dst);
+            }
           }
-          // partly covered page: its 8-row sub-blocks that lie inside the item
-          const int r0 = sg * p.seg_rows;
-          for (int k8 = r0 >> 3; k8 < ((r0 + p.seg_rows) >> 3); ++k8) {
-            if (k8 < lo8 || k8 >= hi8) continue;
-            for (int b = 0; b < nbox; ++b)
-              tma_store_2d(&p.pool_map8[t.ch], st + b * BOX_BYTES + (uint32_t)k8 * 1024u, col0 + b * BOX_COLS,
-                           seg_y[sg] + (k8 * 8 - r0));
-          }
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
+          mbar_arrive(&sm.empty[s]);
         }
-        bulk_commit_group();
-        bulk_wait_group_read0();  // the stage may be refilled once the stores have read it
-        mbar_arrive(&sm.empty[s]);
       }
-      bulk_wait_group0();
+      // the stages must outlive the stores' reads of them; the writes
+      // themselves complete before the grid does
+      bulk_wait_group_read0();
     }
   } else {
     // ================= epilogue (warps 3..10) =================
@@ -948,13 +1009,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     Walker w;
     walker_init(w);
     int32_t table_item[2] = {-1, -1};  // item whose phases each table holds
-    uint32_t it = 0, pt = 0;  // tiles of this CTA, patched tiles
+    uint32_t it = 0, pt = 0, uix = 0;  // tiles, patched tiles, units of this CTA
     bool ok = true;  // warp-uniform: every wait of this warp so far succeeded
-    for (int64_t g = blockIdx.x; g < total; g += gridDim.x, ++it) {
-      const int64_t rb = g / p.n_cb;
-      walk_to(p, w, rb);
-      Tile t = decode(p, w, rb);
-      t.cb = p.cb_first + (int)(g - rb * p.n_cb);
+    Unit un;
+    for (int64_t u = blockIdx.x; unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x, ++uix) {
+      walk_to(p, w, un.rb);
+      Tile t = decode(p, w, un.rb);
       const bool patched = kPatch && w.patch >= 0;
       const bool rot = p.rotate && t.ch == 0;
       // destination of row r: rows of whole page segments go out with the TMA
@@ -982,10 +1042,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
         if (tok >= 0 && tok < w.T) crow = p.comp_row_offset[w.chunk] + (int64_t)t.layer * w.T + tok;
         if (t.ch == 0) kscale = p.k_scale[(int64_t)w.chunk * p.num_layers + t.layer];
       }
-      // phase tables alternate by tile parity: their previous readers
+      // phase tables alternate by unit parity: their previous readers
       // finished before the last joint barrier
-      float2* cs = sm.cs + (it & 1u) * pairs_pad(p.n_pairs);
-      if (h == 1 && rot && w.item != table_item[it & 1u]) {
+      float2* cs = sm.cs + (uix & 1u) * pairs_pad(p.n_pairs);
+      if (h == 1 && rot && w.item != table_item[uix & 1u]) {
         float* csf = reinterpret_cast<float*>(cs);
         for (int i = et - 128; i < p.n_pairs; i += 128) {
           const float2 v = phase_cs(i < p.sec_end0 ? w.d0 : (i < p.sec_end1 ? w.d1 : w.d2), p.theta[i]);
@@ -993,10 +1053,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           csf[4 * (i >> 1) + 2 + (i & 1)] = v.y;
         }
       }
-      if (rot) table_item[it & 1u] = w.item;
+      if (rot) table_item[uix & 1u] = w.item;
       if (!named_bar_and(1, EPI_THREADS, ok)) break;  // joint decision, and the table is ready
 
-      {
+      for (int cbi = un.cb0; cbi < un.cb1; ++cbi, ++it) {
+        t.cb = p.cb_first + cbi;
         const int s = (int)(it % (uint32_t)p.stages);
         const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
         const uint32_t buf = pt & 1u;

@@ -16,6 +16,28 @@ def test_patch_formation_flops_per_slab_and_launch():
     assert 896 * per_slab == pytest.approx(2.938e11, rel=1e-3)
 
 
+def test_patch_formation_bytes_are_six_delta_reads_plus_the_factors():
+    # q = 2: Y, (Z, Y) twice, B -> 6 fp32 reads of each 1024 x 512 slab; U_m, V_m bf16 once
+    per_slab = 6 * 1024 * 512 * 4 + (1024 + 512) * 32 * 2
+    assert bench.factor_bytes(896, 1024, 512, 32, 2) == 896 * per_slab
+    assert 896 * 6 * 1024 * 512 * 4 == pytest.approx(11.27e9, rel=1e-3)
+
+
+def test_host_cores_and_the_oracle_sample_shapes():
+    assert bench.host_cores() >= 1
+    for name in ("gqa_video", "mla_lite", "long_video", "sliding_window"):
+        full = bench.W.WORKLOADS[name]()
+        wl = bench.oracle_sample_workload(name, 1, 128)
+        # the same layers, row width, rank and page size as the workload; one chunk, truncated
+        assert (wl.num_layers, wl.D, wl.rank, wl.page_size, wl.mode) == (
+            full.num_layers, full.D, full.rank, full.page_size, full.mode)
+        assert len(wl.items) == 1 and int(wl.items["n_tokens"][0]) == 128
+
+
+def test_configs_cover_the_other_four_workloads():
+    assert sorted(bench.CONFIG_ORDER + ["long_video"]) == sorted(bench.W.WORKLOADS)
+
+
 def test_traffic_comes_from_a_capture_of_the_current_sources_only(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     for f in bench.KERNEL_SOURCES:

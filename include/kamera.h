@@ -368,7 +368,7 @@ kamera_status kamera_reuse_compressed(const kamera_model_desc* model, const kame
 typedef struct {
   int32_t bn;             /* tile width in columns: 64, 128, 192 or 256 */
   int32_t stages;         /* canonical tile stages in shared memory: 2..6 */
-  int32_t uv_slots;       /* patch-factor slots: 1 or 2 */
+  int32_t uv_slots;       /* patch-factor slots: 1..8 */
   int32_t ksplit;         /* patch factors staged in 1, 2 or 4 parts of the rank */
   int32_t no_pdl;         /* non-zero: launch without programmatic dependent launch */
   int32_t grid;           /* CTAs of the persistent grid, 1..65535; 0 = one per SM */

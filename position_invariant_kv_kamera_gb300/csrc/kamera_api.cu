@@ -172,7 +172,7 @@ kamera_status set_tuning(const kamera_launch_tuning* t) {
       return fail(KAMERA_ERR_INVALID_ARG, "tuning: bn = %d (0, 64, 128, 192 or 256)", v.bn);
     if (v.stages != 0 && (v.stages < 2 || v.stages > 6))
       return fail(KAMERA_ERR_INVALID_ARG, "tuning: stages = %d (0 or 2..6)", v.stages);
-    if (v.uv_slots < 0 || v.uv_slots > 2) return fail(KAMERA_ERR_INVALID_ARG, "tuning: uv_slots = %d", v.uv_slots);
+    if (v.uv_slots < 0 || v.uv_slots > 8) return fail(KAMERA_ERR_INVALID_ARG, "tuning: uv_slots = %d", v.uv_slots);
     if (v.ksplit != 0 && v.ksplit != 1 && v.ksplit != 2 && v.ksplit != 4)
       return fail(KAMERA_ERR_INVALID_ARG, "tuning: ksplit = %d (0, 1, 2 or 4)", v.ksplit);
     if (v.grid < 0 || v.grid > 65535) return fail(KAMERA_ERR_INVALID_ARG, "tuning: grid = %d", v.grid);
@@ -373,38 +373,45 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   const int n_ch_work = mode == MODE_RELOCATE_IN_PLACE ? 1 : n_ch_layout;
   const bool small_call = (int64_t)n_items * model->num_layers * n_ch_work < (int64_t)facts->sms;
   const int cands[4] = {256, 192, 128, 64};
-  for (int ci = 0; ci < 4 && BN == 0; ++ci) {
-    const int bn = cands[small_call ? 3 - ci : ci];
-    if (bn_env && bn != bn_env) continue;
-    if (D % bn != 0) continue;
-    if (comp && bn % 128 != 0) continue;  // 128-column K boxes; 16-byte V code boxes
-    bool whole = true;  // every rotate-half pair inside one column block
-    for (int g = 0; g < n_groups; ++g)
-      if (p.group_kind[g] > 0 && (g * 32) / bn != ((g + p.group_kind[g]) * 32) / bn) whole = false;
-    if (!whole) continue;
-    const uint32_t sb = (uint32_t)bn * (comp ? 384u : 256u);
-    // preference: two patch-factor slots (the factor loads then run ahead of
-    // the MMA), then canonical stages (they carry the HBM stream), then whole
-    // (unsplit) patch factors
-    for (int u = use_patch ? 2 : 1; u >= 1 && BN == 0; --u) {
-      if (uv_env && use_patch && u != uv_env) continue;
+  // Shape preference, measured on the three patched workloads: double-buffered
+  // patch-factor slots with at most one trip through them per tile (K chunks
+  // <= slots; the factor loads then keep pace with the canonical stream), then
+  // as many canonical stages as fit (they carry the HBM stream), then the
+  // widest factor chunks (whole rows of up to 128 bytes per TMA request).  A
+  // second pass drops the first rule when nothing fits under it.
+  const int u_max = use_patch ? (uv_env > 2 ? uv_env : 2) : 1;
+  for (int pass = 0; pass < 2 && BN == 0; ++pass) {
+    for (int ci = 0; ci < 4 && BN == 0; ++ci) {
+      const int bn = cands[small_call ? 3 - ci : ci];
+      if (bn_env && bn != bn_env) continue;
+      if (D % bn != 0) continue;
+      if (comp && bn % 128 != 0) continue;  // 128-column K boxes; 16-byte V code boxes
+      bool whole = true;  // every rotate-half pair inside one column block
+      for (int g = 0; g < n_groups; ++g)
+        if (p.group_kind[g] > 0 && (g * 32) / bn != ((g + p.group_kind[g]) * 32) / bn) whole = false;
+      if (!whole) continue;
+      const uint32_t sb = (uint32_t)bn * (comp ? 384u : 256u);
       for (int s = 6; s >= 2 && BN == 0; --s) {
         if (st_env && s != st_env) continue;
         for (int ks = 1; ks <= (use_patch ? 4 : 1) && BN == 0; ks *= 2) {
           if (ks_env && use_patch && ks != ks_env) continue;
           if (use_patch && (rank / ks) % 16 != 0 && !(ks == 1 && rank == 8)) continue;  // whole K=16 steps
-          const int kg = use_patch ? (rank / 8 / ks < 2 ? 2 : rank / 8 / ks) : 0;
-          const uint32_t ub = use_patch ? (uint32_t)(BM + bn) * kg * 16u : 0u;
-          const uint64_t need =
-              (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + table_bytes + smem_extra_bytes(s, u, n_pairs);
-          if (need > (uint64_t)facts->smem_optin) continue;
-          BN = bn;
-          stages = s;
-          uv_slots = use_patch ? u : 0;
-          ksplit = use_patch ? ks : 1;
-          kg_alloc = kg;
-          stage_bytes = sb;
-          uv_slot_bytes = ub;
+          for (int u = u_max; u >= 1 && BN == 0; --u) {
+            if (uv_env && use_patch && u != uv_env) continue;
+            if (pass == 0 && use_patch && !uv_env && !ks_env && (u < 2 || ks > u)) continue;
+            const int kg = use_patch ? (rank / 8 / ks < 2 ? 2 : rank / 8 / ks) : 0;
+            const uint32_t ub = use_patch ? (uint32_t)(BM + bn) * kg * 16u : 0u;
+            const uint64_t need = (uint64_t)s * sb + (uint64_t)(use_patch ? u : 0) * ub + table_bytes +
+                                  smem_extra_bytes(s, u, n_pairs);
+            if (need > (uint64_t)facts->smem_optin) continue;
+            BN = bn;
+            stages = s;
+            uv_slots = use_patch ? u : 0;
+            ksplit = use_patch ? ks : 1;
+            kg_alloc = kg;
+            stage_bytes = sb;
+            uv_slot_bytes = ub;
+          }
         }
       }
     }
@@ -529,14 +536,31 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     p.patch_len = patches->len;
     p.patch_elems = patches->n_elems;
     p.n_patches = patches->n_patches;
-    const cuuint64_t dims[3] = {8, (cuuint64_t)(patch_rows > 0 ? patch_rows : 1), (cuuint64_t)(rank / 8)};
-    const cuuint64_t strides[2] = {(cuuint64_t)rank * 2, 16};
-    const cuuint32_t ubox[3] = {8, (cuuint32_t)BM, (cuuint32_t)(rank / 8 / ksplit)};
-    const cuuint32_t vbox[3] = {8, (cuuint32_t)BN, (cuuint32_t)(rank / 8 / ksplit)};
-    if (kamera_status st = encode(&p.u_map, patches->data, 3, dims, strides, ubox, CU_TENSOR_MAP_SWIZZLE_NONE, "U"))
-      return st;
-    if (kamera_status st = encode(&p.v_map, patches->data, 3, dims, strides, vbox, CU_TENSOR_MAP_SWIZZLE_NONE, "V"))
-      return st;
+    const int kw = rank / ksplit;  // K elements per chunk
+    if (kw >= 16) {
+      // whole chunk rows (2 kw = 32, 64 or 128 bytes) per TMA row, swizzled at that width: the
+      // K-major layout tcgen05.mma reads with the matching swizzle mode
+      p.uv_row_bytes = 2 * kw;
+      const CUtensorMapSwizzle swz = kw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                     : (kw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+      const cuuint64_t dims[2] = {(cuuint64_t)rank, (cuuint64_t)(patch_rows > 0 ? patch_rows : 1)};
+      const cuuint64_t strides[1] = {(cuuint64_t)rank * 2};
+      const cuuint32_t ubox[2] = {(cuuint32_t)kw, (cuuint32_t)BM};
+      const cuuint32_t vbox[2] = {(cuuint32_t)kw, (cuuint32_t)BN};
+      if (kamera_status st = encode(&p.u_map, patches->data, 2, dims, strides, ubox, swz, "U")) return st;
+      if (kamera_status st = encode(&p.v_map, patches->data, 2, dims, strides, vbox, swz, "V")) return st;
+    } else {
+      // rank 8: 16-byte rows as K-major core matrices (8 rows x 16 bytes), one K group per chunk
+      p.uv_row_bytes = 0;
+      const cuuint64_t dims[3] = {8, (cuuint64_t)(patch_rows > 0 ? patch_rows : 1), (cuuint64_t)(rank / 8)};
+      const cuuint64_t strides[2] = {(cuuint64_t)rank * 2, 16};
+      const cuuint32_t ubox[3] = {8, (cuuint32_t)BM, (cuuint32_t)(rank / 8 / ksplit)};
+      const cuuint32_t vbox[3] = {8, (cuuint32_t)BN, (cuuint32_t)(rank / 8 / ksplit)};
+      if (kamera_status st = encode(&p.u_map, patches->data, 3, dims, strides, ubox, CU_TENSOR_MAP_SWIZZLE_NONE, "U"))
+        return st;
+      if (kamera_status st = encode(&p.v_map, patches->data, 3, dims, strides, vbox, CU_TENSOR_MAP_SWIZZLE_NONE, "V"))
+        return st;
+    }
   }
 
   // ---- launch ----------------------------------------------------------------------------------------------

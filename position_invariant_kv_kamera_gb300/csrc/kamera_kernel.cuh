@@ -16,15 +16,16 @@
 // (384 threads, one CTA per SM):
 //   warp 0      TMA producer: the canonical tile (64-column boxes, 128B
 //               swizzle; from the chunk store, or page by page from the pool
-//               for the in-place modes) and, for patched items, the U tile
-//               [128 x m] and V tile [BN x m] (no-swizzle K-major core-matrix
-//               layout) into a ring of shared-memory stages.
+//               for the in-place modes) into a ring of shared-memory stages.
 //   warp 1      owns TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16
 //               steps): P = U . V^T into an fp32 TMEM accumulator, two buffers.
 //   warp 2      TMA store issuer: whole page segments of the finished tile go
 //               to the pool with cp.async.bulk.tensor stores (8-row boxes for
 //               the in-item part of partly covered pages).
-//   warp 11     TMA producer of the patch factors (U and V tiles).
+//   warp 11     TMA producer of the patch factors: the U tile [128 x m] and
+//               the V tile [BN x m] of each tile, in K chunks of m / ksplit,
+//               as whole chunk rows swizzled at their width (K-major; rank 8:
+//               core matrices with a zeroed second K group), into slots.
 //   warps 3-10  epilogue, two warps per TMEM lane quadrant, each half taking
 //               half of the tile's rotation units: tcgen05.ld the patch row,
 //               rotate the key row's RoPE pairs by delta*theta_i (fp64 angle
@@ -75,8 +76,8 @@ struct Params {
   CUtensorMap src_map;      // chunk store as rows [rows][D]: box 64 x 128, 128B swizzle
   CUtensorMap pool_map[2];  // pool K / V as rows [L*pages*P][D]: box 64 x S (S = min(P,128)), 128B swizzle
   CUtensorMap pool_map8[2]; // the same with 8-row boxes, for partly covered page segments
-  CUtensorMap u_map;        // patch store as (8, rows, m/8): box (8, 128, m/8/ksplit)
-  CUtensorMap v_map;        // patch store as (8, rows, m/8): box (8, BN, m/8/ksplit)
+  CUtensorMap u_map;        // patch store: rows [rows][m], box (m/ksplit, 128), swizzled; rank 8: (8, rows, 1)
+  CUtensorMap v_map;        // the same with BN-row boxes
   const kamera_reuse_item* items;
   int32_t n_items;
   int32_t src_pool;  // 0: gather from the chunk store, 1: in place from the pool
@@ -93,6 +94,8 @@ struct Params {
   int32_t ksplit;      // patch factors staged in this many K chunks per tile
   int32_t ksteps;      // K=16 MMA steps per chunk: ceil(rank / ksplit / 16)
   int32_t kg_alloc;    // 8-element K groups held in smem per operand row and chunk (>= 2)
+  int32_t uv_row_bytes;  // bytes of one operand row of a chunk, swizzled at that width (32/64/128);
+                         // 0: rank 8, K-major core matrices with a zeroed second K group
   int32_t need_patch;  // items without a patch have no work (patch-only mode)
   uint16_t* pool[2];
   int64_t num_pages;
@@ -477,6 +480,23 @@ __device__ __forceinline__ void epi_plain16(const Src& src, const RowView& rv, i
   put16(a0, a1, pack8_f2(x), pack8_f2(x + 4), gdst, c0);
 }
 
+// 32 patched columns without rotation, one TMEM load and one wait for all of
+// them: out = x + P.
+template <bool kComp, class Src>
+__device__ __forceinline__ void epi_plain32_patched(const Src& src, const RowView& rv, int c0, uint32_t taddr,
+                                                    uint16_t* gdst) {
+  uint32_t acc[32];
+  tmem_ld32(taddr + (uint32_t)c0, acc);
+  float2 x[16];
+  src.load16(c0, x);
+  src.load16(c0 + 16, x + 8);
+  tmem_ld_wait();
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = add_f2(x[e], acc_f2(acc, e));
+  put16(rv.chunk(c0), rv.chunk(c0 + 8), pack8_f2(x), pack8_f2(x + 4), gdst, c0);
+  put16(rv.chunk(c0 + 16), rv.chunk(c0 + 24), pack8_f2(x + 8), pack8_f2(x + 12), gdst, c0 + 16);
+}
+
 // 16 rotate-half pairs (cA + e, cB + e), pair index pb + e, two pairs per
 // paired operation:  a' = a cos - b sin,  b' = b cos + a sin.
 template <bool kPatched, bool kCanonicalFrame, class Src>
@@ -565,8 +585,12 @@ __device__ __forceinline__ void epi_row(const Params& p, const Src& src, const R
     if (owner != h) continue;
     const int c0 = gl * 32;
     if (kind == GK_PLAIN) {
-      epi_plain16<kPatched, kComp>(src, rv, c0, taddr, gdst);
-      epi_plain16<kPatched, kComp>(src, rv, c0 + 16, taddr, gdst);
+      if (kPatched) {
+        epi_plain32_patched<kComp>(src, rv, c0, taddr, gdst);
+      } else {
+        epi_plain16<kPatched, kComp>(src, rv, c0, taddr, gdst);
+        epi_plain16<kPatched, kComp>(src, rv, c0 + 16, taddr, gdst);
+      }
     } else if (kind == GK_INTERLEAVED) {
       const int pb = p.pair_base[g];
       epi_interleaved16<kPatched, kCanonicalFrame>(src, rv, c0, pb, taddr, cs, gdst);
@@ -888,9 +912,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
             if (!wait_bounded(&sm.uv_empty[ui], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
             uint8_t* slot = sm.uv + (size_t)ui * uv_bytes;
             mbar_arrive_expect_tx(&sm.uv_full[ui], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
-            tma_load_3d(slot, &p.u_map, &sm.uv_full[ui], 0, u_row, kc * kg_chunk, pol_uv);
-            tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], 0,
-                        (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN), kc * kg_chunk, pol_uv);
+            const int32_t v_row = (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN);
+            if (p.uv_row_bytes) {  // whole chunk rows, one request per row
+              tma_load_2d(slot, &p.u_map, &sm.uv_full[ui], kc * kg_chunk * 8, u_row, pol_uv);
+              tma_load_2d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], kc * kg_chunk * 8, v_row, pol_uv);
+            } else {
+              tma_load_3d(slot, &p.u_map, &sm.uv_full[ui], 0, u_row, kc * kg_chunk, pol_uv);
+              tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], 0, v_row, kc * kg_chunk, pol_uv);
+            }
           }
         }
       }
@@ -923,8 +952,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
             tc_fence_after_sync();
             const uint32_t ua = smem_addr(sm.uv + (size_t)ui * uv_bytes), va = ua + p.u_bytes;
             for (int k = 0; k < p.ksteps; ++k) {
-              const uint64_t ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
-              const uint64_t bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+              uint64_t ad, bd;
+              if (p.uv_row_bytes) {  // K step k: 32 bytes into the swizzled rows
+                ad = umma_desc_kmajor_sw(ua + (uint32_t)k * 32u, (uint32_t)p.uv_row_bytes);
+                bd = umma_desc_kmajor_sw(va + (uint32_t)k * 32u, (uint32_t)p.uv_row_bytes);
+              } else {
+                ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
+                bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
+              }
               umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
             }
             umma_commit(&sm.uv_empty[ui]);

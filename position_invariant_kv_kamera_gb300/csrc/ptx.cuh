@@ -207,6 +207,23 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor_noswizzle(uint32_t saddr, u
   return d;
 }
 
+// Shared-memory matrix descriptor for tcgen05.mma, K-major, swizzled: rows of
+// row_bytes (32, 64 or 128) as TMA writes them with the swizzle of the same
+// width, 8-row groups row_bytes * 8 apart (sbo); the tile starts on a boundary
+// of that group size, so the base-offset field stays 0.  A K step of 16 bf16
+// (32 bytes) inside the row advances the start address by 32 bytes.  Swizzle
+// field (bits [61,64)): 6 = 32 B, 4 = 64 B, 2 = 128 B.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_sw(uint32_t saddr, uint32_t row_bytes) {
+  const uint64_t mode = row_bytes == 128 ? 2 : (row_bytes == 64 ? 4 : 6);
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;  // leading byte offset: unused for swizzled K-major
+  d |= static_cast<uint64_t>(((8u * row_bytes) & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= mode << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16, both
 // K-major, dense, no negation; N>>3 in bits [17,23), M>>4 in bits [24,29).
 __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(uint32_t M, uint32_t N) {

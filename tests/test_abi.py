@@ -193,7 +193,7 @@ def test_launch_tuning_set_get_and_validation(lib):
         t = pk.kamera_get_launch_tuning()
         assert (t.bn, t.stages, t.uv_slots, t.ksplit, t.no_pdl, t.grid, t.wait_limit_ns,
                 t.test_unarm_first_stage, t.cache_hints) == (128, 3, 1, 2, 1, 40, 1_000_000, 1, -1)
-        for bad in ({"bn": 96}, {"stages": 1}, {"stages": 7}, {"uv_slots": 3}, {"ksplit": 3}, {"grid": -1},
+        for bad in ({"bn": 96}, {"stages": 1}, {"stages": 7}, {"uv_slots": 9}, {"ksplit": 3}, {"grid": -1},
                     {"grid": 70000}, {"wait_limit_ns": 10}, {"wait_limit_ns": 61_000_000_000}, {"cache_hints": -2},
                     {"cache_hints": 8}):
             assert pk.kamera_set_launch_tuning(raise_on_error=False, **bad) == pk.KAMERA_ERR_INVALID_ARG, bad

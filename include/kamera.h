@@ -359,8 +359,7 @@ kamera_status kamera_reuse_compressed(const kamera_model_desc* model, const kame
  * (kamera_reuse_batched, kamera_relocate, kamera_apply_patch,
  * kamera_reuse_compressed); a field left 0 keeps the library's own choice.
  * It exists for tuning sweeps and tests: the output bits do not depend on
- * bn, stages, uv_slots, ksplit, no_pdl, grid
- * or cache_hints.  A shape that does not fit
+ * bn, stages, uv_slots, ksplit, no_pdl or grid.  A shape that does not fit
  * a call (e.g. bn not dividing D) makes that call return
  * KAMERA_ERR_UNSUPPORTED.  Thread-safe; calls already enqueued keep the
  * setting they were launched with.
@@ -380,9 +379,7 @@ typedef struct {
    * releases its tensor memory and exits; the pool rows of the call are
    * incomplete.  This exercises the expiry path without any fault. */
   int32_t test_unarm_first_stage;
-  int32_t cache_hints;    /* L2 eviction hints of the TMA copies, a bit mask: 1 = canonical loads
-                             evict-first, 2 = pool stores evict-first, 4 = patch factors
-                             evict-last; -1 = none; 0 = the library's choice */
+  int32_t reserved;       /* 0 */
 } kamera_launch_tuning;
 
 /* Set the process-wide tuning (NULL: back to the defaults, all fields 0).

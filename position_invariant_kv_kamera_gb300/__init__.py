@@ -72,7 +72,7 @@ class kamera_launch_tuning(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("stages", ctypes.c_int32), ("uv_slots", ctypes.c_int32),
                 ("ksplit", ctypes.c_int32), ("no_pdl", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("test_unarm_first_stage", ctypes.c_int32),
-                ("cache_hints", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32)]
 
 
 # kamera_reuse_item as a numpy record (32 bytes, naturally aligned)

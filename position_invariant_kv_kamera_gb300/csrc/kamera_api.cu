@@ -150,9 +150,6 @@ const Codebook& codebook() {
 
 enum Mode { MODE_REUSE = 0, MODE_RELOCATE_IN_PLACE = 1, MODE_PATCH_IN_PLACE = 2 };
 
-// L2 eviction hints of the reuse kernel's TMA copies when the tuning leaves them to the library
-constexpr int kDefaultCacheHints = 0;
-
 // Process-wide launch tuning (kamera_set_launch_tuning): copied under the lock
 // at each call, so a call never sees a half-written setting.
 kamera_launch_tuning g_tuning = {};
@@ -179,8 +176,7 @@ kamera_status set_tuning(const kamera_launch_tuning* t) {
     if (v.wait_limit_ns != 0 && (v.wait_limit_ns < 1000 || v.wait_limit_ns > 60000000000ll))
       return fail(KAMERA_ERR_INVALID_ARG, "tuning: wait_limit_ns = %lld (0 or 1e3 .. 6e10)",
                   (long long)v.wait_limit_ns);
-    if (v.cache_hints < -1 || v.cache_hints > 7)
-      return fail(KAMERA_ERR_INVALID_ARG, "tuning: cache_hints = %d (-1, 0 or a mask of 1, 2, 4)", v.cache_hints);
+    if (v.reserved != 0) return fail(KAMERA_ERR_INVALID_ARG, "tuning: reserved must be 0");
   }
   std::lock_guard<std::mutex> lk(g_tuning_mu);
   g_tuning = v;
@@ -462,7 +458,6 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
   p.err_flag = err_flag;
   p.wait_limit_ns = tune.wait_limit_ns > 0 ? (uint64_t)tune.wait_limit_ns : WAIT_LIMIT_NS;
   p.test_unarm = tune.test_unarm_first_stage ? 1 : 0;
-  p.cache_hints = tune.cache_hints < 0 ? 0 : (tune.cache_hints > 0 ? tune.cache_hints : kDefaultCacheHints);
   if (mode == MODE_RELOCATE_IN_PLACE) {
     // only the column blocks that hold rotated groups change
     int lo = D / BN, hi = -1;

@@ -124,8 +124,6 @@ struct Params {
   int32_t* err_flag;
   uint64_t wait_limit_ns;  // bound of every wait
   int32_t test_unarm;      // test only: the producer leaves its first stage unfilled (the waits on it run out)
-  int32_t cache_hints;     // L2 eviction hints: 1 canonical loads evict-first, 2 pool stores evict-first,
-                           // 4 patch factors evict-last
   // compressed canonical store (kComp)
   CUtensorMap kc_map;  // K codes as rows [rows][D] uint8: box 128 x 128, 128B swizzle
   CUtensorMap vc_map;  // V codes as rows [rows][3D/8] uint8: box 3BN/8 x 128, no swizzle
@@ -244,27 +242,28 @@ __device__ __forceinline__ Tile decode(const Params& p, const Walker& w, int64_t
   return t;
 }
 
-// Work unit u of the schedule: units [0, full_rb) are whole row blocks, the
-// rest single tiles of the remaining row blocks (tile tt of them is column
-// block tt mod n_cb of row block full_rb + tt / n_cb).  False past the end.
+// Work unit u < full_rb + tail_tiles of the schedule: units [0, full_rb) are
+// whole row blocks, the rest single tiles of the remaining row blocks (tile tt
+// of them is column block tt mod n_cb of row block full_rb + tt / n_cb).  The
+// tail holds fewer than gridDim.x * n_cb tiles, so its index fits 32 bits.
 struct Unit {
   int64_t rb;
   int cb0, cb1;  // column blocks [cb0, cb1) relative to cb_first
 };
 
-__device__ __forceinline__ bool unit_at(int64_t u, int64_t full_rb, int64_t tail_tiles, int n_cb, Unit& x) {
+__device__ __forceinline__ Unit unit_of(int64_t u, int64_t full_rb, int n_cb) {
+  Unit x;
   if (u < full_rb) {
     x.rb = u;
     x.cb0 = 0;
     x.cb1 = n_cb;
-    return true;
+  } else {
+    const uint32_t tt = (uint32_t)(u - full_rb), q = tt / (uint32_t)n_cb;
+    x.rb = full_rb + q;
+    x.cb0 = (int)(tt - q * (uint32_t)n_cb);
+    x.cb1 = x.cb0 + 1;
   }
-  const int64_t tt = u - full_rb;
-  if (tt >= tail_tiles) return false;
-  x.rb = full_rb + tt / n_cb;
-  x.cb0 = (int)(tt - (tt / n_cb) * n_cb);
-  x.cb1 = x.cb0 + 1;
-  return true;
+  return x;
 }
 
 // A page segment of a tile (rows [sg*S, sg*S + S)): its pool row, or -1 when
@@ -480,23 +479,6 @@ __device__ __forceinline__ void epi_plain16(const Src& src, const RowView& rv, i
   put16(a0, a1, pack8_f2(x), pack8_f2(x + 4), gdst, c0);
 }
 
-// 32 patched columns without rotation, one TMEM load and one wait for all of
-// them: out = x + P.
-template <bool kComp, class Src>
-__device__ __forceinline__ void epi_plain32_patched(const Src& src, const RowView& rv, int c0, uint32_t taddr,
-                                                    uint16_t* gdst) {
-  uint32_t acc[32];
-  tmem_ld32(taddr + (uint32_t)c0, acc);
-  float2 x[16];
-  src.load16(c0, x);
-  src.load16(c0 + 16, x + 8);
-  tmem_ld_wait();
-#pragma unroll
-  for (int e = 0; e < 16; ++e) x[e] = add_f2(x[e], acc_f2(acc, e));
-  put16(rv.chunk(c0), rv.chunk(c0 + 8), pack8_f2(x), pack8_f2(x + 4), gdst, c0);
-  put16(rv.chunk(c0 + 16), rv.chunk(c0 + 24), pack8_f2(x + 8), pack8_f2(x + 12), gdst, c0 + 16);
-}
-
 // 16 rotate-half pairs (cA + e, cB + e), pair index pb + e, two pairs per
 // paired operation:  a' = a cos - b sin,  b' = b cos + a sin.
 template <bool kPatched, bool kCanonicalFrame, class Src>
@@ -585,12 +567,8 @@ __device__ __forceinline__ void epi_row(const Params& p, const Src& src, const R
     if (owner != h) continue;
     const int c0 = gl * 32;
     if (kind == GK_PLAIN) {
-      if (kPatched) {
-        epi_plain32_patched<kComp>(src, rv, c0, taddr, gdst);
-      } else {
-        epi_plain16<kPatched, kComp>(src, rv, c0, taddr, gdst);
-        epi_plain16<kPatched, kComp>(src, rv, c0 + 16, taddr, gdst);
-      }
+      epi_plain16<kPatched, kComp>(src, rv, c0, taddr, gdst);
+      epi_plain16<kPatched, kComp>(src, rv, c0 + 16, taddr, gdst);
     } else if (kind == GK_INTERLEAVED) {
       const int pb = p.pair_base[g];
       epi_interleaved16<kPatched, kCanonicalFrame>(src, rv, c0, pb, taddr, cs, gdst);
@@ -712,58 +690,63 @@ __device__ __forceinline__ void epi_vhalf(const RowView& rv, uint32_t codes, flo
 
 // ---- canonical-tile copies -----------------------------------------------------------------------
 
-// Where the canonical rows of one row block come from.
+// Where the canonical rows of one row block come from: the store (or code)
+// row of tile row 0, the bytes the loads of one tile deliver, the channel,
+// and, in place, the pool row of each page segment (-1 = none).  The scalars
+// stay apart from the segment array so that they live in registers.
 struct SrcRB {
-  Tile t;
-  int32_t src_row;        // store (or code) row of tile row 0
-  int32_t seg_y[BM / 8];  // in place: pool row of each page segment, -1 = none
-  uint32_t bytes;         // bytes the loads of one tile deliver
+  int32_t src_row;
+  uint32_t bytes;
+  int32_t ch;
 };
 
 template <bool kComp>
-__device__ __forceinline__ void rb_source(const Params& p, Walker& w, int64_t rb, int nbox, int nseg, SrcRB& c) {
+__device__ __forceinline__ SrcRB rb_source(const Params& p, Walker& w, int64_t rb, int nbox, int nseg,
+                                           int32_t (&seg_y)[BM / 8]) {
   walk_to(p, w, rb);
-  c.t = decode(p, w, rb);
+  const Tile t = decode(p, w, rb);
+  SrcRB c;
+  c.ch = t.ch;
   c.bytes = (uint32_t)nbox * BOX_BYTES;
   if (p.src_pool && !kComp) {
     c.bytes = 0;
     for (int sg = 0; sg < nseg; ++sg) {
-      c.seg_y[sg] = segment(p, w, c.t, sg).y;
-      if (c.seg_y[sg] >= 0) c.bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
+      seg_y[sg] = segment(p, w, t, sg).y;
+      if (seg_y[sg] >= 0) c.bytes += (uint32_t)nbox * (uint32_t)p.seg_rows * 128u;
     }
   }
-  const int64_t t0 = c.t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
+  const int64_t t0 = t.pos0 - w.dst_pos;  // chunk token of tile row 0 (may be < 0)
   c.src_row = 0;
   if (kComp) {
-    c.src_row = (int32_t)(p.comp_row_offset[w.chunk] + (int64_t)c.t.layer * w.T + t0);
-    c.bytes = c.t.ch == 0 ? (uint32_t)p.BN * (uint32_t)BM : (uint32_t)(3 * p.BN / 8) * (uint32_t)BM;
+    c.src_row = (int32_t)(p.comp_row_offset[w.chunk] + (int64_t)t.layer * w.T + t0);
+    c.bytes = t.ch == 0 ? (uint32_t)p.BN * (uint32_t)BM : (uint32_t)(3 * p.BN / 8) * (uint32_t)BM;
   } else if (!p.src_pool) {
-    c.src_row = (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)c.t.layer * p.n_ch_layout + c.t.ch) * w.T + t0);
+    c.src_row = (int32_t)(p.store_off[w.chunk] / p.D + ((int64_t)t.layer * p.n_ch_layout + t.ch) * w.T + t0);
   }
+  return c;
 }
 
-// The TMA loads of column block cbi of a row block into stage st, with the
-// L2 eviction policy pol (0: none).
+// The TMA loads of column block cbi of a row block into stage st.
 template <bool kComp>
-__device__ __forceinline__ void tile_copy(const Params& p, const SrcRB& c, int cbi, int nbox, int nseg, uint8_t* st,
-                                          uint64_t* bar, uint64_t pol) {
+__device__ __forceinline__ void tile_copy(const Params& p, const SrcRB c, const int32_t (&seg_y)[BM / 8], int cbi,
+                                          int nbox, int nseg, uint8_t* st, uint64_t* bar) {
   const int col0 = (p.cb_first + cbi) * p.BN;
   if (kComp) {
-    if (c.t.ch == 0) {
+    if (c.ch == 0) {
       for (int b = 0; b < p.BN / 128; ++b)
-        tma_load_2d(st + p.out_bytes + b * BOX_BYTES, &p.kc_map, bar, col0 + b * 128, c.src_row, pol);
+        tma_load_2d(st + p.out_bytes + b * BOX_BYTES, &p.kc_map, bar, col0 + b * 128, c.src_row);
     } else {
-      tma_load_2d(st + p.out_bytes, &p.vc_map, bar, (p.cb_first + cbi) * (3 * p.BN / 8), c.src_row, pol);
+      tma_load_2d(st + p.out_bytes, &p.vc_map, bar, (p.cb_first + cbi) * (3 * p.BN / 8), c.src_row);
     }
   } else if (!p.src_pool) {
     for (int b = 0; b < nbox; ++b)
-      tma_load_2d(st + b * BOX_BYTES, &p.src_map, bar, col0 + b * BOX_COLS, c.src_row, pol);
+      tma_load_2d(st + b * BOX_BYTES, &p.src_map, bar, col0 + b * BOX_COLS, c.src_row);
   } else {
     for (int sg = 0; sg < nseg; ++sg) {
-      if (c.seg_y[sg] < 0) continue;
+      if (seg_y[sg] < 0) continue;
       for (int b = 0; b < nbox; ++b)
-        tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[c.t.ch], bar,
-                    col0 + b * BOX_COLS, c.seg_y[sg], pol);
+        tma_load_2d(st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u, &p.pool_map[c.ch], bar,
+                    col0 + b * BOX_COLS, seg_y[sg]);
     }
   }
 }
@@ -794,7 +777,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       err |= __shfl_xor_sync(0xFFFFFFFFu, err, o);
     }
     if (lane == 0) {
-      sm.misc->full_rb = n / gridDim.x * gridDim.x;
+      // the compressed variant deals whole row blocks only: its decode epilogue
+      // is register-bound, and the tail split's loop state measurably slows it
+      sm.misc->full_rb = kComp ? n : n / gridDim.x * gridDim.x;
       sm.misc->tail_tiles = (n - sm.misc->full_rb) * p.n_cb;
       if (blockIdx.x == 0 && err && p.err_flag) atomicOr(p.err_flag, err);
     }
@@ -846,7 +831,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const int64_t full_rb = sm.misc->full_rb, tail_tiles = sm.misc->tail_tiles;
+  const int64_t full_rb = sm.misc->full_rb, n_units = kComp ? full_rb : full_rb + sm.misc->tail_tiles;
   const uint32_t tmem_base = kPatch ? sm.misc->tmem_base : 0u;
   const int nbox = p.BN / BOX_COLS;
   const int nseg = BM / p.seg_rows;
@@ -861,22 +846,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       } else {
         tma_prefetch_desc(p.src_pool ? &p.pool_map[0] : &p.src_map);
       }
-      const uint64_t pol_src = (p.cache_hints & 1) ? l2_policy_evict_first() : 0ull;
       Walker w;
       walker_init(w);
       uint32_t it = 0;  // tiles loaded (stage fills)
       bool go = true;
-      Unit un;
-      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
-        SrcRB c;
-        rb_source<kComp>(p, w, un.rb, nbox, nseg, c);
+      for (int64_t u = blockIdx.x; go && u < n_units; u += gridDim.x) {
+        const Unit un = kComp ? Unit{u, 0, p.n_cb} : unit_of(u, full_rb, p.n_cb);
+        int32_t seg_y[BM / 8];
+        const SrcRB c = rb_source<kComp>(p, w, un.rb, nbox, nseg, seg_y);
         for (int cbi = un.cb0; cbi < un.cb1; ++cbi, ++it) {
           const int s = (int)(it % (uint32_t)p.stages);
           const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
           if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
           if (p.test_unarm && it == 0) continue;  // test only: this stage's barrier is never armed
           mbar_arrive_expect_tx(&sm.full[s], c.bytes);
-          tile_copy<kComp>(p, c, cbi, nbox, nseg, sm.stages + (size_t)s * p.stage_bytes, &sm.full[s], pol_src);
+          tile_copy<kComp>(p, c, seg_y, cbi, nbox, nseg, sm.stages + (size_t)s * p.stage_bytes, &sm.full[s]);
         }
       }
       // drain: every stage's last fill must have landed before the CTA exits
@@ -893,11 +877,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       tma_prefetch_desc(&p.v_map);
       Walker w;
       walker_init(w);
-      const uint64_t pol_uv = (p.cache_hints & 4) ? l2_policy_evict_last() : 0ull;
       uint32_t pu = 0;
       bool go = true;
-      Unit un;
-      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+      for (int64_t u = blockIdx.x; go && u < n_units; u += gridDim.x) {
+        const Unit un = kComp ? Unit{u, 0, p.n_cb} : unit_of(u, full_rb, p.n_cb);
         walk_to(p, w, un.rb);
         if (w.patch < 0) continue;
         const Tile t = decode(p, w, un.rb);
@@ -914,11 +897,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
             mbar_arrive_expect_tx(&sm.uv_full[ui], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
             const int32_t v_row = (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN);
             if (p.uv_row_bytes) {  // whole chunk rows, one request per row
-              tma_load_2d(slot, &p.u_map, &sm.uv_full[ui], kc * kg_chunk * 8, u_row, pol_uv);
-              tma_load_2d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], kc * kg_chunk * 8, v_row, pol_uv);
+              tma_load_2d(slot, &p.u_map, &sm.uv_full[ui], kc * kg_chunk * 8, u_row);
+              tma_load_2d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], kc * kg_chunk * 8, v_row);
             } else {
-              tma_load_3d(slot, &p.u_map, &sm.uv_full[ui], 0, u_row, kc * kg_chunk, pol_uv);
-              tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], 0, v_row, kc * kg_chunk, pol_uv);
+              tma_load_3d(slot, &p.u_map, &sm.uv_full[ui], 0, u_row, kc * kg_chunk);
+              tma_load_3d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], 0, v_row, kc * kg_chunk);
             }
           }
         }
@@ -934,12 +917,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     if (kPatch && lane == 0) {
       const uint32_t idesc = umma_idesc_bf16_f32(BM, (uint32_t)p.BN);
       const uint32_t lbo_u = BM * 16u, lbo_v = (uint32_t)p.BN * 16u;
+      const bool sw = p.uv_row_bytes != 0;
+      const uint32_t ainc = sw ? 2u : (2u * lbo_u) >> 4, binc = sw ? 2u : (2u * lbo_v) >> 4;
       Walker w;
       walker_init(w);
       uint32_t pt = 0, pc = 0;  // patched tiles, patch-factor chunks
       bool issued = false, go = true;
-      Unit un;
-      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+      for (int64_t u = blockIdx.x; go && u < n_units; u += gridDim.x) {
+        const Unit un = kComp ? Unit{u, 0, p.n_cb} : unit_of(u, full_rb, p.n_cb);
         walk_to(p, w, un.rb);
         if (w.patch < 0) continue;
         for (int cbi = un.cb0; cbi < un.cb1 && go; ++cbi, ++pt) {
@@ -951,17 +936,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
             if (!wait_bounded(&sm.uv_full[ui], uph, sm.misc, p.err_flag)) { go = false; break; }
             tc_fence_after_sync();
             const uint32_t ua = smem_addr(sm.uv + (size_t)ui * uv_bytes), va = ua + p.u_bytes;
-            for (int k = 0; k < p.ksteps; ++k) {
-              uint64_t ad, bd;
-              if (p.uv_row_bytes) {  // K step k: 32 bytes into the swizzled rows
-                ad = umma_desc_kmajor_sw(ua + (uint32_t)k * 32u, (uint32_t)p.uv_row_bytes);
-                bd = umma_desc_kmajor_sw(va + (uint32_t)k * 32u, (uint32_t)p.uv_row_bytes);
-              } else {
-                ad = umma_desc_kmajor_noswizzle(ua + (uint32_t)k * 2u * lbo_u, lbo_u, 128u);
-                bd = umma_desc_kmajor_noswizzle(va + (uint32_t)k * 2u * lbo_v, lbo_v, 128u);
-              }
-              umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad, bd, idesc, (kc > 0 || k > 0) ? 1u : 0u);
-            }
+            // descriptors of K step 0; step k starts k x (32 bytes into the swizzled rows, or two
+            // core-matrix K groups) further, i.e. k x ainc / binc in the start-address field
+            const uint64_t ad0 = sw ? umma_desc_kmajor_sw(ua, (uint32_t)p.uv_row_bytes)
+                                    : umma_desc_kmajor_noswizzle(ua, lbo_u, 128u);
+            const uint64_t bd0 = sw ? umma_desc_kmajor_sw(va, (uint32_t)p.uv_row_bytes)
+                                    : umma_desc_kmajor_noswizzle(va, lbo_v, 128u);
+            for (int k = 0; k < p.ksteps; ++k)
+              umma_bf16(tmem_base + buf * (uint32_t)p.BN, ad0 + (uint64_t)(k * ainc), bd0 + (uint64_t)(k * binc),
+                        idesc, (kc > 0 || k > 0) ? 1u : 0u);
             umma_commit(&sm.uv_empty[ui]);
             issued = true;
           }
@@ -979,11 +962,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     if (lane == 0) {
       Walker w;
       walker_init(w);
-      const uint64_t pol_dst = (p.cache_hints & 2) ? l2_policy_evict_first() : 0ull;
       uint32_t it = 0;
       bool go = true;
-      Unit un;
-      for (int64_t u = blockIdx.x; go && unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x) {
+      for (int64_t u = blockIdx.x; go && u < n_units; u += gridDim.x) {
+        const Unit un = kComp ? Unit{u, 0, p.n_cb} : unit_of(u, full_rb, p.n_cb);
         walk_to(p, w, un.rb);
         const Tile t = decode(p, w, un.rb);
         int32_t seg_y[BM / 8];  // pool row of each valid page segment, else -1
@@ -1012,7 +994,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
             if (seg_full[sg]) {
               for (int b = 0; b < nbox; ++b)
                 tma_store_2d(&p.pool_map[t.ch], st + b * BOX_BYTES + (uint32_t)sg * p.seg_rows * 128u,
-                             col0 + b * BOX_COLS, seg_y[sg], pol_dst);
+                             col0 + b * BOX_COLS, seg_y[sg]);
               continue;
             }
             // partly covered page: its 8-row sub-blocks that lie inside the item
@@ -1021,7 +1003,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
               if (k8 < lo8 || k8 >= hi8) continue;
               for (int b = 0; b < nbox; ++b)
                 tma_store_2d(&p.pool_map8[t.ch], st + b * BOX_BYTES + (uint32_t)k8 * 1024u, col0 + b * BOX_COLS,
-                             seg_y[sg] + (k8 * 8 - r0), pol_dst);
+                             seg_y[sg] + (k8 * 8 - r0));
             }
           }
           bulk_commit_group();
@@ -1046,8 +1028,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     int32_t table_item[2] = {-1, -1};  // item whose phases each table holds
     uint32_t it = 0, pt = 0, uix = 0;  // tiles, patched tiles, units of this CTA
     bool ok = true;  // warp-uniform: every wait of this warp so far succeeded
-    Unit un;
-    for (int64_t u = blockIdx.x; unit_at(u, full_rb, tail_tiles, p.n_cb, un); u += gridDim.x, ++uix) {
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++uix) {
+      const Unit un = kComp ? Unit{u, 0, p.n_cb} : unit_of(u, full_rb, p.n_cb);
       walk_to(p, w, un.rb);
       Tile t = decode(p, w, un.rb);
       const bool patched = kPatch && w.patch >= 0;

@@ -189,13 +189,12 @@ def test_launch_tuning_set_get_and_validation(lib):
     bound) with NULL.  Host-only calls."""
     try:
         pk.kamera_set_launch_tuning(bn=128, stages=3, uv_slots=1, ksplit=2, no_pdl=1, grid=40,
-                                    wait_limit_ns=1_000_000, test_unarm_first_stage=1, cache_hints=-1)
+                                    wait_limit_ns=1_000_000, test_unarm_first_stage=1)
         t = pk.kamera_get_launch_tuning()
         assert (t.bn, t.stages, t.uv_slots, t.ksplit, t.no_pdl, t.grid, t.wait_limit_ns,
-                t.test_unarm_first_stage, t.cache_hints) == (128, 3, 1, 2, 1, 40, 1_000_000, 1, -1)
+                t.test_unarm_first_stage) == (128, 3, 1, 2, 1, 40, 1_000_000, 1)
         for bad in ({"bn": 96}, {"stages": 1}, {"stages": 7}, {"uv_slots": 9}, {"ksplit": 3}, {"grid": -1},
-                    {"grid": 70000}, {"wait_limit_ns": 10}, {"wait_limit_ns": 61_000_000_000}, {"cache_hints": -2},
-                    {"cache_hints": 8}):
+                    {"grid": 70000}, {"wait_limit_ns": 10}, {"wait_limit_ns": 61_000_000_000}, {"reserved": 1}):
             assert pk.kamera_set_launch_tuning(raise_on_error=False, **bad) == pk.KAMERA_ERR_INVALID_ARG, bad
         # a rejected setting leaves the previous one in place
         assert pk.kamera_get_launch_tuning().bn == 128

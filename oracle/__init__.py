@@ -120,6 +120,9 @@ def _declare(lib):
     lib.oracle_row.restype = None
     lib.oracle_check_rows.argtypes = [ctypes.POINTER(Model), P, i32, P, i32, i32, P, P, P, i32, P, i32, f64, P, P]
     lib.oracle_check_rows.restype = i64
+    lib.oracle_check_rows_compressed.argtypes = [ctypes.POINTER(Model), P, ctypes.POINTER(CStore), i32, i32, i32,
+                                                 i32, P, i32, P, P, i32, P, f64, P, P]
+    lib.oracle_check_rows_compressed.restype = i64
     lib.oracle_slot.argtypes = [P, i32, i64, i32, i32, i64]
     lib.oracle_slot.restype = i64
     lib.oracle_reuse.argtypes = [ctypes.POINTER(Model), P, i32] + [P, P, P, i32] + [P, P, P, i32, i32] + [
@@ -256,6 +259,32 @@ def check_rows(m: Model, th, channel: int, delta, src_bits, got_bits, u_bits=Non
     bad = lib.oracle_check_rows(ctypes.byref(m), _ptr(th), int(channel), _ptr(d), int(bool(rotate)), int(n),
                                 _ptr(src), _ptr(u_bits), _ptr(v_bits), rank, _ptr(got), int(n_exact), float(abs_tol),
                                 ctypes.byref(mx), ctypes.byref(first))
+    return int(bad), float(mx.value), int(first.value)
+
+
+def check_rows_compressed(m: Model, th, cs: "Compressed", chunk: int, layer: int, channel: int, t0: int, delta,
+                          got_bits, u_bits=None, v_bits=None, abs_tol: float = 1e-3, lib=None):
+    """check_rows for rows reused from the compressed store cs: tokens
+    t0 .. t0 + n - 1 of (chunk, layer, channel), decoded by the oracle, then
+    rotated and patched.  Returns (n_bad, max_err, first_bad)."""
+    lib = lib or load()
+    got = np.ascontiguousarray(got_bits, dtype=np.uint16)
+    n, D = got.shape
+    assert D == row_dim(m)
+    rank = 0
+    if u_bits is not None:
+        u_bits = np.ascontiguousarray(u_bits, dtype=np.uint16)
+        v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+        rank = int(u_bits.shape[1])
+        assert u_bits.shape == (n, rank) and v_bits.shape == (D, rank)
+    th = _c(th, np.float64)
+    d = _deltas(delta)
+    st = cs.struct()
+    mx = ctypes.c_double(0.0)
+    first = ctypes.c_int64(-1)
+    bad = lib.oracle_check_rows_compressed(ctypes.byref(m), _ptr(th), ctypes.byref(st), int(chunk), int(layer),
+                                           int(channel), int(t0), _ptr(d), int(n), _ptr(u_bits), _ptr(v_bits), rank,
+                                           _ptr(got), float(abs_tol), ctypes.byref(mx), ctypes.byref(first))
     return int(bad), float(mx.value), int(first.value)
 
 

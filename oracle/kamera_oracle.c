@@ -663,6 +663,29 @@ void oracle_orbit_mean(const float* deltas, int32_t n, int64_t stride, int64_t n
  * Returns the number of failing elements; *max_err is the largest |got - ref|
  * seen, *first_bad the index i*D + j of the first failure (or -1).  No state
  * outside its arguments, so callers may run blocks on several threads. */
+/* The comparison of one row (D values) against its fp64 reference; updates
+ * the failure count, the largest error and the first failing index (base = the
+ * row's first element index).  exact: the canonical bits that columns
+ * [0, n_exact) must equal, or NULL. */
+static void compare_row(int32_t D, const double* ref, const uint16_t* got, const uint16_t* exact, int32_t n_exact,
+                        double abs_tol, int64_t base, int64_t* bad, double* worst, int64_t* first_bad) {
+  for (int32_t j = 0; j < D; ++j) {
+    double g = bf16_bits_to_f64(got[j]);
+    double err = fabs(g - ref[j]);
+    int e2 = 0;
+    double a = fabs(ref[j]);
+    frexp(a > 0x1p-126 ? a : 0x1p-126, &e2); /* a = f * 2^e2, f in [0.5, 1): floor(log2 a) = e2 - 1 */
+    double tol = ldexp(1.0, e2 - 1 - 7) + abs_tol;
+    int ok = err <= tol; /* false for NaN */
+    if (exact != NULL && j < n_exact && got[j] != exact[j]) ok = 0;
+    if (err > *worst) *worst = err;
+    if (!ok) {
+      if (*first_bad < 0) *first_bad = base + j;
+      ++*bad;
+    }
+  }
+}
+
 int64_t oracle_check_rows(const oracle_model* m, const double* theta, int32_t channel, const int64_t* deltas,
                           int32_t rotate, int32_t n_rows, const uint16_t* src, const uint16_t* u,
                           const uint16_t* vmat, int32_t rank, const uint16_t* got, int32_t n_exact, double abs_tol,
@@ -679,26 +702,45 @@ int64_t oracle_check_rows(const oracle_model* m, const double* theta, int32_t ch
     for (int64_t e = 0; e < (int64_t)D * rank; ++e) v[e] = bf16_bits_to_f64(vmat[e]);
   for (int32_t i = 0; i < n_rows; ++i) {
     const uint16_t* srow = src + (int64_t)i * D;
-    const uint16_t* grow = got + (int64_t)i * D;
     for (int32_t j = 0; j < D; ++j) s[j] = bf16_bits_to_f64(srow[j]);
     if (u != NULL)
       for (int32_t r = 0; r < rank; ++r) ur[r] = bf16_bits_to_f64(u[(int64_t)i * rank + r]);
     oracle_row(m, theta, channel, deltas, rotate, s, u != NULL ? ur : NULL, v, rank, ref);
-    for (int32_t j = 0; j < D; ++j) {
-      double g = bf16_bits_to_f64(grow[j]);
-      double err = fabs(g - ref[j]);
-      int e2 = 0;
-      double a = fabs(ref[j]);
-      frexp(a > 0x1p-126 ? a : 0x1p-126, &e2); /* a = f * 2^e2, f in [0.5, 1): floor(log2 a) = e2 - 1 */
-      double tol = ldexp(1.0, e2 - 1 - 7) + abs_tol;
-      int ok = err <= tol; /* false for NaN */
-      if (j < n_exact && grow[j] != srow[j]) ok = 0;
-      if (err > worst) worst = err;
-      if (!ok) {
-        if (*first_bad < 0) *first_bad = (int64_t)i * D + j;
-        ++bad;
-      }
-    }
+    compare_row(D, ref, got + (int64_t)i * D, srow, n_exact, abs_tol, (int64_t)i * D, &bad, &worst, first_bad);
+  }
+  free(v);
+  free(s);
+  free(ur);
+  free(ref);
+  *max_err = worst;
+  return bad;
+}
+
+/* The same check for rows reused from a compressed store: the canonical row
+ * of token t0 + i of (chunk, layer, channel) is decoded with oracle_decode_row
+ * (real-valued, no bf16 rounding), then rotated, patched and compared as
+ * above. */
+int64_t oracle_check_rows_compressed(const oracle_model* m, const double* theta, const oracle_cstore* cs,
+                                     int32_t chunk, int32_t layer, int32_t channel, int32_t t0,
+                                     const int64_t* deltas, int32_t n_rows, const uint16_t* u, const uint16_t* vmat,
+                                     int32_t rank, const uint16_t* got, double abs_tol, double* max_err,
+                                     int64_t* first_bad) {
+  int32_t D = oracle_row_dim(m);
+  double* v = (double*)calloc((size_t)D * (size_t)(rank > 0 ? rank : 1), sizeof(double));
+  double* s = (double*)malloc((size_t)D * sizeof(double));
+  double* ur = (double*)malloc((size_t)(rank > 0 ? rank : 1) * sizeof(double));
+  double* ref = (double*)malloc((size_t)D * sizeof(double));
+  int64_t bad = 0;
+  double worst = 0.0;
+  *first_bad = -1;
+  if (u != NULL)
+    for (int64_t e = 0; e < (int64_t)D * rank; ++e) v[e] = bf16_bits_to_f64(vmat[e]);
+  for (int32_t i = 0; i < n_rows; ++i) {
+    oracle_decode_row(m, cs, chunk, layer, channel, t0 + i, s);
+    if (u != NULL)
+      for (int32_t r = 0; r < rank; ++r) ur[r] = bf16_bits_to_f64(u[(int64_t)i * rank + r]);
+    oracle_row(m, theta, channel, deltas, 1, s, u != NULL ? ur : NULL, v, rank, ref);
+    compare_row(D, ref, got + (int64_t)i * D, NULL, 0, abs_tol, (int64_t)i * D, &bad, &worst, first_bad);
   }
   free(v);
   free(s);

@@ -10,8 +10,8 @@ copies of the seeded generator's output, which the kernels read), and
 applies the comparison rule -- on all host cores, one item block per task.
 Properties that hold at any size (which slots are written, sentinel slots
 untouched, bit-exact copies) are checked over the whole pool on the device.
-The compressed-store case decodes rows with the oracle's O(d^2) decoder and
-stays sampled."""
+The compressed-store case decodes every row with the oracle's decoder
+(``oracle.check_rows_compressed``)."""
 import os
 from concurrent.futures import ThreadPoolExecutor
 
@@ -273,11 +273,44 @@ def test_full_long_video():
     torch.cuda.empty_cache()
 
 
+def _check_every_row_compressed(wl, t, ocs):
+    """Every row every item wrote from the compressed store, against the oracle
+    (decode, rotate, patch), layer by layer and item block by item block on all
+    host cores."""
+    m = _oracle_model(wl)
+    th = H.oracle_theta(wl)
+    L, D = wl.num_layers, wl.D
+    items = [it for it in wl.items if int(it["n_tokens"]) > 0]
+    dst = [_dest_rows(wl, it) for it in items]
+    bounds = np.cumsum([0] + [len(d) for d in dst])
+    all_dst = np.concatenate(dst)
+    patch2d = t["patch"].view(-1, wl.rank)
+    failures = []
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        for layer in range(L):
+            for ch in range(2):
+                pool = t["pool_k"] if ch == 0 else t["pool_v"]
+                got = _gather(pool.view(L, -1, D)[layer], all_dst)
+                futs = []
+                for k, it in enumerate(items):
+                    T, pid = int(it["n_tokens"]), int(it["patch_id"])
+                    base = int(wl.patch_off[pid]) // wl.rank + (layer * 2 + ch) * (T + D)
+                    u = _gather(patch2d, base + np.arange(T))
+                    v = _gather(patch2d, base + T + np.arange(D))
+                    futs.append((k, ex.submit(oracle.check_rows_compressed, m, th, ocs, int(it["chunk_id"]), layer, ch,
+                                              0, int(it["delta"]), got[bounds[k]:bounds[k + 1]], u, v)))
+                for k, f in futs:
+                    n_bad, max_err, first = f.result()
+                    if n_bad:
+                        failures.append((layer, ch, k, n_bad, max_err, divmod(first, D)))
+    assert not failures, failures[:10]
+
+
 def test_full_gqa_video_compressed():
     """The headline batch reused from a compressed store at full size (458,752
     store rows, 0.33 GB of codes) in the bench's launch configuration, with
-    seeded random contents; sampled rows are decoded and recomputed by the
-    oracle one by one."""
+    seeded random contents: every written row is decoded and recomputed by the
+    oracle, and sampled rows once more from host-regenerated patch factors."""
     wl = W.gqa_video()
     arrs = H.comp_arrays(wl.random_compressed())
     cstore, _ct = H.device_compressed(arrs, torch)
@@ -301,3 +334,4 @@ def test_full_gqa_video_compressed():
         got = H.to_bits((t["pool_k"] if ch == 0 else t["pool_v"])[layer, page, slot])
         ok = H.within_tol(H.bits_to_f64(got), ref)
         assert ok.all(), (i, layer, ch, tok, np.abs(H.bits_to_f64(got) - ref).max())
+    _check_every_row_compressed(wl, t, ocs)

@@ -6,7 +6,9 @@ largest workloads can be checked on all host cores.  Here it is pinned to
 (a) the rule as the Python harness states it -- planted errors at and across
 the tolerance edge, NaN, the exact-copy columns -- and (b) the oracle's row
 function itself: a correctly rounded block passes, a block from a wrong
-shift, a dropped patch or a transposed V fails."""
+shift, a dropped patch or a transposed V fails.  ``oracle.check_rows_compressed``
+(rows decoded from a compressed store first) is pinned to the oracle's whole
+compressed reuse operator."""
 import numpy as np
 import pytest
 
@@ -123,3 +125,42 @@ def test_m_rope_section_shifts_are_applied():
 def _fields(m, frame):
     return (m.family, m.num_layers, m.num_kv_heads, m.head_dim, m.rope_dim, m.latent_dim, m.pairing, frame,
             tuple(m.sections))
+
+
+def test_compressed_rows_check_against_the_oracle_operator():
+    """oracle.check_rows_compressed (decode, rotate, patch, compare) agrees with
+    the oracle's whole compressed reuse operator: its pool image, rounded to
+    bf16, passes row block by row block; a planted error, the wrong chunk or
+    the wrong shift fails."""
+    from synth import workloads as W
+
+    wl = W.gqa_video(num_layers=2, n_chunks=3, T=70, rank=16, page_size=16).replace(num_kv_heads=2)
+    m = oracle.model(wl.family, wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.rope_dim, wl.latent_dim,
+                     wl.pairing, wl.patch_frame)
+    th = oracle.theta(wl.rope_base, wl.rope_dim)
+    arrs = H.comp_arrays(wl.random_compressed())
+    cs = H.oracle_store(arrs)
+    err, ref_k, ref_v, wk, wv = H.oracle_reference_compressed(wl, cs)
+    assert err == 0
+    D, P = wl.D, wl.page_size
+    for ch, ref in ((0, ref_k), (1, ref_v)):
+        for it in wl.items:
+            T, c, pid = int(it["n_tokens"]), int(it["chunk_id"]), int(it["patch_id"])
+            pos = int(it["dst_pos"]) + np.arange(T)
+            pages, slots = wl.block_table[0, pos // P], pos % P
+            for layer in range(wl.num_layers):
+                got = _bf16(ref[layer, pages, slots])
+                u = wl.u_rows(pid, layer, ch)
+                v = wl.v_rows(pid, layer, ch)
+                args = (m, th, cs, c, layer, ch, 0, int(it["delta"]))
+                assert oracle.check_rows_compressed(*args, got, u, v)[0] == 0
+                bad = got.copy()
+                bad[T // 2, D // 3] ^= np.uint16(0x0040)  # a few ulps off
+                n_bad, _, first = oracle.check_rows_compressed(*args, bad, u, v)
+                assert n_bad == 1 and first == (T // 2) * D + D // 3
+                other = (c + 1) % len(wl.chunk_lens)
+                assert oracle.check_rows_compressed(m, th, cs, other, layer, ch, 0, int(it["delta"]), got, u,
+                                                    v)[0] > 0
+                if ch == 0:
+                    assert oracle.check_rows_compressed(m, th, cs, c, layer, ch, 0, int(it["delta"]) + 1, got, u,
+                                                        v)[0] > 0

@@ -532,7 +532,7 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
     p.patch_elems = patches->n_elems;
     p.n_patches = patches->n_patches;
     const int kw = rank / ksplit;  // K elements per chunk
-    if (kw >= 16) {
+    if (kw >= 16 && !comp) {  // (the compressed variant measured faster with core-matrix boxes)
       // whole chunk rows (2 kw = 32, 64 or 128 bytes) per TMA row, swizzled at that width: the
       // K-major layout tcgen05.mma reads with the matching swizzle mode
       p.uv_row_bytes = 2 * kw;
@@ -545,7 +545,7 @@ kamera_status launch(Mode mode, const kamera_model_desc* model, const kamera_chu
       if (kamera_status st = encode(&p.u_map, patches->data, 2, dims, strides, ubox, swz, "U")) return st;
       if (kamera_status st = encode(&p.v_map, patches->data, 2, dims, strides, vbox, swz, "V")) return st;
     } else {
-      // rank 8: 16-byte rows as K-major core matrices (8 rows x 16 bytes), one K group per chunk
+      // rank 8 (16-byte rows) and the compressed variant: K-major core matrices (8 rows x 16 bytes)
       p.uv_row_bytes = 0;
       const cuuint64_t dims[3] = {8, (cuuint64_t)(patch_rows > 0 ? patch_rows : 1), (cuuint64_t)(rank / 8)};
       const cuuint64_t strides[2] = {(cuuint64_t)rank * 2, 16};

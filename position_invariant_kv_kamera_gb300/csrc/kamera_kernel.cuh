@@ -24,8 +24,9 @@
 //               the in-item part of partly covered pages).
 //   warp 11     TMA producer of the patch factors: the U tile [128 x m] and
 //               the V tile [BN x m] of each tile, in K chunks of m / ksplit,
-//               as whole chunk rows swizzled at their width (K-major; rank 8:
-//               core matrices with a zeroed second K group), into slots.
+//               as whole chunk rows swizzled at their width (K-major), or --
+//               rank 8 and the compressed variant -- as 16-byte core matrices
+//               (rank 8 with a zeroed second K group), into slots.
 //   warps 3-10  epilogue, two warps per TMEM lane quadrant, each half taking
 //               half of the tile's rotation units: tcgen05.ld the patch row,
 //               rotate the key row's RoPE pairs by delta*theta_i (fp64 angle
@@ -349,11 +350,11 @@ __host__ __device__ constexpr uint32_t smem_extra_bytes(int stages, int uv_slots
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, SmemMisc* misc, int32_t* err_flag,
                                              bool honour_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = global_timer_ns(), limit = misc->wait_limit;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && *reinterpret_cast<volatile int32_t*>(&misc->abort_flag)) return false;
-    if (global_timer_ns() - t0 > misc->wait_limit) {
+    if (global_timer_ns() - t0 > limit) {
       *reinterpret_cast<volatile int32_t*>(&misc->abort_flag) = 1;
       if (err_flag) atomicOr(err_flag, KAMERA_EFLAG_TIMEOUT);
       return false;
@@ -849,6 +850,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
       Walker w;
       walker_init(w);
       uint32_t it = 0;  // tiles loaded (stage fills)
+      const uint32_t unarm_it = p.test_unarm ? 0u : 0xFFFFFFFFu;  // test only: the fill left unarmed
       bool go = true;
       for (int64_t u = blockIdx.x; go && u < n_units; u += gridDim.x) {
         const Unit un = kComp ? Unit{u, 0, p.n_cb} : unit_of(u, full_rb, p.n_cb);
@@ -858,7 +860,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
           const int s = (int)(it % (uint32_t)p.stages);
           const uint32_t ph = (it / (uint32_t)p.stages) & 1u;
           if (!wait_bounded(&sm.empty[s], ph ^ 1u, sm.misc, p.err_flag)) { go = false; break; }
-          if (p.test_unarm && it == 0) continue;  // test only: this stage's barrier is never armed
+          if (it == unarm_it) continue;  // test only: this stage's barrier is never armed
           mbar_arrive_expect_tx(&sm.full[s], c.bytes);
           tile_copy<kComp>(p, c, seg_y, cbi, nbox, nseg, sm.stages + (size_t)s * p.stage_bytes, &sm.full[s]);
         }
@@ -896,7 +898,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
             uint8_t* slot = sm.uv + (size_t)ui * uv_bytes;
             mbar_arrive_expect_tx(&sm.uv_full[ui], (uint32_t)(BM + p.BN) * (uint32_t)kg_chunk * 16u);
             const int32_t v_row = (int32_t)(prow + w.T + (int64_t)(p.cb_first + cbi) * p.BN);
-            if (p.uv_row_bytes) {  // whole chunk rows, one request per row
+            if (!kComp && p.uv_row_bytes) {  // whole chunk rows, one request per row
               tma_load_2d(slot, &p.u_map, &sm.uv_full[ui], kc * kg_chunk * 8, u_row);
               tma_load_2d(slot + p.u_bytes, &p.v_map, &sm.uv_full[ui], kc * kg_chunk * 8, v_row);
             } else {
@@ -917,7 +919,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) reuse_kernel(const __grid_cons
     if (kPatch && lane == 0) {
       const uint32_t idesc = umma_idesc_bf16_f32(BM, (uint32_t)p.BN);
       const uint32_t lbo_u = BM * 16u, lbo_v = (uint32_t)p.BN * 16u;
-      const bool sw = p.uv_row_bytes != 0;
+      const bool sw = !kComp && p.uv_row_bytes != 0;
       const uint32_t ainc = sw ? 2u : (2u * lbo_u) >> 4, binc = sw ? 2u : (2u * lbo_v) >> 4;
       Walker w;
       walker_init(w);

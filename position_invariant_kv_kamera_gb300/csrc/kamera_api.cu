@@ -704,6 +704,42 @@ kamera_status factor_shape(const kamera_factor_desc* d, FactorShape* fs) {
   return KAMERA_OK;
 }
 
+// The tensor maps of the aligned instance's tall products (the table beside FactorMap).
+kamera_status factor_maps(factor::FParams* f, int grid) {
+  using namespace factor;
+  const cuuint64_t T = (cuuint64_t)f->T, D = (cuuint64_t)f->D, k = (cuuint64_t)f->k, kp = (cuuint64_t)f->kp;
+  const cuuint64_t m = (cuuint64_t)f->m, n = (cuuint64_t)f->n_slabs, g = (cuuint64_t)grid;
+  const cuuint64_t slab = f->n_slabs > 1 ? (cuuint64_t)f->delta_stride : T * D;  // a single slab: any stride
+  const cuuint64_t wpc = (cuuint64_t)f->work_per_cta;
+  const float* Y = f->work;
+  const float* Z = Y + kp * T;
+  const float* Bw = Z + kp * D;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B, AT = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+  struct Spec {
+    int idx;
+    const void* base;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    CUtensorMapSwizzle swz;
+    const char* what;
+  };
+  const Spec specs[] = {
+      {MAP_DELTA_K, f->delta, {D, T, n}, {D * 4, slab * 4}, {32, 128, 1}, SW, "delta (K-major)"},
+      {MAP_DELTA_MN, f->delta, {D, T, n}, {D * 4, slab * 4}, {32, 32, 1}, AT, "delta (M-major)"},
+      {MAP_OMEGA_MN, f->omega, {k, D, 1}, {k * 4, k * D * 4}, {32, 32, 1}, AT, "omega"},
+      {MAP_Y_K, Y, {T, kp, g}, {T * 4, wpc * 4}, {32, 64, 1}, SW, "Y (K-major)"},
+      {MAP_Z_K, Z, {D, kp, g}, {D * 4, wpc * 4}, {32, 64, 1}, SW, "Z (K-major)"},
+      {MAP_Y_MN, Y, {T, kp, g}, {T * 4, wpc * 4}, {32, 32, 1}, AT, "Y (M-major)"},
+      {MAP_W_MN, Z, {m, kp, g}, {m * 4, wpc * 4}, {32, 32, 1}, AT, "W_m"},
+      {MAP_B_MN, Bw, {D, kp, g}, {D * 4, wpc * 4}, {32, 32, 1}, AT, "B (M-major)"},
+  };
+  for (const Spec& sp : specs)
+    if (kamera_status st = encode(&f->maps[sp.idx], sp.base, 3, sp.dims, sp.strides, sp.box, sp.swz, sp.what,
+                                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return st;
+  return KAMERA_OK;
+}
+
 // The aligned instance when the shapes and pointers allow it (the conditions of
 // factor_kernel<true>), else the one with run-time fallbacks.
 kamera_status launch_factor(const factor::FParams& fp, int grid, uint32_t smem, kamera_stream_t stream) {
@@ -725,7 +761,14 @@ kamera_status launch_factor(const factor::FParams& fp, int grid, uint32_t smem, 
                        ((reinterpret_cast<uintptr_t>(fp.delta) | reinterpret_cast<uintptr_t>(fp.omega) |
                          reinterpret_cast<uintptr_t>(fp.work)) & 15u) == 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = aligned ? factor::launch_aligned(fp, grid, smem, s) : factor::launch_general(fp, grid, smem, s);
+  cudaError_t e;
+  if (aligned) {
+    factor::FParams fa = fp;
+    if (kamera_status st = factor_maps(&fa, grid)) return st;
+    e = factor::launch_aligned(fa, grid, smem, s);
+  } else {
+    e = factor::launch_general(fp, grid, smem, s);
+  }
   if (e != cudaSuccess) return fail(KAMERA_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   return KAMERA_OK;
 }

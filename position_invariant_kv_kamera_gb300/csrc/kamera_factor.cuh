@@ -32,6 +32,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace kamera {
 namespace factor {
 
@@ -45,7 +47,21 @@ constexpr int GT = 64;     // GEMM tile (rows and columns)
 constexpr int GK = 16;     // GEMM K step
 constexpr int MAX_SWEEPS = 20;
 
+// The operands of the aligned instance's tensor-core products as TMA tensor maps,
+// encoded by the host per launch, all 3-D (x contiguous, y rows, z the slab or the
+// CTA) over fp32:
+//   MAP_DELTA_K   Delta {D, T, n_slabs}, box {32, 128, 1}, 128-byte swizzle (A K-major)
+//   MAP_DELTA_MN  Delta {D, T, n_slabs}, box {32, 32, 1}, 128-byte swizzle of 32-byte atoms (A M-major)
+//   MAP_OMEGA_MN  Omega {k, D, 1}, box {32, 32, 1}, 32-byte atoms (B N-major)
+//   MAP_Y_K       Y as [kp][T] per CTA {T, kp, grid}, box {32, 64, 1}, 128-byte swizzle (B K-major)
+//   MAP_Z_K       Z as [kp][D] per CTA {D, kp, grid}, box {32, 64, 1}, 128-byte swizzle (B K-major)
+//   MAP_Y_MN      Y {T, kp, grid}, box {32, 32, 1}, 32-byte atoms (A M-major)
+//   MAP_W_MN      W_m as [kp][m] at the start of Z {m, kp, grid}, box {32, 32, 1}, 32-byte atoms (B N-major)
+//   MAP_B_MN      B as [kp][D] per CTA {D, kp, grid}, box {32, 32, 1}, 32-byte atoms (A M-major)
+enum FactorMap { MAP_DELTA_K, MAP_DELTA_MN, MAP_OMEGA_MN, MAP_Y_K, MAP_Z_K, MAP_Y_MN, MAP_W_MN, MAP_B_MN, N_FACTOR_MAPS };
+
 struct FParams {
+  CUtensorMap maps[N_FACTOR_MAPS];  // the aligned instance only
   const float* delta;    // [n_slabs][T][D]
   int64_t delta_stride;  // elements between slabs
   int32_t n_slabs, T, D, m, k, kp, power_iters;
@@ -908,9 +924,205 @@ __device__ void gemm_tall(int M, int N, int K, const float* A, int64_t a_ld, con
   __syncthreads();
 }
 
-// Shared memory of one CTA, in floats, for a given kp and m.
+// ---- tall-skinny products on the 5th-generation tensor cores -------------------------------
+// The products of the aligned instance with N <= 64: tcgen05.mma kind::tf32 into fp32
+// accumulators of 128 TMEM lanes x 64 columns (N padded to 64 with zero columns of B),
+// two of them, so that the epilogue of one 128-row tile overlaps the MMAs of the next.
+// The operands arrive by TMA in TC_RING_STAGES stages of 24 KB (K = 32), in the
+// canonical layouts the MMA reads: a K-contiguous operand K-major (128-byte rows, the
+// 128-byte swizzle), an M- or N-contiguous one MN-major (K rows of 32 values, 128
+// bytes, with the 128-byte swizzle of 32-byte atomicity that tcgen05 reads for
+// 32-bit MN-major operands; atoms of 32 along M or N 4096 bytes apart), so neither
+// needs a transposition.  One thread issues the copies (a stage is refilled once the
+// MMAs that read it committed), one issues the MMAs (four K = 8 per stage), and warps
+// 4-7 move each finished accumulator to C; the stages of all the tiles of a product
+// form one stream.  The tensor core takes the upper 19 bits of each fp32 word (tf32 by
+// truncation): the deficits are read as they are, and every operand this kernel
+// writes itself (the fp32 products' outputs, the final Q, W_m) is stored rounded to
+// the nearest tf32 value, so that for those the truncation is exact.  Out-of-range
+// rows and columns arrive as zeros.
+constexpr int TC_RING_STAGES = 4;
+constexpr int TC_N = 64;                       // accumulator columns: N <= TC_N
+constexpr uint32_t TCA_BYTES = TM * TK * 4;    // A stage: 128 x 32 fp32
+constexpr uint32_t TCB_BYTES = TC_N * TK * 4;  // B stage: 64 x 32 fp32
+constexpr uint32_t TC_STAGE_BYTES = TCA_BYTES + TCB_BYTES;
+constexpr int TC_RING_FLOATS = (TC_RING_STAGES * TC_STAGE_BYTES + 1024) / 4;  // + alignment to 1024 bytes
+constexpr uint32_t TC_TMEM_COLS = 2 * TC_N;
+
+struct TcState {  // per CTA, in shared memory
+  uint64_t full[TC_RING_STAGES];   // stage landed
+  uint64_t empty[TC_RING_STAGES];  // stage's MMAs completed
+  uint64_t accfull[2];             // accumulator b holds a finished tile
+  uint64_t accempty[2];            // accumulator b was read out (one arrival per epilogue warp)
+  uint32_t tmem;
+};
+
+// Position of a CTA in its stream of tensor-core stages and tiles, across products:
+// the phases of the barriers follow from it.
+struct TcCursor {
+  uint32_t stage = 0, tile = 0;
+};
+
+// fp32 -> the nearest tf32 value (ties away from zero), as an fp32 word whose low 13
+// bits are zero: operands this kernel writes for later products are stored rounded,
+// so that the tensor core's truncation leaves them unchanged.
+__device__ __forceinline__ float tf32_rn(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+
+// Bounded wait (2 s): on expiry it returns and the products are wrong, the kernel
+// never hangs.
+__device__ __forceinline__ void tc_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > 2000000000ull) return;
+}
+
+// Set-up and tear-down of the accumulators and the barriers; whole CTA.
+__device__ __forceinline__ void tc_setup(TcState* tc) {
+  if (threadIdx.x < 32) {
+    tmem_alloc(&tc->tmem, TC_TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TC_RING_STAGES; ++i) {
+      mbar_init(&tc->full[i], 1);
+      mbar_init(&tc->empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tc->accfull[b], 1);
+      mbar_init(&tc->accempty[b], 4);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+}
+
+__device__ __forceinline__ void tc_teardown(TcState* tc) {
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (threadIdx.x < 32) tmem_dealloc(tc->tmem, TC_TMEM_COLS);
+}
+
+// C = A B (M x N, N <= 64) with A(i, l) and B(l, j) read through the tensor maps amap
+// and bmap at slab or CTA coordinate az / bz.  kAK: A is K-contiguous (map box
+// {32 along K, 128 rows}), else M-contiguous (box {32 along M, 32 K rows}, four per
+// stage); kBK: B is K-contiguous (box {32 along K, 64 columns}), else N-contiguous
+// (box {32 along N, 32 K rows}, two per stage).  Element (i, j) of C goes to
+// C[i*c_rs + j*c_cs].  Whole CTA.
+template <typename OutT, bool kAK, bool kBK>
+__device__ void gemm_tall_tma(int M, int N, int K, const CUtensorMap* amap, int az, const CUtensorMap* bmap, int bz,
+                              OutT* C, int64_t c_rs, int64_t c_cs, float* ring, TcState* tc, TcCursor& cur) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int R = TC_RING_STAGES;
+  const uint32_t pad = ((smem_u32(ring) + 1023u) & ~1023u) - smem_u32(ring);
+  unsigned char* stages = reinterpret_cast<unsigned char*>(ring) + pad;
+  const int nsteps = (K + TK - 1) / TK, ntiles = (M + TM - 1) / TM, total = nsteps * ntiles;
+  const uint32_t g0 = cur.stage, t0 = cur.tile;
+  constexpr uint32_t IDESC = umma_idesc_tf32_f32(TM, TC_N, !kAK, !kBK);
+  // the operands this CTA wrote with plain stores (earlier products, the
+  // orthonormalisation), and the plain uses of the ring since the last product,
+  // ordered before the TMA traffic
+  fence_proxy_async_global();
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {  // copies
+    for (int idx = 0; idx < total; ++idx) {
+      const uint32_t g = g0 + (uint32_t)idx, slot = g % R;
+      if (g >= (uint32_t)R) tc_wait(&tc->empty[slot], ((g / R) - 1u) & 1u);
+      const int tt = idx / nsteps, i0 = tt * TM, l0 = (idx - tt * nsteps) * TK;
+      unsigned char* sA = stages + slot * TC_STAGE_BYTES;
+      unsigned char* sB = sA + TCA_BYTES;
+      uint64_t* bar = &tc->full[slot];
+      mbar_arrive_expect_tx(bar, TC_STAGE_BYTES);
+      if (kAK) {
+        tma_load_3d(sA, amap, bar, l0, i0, az);
+      } else {
+#pragma unroll
+        for (int a = 0; a < TM / 32; ++a) tma_load_3d(sA + 4096 * a, amap, bar, i0 + 32 * a, l0, az);
+      }
+      if (kBK) {
+        tma_load_3d(sB, bmap, bar, l0, 0, bz);
+      } else {
+#pragma unroll
+        for (int b = 0; b < TC_N / 32; ++b) tma_load_3d(sB + 4096 * b, bmap, bar, 32 * b, l0, bz);
+      }
+    }
+  } else if (tid == 32) {  // MMAs
+    int tt = 0, st = 0;
+    for (int idx = 0; idx < total; ++idx) {
+      const uint32_t g = g0 + (uint32_t)idx, slot = g % R, gt = t0 + (uint32_t)tt, acc = tc->tmem + (gt & 1u) * TC_N;
+      if (st == 0 && gt >= 2u) tc_wait(&tc->accempty[gt & 1u], ((gt >> 1) - 1u) & 1u);
+      tc_wait(&tc->full[slot], (g / R) & 1u);
+      tc_fence_after_sync();
+      const uint32_t sA = smem_u32(stages + slot * TC_STAGE_BYTES), sB = sA + TCA_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < TK / 8; ++ks) {  // K = 8 per MMA: 32 bytes of a K-major row, two MN-major K groups
+        const uint64_t ad = kAK ? umma_desc_kmajor_sw(sA + 32u * ks, 128u)
+                                : umma_desc_mnmajor_sw128b32(sA + 1024u * ks, 4096u, 512u);
+        const uint64_t bd = kBK ? umma_desc_kmajor_sw(sB + 32u * ks, 128u)
+                                : umma_desc_mnmajor_sw128b32(sB + 1024u * ks, 4096u, 512u);
+        umma_tf32(acc, ad, bd, IDESC, (st > 0 || ks > 0) ? 1u : 0u);
+      }
+      umma_commit(&tc->empty[slot]);
+      if (st == nsteps - 1) umma_commit(&tc->accfull[gt & 1u]);
+      if (++st == nsteps) {
+        st = 0;
+        ++tt;
+      }
+    }
+  } else if (warp >= 4) {  // epilogue: warp w reads TMEM lanes 32 (w - 4) .. +31, its rows of the tile
+    const int q = warp - 4;
+    for (int tt = 0; tt < ntiles; ++tt) {
+      const uint32_t gt = t0 + (uint32_t)tt;
+      tc_wait(&tc->accfull[gt & 1u], (gt >> 1) & 1u);
+      __syncwarp();
+      tc_fence_after_sync();
+      const int gi = tt * TM + 32 * q + lane;
+      for (int cb = 0; cb < N; cb += 32) {
+        uint32_t v[32];
+        tmem_ld32(tc->tmem + ((uint32_t)(32 * q) << 16) + (gt & 1u) * TC_N + (uint32_t)cb, v);
+        tmem_ld_wait();
+        if (gi < M) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (cb + j < N) {
+              const float x = __uint_as_float(v[j]);
+              if constexpr (sizeof(OutT) == 2) {
+                __nv_bfloat16 hv = __float2bfloat16_rn(x);
+                C[gi * c_rs + (cb + j) * c_cs] = *reinterpret_cast<uint16_t*>(&hv);
+              } else {
+                C[gi * c_rs + (cb + j) * c_cs] = tf32_rn(x);  // an operand of a later product
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tc->accempty[gt & 1u]);
+    }
+  }
+  cur.stage = g0 + (uint32_t)total;
+  cur.tile = t0 + (uint32_t)ntiles;
+  __syncthreads();  // C is written; the ring is free for the caller once its MMAs completed (seen above)
+}
+
+// Shared memory of one CTA, in floats, for a given kp and m.  The first region holds
+// the GEMM stages while the Delta products, the orthonormalisations and the output
+// products run, and C, W and Ws (the eigenproblem) at its end while they do not; the
+// fp32 GEMM tiles at its start serve the products with C alive.
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int eig_floats(int kp, int m) { return 2 * kp * (kp + 1) + kp * m; }
+__host__ __device__ constexpr int region_floats(int kp, int m) {
+  return cmax(cmax(RING_FLOATS, TC_RING_FLOATS), 2 * TILE_FLOATS + eig_floats(kp, m));
+}
 __host__ __device__ constexpr int factor_smem_floats(int kp, int m) {
-  return RING_FLOATS + 2 * kp * (kp + 1) + kp * m + kp * OB + 2 * kp + 32 + kp + OB * OB + 3 * OB + 4;
+  return region_floats(kp, m) + kp * OB + 2 * kp + 32 + kp + OB * OB + 3 * OB + 4;
 }
 
 // kAligned: T, D, k and the slab stride are multiples of 4 and Delta, Omega and the
@@ -921,14 +1133,15 @@ template <bool kAligned>
 __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constant__ FParams p) {
   extern __shared__ __align__(16) float fsm[];
   const int T = p.T, D = p.D, k = p.k, kp = p.kp, m = p.m;
-  float* ring = fsm;                  // RING_FLOATS: the tensor-core GEMMs' stages
+  float* ring = fsm;                  // the tensor-core GEMMs' stages
   float* sA = ring;                   // the first two fp32-GEMM tiles overlay the ring
   float* sB = sA + TILE_FLOATS;
-  float* C = ring + RING_FLOATS;      // kp*(kp+1)
+  const int region = region_floats(kp, m);
+  float* C = ring + region - eig_floats(kp, m);  // kp*(kp+1), past the fp32 tiles
   const int ld = kp + 1;              // row stride of C and W: rows fall on different banks
   float* W = C + kp * ld;             // kp*ld
   float* Ws = W + kp * ld;            // kp*m: sorted leading eigenvectors
-  float* cblk = Ws + kp * m;          // kp*OB: projection coefficients of a column block
+  float* cblk = ring + region;        // kp*OB: projection coefficients of a column block
   float* rot = cblk + kp * OB;        // 2*kp
   float* red = rot + 2 * kp;          // 32
   int* perm = reinterpret_cast<int*>(red + 32);  // kp
@@ -948,7 +1161,11 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
                                      15u) == 0);
   // the tensor-core panel primitives need 16-byte aligned panel columns
   const bool panel_ok = kAligned || (((T | D) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.work) & 15u) == 0);
-  const bool tall = ring_ok && kp <= TN;  // every product in one column tile
+  // every product in one column tile: up to 64 columns on tcgen05, 48 on mma.sync
+  const bool tall = ring_ok && kp <= (kAligned ? TC_N : TN);
+  __shared__ TcState tcs;  // the aligned instance's accumulator and stage barriers
+  TcCursor tcur;           // this CTA's tensor-core stages and tiles so far (the barriers' phases)
+  if (kAligned && tall) tc_setup(&tcs);
   auto orth = [&](float* X, int n) {
     if (panel_ok)
       orth_block<true>(X, n, k, cblk, rmat, inv_diag, thr, ring);
@@ -960,32 +1177,63 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
     // Y = Delta Omega (columns k..kp-1 stay zero)
     for (int64_t e = threadIdx.x; e < (int64_t)kp * T; e += THREADS) Y[e] = 0.f;
     __syncthreads();
-    if (tall)
-      gemm_tall<float, true, false, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
-    else if (ring_ok)
+    if (tall) {
+      if constexpr (kAligned)
+        gemm_tall_tma<float, true, false>(T, k, D, &p.maps[MAP_DELTA_K], s, &p.maps[MAP_OMEGA_MN], 0, Y, 1, T, ring,
+                                          &tcs, tcur);
+      else
+        gemm_tall<float, true, false, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
+    } else if (ring_ok)
       gemm_tc<float, true, false, true, false>(T, k, D, A, D, p.omega, k, Y, 1, T, ring);
     else
       gemm<float, false, true, false, true>(T, k, D, A, D, 1, p.omega, k, 1, Y, 1, T, sA, sB);
     orth(Y, T);
     for (int it = 0; it < p.power_iters; ++it) {
-      if (tall)  // Z = Delta^T Q
-        gemm_tall<float, false, true, true, false>(D, k, T, A, D, Y, T, Z, 1, D, ring);
-      else if (ring_ok)
+      if (tall) {  // Z = Delta^T Q
+        if constexpr (kAligned)
+          gemm_tall_tma<float, false, true>(D, k, T, &p.maps[MAP_DELTA_MN], s, &p.maps[MAP_Y_K], blockIdx.x, Z, 1, D,
+                                            ring, &tcs, tcur);
+        else
+          gemm_tall<float, false, true, true, false>(D, k, T, A, D, Y, T, Z, 1, D, ring);
+      } else if (ring_ok)
         gemm_tc<float, false, true, true, false>(D, k, T, A, D, Y, T, Z, 1, D, ring);
       else
         gemm<float, false, false, true, true>(D, k, T, A, 1, D, Y, 1, T, Z, 1, D, sA, sB);
       orth(Z, D);
-      if (tall)  // Y = Delta Z
-        gemm_tall<float, true, true, true, false>(T, k, D, A, D, Z, D, Y, 1, T, ring);
-      else if (ring_ok)
+      if (tall) {  // Y = Delta Z
+        if constexpr (kAligned)
+          gemm_tall_tma<float, true, true>(T, k, D, &p.maps[MAP_DELTA_K], s, &p.maps[MAP_Z_K], blockIdx.x, Y, 1, T,
+                                           ring, &tcs, tcur);
+        else
+          gemm_tall<float, true, true, true, false>(T, k, D, A, D, Z, D, Y, 1, T, ring);
+      } else if (ring_ok)
         gemm_tc<float, true, true, true, false>(T, k, D, A, D, Z, D, Y, 1, T, ring);
       else
         gemm<float, false, true, true, true>(T, k, D, A, D, 1, Z, 1, D, Y, 1, T, sA, sB);
       orth(Y, T);
     }
-    if (tall)  // B = Q^T Delta, formed as B^T = Delta^T Q (D x k, column j = row j of B)
-      gemm_tall<float, false, true, true, false>(D, k, T, A, D, Y, T, B, 1, D, ring);
-    else if (ring_ok)  // B = Q^T Delta
+    if constexpr (kAligned) {  // the final Q, an operand of B = Q^T Delta and U_m = Q W_m: rounded to tf32
+      if (tall) {  // k * T is a multiple of 4 and Y 16-byte aligned here
+        float4* y4 = reinterpret_cast<float4*>(Y);
+#pragma unroll 4
+        for (int64_t e = threadIdx.x; e < (int64_t)k * T / 4; e += THREADS) {
+          float4 v = y4[e];
+          v.x = tf32_rn(v.x);
+          v.y = tf32_rn(v.y);
+          v.z = tf32_rn(v.z);
+          v.w = tf32_rn(v.w);
+          y4[e] = v;
+        }
+        __syncthreads();
+      }
+    }
+    if (tall) {  // B = Q^T Delta, formed as B^T = Delta^T Q (D x k, column j = row j of B)
+      if constexpr (kAligned)
+        gemm_tall_tma<float, false, true>(D, k, T, &p.maps[MAP_DELTA_MN], s, &p.maps[MAP_Y_K], blockIdx.x, B, 1, D,
+                                          ring, &tcs, tcur);
+      else
+        gemm_tall<float, false, true, true, false>(D, k, T, A, D, Y, T, B, 1, D, ring);
+    } else if (ring_ok)  // B = Q^T Delta
       gemm_tc<float, true, false, false, true>(k, D, T, Y, T, A, D, B, D, 1, ring);
     else
       gemm<float, false, true, false, true>(k, D, T, Y, T, 1, A, D, 1, B, D, 1, sA, sB);
@@ -1012,15 +1260,23 @@ __global__ void __launch_bounds__(THREADS, 2) factor_kernel(const __grid_constan
     uint16_t* uo = p.u_out + (int64_t)s * p.out_stride;
     uint16_t* vo = p.v_out + (int64_t)s * p.out_stride;
     if (tall && D >= m) {  // W_m through the free Z region, and both products on the tensor cores
-      for (int e = threadIdx.x; e < kp * m; e += THREADS) Z[e] = Ws[e];
+      for (int e = threadIdx.x; e < kp * m; e += THREADS) Z[e] = kAligned ? tf32_rn(Ws[e]) : Ws[e];
       __syncthreads();
-      gemm_tall<uint16_t, false, false, false, false>(T, m, kp, Y, T, Z, m, uo, m, 1, ring);  // U_m = Q W_m
-      gemm_tall<uint16_t, false, false, false, false>(D, m, kp, B, D, Z, m, vo, m, 1, ring);  // V_m = B^T W_m
+      if constexpr (kAligned) {
+        gemm_tall_tma<uint16_t, false, false>(T, m, kp, &p.maps[MAP_Y_MN], blockIdx.x, &p.maps[MAP_W_MN], blockIdx.x,
+                                              uo, m, 1, ring, &tcs, tcur);  // U_m = Q W_m
+        gemm_tall_tma<uint16_t, false, false>(D, m, kp, &p.maps[MAP_B_MN], blockIdx.x, &p.maps[MAP_W_MN], blockIdx.x,
+                                              vo, m, 1, ring, &tcs, tcur);  // V_m = B^T W_m
+      } else {
+        gemm_tall<uint16_t, false, false, false, false>(T, m, kp, Y, T, Z, m, uo, m, 1, ring);  // U_m = Q W_m
+        gemm_tall<uint16_t, false, false, false, false>(D, m, kp, B, D, Z, m, vo, m, 1, ring);  // V_m = B^T W_m
+      }
     } else {
       gemm<uint16_t, false, false, false>(T, m, kp, Y, 1, T, Ws, m, 1, uo, m, 1, sA, sB);  // U_m = Q W_m
       gemm<uint16_t, false, false, false>(D, m, kp, B, 1, D, Ws, m, 1, vo, m, 1, sA, sB);  // V_m = B^T W_m
     }
   }
+  if (kAligned && tall) tc_teardown(&tcs);
 }
 
 __host__ __device__ constexpr uint32_t factor_smem_bytes(int kp, int m) {

@@ -58,6 +58,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// generic-proxy writes to global memory -> visible to the async proxy (TMA loads)
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---- TMA ------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -189,6 +194,42 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor_sw(uint32_t saddr, uint32_t
   d |= static_cast<uint64_t>(1) << 46;
   d |= mode << 61;
   return d;
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma, MN-major 32-bit operands
+// (kind::tf32), 128-byte swizzle with 32-byte atomicity (swizzle field 1): each K
+// row holds 128 contiguous bytes along M (or N) whose four 32-byte units are
+// permuted by XOR with the row's index within its group of 4 rows (address bits
+// [5,7) ^= bits [7,9)); atoms of 32 values along M (or N) are lbo bytes apart,
+// groups of 4 K rows sbo bytes apart.  The tile starts on a 512-byte boundary.
+// (The plain 128-byte swizzle, field 2, is read as zeros for MN-major tf32.)
+__device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128b32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(1) << 61;
+  return d;
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, tf32 inputs (fp32 words of which the tensor
+// core reads the tf32 part), fp32 accumulate; one thread issues.
+__device__ __forceinline__ void umma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::tf32: D fp32, A and B tf32 (format 2);
+// a_mn / b_mn: that operand is MN-major (else K-major); N>>3 in [17,23), M>>4 in [24,29).
+__host__ __device__ constexpr uint32_t umma_idesc_tf32_f32(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16, both

@@ -207,9 +207,12 @@ kamera_status kamera_apply_patch(const kamera_model_desc* model, const kamera_pa
  * Method: randomized range finder with q subspace iterations on a Gaussian
  * test matrix Omega [D][k], k = m + oversample (Halko, Martinsson & Tropp
  * 2011): the products with Delta on tensor cores with tf32 operands and fp32
- * accumulation (relative rounding 2^-11, below the bf16 rounding of the output
- * factors), orthonormalisation and the small eigenproblem in fp32; exact (to
- * that rounding) when rank(Delta) <= k.  The caller passes
+ * accumulation (relative error per operand below 2^-10: when T, D, k and the
+ * slab stride are multiples of 4 and Delta, Omega and the workspace 16-byte
+ * aligned, Delta is read by TMA and truncated to tf32, otherwise rounded,
+ * 2^-11; both below the bf16 rounding of the output factors), the
+ * orthonormalisation and the small eigenproblem in fp32; exact (to that
+ * rounding) when rank(Delta) <= k.  The caller passes
  * Omega, and scratch memory of kamera_factor_workspace_size() bytes.
  */
 typedef struct {

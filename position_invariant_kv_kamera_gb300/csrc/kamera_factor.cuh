@@ -979,6 +979,17 @@ __device__ __forceinline__ void tc_wait(uint64_t* bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 2000000000ull) return;
 }
 
+// A 3-D TMA tile load with an L2 cache policy: the deficit streams through with
+// evict-first, so that it does not push the per-CTA workspace panels out of L2.
+__device__ __forceinline__ void tma_load_3d_policy(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                                   int32_t y, int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Set-up and tear-down of the accumulators and the barriers; whole CTA.
 __device__ __forceinline__ void tc_setup(TcState* tc) {
   if (threadIdx.x < 32) {
@@ -1030,7 +1041,8 @@ __device__ void gemm_tall_tma(int M, int N, int K, const CUtensorMap* amap, int 
   fence_proxy_async_global();
   fence_proxy_async_smem();
   __syncthreads();
-  if (tid == 0) {  // copies
+  if (tid == 0) {  // copies: A (the deficit, or a panel) streams evict-first, B stays in L2
+    const uint64_t pol = evict_first_policy();
     for (int idx = 0; idx < total; ++idx) {
       const uint32_t g = g0 + (uint32_t)idx, slot = g % R;
       if (g >= (uint32_t)R) tc_wait(&tc->empty[slot], ((g / R) - 1u) & 1u);
@@ -1040,10 +1052,10 @@ __device__ void gemm_tall_tma(int M, int N, int K, const CUtensorMap* amap, int 
       uint64_t* bar = &tc->full[slot];
       mbar_arrive_expect_tx(bar, TC_STAGE_BYTES);
       if (kAK) {
-        tma_load_3d(sA, amap, bar, l0, i0, az);
+        tma_load_3d_policy(sA, amap, bar, l0, i0, az, pol);
       } else {
 #pragma unroll
-        for (int a = 0; a < TM / 32; ++a) tma_load_3d(sA + 4096 * a, amap, bar, i0 + 32 * a, l0, az);
+        for (int a = 0; a < TM / 32; ++a) tma_load_3d_policy(sA + 4096 * a, amap, bar, i0 + 32 * a, l0, az, pol);
       }
       if (kBK) {
         tma_load_3d(sB, bmap, bar, l0, 0, bz);

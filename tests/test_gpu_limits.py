@@ -126,3 +126,18 @@ def test_factor_slabs_smaller_than_k(T, D):
     for s in range(2):
         assert np.isfinite(U).all() and np.isfinite(V).all()
         assert_product_matches(U[s], V[s], delta[s].astype(np.float64), (T, D, s))
+
+
+def test_factor_several_slabs_per_cta():
+    """More slabs than resident CTAs (two per SM): each CTA takes three slabs in
+    turn, so its stage and accumulator barriers carry their phases from one
+    slab and product to the next.  Every slab is an exact rank-6 deficit of
+    two 128-row tiles, and every one is reconstructed by U V^T to the bf16
+    rounding of the factors -- a CTA whose barrier phases slipped would read a
+    stale stage or accumulator and miss it."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n, T, D = 3 * 2 * sms, 256, 128
+    deltas = np.stack([gen.low_rank_deficit(22, s, T, D, np.linspace(6, 1, 6)) for s in range(n)])
+    U, V = _factor(deltas, m=8, p=16, q=2)
+    for s in range(n):
+        assert_product_matches(U[s], V[s], deltas[s].astype(np.float64), ("slab", s))

@@ -16,9 +16,12 @@
 //   Q = orth(Y);  q times: Z = orth(Delta^T Q), Q = orth(Delta Z);
 //   B = Q^T Delta  [k][D];  C = B B^T = W Lambda W^T (cyclic Jacobi);
 //   U_m = Q W_m (orthonormal columns),  V_m = B^T W_m (carries Sigma).
-// The four products with Delta run on tensor cores (tf32 operands, fp32
-// accumulation), and so do the panel products of orth() (3xTF32, about fp32
-// accuracy); the rest is fp32 on the CUDA cores.  orth() works on blocks of
+// The four products with Delta and the two output products run on tensor
+// cores (tf32 operands, fp32 accumulation): in the aligned instance as
+// tcgen05.mma fed by TMA, with the accumulators in tensor memory; otherwise as
+// warp-level MMAs fed by cp.async.  The panel products of orth() run as
+// warp-level 3xTF32 MMAs (about fp32 accuracy); the rest is fp32 on the CUDA
+// cores.  orth() works on blocks of
 // 16 columns: each block is projected off the finished columns (again when a
 // column lost more than half its norm), then orthonormalised by Cholesky QR
 // (again when the factor is ill-conditioned); a column whose remainder falls

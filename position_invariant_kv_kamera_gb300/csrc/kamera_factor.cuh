@@ -734,6 +734,8 @@ static __device__ void jacobi_eig(float* C, float* W, int kp, int ld, float* rot
   for (int e = tid; e < kp * kp; e += THREADS) W[(e / kp) * ld + e % kp] = (e / kp == e % kp) ? 1.f : 0.f;
   __syncthreads();
   const int half = kp / 2;
+  // (row, column) of element tid of a half-wide index space, and the step of THREADS elements
+  const int e_i0 = tid / half, e_j0 = tid - e_i0 * half, e_qs = THREADS / half, e_rs = THREADS - e_qs * half;
   for (int sweep = 0; sweep < MAX_SWEEPS; ++sweep) {
     float off = 0.f, tot = 0.f;
     for (int e = tid; e < kp * kp; e += THREADS) {
@@ -753,8 +755,10 @@ static __device__ void jacobi_eig(float* C, float* W, int kp, int ld, float* rot
         const float app = C[p * ld + p], aqq = C[q * ld + q], apq = C[p * ld + q];
         float c = 1.f, s = 0.f;
         if (apq != 0.f && fabsf(apq) > 1e-30f) {
-          const float zeta = (aqq - app) / (2.f * apq);
-          const float t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
+          // the angle in fast arithmetic: a rotation that leaves a small a_pq is
+          // corrected by the next sweep, and the rotation itself stays orthogonal
+          const float zeta = __fdividef(aqq - app, 2.f * apq);
+          const float t = copysignf(__fdividef(1.f, fabsf(zeta) + sqrtf(1.f + zeta * zeta)), zeta);
           c = rsqrtf(1.f + t * t);
           s = c * t;
         }
@@ -767,31 +771,42 @@ static __device__ void jacobi_eig(float* C, float* W, int kp, int ld, float* rot
       // B_ij (rows p_i, q_i; columns p_j, q_j), each of which becomes G_i B_ij G_j^T
       // with G = [c -s; s c]; W <- W G^T on the column pairs.  One step, each
       // element read and written once.
-      for (int i = tid >> 3; i < half; i += THREADS / 8) {
+      // Block e = i * half + j of C and pair e = jr * half + i of W for e = tid, tid +
+      // THREADS, ...: every thread takes about the same share (indexes stepped
+      // without division).
+      for (int e = tid, i = e_i0, j = e_j0; e < half * half; e += THREADS) {
         const float4 ri = *reinterpret_cast<const float4*>(rot + 4 * i);
+        const float4 rj = *reinterpret_cast<const float4*>(rot + 4 * j);
         const int pi = __float_as_int(ri.x), qi = __float_as_int(ri.y);
-        for (int j = tid & 7; j < half; j += 8) {
-          const float4 rj = *reinterpret_cast<const float4*>(rot + 4 * j);
-          const int pj = __float_as_int(rj.x), qj = __float_as_int(rj.y);
-          const float b00 = C[pi * ld + pj], b01 = C[pi * ld + qj], b10 = C[qi * ld + pj], b11 = C[qi * ld + qj];
-          // rows: G_i B
-          const float u00 = ri.z * b00 - ri.w * b10, u01 = ri.z * b01 - ri.w * b11;
-          const float u10 = ri.w * b00 + ri.z * b10, u11 = ri.w * b01 + ri.z * b11;
-          // columns: (G_i B) G_j^T
-          C[pi * ld + pj] = rj.z * u00 - rj.w * u01;
-          C[pi * ld + qj] = rj.w * u00 + rj.z * u01;
-          C[qi * ld + pj] = rj.z * u10 - rj.w * u11;
-          C[qi * ld + qj] = rj.w * u10 + rj.z * u11;
+        const int pj = __float_as_int(rj.x), qj = __float_as_int(rj.y);
+        const float b00 = C[pi * ld + pj], b01 = C[pi * ld + qj], b10 = C[qi * ld + pj], b11 = C[qi * ld + qj];
+        // rows: G_i B
+        const float u00 = ri.z * b00 - ri.w * b10, u01 = ri.z * b01 - ri.w * b11;
+        const float u10 = ri.w * b00 + ri.z * b10, u11 = ri.w * b01 + ri.z * b11;
+        // columns: (G_i B) G_j^T
+        C[pi * ld + pj] = rj.z * u00 - rj.w * u01;
+        C[pi * ld + qj] = rj.w * u00 + rj.z * u01;
+        C[qi * ld + pj] = rj.z * u10 - rj.w * u11;
+        C[qi * ld + qj] = rj.w * u10 + rj.z * u11;
+        j += e_rs;
+        i += e_qs;
+        if (j >= half) {
+          j -= half;
+          ++i;
         }
       }
-      for (int jr = tid >> 2; jr < kp; jr += THREADS / 4) {
+      for (int e = tid, jr = e_i0, i = e_j0; e < kp * half; e += THREADS) {
+        const float4 ri = *reinterpret_cast<const float4*>(rot + 4 * i);
         float* w = W + jr * ld;
-        for (int i = tid & 3; i < half; i += 4) {
-          const float4 ri = *reinterpret_cast<const float4*>(rot + 4 * i);
-          const int pi = __float_as_int(ri.x), qi = __float_as_int(ri.y);
-          const float xp = w[pi], xq = w[qi];
-          w[pi] = ri.z * xp - ri.w * xq;
-          w[qi] = ri.w * xp + ri.z * xq;
+        const int pi = __float_as_int(ri.x), qi = __float_as_int(ri.y);
+        const float xp = w[pi], xq = w[qi];
+        w[pi] = ri.z * xp - ri.w * xq;
+        w[qi] = ri.w * xp + ri.z * xq;
+        i += e_rs;
+        jr += e_qs;
+        if (i >= half) {
+          i -= half;
+          ++jr;
         }
       }
       __syncthreads();
